@@ -1,0 +1,331 @@
+// Host side of the C ABI declared in include/dm.h: argument validation, TMA
+// descriptor encoding, the device status word, and dispatch to the kernels.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "dm_internal.h"
+
+namespace {
+
+using dm::kDefaultWaitLimitNs;
+
+constexpr int kMaxDevices = 64;
+constexpr int kTileRows = 128;
+
+__device__ unsigned int g_status_word;  // DM_OK or the first error a kernel recorded
+
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+int g_dev_ok[kMaxDevices] = {};  // 0 unknown, 1 sm_103, -1 other
+unsigned long long g_wait_limit_ns = 0;
+int g_stall_test = 0;
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks the current device once (sm_103), and looks up the status word's
+// device address and the TMA descriptor encoder.
+dm_status device_state(unsigned int** status) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DM_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_dev_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return DM_ERR_CUDA;
+    g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  if (g_dev_ok[dev] != 1) return DM_ERR_UNSUPPORTED;
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return DM_ERR_CUDA;
+    g_status_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return DM_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  *status = g_status_ptr[dev];
+  return DM_OK;
+}
+
+// FP8 codes viewed as [BH][N][d]; box = 128 rows x d, hardware swizzle of width d.
+dm_status encode_codes_map(CUtensorMap* m, const uint8_t* codes, int BH, int N, int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d, (cuuint64_t)d * (cuuint64_t)N};
+  cuuint32_t box[3] = {(cuuint32_t)d, (cuuint32_t)kTileRows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(codes), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DM_OK : DM_ERR_CUDA;
+}
+
+dm_status check_params(const dm_attn_params* p) {
+  if (!p) return DM_ERR_INVALID_ARG;
+  if (p->B < 0 || p->Hq <= 0 || p->Hkv <= 0 || p->N < 0) return DM_ERR_SHAPE;
+  if (p->d != 64 && p->d != 128) return DM_ERR_SHAPE;
+  if (p->Hq % p->Hkv != 0) return DM_ERR_SHAPE;
+  if ((long long)p->B * p->Hq * p->N * p->d >= (1ll << 31)) return DM_ERR_SHAPE;
+  if (!std::isfinite(p->softmax_scale)) return DM_ERR_INVALID_ARG;
+  return DM_OK;
+}
+
+bool is_empty(const dm_attn_params* p) { return p->B == 0 || p->N == 0; }
+
+dm_status check_fp8(const dm_fp8_tensor& t) {
+  if (!t.codes || !t.scales) return DM_ERR_INVALID_ARG;
+  if (!aligned16(t.codes) || !aligned16(t.scales)) return DM_ERR_ALIGNMENT;
+  return DM_OK;
+}
+
+dm_status check_ptr(const void* ptr) {
+  if (!ptr) return DM_ERR_INVALID_ARG;
+  return aligned16(ptr) ? DM_OK : DM_ERR_ALIGNMENT;
+}
+
+bool valid_dtype(dm_dtype t) { return t == DM_F32 || t == DM_BF16; }
+bool valid_mode(dm_delta_mode m) {
+  return m == DM_DELTA_MATCHED || m == DM_DELTA_STALE_DO || m == DM_DELTA_STALE_DOHAT;
+}
+
+dm::AttnArgs make_args(const dm_attn_params* p, unsigned int* status) {
+  dm::AttnArgs a{};
+  a.B = p->B, a.Hq = p->Hq, a.Hkv = p->Hkv, a.N = p->N;
+  a.T = (p->N + kTileRows - 1) / kTileRows;
+  a.causal = p->causal ? 1 : 0;
+  a.sigma = p->softmax_scale > 0.f ? p->softmax_scale : (float)(1.0 / std::sqrt((double)p->d));
+  a.status = status;
+  std::lock_guard<std::mutex> lock(g_mu);
+  a.wait_limit_ns = g_wait_limit_ns ? g_wait_limit_ns : kDefaultWaitLimitNs;
+  return a;
+}
+
+#define DM_TRY(expr)            \
+  do {                          \
+    dm_status _s = (expr);      \
+    if (_s != DM_OK) return _s; \
+  } while (0)
+
+inline dm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DM_OK : DM_ERR_CUDA; }
+
+dm_status check_delta_inputs(dm_delta_mode mode, dm_fp8_tensor q, dm_fp8_tensor k, dm_fp8_tensor v,
+                             dm_fp8_tensor do_hat, const float* lse, const void* dO, dm_dtype do_dtype,
+                             const void* O, dm_dtype o_dtype) {
+  switch (mode) {
+    case DM_DELTA_MATCHED:
+      DM_TRY(check_fp8(q));
+      DM_TRY(check_fp8(k));
+      DM_TRY(check_fp8(v));
+      DM_TRY(check_fp8(do_hat));
+      DM_TRY(check_ptr(lse));
+      return DM_OK;
+    case DM_DELTA_STALE_DO:
+      DM_TRY(check_ptr(dO));
+      DM_TRY(check_ptr(O));
+      if (!valid_dtype(do_dtype) || !valid_dtype(o_dtype)) return DM_ERR_DTYPE;
+      return DM_OK;
+    case DM_DELTA_STALE_DOHAT:
+      DM_TRY(check_fp8(do_hat));
+      DM_TRY(check_ptr(O));
+      if (!valid_dtype(o_dtype)) return DM_ERR_DTYPE;
+      return DM_OK;
+  }
+  return DM_ERR_INVALID_ARG;
+}
+
+dm_status delta_impl(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor q, dm_fp8_tensor k,
+                     dm_fp8_tensor v, dm_fp8_tensor do_hat, const float* lse, const void* dO, dm_dtype do_dtype,
+                     const void* O, dm_dtype o_dtype, float* delta, unsigned int* status, cudaStream_t st) {
+  dm::AttnArgs a = make_args(p, status);
+  if (mode == DM_DELTA_MATCHED) {
+    dm::DeltaLaunch f{};
+    DM_TRY(encode_codes_map(&f.tmQ, q.codes, p->B * p->Hq, p->N, p->d));
+    DM_TRY(encode_codes_map(&f.tmK, k.codes, p->B * p->Hkv, p->N, p->d));
+    DM_TRY(encode_codes_map(&f.tmV, v.codes, p->B * p->Hkv, p->N, p->d));
+    DM_TRY(encode_codes_map(&f.tmDO, do_hat.codes, p->B * p->Hq, p->N, p->d));
+    a.q_scales = q.scales, a.k_scales = k.scales, a.v_scales = v.scales, a.do_scales = do_hat.scales;
+    f.args = a;
+    f.lse = lse;
+    f.delta = delta;
+    return cuda_status(dm::launch_delta_matched(f, p->d, st));
+  }
+  a.do_scales = do_hat.scales;
+  return cuda_status(dm::launch_delta_stale(a, p->d, mode, dO, do_dtype, do_hat.codes, O, o_dtype, delta, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+int dm_version(void) { return 100; }
+
+const char* dm_status_string(dm_status s) {
+  switch (s) {
+    case DM_OK: return "DM_OK";
+    case DM_ERR_INVALID_ARG: return "DM_ERR_INVALID_ARG";
+    case DM_ERR_SHAPE: return "DM_ERR_SHAPE";
+    case DM_ERR_DTYPE: return "DM_ERR_DTYPE";
+    case DM_ERR_ALIGNMENT: return "DM_ERR_ALIGNMENT";
+    case DM_ERR_UNSUPPORTED: return "DM_ERR_UNSUPPORTED";
+    case DM_ERR_CUDA: return "DM_ERR_CUDA";
+    case DM_ERR_TIMEOUT: return "DM_ERR_TIMEOUT";
+  }
+  return "DM_ERR_UNKNOWN";
+}
+
+dm_status dm_set_knob(dm_knob knob, long long value) {
+  if (value < 0) return DM_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  switch (knob) {
+    case DM_KNOB_WAIT_LIMIT_NS: g_wait_limit_ns = (unsigned long long)value; return DM_OK;
+    case DM_KNOB_STALL_TEST: g_stall_test = value ? 1 : 0; return DM_OK;
+  }
+  return DM_ERR_INVALID_ARG;
+}
+
+dm_status dm_get_status(void* stream) {
+  unsigned int* status = nullptr;
+  DM_TRY(device_state(&status));
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return DM_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v)) != cudaSuccess) return DM_ERR_CUDA;
+  if (v != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return DM_ERR_CUDA;
+  }
+  return v == 0 ? DM_OK : (dm_status)v;
+}
+
+dm_status dm_quantize(const void* x, dm_dtype x_dtype, int B, int H, int N, int d, dm_fp8 fmt, uint8_t* codes,
+                      float* scales, uint8_t* codes_t, void* stream) {
+  if (!valid_dtype(x_dtype)) return DM_ERR_DTYPE;
+  if (fmt != DM_E4M3 && fmt != DM_E5M2) return DM_ERR_INVALID_ARG;
+  if (B < 0 || H <= 0 || N < 0 || (d != 64 && d != 128)) return DM_ERR_SHAPE;
+  if ((long long)B * H * N * d >= (1ll << 31)) return DM_ERR_SHAPE;
+  if (B == 0 || N == 0) return DM_OK;  // empty input: nothing to do, pointers may be NULL
+  DM_TRY(check_ptr(x));
+  DM_TRY(check_ptr(codes));
+  DM_TRY(check_ptr(scales));
+  if (codes_t && !aligned16(codes_t)) return DM_ERR_ALIGNMENT;
+  unsigned int* status = nullptr;
+  DM_TRY(device_state(&status));
+  return cuda_status(dm::launch_quantize(x, x_dtype, B, H, N, d, fmt, codes, scales, codes_t, as_stream(stream)));
+}
+
+dm_status dm_attn_fwd(const dm_attn_params* p, dm_fp8_tensor q, dm_fp8_tensor k, dm_fp8_tensor v, void* O,
+                      dm_dtype o_dtype, float* lse, void* stream) {
+  DM_TRY(check_params(p));
+  if (!valid_dtype(o_dtype)) return DM_ERR_DTYPE;
+  if (is_empty(p)) return DM_OK;  // empty input: nothing to do, pointers may be NULL
+  DM_TRY(check_fp8(q));
+  DM_TRY(check_fp8(k));
+  DM_TRY(check_fp8(v));
+  DM_TRY(check_ptr(O));
+  DM_TRY(check_ptr(lse));
+  unsigned int* status = nullptr;
+  DM_TRY(device_state(&status));
+  dm::FwdLaunch f{};
+  DM_TRY(encode_codes_map(&f.tmQ, q.codes, p->B * p->Hq, p->N, p->d));
+  DM_TRY(encode_codes_map(&f.tmK, k.codes, p->B * p->Hkv, p->N, p->d));
+  DM_TRY(encode_codes_map(&f.tmV, v.codes, p->B * p->Hkv, p->N, p->d));
+  f.args = make_args(p, status);
+  f.args.q_scales = q.scales, f.args.k_scales = k.scales, f.args.v_scales = v.scales;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    f.args.stall_test = g_stall_test;
+    g_stall_test = 0;
+  }
+  f.O = O;
+  f.lse = lse;
+  return cuda_status(dm::launch_attn_fwd(f, p->d, o_dtype == DM_BF16, as_stream(stream)));
+}
+
+dm_status dm_attn_delta(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor q, dm_fp8_tensor k,
+                        dm_fp8_tensor v, dm_fp8_tensor do_hat, const float* lse, const void* dO, dm_dtype do_dtype,
+                        const void* O, dm_dtype o_dtype, float* delta, void* stream) {
+  DM_TRY(check_params(p));
+  if (!valid_mode(mode)) return DM_ERR_INVALID_ARG;
+  if (is_empty(p)) return DM_OK;
+  DM_TRY(check_delta_inputs(mode, q, k, v, do_hat, lse, dO, do_dtype, O, o_dtype));
+  DM_TRY(check_ptr(delta));
+  unsigned int* status = nullptr;
+  DM_TRY(device_state(&status));
+  return delta_impl(p, mode, q, k, v, do_hat, lse, dO, do_dtype, O, o_dtype, delta, status, as_stream(stream));
+}
+
+size_t dm_attn_bwd_workspace_size(const dm_attn_params* p) {
+  if (check_params(p) != DM_OK) return 0;
+  const size_t bytes = (size_t)p->B * p->Hq * p->N * sizeof(float);
+  return (bytes + 255) & ~(size_t)255;
+}
+
+dm_status dm_attn_bwd(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor q, dm_fp8_tensor k,
+                      dm_fp8_tensor v, dm_fp8_tensor do_hat, const float* lse, const float* delta, const void* dO,
+                      dm_dtype do_dtype, const void* O, dm_dtype o_dtype, float* dQ, float* dK, float* dV,
+                      const dm_diag* diag, void* workspace, size_t workspace_bytes, void* stream) {
+  DM_TRY(check_params(p));
+  if (!valid_mode(mode)) return DM_ERR_INVALID_ARG;
+  if (is_empty(p)) return DM_OK;
+  DM_TRY(check_fp8(q));
+  DM_TRY(check_fp8(k));
+  DM_TRY(check_fp8(v));
+  DM_TRY(check_fp8(do_hat));
+  DM_TRY(check_ptr(lse));
+  DM_TRY(check_ptr(dQ));
+  DM_TRY(check_ptr(dK));
+  DM_TRY(check_ptr(dV));
+  dm_diag dg{};
+  if (diag) {
+    dg = *diag;
+    for (float* ptr : {dg.rowsum_pre, dg.abssum_pre, dg.rowsum_post, dg.abssum_post})
+      if (ptr && !aligned16(ptr)) return DM_ERR_ALIGNMENT;
+  }
+  const float* dl = delta;
+  if (delta) {
+    DM_TRY(check_ptr(delta));
+  } else {
+    DM_TRY(check_delta_inputs(mode, q, k, v, do_hat, lse, dO, do_dtype, O, o_dtype));
+    DM_TRY(check_ptr(workspace));
+    if (workspace_bytes < dm_attn_bwd_workspace_size(p)) return DM_ERR_INVALID_ARG;
+  }
+  unsigned int* status = nullptr;
+  DM_TRY(device_state(&status));
+  cudaStream_t st = as_stream(stream);
+  if (!delta) {
+    float* ws = static_cast<float*>(workspace);
+    DM_TRY(delta_impl(p, mode, q, k, v, do_hat, lse, dO, do_dtype, O, o_dtype, ws, status, st));
+    dl = ws;
+  }
+  DM_TRY(cuda_status(dm::launch_zero(dQ, (size_t)p->B * p->Hq * p->N * p->d, st)));
+  const size_t nrow = (size_t)p->B * p->Hq * p->N;
+  for (float* ptr : {dg.rowsum_pre, dg.abssum_pre, dg.rowsum_post, dg.abssum_post})
+    if (ptr) DM_TRY(cuda_status(dm::launch_zero(ptr, nrow, st)));
+  dm::BwdLaunch f{};
+  DM_TRY(encode_codes_map(&f.tmQ, q.codes, p->B * p->Hq, p->N, p->d));
+  DM_TRY(encode_codes_map(&f.tmK, k.codes, p->B * p->Hkv, p->N, p->d));
+  DM_TRY(encode_codes_map(&f.tmV, v.codes, p->B * p->Hkv, p->N, p->d));
+  DM_TRY(encode_codes_map(&f.tmDO, do_hat.codes, p->B * p->Hq, p->N, p->d));
+  f.args = make_args(p, status);
+  f.args.q_scales = q.scales, f.args.k_scales = k.scales, f.args.v_scales = v.scales;
+  f.args.do_scales = do_hat.scales;
+  f.lse = lse;
+  f.delta = dl;
+  f.dQ = dQ, f.dK = dK, f.dV = dV;
+  f.diag = dg;
+  return cuda_status(dm::launch_attn_bwd(f, p->d, st));
+}
+
+}  // extern "C"

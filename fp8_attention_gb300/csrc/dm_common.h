@@ -1,0 +1,27 @@
+// Definitions shared by the host API and the kernels of libdm.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/dm.h"
+
+namespace dm {
+
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;  // 2 s
+
+// Arguments common to the attention kernels (all device pointers).
+struct AttnArgs {
+  int B, Hq, Hkv, N, T;      // T = ceil(N / 128)
+  int causal;
+  float sigma;               // softmax scale
+  const float* q_scales;     // [B][Hq][T]
+  const float* k_scales;     // [B][Hkv][T]
+  const float* v_scales;     // [B][Hkv][T]
+  const float* do_scales;    // [B][Hq][T]
+  unsigned int* status;      // device status word
+  unsigned long long wait_limit_ns;
+  int stall_test;            // 1: the MMA warp waits on a barrier nothing signals
+};
+
+}  // namespace dm

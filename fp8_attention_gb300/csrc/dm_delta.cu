@@ -1,0 +1,219 @@
+// Matched softmax row correction ("Delta-Matching for reliable FP8 attention
+// training", section 03): delta_i = sum_j P_ij * dP^_ij with P = exp(S - LSE)
+// the FP32 softmax before quantisation and dP^ = dO^ V^T the FP32 result of
+// the FP8 matmul.  This is the separate correction pass: one CTA per (batch,
+// query head, 128-row query tile), recomputing S = Q K^T and dP^ = dO^ V^T
+// on tcgen05 tile by tile.
+//
+// Warp roles (320 threads):
+//   warp 0      TMA: Q and dO tiles once, K/V tiles double-buffered
+//   warp 1      MMA: S(t) into TMEM S[t%2], dP(t) into TMEM dP[t%2]
+//   warps 2-9   two warpgroups, one thread per (query row, half of the key
+//               columns): P = exp2(S*c1 - LSE*log2e), sum P*dP, scaled by
+//               s_dO * s_V,t per key tile
+// TMEM columns: S[0] 0, S[1] 128, dP[0] 256, dP[1] 384.
+#include <cudaTypedefs.h>
+
+#include "dm_device.cuh"
+#include "dm_internal.h"
+
+namespace dm {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct DeltaLayout {
+  static constexpr int kTileBytes = kTile * D;
+  static constexpr int kQ = 0;
+  static constexpr int kDO = kQ + kTileBytes;
+  static constexpr int kK = kDO + kTileBytes;      // 2 stages
+  static constexpr int kV = kK + 2 * kTileBytes;   // 2 stages
+  static constexpr int kBytes = kV + 2 * kTileBytes;
+  static constexpr int kDynSmem = kBytes + 1024;
+};
+
+struct DeltaBars {
+  uint64_t q, kfull[2], kempty[2], vfull[2], vempty[2], sfull[2], dpfull[2], tempty[2], mma_done;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_delta_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                      const AttnArgs a, const float* __restrict__ lse, float* __restrict__ delta) {
+  using L = DeltaLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ DeltaBars bars;
+  __shared__ float s_part[kTile];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int BH = a.B * a.Hq;
+  const int qt = a.T - 1 - (int)(blockIdx.x / BH);
+  const int bh = (int)(blockIdx.x % BH);
+  const int b = bh / a.Hq, h = bh % a.Hq;
+  const int bg = b * a.Hkv + h / (a.Hq / a.Hkv);
+  const int q0 = qt * kTile;
+  const int nkv = a.causal ? qt + 1 : a.T;
+
+  Watchdog wd{&s_abort, a.status, a.wait_limit_ns};
+  if (tid == 0) {
+    s_abort = 0;
+    mbar_init(&bars.q, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars.kfull[s], 1);
+      mbar_init(&bars.kempty[s], 1);
+      mbar_init(&bars.vfull[s], 1);
+      mbar_init(&bars.vempty[s], 1);
+      mbar_init(&bars.sfull[s], 1);
+      mbar_init(&bars.dpfull[s], 1);
+      mbar_init(&bars.tempty[s], 8);
+    }
+    mbar_init(&bars.mma_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s_tmem, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmDO);
+      mbar_arrive_expect_tx(&bars.q, 2 * L::kTileBytes);
+      tma_load_3d(sm + L::kQ, &tmQ, &bars.q, 0, q0, bh);
+      tma_load_3d(sm + L::kDO, &tmDO, &bars.q, 0, q0, bh);
+      int issued = 0;
+      for (int t = 0; t < nkv; ++t) {
+        const int s = t & 1;
+        const uint32_t ph = (t >> 1) & 1;
+        if (!wait(&bars.kempty[s], ph ^ 1, wd)) break;
+        if (!wait(&bars.vempty[s], ph ^ 1, wd)) break;
+        mbar_arrive_expect_tx(&bars.kfull[s], L::kTileBytes);
+        tma_load_3d(sm + L::kK + s * L::kTileBytes, &tmK, &bars.kfull[s], 0, t * kTile, bg);
+        mbar_arrive_expect_tx(&bars.vfull[s], L::kTileBytes);
+        tma_load_3d(sm + L::kV + s * L::kTileBytes, &tmV, &bars.vfull[s], 0, t * kTile, bg);
+        issued = t + 1;
+      }
+      wait_drain(&bars.q, 0, a.wait_limit_ns);
+      for (int t = max(0, issued - 2); t < issued; ++t) {
+        wait_drain(&bars.kfull[t & 1], (t >> 1) & 1, a.wait_limit_ns);
+        wait_drain(&bars.vfull[t & 1], (t >> 1) & 1, a.wait_limit_ns);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_f8(0, 0, 0, 0, kTile, kTile);   // Q K^T
+      constexpr uint32_t kIdDP = idesc_f8(1, 0, 0, 0, kTile, kTile);  // dO^ (E5M2) V^T (E4M3)
+      bool ok = wait(&bars.q, 0, wd);
+      tc_fence_after();
+      const uint32_t sQ = smem_u32(sm + L::kQ), sDO = smem_u32(sm + L::kDO);
+      for (int t = 0; t < nkv && ok; ++t) {
+        const int s = t & 1;
+        const uint32_t ph = (t >> 1) & 1;
+        ok = wait(&bars.tempty[s], ph ^ 1, wd) && wait(&bars.kfull[s], ph, wd);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sK = smem_u32(sm + L::kK + s * L::kTileBytes);
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k)
+          mma_f8(tmem + s * 128, SwTile<D>::kmajor(sQ, k), SwTile<D>::kmajor(sK, k), kIdS, k > 0);
+        mma_commit(&bars.sfull[s]);
+        mma_commit(&bars.kempty[s]);
+        ok = wait(&bars.vfull[s], ph, wd);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sV = smem_u32(sm + L::kV + s * L::kTileBytes);
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k)
+          mma_f8(tmem + 256 + s * 128, SwTile<D>::kmajor(sDO, k), SwTile<D>::kmajor(sV, k), kIdDP, k > 0);
+        mma_commit(&bars.dpfull[s]);
+        mma_commit(&bars.vempty[s]);
+      }
+      mma_commit(&bars.mma_done);
+      wait_drain(&bars.mma_done, 0, a.wait_limit_ns);
+    }
+  } else {
+    const int wg = (warp - 2) >> 2;  // key-column half
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int qi = q0 + row;
+    const bool row_valid = qi < a.N;
+    const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16) + wg * 64;
+    const float sq = a.q_scales[bh * a.T + qt];
+    const float sdo = a.do_scales[bh * a.T + qt];
+    const float lse2 = row_valid ? lse[(size_t)bh * a.N + qi] * kLog2e : 0.0f;
+    float dl = 0.0f;
+    for (int t = 0; t < nkv; ++t) {
+      const int s = t & 1;
+      const uint32_t ph = (t >> 1) & 1;
+      const float c1 = a.sigma * sq * a.k_scales[bg * a.T + t] * kLog2e;
+      const float c2 = sdo * a.v_scales[bg * a.T + t];
+      const int j0 = t * kTile + wg * 64;
+      int jlim = min(64, a.N - j0);
+      if (a.causal) jlim = min(jlim, qi - j0 + 1);
+      float sv[64], dp[64];
+      wait(&bars.sfull[s], ph, wd);
+      tc_fence_after();
+      tmem_ld32(tl + s * 128, *reinterpret_cast<float(*)[32]>(&sv[0]));
+      tmem_ld32(tl + s * 128 + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
+      wait(&bars.dpfull[s], ph, wd);
+      tc_fence_after();
+      tmem_ld32(tl + 256 + s * 128, *reinterpret_cast<float(*)[32]>(&dp[0]));
+      tmem_ld32(tl + 256 + s * 128 + 32, *reinterpret_cast<float(*)[32]>(&dp[32]));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.tempty[s]);
+      float part0 = 0.0f, part1 = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 64; c += 2) {
+        const float p0 = (c < jlim) ? ex2(fmaf(sv[c], c1, -lse2)) : 0.0f;
+        const float p1 = (c + 1 < jlim) ? ex2(fmaf(sv[c + 1], c1, -lse2)) : 0.0f;
+        part0 = fmaf(p0, dp[c], part0);
+        part1 = fmaf(p1, dp[c + 1], part1);
+      }
+      dl = fmaf(part0 + part1, c2, dl);
+    }
+    if (wg == 1) s_part[row] = dl;
+    named_bar_sync(1, 256);
+    if (wg == 0 && row_valid) delta[(size_t)bh * a.N + qi] = dl + s_part[row];
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_t(const DeltaLaunch& f, cudaStream_t st) {
+  auto k = attn_delta_kernel<D>;
+  constexpr int smem = DeltaLayout<D>::kDynSmem;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = (unsigned)(f.args.B * f.args.Hq * f.args.T);
+  k<<<grid, kThreads, smem, st>>>(f.tmQ, f.tmK, f.tmV, f.tmDO, f.args, f.lse, f.delta);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_delta_matched(const DeltaLaunch& f, int d, cudaStream_t st) {
+  return d == 128 ? launch_t<128>(f, st) : launch_t<64>(f, st);
+}
+
+}  // namespace dm

@@ -1,0 +1,304 @@
+// Device-side building blocks for the sm_103a kernels: mbarriers with bounded
+// waits, TMA tile loads, tcgen05 (TMEM allocation, FP8 MMA, TMEM loads and
+// stores), shared-memory matrix descriptors, and packed FP8 conversions.
+// Everything is inline PTX written from the PTX ISA; no CUTLASS/CuTe.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "dm_common.h"
+
+namespace dm {
+
+constexpr int kTile = 128;  // rows of a query/key tile and of an MMA M dimension
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ------------------------------------------------------------------ mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Watchdog shared by all waits of one CTA.  Every wait is bounded: after
+// `limit_ns` without progress the waiting thread records DM_ERR_TIMEOUT in the
+// device status word and raises the CTA's abort flag; from then on every wait
+// of the CTA returns immediately, so all roles run their (counted) loops to
+// the end without blocking and the kernel exits normally.
+struct Watchdog {
+  volatile int* abort_flag;  // shared memory
+  unsigned int* status;      // global status word
+  unsigned long long limit_ns;
+};
+
+static __device__ __noinline__ bool wait_slow(uint64_t* bar, uint32_t parity, const Watchdog& wd) {
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*wd.abort_flag) return false;
+    if (globaltimer() - t0 > wd.limit_ns) {
+      *wd.abort_flag = 1;
+      atomicCAS(wd.status, 0u, (unsigned)DM_ERR_TIMEOUT);
+      __threadfence();
+      return false;
+    }
+  }
+}
+
+// Returns true when the phase with `parity` completed, false on abort.
+__device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, const Watchdog& wd) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, wd);
+}
+
+// Wait bounded only by time (not by the abort flag): used at teardown so that
+// a CTA never exits while its own TMA copies or MMAs are still in flight.
+static __device__ __noinline__ bool wait_drain(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer() - t0 > limit_ns) return false;
+  return true;
+}
+
+// ----------------------------------------------------------------------- TMA
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 3-D tiled load: coordinates (c0 innermost, c1, c2) in elements.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                            int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ------------------------------------------------------------------- tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T with FP8 operands, FP32 accumulation.
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The mbarrier tracks completion of all prior tcgen05 async ops of this thread.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+// Instruction descriptor for kind::f8f6f4 with FP32 accumulator.
+//   bits 4-5 D format (1 = F32), 7-9 A format, 10-12 B format (0 = E4M3,
+//   1 = E5M2), 15 A major, 16 B major (0 = K-major, 1 = MN-major),
+//   17-22 N >> 3, 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t idesc_f8(uint32_t a_fmt, uint32_t b_fmt, uint32_t a_mn, uint32_t b_mn,
+                                                uint32_t M, uint32_t N) {
+  return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) |
+         ((M >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): start address >> 4 in
+// bits 0-13, leading-dimension byte offset >> 4 in 16-29, stride-dimension
+// byte offset >> 4 in 32-45, fixed 0b001 in 46-48, swizzle mode in 61-63
+// (2 = 128-byte, 4 = 64-byte).
+enum : uint32_t { kSwizzle128 = 2, kSwizzle64 = 4 };
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t swz) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | ((uint64_t)swz << 61);
+}
+
+// A [rows][row_bytes] FP8 tile in shared memory, rows contiguous, written by
+// TMA (or by threads) with the hardware swizzle of width row_bytes (128 or
+// 64).  Two views:
+//  * K-major: MMA rows = tile rows, K = the row's bytes.  K step k (32 FP8
+//    elements) starts 32*k bytes into the row.
+//  * MN-major: MMA M/N = the row's bytes, K = tile rows.  K step k starts at
+//    row 32*k.
+// In both views 8 rows form one swizzle atom (SBO = 8 * row_bytes).
+template <int ROW_BYTES>
+struct SwTile {
+  static_assert(ROW_BYTES == 128 || ROW_BYTES == 64, "row width");
+  static constexpr uint32_t kSwz = ROW_BYTES == 128 ? kSwizzle128 : kSwizzle64;
+  static constexpr uint32_t kSbo = 8 * ROW_BYTES;
+  __device__ static uint64_t kmajor(uint32_t base, int kstep) {
+    return smem_desc(base + 32u * kstep, 16u, kSbo, kSwz);
+  }
+  __device__ static uint64_t mnmajor(uint32_t base, int kstep) {
+    return smem_desc(base + 32u * ROW_BYTES * kstep, 16u * 1024u, kSbo, kSwz);
+  }
+  // Byte offset of 16-byte chunk `c` of row `r` (for threads writing the
+  // tile): the swizzle XORs address bits [4, 4+b) with bits [7, 7+b), b = 3
+  // for 128-byte rows and 2 for 64-byte rows (tile base 1024-byte aligned).
+  __device__ static uint32_t chunk_offset(int r, int c) {
+    const uint32_t a = (uint32_t)(r * ROW_BYTES + c * 16);
+    constexpr uint32_t kMask = ROW_BYTES == 128 ? 7u : 3u;
+    return a ^ (((a >> 7) & kMask) << 4);
+  }
+};
+
+// 32 lanes x 32 consecutive 32-bit columns.  Lane quarter of the warp is
+// (warp_id % 4); taddr must carry that lane base in bits 16+.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  const uint32_t* r = reinterpret_cast<const uint32_t*>(v);
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ------------------------------------------------------------------ numerics
+// Four FP32 values -> four FP8 codes (round to nearest even, saturating),
+// byte k of the result holds value k.
+__device__ __forceinline__ uint32_t pack4_e4m3(float x0, float x1, float x2, float x3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
+  return r;
+}
+__device__ __forceinline__ uint32_t pack4_e5m2(float x0, float x1, float x2, float x3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e5m2x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e5m2x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
+  return r;
+}
+template <int FMT>
+__device__ __forceinline__ uint32_t pack4(float x0, float x1, float x2, float x3) {
+  return FMT == 0 ? pack4_e4m3(x0, x1, x2, x3) : pack4_e5m2(x0, x1, x2, x3);
+}
+
+// Two FP8 codes (low byte first) -> two exact FP32 values, via f16x2.
+template <int FMT>
+__device__ __forceinline__ float2 unpack2(uint16_t codes) {
+  uint32_t h2;
+  if (FMT == 0)
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
+  else
+    asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(codes));
+  __half2 h = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(h);
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Tile quantiser scale rule (see dm.h): returns s and sets r; s = r = 0 when
+// the tile is flushed.
+template <int FMT>
+__device__ __forceinline__ float tile_scale(float amax, float& r) {
+  constexpr float kFmax = FMT == 0 ? 448.0f : 57344.0f;
+  if (!(amax >= 0x1p-96f)) {
+    r = 0.0f;
+    return 0.0f;
+  }
+  r = __fdiv_rn(kFmax, amax);
+  return __fdiv_rn(amax, kFmax);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+}  // namespace dm

@@ -1,0 +1,244 @@
+// Bandwidth-bound kernels: the per-tile FP8 quantiser, the stale row
+// corrections, and a zero fill.
+//
+// Quantiser: block scales of "Delta-Matching for reliable FP8 attention
+// training", section 01 ("What changes in FP8?"), with the amax rule stated
+// in dm.h; one CTA per 128-row x d tile, the tile held in registers between
+// the amax reduction and the encode, 16-byte coalesced loads.
+//
+// Stale corrections: delta_i = <dO_i, O_i> (section 01, "Why can we reuse the
+// forward output?") and delta_i = <dO^_i, O_i> (section 03), one warp per row.
+#include <cuda_bf16.h>
+
+#include "dm_device.cuh"
+#include "dm_internal.h"
+
+namespace dm {
+namespace {
+
+constexpr int kQThreads = 256;
+
+template <typename T>
+struct Vec;
+template <>
+struct Vec<float> {
+  static constexpr int kElems = 4;  // 16 bytes
+  __device__ static void load(const float* p, float* out) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(p));
+    out[0] = v.x, out[1] = v.y, out[2] = v.z, out[3] = v.w;
+  }
+};
+template <>
+struct Vec<__nv_bfloat16> {
+  static constexpr int kElems = 8;
+  __device__ static void load(const __nv_bfloat16* p, float* out) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      out[2 * k] = __uint_as_float(w[k] << 16);
+      out[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+  }
+};
+
+// One CTA per (b*h, tile).  Supports d in {64, 128}.
+template <typename T, int FMT, int D>
+__global__ void __launch_bounds__(kQThreads) quantize_kernel(const T* __restrict__ x, int N, int T_tiles,
+                                                             uint8_t* __restrict__ codes,
+                                                             float* __restrict__ scales,
+                                                             uint8_t* __restrict__ codes_t) {
+  constexpr int V = Vec<T>::kElems;
+  constexpr int kVecs = kTile * D / V;     // vectors in a full tile
+  constexpr int kPer = kVecs / kQThreads;  // per thread
+  __shared__ float s_red[kQThreads / 32];
+  __shared__ __align__(16) uint8_t s_codes[kTile * D];
+
+  const int tile = blockIdx.x;
+  const int bh = tile / T_tiles, t = tile % T_tiles;
+  const int rows = min(kTile, N - t * kTile);
+  const size_t base = ((size_t)bh * N + (size_t)t * kTile) * D;
+  const int nvec = rows * D / V;
+
+  float v[kPer][V];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int idx = threadIdx.x + i * kQThreads;
+    if (idx < nvec) {
+      Vec<T>::load(x + base + (size_t)idx * V, v[i]);
+#pragma unroll
+      for (int k = 0; k < V; ++k) amax = fmaxf(amax, fabsf(v[i][k]));
+    } else {
+#pragma unroll
+      for (int k = 0; k < V; ++k) v[i][k] = 0.0f;
+    }
+  }
+  amax = warp_max(amax);
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = s_red[0];
+#pragma unroll
+  for (int w = 1; w < kQThreads / 32; ++w) amax = fmaxf(amax, s_red[w]);
+  float r;
+  const float s = tile_scale<FMT>(amax, r);
+  if (threadIdx.x == 0) scales[tile] = s;
+
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int idx = threadIdx.x + i * kQThreads;
+    if (idx >= nvec) continue;
+    uint32_t w[V / 4];
+#pragma unroll
+    for (int k = 0; k < V / 4; ++k)
+      w[k] = pack4<FMT>(__fmul_rn(v[i][4 * k], r), __fmul_rn(v[i][4 * k + 1], r), __fmul_rn(v[i][4 * k + 2], r),
+                        __fmul_rn(v[i][4 * k + 3], r));
+    uint8_t* dst = codes + base + (size_t)idx * V;
+    if constexpr (V == 8) {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+      if (codes_t) *reinterpret_cast<uint2*>(s_codes + idx * V) = make_uint2(w[0], w[1]);
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = w[0];
+      if (codes_t) *reinterpret_cast<uint32_t*>(s_codes + idx * V) = w[0];
+    }
+  }
+  if (codes_t) {
+    // transposed copy [bh][d][N]
+    __syncthreads();
+    uint8_t* out = codes_t + (size_t)bh * D * N + (size_t)t * kTile;
+    for (int e = threadIdx.x; e < D * kTile; e += kQThreads) {
+      const int c = e / kTile, rr = e % kTile;
+      if (rr < rows) out[(size_t)c * N + rr] = s_codes[rr * D + c];
+    }
+  }
+}
+
+template <typename T, int FMT>
+cudaError_t quantize_t(const T* x, int BH, int N, int d, uint8_t* codes, float* scales, uint8_t* codes_t,
+                       cudaStream_t st) {
+  const int T_tiles = (N + kTile - 1) / kTile;
+  const unsigned grid = (unsigned)(BH * T_tiles);
+  if (d == 128)
+    quantize_kernel<T, FMT, 128><<<grid, kQThreads, 0, st>>>(x, N, T_tiles, codes, scales, codes_t);
+  else
+    quantize_kernel<T, FMT, 64><<<grid, kQThreads, 0, st>>>(x, N, T_tiles, codes, scales, codes_t);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- stale delta
+__device__ __forceinline__ void load_row(const float* p, int k0, int n, float* out) {
+  for (int k = 0; k < n; k += 2) {
+    const float2 v = *reinterpret_cast<const float2*>(p + k0 + k);
+    out[k] = v.x, out[k + 1] = v.y;
+  }
+}
+__device__ __forceinline__ void load_row(const __nv_bfloat16* p, int k0, int n, float* out) {
+  for (int k = 0; k < n; k += 2) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(p + k0 + k);
+    out[k] = __uint_as_float(w << 16), out[k + 1] = __uint_as_float(w & 0xFFFF0000u);
+  }
+}
+
+// MODE 1: delta = <dO, O>; MODE 2: delta = s_dO * <codes(dO^), O>.  One warp
+// per row, each lane holds d/32 consecutive channels.
+template <int MODE, int D, typename TD, typename TO>
+__global__ void __launch_bounds__(256) stale_delta_kernel(const TD* __restrict__ dO,
+                                                          const uint8_t* __restrict__ do_codes,
+                                                          const float* __restrict__ do_scales,
+                                                          const TO* __restrict__ O, long long rows, int N,
+                                                          int T_tiles, float* __restrict__ delta) {
+  constexpr int PER = D / 32;
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const size_t off = (size_t)row * D;
+  float o[PER], g[PER];
+  load_row(O + off, lane * PER, PER, o);
+  float sc = 1.0f;
+  if (MODE == 1) {
+    load_row(dO + off, lane * PER, PER, g);
+  } else {
+    const long long bh = row / N;
+    const int n = (int)(row % N);
+    sc = do_scales[bh * T_tiles + n / kTile];
+#pragma unroll
+    for (int k = 0; k < PER; k += 2) {
+      const float2 f = unpack2<1>(*reinterpret_cast<const uint16_t*>(do_codes + off + lane * PER + k));
+      g[k] = f.x, g[k + 1] = f.y;
+    }
+  }
+  float acc = 0.0f;
+#pragma unroll
+  for (int k = 0; k < PER; ++k) acc = fmaf(g[k], o[k], acc);
+  acc = warp_sum(acc);
+  if (lane == 0) delta[row] = acc * sc;
+}
+
+template <int MODE, int D, typename TD>
+cudaError_t stale_o(const TD* dO, const uint8_t* codes, const float* scales, const void* O, dm_dtype o_t,
+                    long long rows, int N, int T, float* delta, cudaStream_t st) {
+  const unsigned grid = (unsigned)((rows + 7) / 8);
+  if (o_t == DM_BF16)
+    stale_delta_kernel<MODE, D, TD, __nv_bfloat16><<<grid, 256, 0, st>>>(
+        dO, codes, scales, reinterpret_cast<const __nv_bfloat16*>(O), rows, N, T, delta);
+  else
+    stale_delta_kernel<MODE, D, TD, float><<<grid, 256, 0, st>>>(dO, codes, scales,
+                                                                 reinterpret_cast<const float*>(O), rows, N, T,
+                                                                 delta);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t stale_d(const AttnArgs& a, dm_delta_mode mode, const void* dO, dm_dtype do_t, const uint8_t* codes,
+                    const void* O, dm_dtype o_t, float* delta, cudaStream_t st) {
+  const long long rows = (long long)a.B * a.Hq * a.N;
+  if (mode == DM_DELTA_STALE_DOHAT)
+    return stale_o<2, D, float>(nullptr, codes, a.do_scales, O, o_t, rows, a.N, a.T, delta, st);
+  if (do_t == DM_BF16)
+    return stale_o<1, D, __nv_bfloat16>(reinterpret_cast<const __nv_bfloat16*>(dO), nullptr, nullptr, O, o_t,
+                                        rows, a.N, a.T, delta, st);
+  return stale_o<1, D, float>(reinterpret_cast<const float*>(dO), nullptr, nullptr, O, o_t, rows, a.N, a.T,
+                              delta, st);
+}
+
+__global__ void zero_kernel(float* __restrict__ p, size_t n) {
+  const size_t n4 = n / 4;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  const size_t i0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  float4* p4 = reinterpret_cast<float4*>(p);
+  for (size_t i = i0; i < n4; i += stride) p4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (size_t i = 4 * n4 + i0; i < n; i += stride) p[i] = 0.0f;
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const void* x, dm_dtype xt, int B, int H, int N, int d, dm_fp8 fmt, uint8_t* codes,
+                            float* scales, uint8_t* codes_t, cudaStream_t st) {
+  const int BH = B * H;
+  if (xt == DM_BF16) {
+    auto p = reinterpret_cast<const __nv_bfloat16*>(x);
+    return fmt == DM_E4M3 ? quantize_t<__nv_bfloat16, 0>(p, BH, N, d, codes, scales, codes_t, st)
+                          : quantize_t<__nv_bfloat16, 1>(p, BH, N, d, codes, scales, codes_t, st);
+  }
+  auto p = reinterpret_cast<const float*>(x);
+  return fmt == DM_E4M3 ? quantize_t<float, 0>(p, BH, N, d, codes, scales, codes_t, st)
+                        : quantize_t<float, 1>(p, BH, N, d, codes, scales, codes_t, st);
+}
+
+cudaError_t launch_delta_stale(const AttnArgs& a, int d, dm_delta_mode mode, const void* dO, dm_dtype do_t,
+                               const uint8_t* do_codes, const void* O, dm_dtype o_t, float* delta,
+                               cudaStream_t st) {
+  return d == 128 ? stale_d<128>(a, mode, dO, do_t, do_codes, O, o_t, delta, st)
+                  : stale_d<64>(a, mode, dO, do_t, do_codes, O, o_t, delta, st);
+}
+
+// p must be 16-byte aligned.
+cudaError_t launch_zero(float* p, size_t n, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  size_t blocks = (n / 4 + 255) / 256 + 1;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  zero_kernel<<<(unsigned)blocks, 256, 0, st>>>(p, n);
+  return cudaGetLastError();
+}
+
+}  // namespace dm

@@ -1,0 +1,45 @@
+// Host-side launch interfaces between the API layer (dm_api.cu) and the
+// kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "dm_common.h"
+
+namespace dm {
+
+struct FwdLaunch {
+  CUtensorMap tmQ, tmK, tmV;  // [B*H][N][d] FP8 codes, box 128 x d, hardware swizzle of width d
+  AttnArgs args;
+  void* O;
+  float* lse;
+};
+
+struct DeltaLaunch {
+  CUtensorMap tmQ, tmK, tmV, tmDO;
+  AttnArgs args;
+  const float* lse;
+  float* delta;
+};
+
+struct BwdLaunch {
+  CUtensorMap tmQ, tmK, tmV, tmDO;
+  AttnArgs args;
+  const float* lse;
+  const float* delta;
+  float *dQ, *dK, *dV;
+  dm_diag diag;
+};
+
+cudaError_t launch_quantize(const void* x, dm_dtype xt, int B, int H, int N, int d, dm_fp8 fmt, uint8_t* codes,
+                            float* scales, uint8_t* codes_t, cudaStream_t st);
+cudaError_t launch_attn_fwd(const FwdLaunch& f, int d, bool o_bf16, cudaStream_t st);
+cudaError_t launch_delta_matched(const DeltaLaunch& f, int d, cudaStream_t st);
+cudaError_t launch_delta_stale(const AttnArgs& a, int d, dm_delta_mode mode, const void* dO, dm_dtype do_t,
+                               const uint8_t* do_codes, const void* O, dm_dtype o_t, float* delta,
+                               cudaStream_t st);
+cudaError_t launch_zero(float* p, size_t n, cudaStream_t st);
+cudaError_t launch_attn_bwd(const BwdLaunch& f, int d, cudaStream_t st);
+
+}  // namespace dm

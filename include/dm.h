@@ -1,0 +1,173 @@
+/*
+ * dm.h -- C ABI of libdm: FP8 flash attention with the Delta-Matching
+ * softmax correction, for one NVIDIA GB300 (sm_103a).
+ *
+ * Method: "Delta-Matching for reliable FP8 attention training" (project
+ * page).  Section 01 ("Write down softmax backward") defines the attention
+ * forward S = sigma*Q*K^T, P = softmax_row(S), O = P*V and its backward
+ * dV = P^T dO, dP = dO V^T, dS = P o (dP - delta), dQ = sigma*dS*K,
+ * dK = sigma*dS^T*Q with the row correction delta_i.  Section 01 ("What
+ * changes in FP8?") puts every matmul on decoded block-scaled FP8 operands
+ * with FP32 accumulation; section 03 defines the matched correction
+ * delta_i = sum_j P_ij * dP^_ij, with P the FP32 softmax before it is
+ * quantised and dP^ the FP32 result of the FP8 product dO^ V^T.  The two
+ * stale corrections, <dO_i, O_i> (section 01) and <dO^_i, O_i> (section 03,
+ * last paragraph), are kept as diagnostic modes.
+ *
+ * Conventions shared by every call
+ *  - Tensors are contiguous row-major [B][H][N][d] (d fastest).  Query heads
+ *    are Hq, key/value heads Hkv; query head h reads kv head h / (Hq/Hkv).
+ *  - Every pointer is DEVICE memory owned by the caller, except `p`/`diag`
+ *    struct pointers, which are host memory read during the call.  The library
+ *    allocates no memory and keeps no state between calls other than the TMA
+ *    entry point it looks up once and a device status word.
+ *  - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and is asynchronous; the call returns after the launches.
+ *  - Arguments are validated before any launch.  On an error nothing is
+ *    launched and no output is touched.
+ *  - FP8 tensors (dm_fp8_tensor) hold codes uint8 [B][H][N][d] and one FP32
+ *    scale per 128-row x d tile, scales float [B][H][ceil(N/128)]; the decoded
+ *    value of a code is scale * value(code).
+ *  - Supported shapes: d in {64, 128}; any N >= 0 (ragged tails are masked);
+ *    Hq % Hkv == 0; B*Hq*N*d < 2^31.  B == 0 or N == 0 is a valid no-op.
+ *  - Device pointers must be 16-byte aligned.
+ *  - The device must be compute capability 10.3 (sm_103a build).
+ *
+ * Precision contract (the pages leave these steps open; this is the reading
+ * implemented and checked against the CPU oracle):
+ *  - tile quantiser: amax = max|x| over the tile; if amax < 2^-96 the tile
+ *    gets scale 0 and all-zero codes; else s = amax/FMAX, r = FMAX/amax (IEEE
+ *    fp32 divisions), code = RNE_satfinite(fp32(x*r)); FMAX = 448 (E4M3) or
+ *    57344 (E5M2);
+ *  - forward P is quantised in one pass: key tiles in ascending order,
+ *    P~ = exp(S - running row max) in FP32, one E4M3 scale per 128x128 tile
+ *    of P~, the row sum l taken from the unquantised P~;
+ *  - backward P = exp(S - LSE) in FP32, quantised E4M3 per 128x128 tile;
+ *    dS = P*(dP^ - delta) in FP32, quantised E5M2 per 128x128 tile.
+ */
+#ifndef DM_H_
+#define DM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DM_OK = 0,
+  DM_ERR_INVALID_ARG = 1, /* null pointer, bad enum value, bad flag */
+  DM_ERR_SHAPE = 2,       /* unsupported or inconsistent B/H/N/d */
+  DM_ERR_DTYPE = 3,       /* dtype not accepted for that argument */
+  DM_ERR_ALIGNMENT = 4,   /* a device pointer is not 16-byte aligned */
+  DM_ERR_UNSUPPORTED = 5, /* device is not sm_103, or feature not built */
+  DM_ERR_CUDA = 6,        /* a CUDA runtime/driver call or launch failed */
+  DM_ERR_TIMEOUT = 7      /* a kernel's bounded wait expired (see dm_get_status) */
+} dm_status;
+
+typedef enum { DM_F32 = 0, DM_BF16 = 1 } dm_dtype;
+typedef enum { DM_E4M3 = 0, DM_E5M2 = 1 } dm_fp8;
+typedef enum {
+  DM_DELTA_MATCHED = 0,    /* delta_i = sum_j P_ij dP^_ij (section 03)          */
+  DM_DELTA_STALE_DO = 1,   /* delta_i = <dO_i, O_i>, dO before its FP8 cast      */
+  DM_DELTA_STALE_DOHAT = 2 /* delta_i = <dO^_i, O_i>, "match dO only" (sec. 03)  */
+} dm_delta_mode;
+
+/* Problem description.  causal: key j visible to query i iff j <= i.
+ * softmax_scale: sigma in S = sigma*Q*K^T; <= 0 selects 1/sqrt(d). */
+typedef struct {
+  int B, Hq, Hkv, N, d;
+  int causal;
+  float softmax_scale;
+} dm_attn_params;
+
+/* A block-scaled FP8 tensor: codes [B][H][N][d], scales [B][H][ceil(N/128)]. */
+typedef struct {
+  const uint8_t* codes;
+  const float* scales;
+} dm_fp8_tensor;
+
+/* Optional per-query-row dS diagnostics, each float [B][Hq][N] (any may be
+ * NULL): sum_j dS_ij and sum_j |dS_ij| before the E5M2 cast, and the same two
+ * sums of the decoded dS^ after it (project page section 03: the post-cast
+ * row-sum residual). */
+typedef struct {
+  float* rowsum_pre;
+  float* abssum_pre;
+  float* rowsum_post;
+  float* abssum_post;
+} dm_diag;
+
+/* dm_quantize -- per-tile FP8 quantisation (block scales of section 01,
+ * "What changes in FP8?").  x: [B][H][N][d] of x_dtype (DM_F32 or DM_BF16).
+ * fmt: DM_E4M3 (Q, K, V) or DM_E5M2 (dO).  Writes codes [B][H][N][d], scales
+ * [B][H][ceil(N/128)], and, if codes_t != NULL, the codes transposed per
+ * (b, h) as [B][H][d][N].  Bit-exact with the tile quantiser rule above. */
+dm_status dm_quantize(const void* x, dm_dtype x_dtype, int B, int H, int N, int d, dm_fp8 fmt,
+                      uint8_t* codes, float* scales, uint8_t* codes_t, void* stream);
+
+/* dm_attn_fwd -- O = P^ V^ and LSE (section 01).  q, k, v: E4M3 tensors of
+ * shapes [B][Hq][N][d], [B][Hkv][N][d], [B][Hkv][N][d].  O: [B][Hq][N][d] of
+ * o_dtype (DM_F32 or DM_BF16).  lse: float [B][Hq][N], natural log of the
+ * softmax denominator including the scale sigma, i.e. LSE_i = ln sum_j
+ * exp(S_ij).  O and LSE are the only saved forward outputs. */
+dm_status dm_attn_fwd(const dm_attn_params* p, dm_fp8_tensor q, dm_fp8_tensor k, dm_fp8_tensor v,
+                      void* O, dm_dtype o_dtype, float* lse, void* stream);
+
+/* dm_attn_delta -- the softmax row correction, float delta [B][Hq][N].
+ *  DM_DELTA_MATCHED:     needs q, k, v, do_hat (E5M2), lse; recomputes S and
+ *                        dP^ = dO^ V^T tile by tile in FP32 (the separate
+ *                        correction pass).  dO and O may be NULL.
+ *  DM_DELTA_STALE_DO:    needs dO (do_dtype) and O (o_dtype).
+ *  DM_DELTA_STALE_DOHAT: needs do_hat and O (o_dtype).  */
+dm_status dm_attn_delta(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor q, dm_fp8_tensor k,
+                        dm_fp8_tensor v, dm_fp8_tensor do_hat, const float* lse, const void* dO,
+                        dm_dtype do_dtype, const void* O, dm_dtype o_dtype, float* delta,
+                        void* stream);
+
+/* dm_attn_bwd -- dQ, dK, dV (section 01) with the five backward matmuls in
+ * FP8.  delta: float [B][Hq][N] from dm_attn_delta, or NULL, in which case it
+ * is computed first for `mode` into `workspace` (which then needs
+ * dm_attn_bwd_workspace_size(p) bytes, 16-byte aligned).  dQ float
+ * [B][Hq][N][d] (overwritten, not accumulated), dK and dV float
+ * [B][Hkv][N][d] (summed over each kv head's query heads).  diag: optional
+ * row-sum diagnostics (NULL = off).  dO/O are needed only when delta is NULL
+ * and the mode is stale.  */
+dm_status dm_attn_bwd(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor q, dm_fp8_tensor k,
+                      dm_fp8_tensor v, dm_fp8_tensor do_hat, const float* lse, const float* delta,
+                      const void* dO, dm_dtype do_dtype, const void* O, dm_dtype o_dtype, float* dQ,
+                      float* dK, float* dV, const dm_diag* diag, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace dm_attn_bwd needs when delta == NULL (0 on bad params). */
+size_t dm_attn_bwd_workspace_size(const dm_attn_params* p);
+
+/* Synchronises `stream`, then returns and clears the device status word of
+ * the current device: DM_ERR_TIMEOUT if a kernel's bounded wait expired since
+ * the last call (its outputs are then undefined), DM_ERR_CUDA if the stream
+ * reports an error, else DM_OK. */
+dm_status dm_get_status(void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* dm_status_string(dm_status s);
+
+/* Library version, 100*major + minor. */
+int dm_version(void);
+
+/* Test and debug knobs (process-wide, default 0):
+ *  DM_KNOB_WAIT_LIMIT_NS: limit of every bounded wait inside the kernels in
+ *                         nanoseconds (0 = built-in default of 2 s);
+ *  DM_KNOB_STALL_TEST:    1 makes the next dm_attn_fwd launch wait on a barrier
+ *                         that nothing signals, so that its bounded wait
+ *                         expires and the kernel returns DM_ERR_TIMEOUT
+ *                         through dm_get_status (used to test the watchdog;
+ *                         the knob resets itself after that launch). */
+typedef enum { DM_KNOB_WAIT_LIMIT_NS = 0, DM_KNOB_STALL_TEST = 1 } dm_knob;
+dm_status dm_set_knob(dm_knob knob, long long value);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DM_H_ */
