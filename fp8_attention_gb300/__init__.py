@@ -1,0 +1,254 @@
+"""Python binding of libdm: FP8 flash attention with the Delta-Matching correction on GB300.
+
+Thin ctypes marshalling over the C ABI in ``include/dm.h`` (same function
+names).  PyTorch only provides device memory and streams; every step of the
+computation runs in the library's sm_103a kernels.  Importing works without
+a GPU, but the first call raises if ``libdm.so`` has not been built
+(``python -c "import __graft_entry__ as g; g.build()"``) -- there is no CPU
+fallback.
+
+FP8 tensors are passed as ``Fp8(codes, scales)``: codes uint8 [B][H][N][d] and
+scales float32 [B][H][ceil(N/128)], both contiguous CUDA tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+from typing import NamedTuple, Optional
+
+import torch
+
+__all__ = [
+    "AttnParams", "Fp8", "DMError", "lib", "dm_version", "dm_status_string", "dm_set_knob",
+    "dm_get_status", "dm_quantize", "dm_attn_fwd", "dm_attn_delta", "dm_attn_bwd",
+    "dm_attn_bwd_workspace_size",
+    "DM_F32", "DM_BF16", "DM_E4M3", "DM_E5M2", "DM_DELTA_MATCHED", "DM_DELTA_STALE_DO",
+    "DM_DELTA_STALE_DOHAT", "DM_KNOB_WAIT_LIMIT_NS", "DM_KNOB_STALL_TEST",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdm.so")
+
+DM_OK, DM_ERR_INVALID_ARG, DM_ERR_SHAPE, DM_ERR_DTYPE, DM_ERR_ALIGNMENT = 0, 1, 2, 3, 4
+DM_ERR_UNSUPPORTED, DM_ERR_CUDA, DM_ERR_TIMEOUT = 5, 6, 7
+DM_F32, DM_BF16 = 0, 1
+DM_E4M3, DM_E5M2 = 0, 1
+DM_DELTA_MATCHED, DM_DELTA_STALE_DO, DM_DELTA_STALE_DOHAT = 0, 1, 2
+DM_KNOB_WAIT_LIMIT_NS, DM_KNOB_STALL_TEST = 0, 1
+TILE = 128
+
+
+class DMError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        super().__init__(f"{where}: {dm_status_string(code)}")
+
+
+class _Params(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("N", ctypes.c_int),
+                ("d", ctypes.c_int), ("causal", ctypes.c_int), ("softmax_scale", ctypes.c_float)]
+
+
+class _Fp8(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
+
+
+class _Diag(ctypes.Structure):
+    _fields_ = [("rowsum_pre", ctypes.c_void_p), ("abssum_pre", ctypes.c_void_p),
+                ("rowsum_post", ctypes.c_void_p), ("abssum_post", ctypes.c_void_p)]
+
+
+@dataclass(frozen=True)
+class AttnParams:
+    B: int
+    Hq: int
+    Hkv: int
+    N: int
+    d: int
+    causal: bool = True
+    softmax_scale: float = 0.0   # <= 0 selects 1/sqrt(d)
+
+    def c(self) -> _Params:
+        return _Params(self.B, self.Hq, self.Hkv, self.N, self.d, int(bool(self.causal)),
+                       float(self.softmax_scale))
+
+    @property
+    def T(self) -> int:
+        return (self.N + TILE - 1) // TILE
+
+
+class Fp8(NamedTuple):
+    codes: torch.Tensor
+    scales: torch.Tensor
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib():
+    """The loaded libdm.so; raises if it has not been built (no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "`python -c \"import __graft_entry__ as g; g.build()\"`")
+            L = ctypes.CDLL(LIB_PATH)
+            P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            PP = ctypes.POINTER(_Params)
+            L.dm_version.restype = I
+            L.dm_status_string.restype = ctypes.c_char_p
+            L.dm_status_string.argtypes = [I]
+            L.dm_set_knob.restype = I
+            L.dm_set_knob.argtypes = [I, ctypes.c_longlong]
+            L.dm_get_status.restype = I
+            L.dm_get_status.argtypes = [P]
+            L.dm_quantize.restype = I
+            L.dm_quantize.argtypes = [P, I, I, I, I, I, I, P, P, P, P]
+            L.dm_attn_fwd.restype = I
+            L.dm_attn_fwd.argtypes = [PP, _Fp8, _Fp8, _Fp8, P, I, P, P]
+            L.dm_attn_delta.restype = I
+            L.dm_attn_delta.argtypes = [PP, I, _Fp8, _Fp8, _Fp8, _Fp8, P, P, I, P, I, P, P]
+            L.dm_attn_bwd.restype = I
+            L.dm_attn_bwd.argtypes = [PP, I, _Fp8, _Fp8, _Fp8, _Fp8, P, P, P, I, P, I, P, P, P,
+                                      ctypes.POINTER(_Diag), P, S, P]
+            L.dm_attn_bwd_workspace_size.restype = S
+            L.dm_attn_bwd_workspace_size.argtypes = [PP]
+            _lib = L
+    return _lib
+
+
+# ---------------------------------------------------------------- marshalling
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libdm must be contiguous")
+    return t.data_ptr() or None
+
+
+def _dtype(t: Optional[torch.Tensor]) -> int:
+    if t is None:
+        return DM_F32
+    return {torch.float32: DM_F32, torch.bfloat16: DM_BF16}.get(t.dtype, -1)
+
+
+def _fp8(x: Optional[Fp8]) -> _Fp8:
+    if x is None:
+        return _Fp8(None, None)
+    return _Fp8(_ptr(x.codes), _ptr(x.scales))
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(rc: int, where: str):
+    if rc != DM_OK:
+        raise DMError(rc, where)
+
+
+def dm_version() -> int:
+    return lib().dm_version()
+
+
+def dm_status_string(code: int) -> str:
+    return lib().dm_status_string(int(code)).decode()
+
+
+def dm_set_knob(knob: int, value: int) -> None:
+    _check(lib().dm_set_knob(int(knob), int(value)), "dm_set_knob")
+
+
+def dm_get_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status code."""
+    return lib().dm_get_status(_stream(stream))
+
+
+def dm_quantize(x: torch.Tensor, fmt: int, codes=None, scales=None, codes_t=None, want_transposed=False,
+                stream=None):
+    """Per 128-row x d tile FP8 quantisation of x [B][H][N][d] (fp32 or bf16) -> Fp8 (+ codes^T)."""
+    B, H, N, d = x.shape
+    T = (N + TILE - 1) // TILE
+    if codes is None:
+        codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((B, H, T), dtype=torch.float32, device=x.device)
+    if want_transposed and codes_t is None:
+        codes_t = torch.empty((B, H, d, N), dtype=torch.uint8, device=x.device)
+    rc = lib().dm_quantize(_ptr(x), _dtype(x), B, H, N, d, int(fmt), _ptr(codes), _ptr(scales), _ptr(codes_t),
+                           _stream(stream))
+    _check(rc, "dm_quantize")
+    out = Fp8(codes, scales)
+    return (out, codes_t) if codes_t is not None else out
+
+
+def dm_attn_fwd(p: AttnParams, q: Fp8, k: Fp8, v: Fp8, O=None, o_dtype=torch.float32, lse=None, stream=None):
+    """Forward: returns (O [B][Hq][N][d], LSE [B][Hq][N])."""
+    dev = q.codes.device
+    if O is None:
+        O = torch.empty((p.B, p.Hq, p.N, p.d), dtype=o_dtype, device=dev)
+    if lse is None:
+        lse = torch.empty((p.B, p.Hq, p.N), dtype=torch.float32, device=dev)
+    cp = p.c()
+    rc = lib().dm_attn_fwd(ctypes.byref(cp), _fp8(q), _fp8(k), _fp8(v), _ptr(O), _dtype(O), _ptr(lse),
+                           _stream(stream))
+    _check(rc, "dm_attn_fwd")
+    return O, lse
+
+
+def dm_attn_delta(p: AttnParams, mode: int, q: Fp8, k: Fp8, v: Fp8, do_hat: Fp8, lse, dO=None, O=None,
+                  delta=None, stream=None):
+    """Softmax row correction delta [B][Hq][N] for the given mode."""
+    ref = lse if lse is not None else O
+    if delta is None:
+        delta = torch.empty((p.B, p.Hq, p.N), dtype=torch.float32, device=ref.device)
+    cp = p.c()
+    rc = lib().dm_attn_delta(ctypes.byref(cp), int(mode), _fp8(q), _fp8(k), _fp8(v), _fp8(do_hat), _ptr(lse),
+                             _ptr(dO), _dtype(dO), _ptr(O), _dtype(O), _ptr(delta), _stream(stream))
+    _check(rc, "dm_attn_delta")
+    return delta
+
+
+def dm_attn_bwd_workspace_size(p: AttnParams) -> int:
+    cp = p.c()
+    return int(lib().dm_attn_bwd_workspace_size(ctypes.byref(cp)))
+
+
+def dm_attn_bwd(p: AttnParams, mode: int, q: Fp8, k: Fp8, v: Fp8, do_hat: Fp8, lse, delta=None, dO=None,
+                O=None, dQ=None, dK=None, dV=None, diag=False, workspace=None, stream=None):
+    """Backward: returns dict with dQ, dK, dV (and the four diagnostic row sums if diag)."""
+    dev = lse.device
+    if dQ is None:
+        dQ = torch.empty((p.B, p.Hq, p.N, p.d), dtype=torch.float32, device=dev)
+    if dK is None:
+        dK = torch.empty((p.B, p.Hkv, p.N, p.d), dtype=torch.float32, device=dev)
+    if dV is None:
+        dV = torch.empty((p.B, p.Hkv, p.N, p.d), dtype=torch.float32, device=dev)
+    out = {"dQ": dQ, "dK": dK, "dV": dV}
+    cdiag = None
+    if diag:
+        names = ("rowsum_pre", "abssum_pre", "rowsum_post", "abssum_post")
+        if isinstance(diag, dict):
+            bufs = {n: diag.get(n) for n in names}
+        else:
+            bufs = {n: torch.empty((p.B, p.Hq, p.N), dtype=torch.float32, device=dev) for n in names}
+        cdiag = _Diag(*[_ptr(bufs[n]) for n in names])
+        out.update({n: t for n, t in bufs.items() if t is not None})
+    ws_bytes = 0
+    if delta is None:
+        ws_bytes = dm_attn_bwd_workspace_size(p)
+        if workspace is None:
+            workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    cp = p.c()
+    rc = lib().dm_attn_bwd(ctypes.byref(cp), int(mode), _fp8(q), _fp8(k), _fp8(v), _fp8(do_hat), _ptr(lse),
+                           _ptr(delta), _ptr(dO), _dtype(dO), _ptr(O), _dtype(O), _ptr(dQ), _ptr(dK), _ptr(dV),
+                           ctypes.byref(cdiag) if cdiag is not None else None, _ptr(workspace), ws_bytes,
+                           _stream(stream))
+    _check(rc, "dm_attn_bwd")
+    return out

@@ -1,0 +1,91 @@
+"""The C-ABI library loads without a GPU and exports every function include/dm.h
+declares; host-side argument validation answers before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp8_attention_gb300 as dm
+from fp8_attention_gb300 import build as dm_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dm_build.build()
+    return dm.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(dm_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("dm_quantize", "dm_attn_fwd", "dm_attn_delta", "dm_attn_bwd", "dm_attn_bwd_workspace_size",
+              "dm_get_status", "dm_status_string"):
+        assert n in names
+
+
+def test_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_version(lib):
+    assert dm.dm_version() == 100
+    for code, name in ((0, "DM_OK"), (2, "DM_ERR_SHAPE"), (7, "DM_ERR_TIMEOUT")):
+        assert dm.dm_status_string(code) == name
+    assert dm.dm_status_string(99) == "DM_ERR_UNKNOWN"
+
+
+def test_knobs(lib):
+    assert lib.dm_set_knob(0, -1) == dm.DM_ERR_INVALID_ARG
+    assert lib.dm_set_knob(7, 1) == dm.DM_ERR_INVALID_ARG
+    assert lib.dm_set_knob(dm.DM_KNOB_WAIT_LIMIT_NS, 0) == 0
+
+
+def _p(B=1, Hq=2, Hkv=1, N=256, d=64, causal=1, scale=0.0):
+    return dm._Params(B, Hq, Hkv, N, d, causal, scale)
+
+
+def test_validation_without_gpu(lib):
+    """Every check below fails before the library touches the CUDA runtime."""
+    A = 0x10000  # aligned fake device addresses: never dereferenced by these calls
+    f = dm._Fp8(A, A)
+    fwd = lib.dm_attn_fwd
+    assert fwd(None, f, f, f, A, 0, A, None) == dm.DM_ERR_INVALID_ARG
+    assert fwd(ctypes.byref(_p(d=96)), f, f, f, A, 0, A, None) == dm.DM_ERR_SHAPE
+    assert fwd(ctypes.byref(_p(Hq=3, Hkv=2)), f, f, f, A, 0, A, None) == dm.DM_ERR_SHAPE
+    assert fwd(ctypes.byref(_p(N=-1)), f, f, f, A, 0, A, None) == dm.DM_ERR_SHAPE
+    assert fwd(ctypes.byref(_p(B=1 << 20, Hq=64, Hkv=1, N=1 << 10, d=128)), f, f, f, A, 0, A, None) \
+        == dm.DM_ERR_SHAPE
+    assert fwd(ctypes.byref(_p()), f, f, f, A, 5, A, None) == dm.DM_ERR_DTYPE
+    assert fwd(ctypes.byref(_p()), dm._Fp8(A + 1, A), f, f, A, 0, A, None) == dm.DM_ERR_ALIGNMENT
+    assert fwd(ctypes.byref(_p()), dm._Fp8(None, A), f, f, A, 0, A, None) == dm.DM_ERR_INVALID_ARG
+    assert fwd(ctypes.byref(_p(scale=float("nan"))), f, f, f, A, 0, A, None) == dm.DM_ERR_INVALID_ARG
+    # empty problems are valid no-ops, even with NULL pointers
+    z = dm._Fp8(None, None)
+    assert fwd(ctypes.byref(_p(B=0)), z, z, z, None, 0, None, None) == 0
+    assert fwd(ctypes.byref(_p(N=0)), z, z, z, None, 0, None, None) == 0
+    assert lib.dm_quantize(None, 0, 0, 2, 128, 64, 0, None, None, None, None) == 0
+    assert lib.dm_quantize(A, 2, 1, 2, 128, 64, 0, A, A, None, None) == dm.DM_ERR_DTYPE
+    assert lib.dm_quantize(A, 0, 1, 2, 128, 64, 2, A, A, None, None) == dm.DM_ERR_INVALID_ARG
+    assert lib.dm_quantize(A, 0, 1, 2, 128, 32, 0, A, A, None, None) == dm.DM_ERR_SHAPE
+    assert lib.dm_attn_delta(ctypes.byref(_p()), 3, f, f, f, f, A, A, 0, A, 0, A, None) == dm.DM_ERR_INVALID_ARG
+    assert lib.dm_attn_delta(ctypes.byref(_p()), 1, f, f, f, f, A, None, 0, A, 0, A, None) \
+        == dm.DM_ERR_INVALID_ARG
+    bwd = lib.dm_attn_bwd
+    assert bwd(ctypes.byref(_p()), 0, f, f, f, f, A, None, None, 0, None, 0, A, A, A, None, A, 16, None) \
+        == dm.DM_ERR_INVALID_ARG  # workspace too small for the internally computed delta
+
+
+def test_workspace_size(lib):
+    assert dm.dm_attn_bwd_workspace_size(dm.AttnParams(2, 4, 2, 1000, 64)) == ((2 * 4 * 1000 * 4 + 255) // 256) * 256
+    assert dm.dm_attn_bwd_workspace_size(dm.AttnParams(2, 4, 3, 1000, 64)) == 0
