@@ -1,0 +1,366 @@
+"""Benchmark: one training step of FP8 attention with the Delta-Matching correction.
+
+A step is the whole hot path on one batch of synthetic inputs resident in HBM:
+quantise Q, K, V (E4M3) and dO (E5M2), forward (O, LSE), matched delta pass,
+backward (dQ, dK, dV).  Default workload: causal GQA at 8K context, B=1, Hq=16,
+Hkv=4, N=8192, d=128, bf16 storage (the configuration the throughput target is
+quoted on).  FLOPs are issued and causal-halved: with U = B*Hq*N^2*d, forward
+2U, delta pass 2U, backward 5U, 9U per step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line.  Under torchrun (N > 1) every rank runs the same-sized
+independent problem on its own GPU (the path shards over independent
+attention problems with no data-path collective: weak scaling); the timed
+region is bracketed by barriers and the max over ranks is reported.
+`--impl reference` times the CPU oracle (a deliberately slow FP64 program) on
+a bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FP8 attn fwd+bwd TFLOP/s (matched delta), % of GB300 dense FP8 peak"
+DEFAULT_WORKLOAD = "gqa_b1_n8192_d128"
+L2_BYTES = 129 * 1024 * 1024
+
+# Dense FP8 peak: the measured bf16 cuBLAS peak times the nominal fp8/bf16 ratio (4.5/2.25).
+FP8_PER_BF16 = 2.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+# DRAM traffic of one backward launch on the default workload, from the ncu
+# capture summarised in profiles/ (valid only for the kernel source it was
+# taken on; reported as null once dm_bwd.cu changes).
+BWD_TRAFFIC = {"sha1": None, "bytes": None}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            mp = json.load(f)
+        return mp, "measured"
+    except (OSError, ValueError):
+        return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "hbm_gbs": 6800.0}, "fallback"
+
+
+def flops_of(w):
+    return w.flops()
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ native
+def run_native(args, rank, world, local_rank):
+    import torch
+
+    import fp8_attention_gb300 as dm
+    from fp8_attention_gb300.inputs import WORKLOADS, make_inputs
+
+    w = WORKLOADS[args.workload]
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    q, k, v, do = make_inputs(w)
+    p = dm.AttnParams(w.B, w.Hq, w.Hkv, w.N, w.d, causal=w.causal)
+    st = torch.cuda.Stream(dev)
+    # inputs resident in HBM
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    # pinned host copies for the end-to-end measurement
+    qh, kh, vh, doh = (t.pin_memory() for t in (q, k, v, do))
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def step(inputs, stream, times=None):
+        qx, kx, vx, dox = inputs
+        marks = [ev() for _ in range(5)]
+        marks[0].record(stream)
+        qq = dm.dm_quantize(qx, dm.DM_E4M3, stream=stream)
+        kk = dm.dm_quantize(kx, dm.DM_E4M3, stream=stream)
+        vv = dm.dm_quantize(vx, dm.DM_E4M3, stream=stream)
+        dd = dm.dm_quantize(dox, dm.DM_E5M2, stream=stream)
+        marks[1].record(stream)
+        O, lse = dm.dm_attn_fwd(p, qq, kk, vv, stream=stream)
+        marks[2].record(stream)
+        delta = dm.dm_attn_delta(p, dm.DM_DELTA_MATCHED, qq, kk, vv, dd, lse, stream=stream)
+        marks[3].record(stream)
+        g = dm.dm_attn_bwd(p, dm.DM_DELTA_MATCHED, qq, kk, vv, dd, lse, delta, stream=stream)
+        marks[4].record(stream)
+        if times is not None:
+            times.append(marks)
+        return g
+
+    launches_per_step = 4 + 1 + 1 + 2  # quantise x4, forward, delta, dQ zero fill + backward
+    inputs = (qd, kd, vd, dod)
+    with torch.cuda.stream(st):
+        for _ in range(args.warmup):
+            flush.zero_()
+            step(inputs, st)
+    torch.cuda.synchronize(dev)
+    if dm.dm_get_status(st) != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    # ---- device-resident timed region
+    marks = []
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        wall0 = time.perf_counter()
+        with torch.cuda.stream(st):
+            for _ in range(args.steps):
+                flush.zero_()          # L2 flush between timed steps (outside the events)
+                step(inputs, st, marks)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - wall0
+    if dist:
+        dist.barrier()
+    status = dm.dm_get_status(st)
+    if status != 0:
+        raise RuntimeError(f"device status {dm.dm_status_string(status)}")
+    per = [[m[i].elapsed_time(m[i + 1]) for i in range(4)] for m in marks]
+    step_ms = [sum(x) for x in per]
+    total_ms = sum(step_ms)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # ---- end to end through the public API, host buffers, copies inside the timed region
+    e2e_marks = []
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh, doh))
+    outs = {"dQ": torch.empty((w.B, w.Hq, w.N, w.d), dtype=torch.float32).pin_memory(),
+            "dK": torch.empty((w.B, w.Hkv, w.N, w.d), dtype=torch.float32).pin_memory(),
+            "dV": torch.empty((w.B, w.Hkv, w.N, w.d), dtype=torch.float32).pin_memory()}
+    d2h = sum(t.numel() * t.element_size() for t in outs.values())
+    e2e_steps = max(3, min(args.steps, 10))
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(st):
+        for _ in range(e2e_steps):
+            flush.zero_()
+            a, b = ev(), ev()
+            a.record(st)
+            dev_in = tuple(h.to(dev, non_blocking=True) for h in (qh, kh, vh, doh))
+            g = step(dev_in, st)
+            for name, host in outs.items():
+                host.copy_(g[name], non_blocking=True)
+            b.record(st)
+            e2e_marks.append((a, b))
+    torch.cuda.synchronize(dev)
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_marks) / e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    fl = flops_of(w)
+    step_flops = fl["fwd"] + fl["delta"] + fl["bwd"]
+    ms_per_step = total_ms / args.steps
+    value = world * step_flops / (ms_per_step * 1e-3) / 1e12
+    mp, src = peaks()
+    fp8_peak = FP8_PER_BF16 * float(mp.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    kernel_ms = {name: statistics.mean(x[i] for x in per)
+                 for i, name in enumerate(("quantize", "fwd", "delta", "bwd"))}
+    bwd_tflops = fl["bwd"] / (kernel_ms["bwd"] * 1e-3) / 1e12
+    src_hash = hashlib.sha1(open(os.path.join(ROOT, "fp8_attention_gb300", "csrc", "dm_bwd.cu"), "rb").read()).hexdigest()
+    traffic = BWD_TRAFFIC["bytes"] if BWD_TRAFFIC["sha1"] == src_hash else None
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8 (e4m3/e5m2 operands, fp32 accumulate)",
+        "data": "synthetic (seeded randn, RMS-normalised Q/K, bf16 storage)",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d, "causal": w.causal,
+                   "delta_mode": "matched", "flop_accounting": "issued, causal-halved, 9U per step",
+                   "l2": "flushed between timed steps (256 MiB write)", "parallelism": f"independent x{world}"},
+        "pct_of_fp8_peak": round(100.0 * value / (world * fp8_peak), 2),
+        "per_kernel_ms": {k2: round(v2, 4) for k2, v2 in kernel_ms.items()},
+        "per_kernel_tflops": {
+            "fwd": round(fl["fwd"] / (kernel_ms["fwd"] * 1e-3) / 1e12, 1),
+            "delta": round(fl["delta"] / (kernel_ms["delta"] * 1e-3) / 1e12, 1),
+            "bwd": round(bwd_tflops, 1)},
+        "roofline": {"kernel": "attn_bwd_kernel<128>", "bound": "tensor", "achieved": round(bwd_tflops, 1),
+                     "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(bwd_tflops / fp8_peak, 4),
+                     "peak_source": f"{src} bf16 burst x {FP8_PER_BF16} (fp8/bf16 nominal ratio)",
+                     "traffic": traffic},
+        "e2e": {"value": round(world * step_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed": round(wall, 3),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if dist:
+        dist.destroy_process_group()
+    return line
+
+
+# ------------------------------------------------------------------ oracle
+def oracle_sample(w, rounds=1):
+    """Time the oracle on a bounded sample of the workload; returns (TFLOP/s, seconds, description)."""
+    import numpy as np
+
+    import oracle
+    from fp8_attention_gb300.inputs import make_inputs
+
+    q, k, v, do = (t.float().numpy() for t in make_inputs(w))
+    T = (w.N + 127) // 128
+    q_tiles = [T - 1 - i for i in range(min(T, 2))]
+    kv_tiles = [T - 1]
+    groups = [(0, g) for g in range(w.Hkv)]
+    G = w.Hq // w.Hkv
+    # issued FLOPs of the sample, counted like the GPU path: per visible
+    # 128x128 tile pair one matmul is 2*128*128*d FLOPs
+    mm = 2.0 * 128 * 128 * w.d
+    pairs_q = sum((t + 1) if w.causal else T for t in q_tiles)
+    per_head = pairs_q * (2 + 2 + 3) * mm + len(kv_tiles) * 4 * mm
+    sample_flops = per_head * G * len(groups) * rounds
+    t0 = time.perf_counter()
+    for _ in range(rounds):
+        oracle.pipeline(q, k, v, do, causal=w.causal, q_tiles=q_tiles, kv_tiles=kv_tiles, groups=groups)
+    secs = time.perf_counter() - t0
+    desc = (f"{len(groups) * G} query heads x query tiles {q_tiles} (fwd, matched delta, dQ) + key tile "
+            f"{kv_tiles} (dK, dV) of {w.name}, FP64 oracle, x{rounds}")
+    return sample_flops / secs / 1e12, secs, desc
+
+
+def cpu_baseline(w):
+    import oracle
+    val, secs, desc = oracle_sample(w)
+    return {"value": round(val, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": desc, "seconds": round(secs, 2)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    from fp8_attention_gb300.inputs import WORKLOADS
+    import oracle
+    w = WORKLOADS[args.workload]
+    oracle.build()
+    for _ in range(args.warmup):
+        oracle_sample(w)
+    vals, total = [], 0.0
+    desc = ""
+    for _ in range(args.steps):
+        val, secs, desc = oracle_sample(w)
+        vals.append(val)
+        total += secs
+    value = statistics.mean(vals)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000 * total / args.steps, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded randn, RMS-normalised Q/K, bf16 storage)",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
+                   "causal": w.causal, "delta_mode": "matched", "flop_accounting": "issued, causal-halved"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_native(args, rank, world, local_rank)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

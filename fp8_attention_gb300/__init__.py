@@ -22,7 +22,7 @@ import torch
 
 __all__ = [
     "AttnParams", "Fp8", "DMError", "lib", "dm_version", "dm_status_string", "dm_set_knob",
-    "dm_get_status", "dm_quantize", "dm_attn_fwd", "dm_attn_delta", "dm_attn_bwd",
+    "dm_get_status", "dm_last_timeout_site", "dm_quantize", "dm_attn_fwd", "dm_attn_delta", "dm_attn_bwd",
     "dm_attn_bwd_workspace_size",
     "DM_F32", "DM_BF16", "DM_E4M3", "DM_E5M2", "DM_DELTA_MATCHED", "DM_DELTA_STALE_DO",
     "DM_DELTA_STALE_DOHAT", "DM_KNOB_WAIT_LIMIT_NS", "DM_KNOB_STALL_TEST",
@@ -105,6 +105,7 @@ def lib():
             L.dm_set_knob.argtypes = [I, ctypes.c_longlong]
             L.dm_get_status.restype = I
             L.dm_get_status.argtypes = [P]
+            L.dm_last_timeout_site.restype = ctypes.c_uint
             L.dm_quantize.restype = I
             L.dm_quantize.argtypes = [P, I, I, I, I, I, I, P, P, P, P]
             L.dm_attn_fwd.restype = I
@@ -167,6 +168,11 @@ def dm_set_knob(knob: int, value: int) -> None:
 def dm_get_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status code."""
     return lib().dm_get_status(_stream(stream))
+
+
+def dm_last_timeout_site() -> int:
+    """kernel * 100 + wait number of the last expired wait reported by dm_get_status (0: none)."""
+    return int(lib().dm_last_timeout_site())
 
 
 def dm_quantize(x: torch.Tensor, fmt: int, codes=None, scales=None, codes_t=None, want_transposed=False,

@@ -16,13 +16,15 @@ using dm::kDefaultWaitLimitNs;
 constexpr int kMaxDevices = 64;
 constexpr int kTileRows = 128;
 
-__device__ unsigned int g_status_word;  // DM_OK or the first error a kernel recorded
+// [0]: DM_OK or the first error a kernel recorded; [1]: site of the first expired wait
+__device__ unsigned int g_status_word[2];
 
 std::mutex g_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 unsigned int* g_status_ptr[kMaxDevices] = {};
 int g_dev_ok[kMaxDevices] = {};  // 0 unknown, 1 sm_103, -1 other
 unsigned long long g_wait_limit_ns = 0;
+unsigned int g_last_site = 0;
 int g_stall_test = 0;
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
@@ -200,13 +202,20 @@ dm_status dm_get_status(void* stream) {
   unsigned int* status = nullptr;
   DM_TRY(device_state(&status));
   if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return DM_ERR_CUDA;
-  unsigned int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v)) != cudaSuccess) return DM_ERR_CUDA;
-  if (v != 0) {
-    const unsigned int zero = 0;
-    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return DM_ERR_CUDA;
+  unsigned int v[2] = {0, 0};
+  if (cudaMemcpyFromSymbol(v, g_status_word, sizeof(v)) != cudaSuccess) return DM_ERR_CUDA;
+  if (v[0] != 0 || v[1] != 0) {
+    const unsigned int zero[2] = {0, 0};
+    if (cudaMemcpyToSymbol(g_status_word, zero, sizeof(zero)) != cudaSuccess) return DM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_last_site = v[1];
   }
-  return v == 0 ? DM_OK : (dm_status)v;
+  return v[0] == 0 ? DM_OK : (dm_status)v[0];
+}
+
+unsigned int dm_last_timeout_site(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  return g_last_site;
 }
 
 dm_status dm_quantize(const void* x, dm_dtype x_dtype, int B, int H, int N, int d, dm_fp8 fmt, uint8_t* codes,

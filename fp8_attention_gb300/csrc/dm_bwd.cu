@@ -165,15 +165,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ph = (n >> 1) & 1;
         const int bh = b * a.Hq + g * G + n / nq;
         const int qt = qt0 + n % nq;
-        if (!wait(&bars.qempty[s], ph ^ 1, wd)) break;
+        if (!wait(&bars.qempty[s], ph ^ 1, wd, 301)) break;
         mbar_arrive_expect_tx(&bars.qfull[s], 2 * L::kTileBytes);
         tma_load_3d(sm + L::kQ + s * L::kTileBytes, &tmQ, &bars.qfull[s], 0, qt * kTile, bh);
         tma_load_3d(sm + L::kDO + s * L::kTileBytes, &tmDO, &bars.qfull[s], 0, qt * kTile, bh);
         issued = n + 1;
       }
-      wait_drain(&bars.kv, 0, a.wait_limit_ns);
+      wait_drain(&bars.kv, 0, wd, 309);
       for (int n = max(0, issued - 2); n < issued; ++n)
-        wait_drain(&bars.qfull[n & 1], (n >> 1) & 1, a.wait_limit_ns);
+        wait_drain(&bars.qfull[n & 1], (n >> 1) & 1, wd, 310);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer
@@ -185,25 +185,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdDQ = idesc_f8(1, 0, 1, 1, kTile, D);      // dS (MN-major) K (MN-major)
       const uint32_t sK = smem_u32(sm + L::kK), sV = smem_u32(sm + L::kV);
       const uint32_t sPt = smem_u32(sm + L::kPt), sDSt = smem_u32(sm + L::kDSt);
-      bool ok = wait(&bars.kv, 0, wd);
+      bool ok = wait(&bars.kv, 0, wd, 302);
       for (int n = 0; n < n_iter && ok; ++n) {
         const int s = n & 1;
         const uint32_t ph = (n >> 1) & 1;
         const uint32_t sQ = smem_u32(sm + L::kQ + s * L::kTileBytes);
         const uint32_t sDO = smem_u32(sm + L::kDO + s * L::kTileBytes);
-        if (!(ok = wait(&bars.qfull[s], ph, wd))) break;
+        if (!(ok = wait(&bars.qfull[s], ph, wd, 303))) break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < D / 32; ++k)
           mma_f8(tmem + 0, SwTile<D>::kmajor(sK, k), SwTile<D>::kmajor(sQ, k), kIdS, k > 0);
         mma_commit(&bars.sfull);
-        if (n >= 1 && !(ok = wait(&bars.dqempty, (n - 1) & 1, wd))) break;
+        if (n >= 1 && !(ok = wait(&bars.dqempty, (n - 1) & 1, wd, 304))) break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < D / 32; ++k)
           mma_f8(tmem + 128, SwTile<D>::kmajor(sV, k), SwTile<D>::kmajor(sDO, k), kIdDP, k > 0);
         mma_commit(&bars.dpfull);
-        if (!(ok = wait(&bars.pds, n & 1, wd))) break;
+        if (!(ok = wait(&bars.pds, n & 1, wd, 305))) break;
         tc_fence_after();
         const int mode_dv = s_mode[0], mode_dk = s_mode[1];
         if (mode_dv) {
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&bars.qempty[s]);
       }
       mma_commit(&bars.mma_done);
-      wait_drain(&bars.mma_done, 0, a.wait_limit_ns);
+      wait_drain(&bars.mma_done, 0, wd, 311);
     }
   } else {
     // -------------------------------------------------------------- compute
@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // P = exp(S - LSE), its tile amax and E4M3 codes
       float p[64];
-      wait(&bars.sfull, n & 1, wd);
+      wait(&bars.sfull, n & 1, wd, 306);
       tc_fence_after();
       tmem_ld32(tl + wg * 64, *reinterpret_cast<float(*)[32]>(&p[0]));
       tmem_ld32(tl + wg * 64 + 32, *reinterpret_cast<float(*)[32]>(&p[32]));
@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // dS = P (dP - delta), its tile amax and E5M2 codes
       float ds[64];
-      wait(&bars.dpfull, n & 1, wd);
+      wait(&bars.dpfull, n & 1, wd, 307);
       tc_fence_after();
       tmem_ld32(tl + 128 + wg * 64, *reinterpret_cast<float(*)[32]>(&ds[0]));
       tmem_ld32(tl + 128 + wg * 64 + 32, *reinterpret_cast<float(*)[32]>(&ds[32]));
@@ -385,23 +385,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 
-      // dQ tile (query rows on TMEM lanes): scale and reduce into global dQ
-      wait(&bars.mma2, n & 1, wd);
+      // dQ tile (query rows on TMEM lanes): scale and reduce into global dQ.
+      // TMEM loads are warp-collective (.sync.aligned): every lane loads, and
+      // only the global reduction is guarded by the row bound.
+      wait(&bars.mma2, n & 1, wd, 312);
       tc_fence_after();
       {
         const float cdq = a.sigma * sds * sk;
         const int qi = qi0 + r;
-        float* dst = dQ + ((size_t)bh * a.N + qi) * D + wg * DH;
+        float v[DH];
 #pragma unroll
-        for (int c = 0; c < DH; c += 32) {
-          float v[32];
-          tmem_ld32(tl + 128 + wg * DH + c, v);
-          tmem_wait_ld();
-          if (qi < a.N && cdq != 0.0f) {
+        for (int c = 0; c < DH; c += 32) tmem_ld32(tl + 128 + wg * DH + c, *reinterpret_cast<float(*)[32]>(&v[c]));
+        tmem_wait_ld();
+        if (qi < a.N && cdq != 0.0f) {
+          float* dst = dQ + ((size_t)bh * a.N + qi) * D + wg * DH;
 #pragma unroll
-            for (int k = 0; k < 32; k += 4)
-              red_add_v4(dst + c + k, v[k] * cdq, v[k + 1] * cdq, v[k + 2] * cdq, v[k + 3] * cdq);
-          }
+          for (int k = 0; k < DH; k += 4)
+            red_add_v4(dst + k, v[k] * cdq, v[k + 1] * cdq, v[k + 2] * cdq, v[k + 3] * cdq);
         }
       }
       tc_fence_before();
@@ -410,29 +410,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // epilogue: dV and dK rows of this key tile, in true units (an
-    // accumulator that never received a contribution holds garbage: write 0)
-    if (kv_valid) {
-      float* dv = dV + ((size_t)bg * a.N + kj) * D + wg * DH;
-      float* dk = dK + ((size_t)bg * a.N + kj) * D + wg * DH;
+    // accumulator that never received a contribution holds garbage: write 0).
+    // All lanes load (warp-collective); only the stores are guarded.
 #pragma unroll
-      for (int c = 0; c < DH; c += 32) {
-        float v[32];
-        tmem_ld32(tl + 256 + wg * DH + c, v);
-        tmem_wait_ld();
-        const float fv = unit_dv;
+    for (int c = 0; c < DH; c += 32) {
+      float v[32], u[32];
+      tmem_ld32(tl + 256 + wg * DH + c, v);
+      tmem_ld32(tl + 384 + wg * DH + c, u);
+      tmem_wait_ld();
+      if (kv_valid) {
+        float* dv = dV + ((size_t)bg * a.N + kj) * D + wg * DH + c;
+        float* dk = dK + ((size_t)bg * a.N + kj) * D + wg * DH + c;
+        const float fv = unit_dv, fk = unit_dk;
 #pragma unroll
-        for (int k = 0; k < 32; k += 4)
-          *reinterpret_cast<float4*>(dv + c + k) =
+        for (int k = 0; k < 32; k += 4) {
+          *reinterpret_cast<float4*>(dv + k) =
               fv == 0.0f ? make_float4(0.f, 0.f, 0.f, 0.f)
                          : make_float4(v[k] * fv, v[k + 1] * fv, v[k + 2] * fv, v[k + 3] * fv);
-        tmem_ld32(tl + 384 + wg * DH + c, v);
-        tmem_wait_ld();
-        const float fk = unit_dk;
-#pragma unroll
-        for (int k = 0; k < 32; k += 4)
-          *reinterpret_cast<float4*>(dk + c + k) =
+          *reinterpret_cast<float4*>(dk + k) =
               fk == 0.0f ? make_float4(0.f, 0.f, 0.f, 0.f)
-                         : make_float4(v[k] * fk, v[k + 1] * fk, v[k + 2] * fk, v[k + 3] * fk);
+                         : make_float4(u[k] * fk, u[k + 1] * fk, u[k + 2] * fk, u[k + 3] * fk);
+        }
       }
     }
   }

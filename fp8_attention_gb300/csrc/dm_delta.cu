@@ -98,31 +98,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < nkv; ++t) {
         const int s = t & 1;
         const uint32_t ph = (t >> 1) & 1;
-        if (!wait(&bars.kempty[s], ph ^ 1, wd)) break;
-        if (!wait(&bars.vempty[s], ph ^ 1, wd)) break;
+        if (!wait(&bars.kempty[s], ph ^ 1, wd, 201)) break;
+        if (!wait(&bars.vempty[s], ph ^ 1, wd, 202)) break;
         mbar_arrive_expect_tx(&bars.kfull[s], L::kTileBytes);
         tma_load_3d(sm + L::kK + s * L::kTileBytes, &tmK, &bars.kfull[s], 0, t * kTile, bg);
         mbar_arrive_expect_tx(&bars.vfull[s], L::kTileBytes);
         tma_load_3d(sm + L::kV + s * L::kTileBytes, &tmV, &bars.vfull[s], 0, t * kTile, bg);
         issued = t + 1;
       }
-      wait_drain(&bars.q, 0, a.wait_limit_ns);
+      wait_drain(&bars.q, 0, wd, 209);
       for (int t = max(0, issued - 2); t < issued; ++t) {
-        wait_drain(&bars.kfull[t & 1], (t >> 1) & 1, a.wait_limit_ns);
-        wait_drain(&bars.vfull[t & 1], (t >> 1) & 1, a.wait_limit_ns);
+        wait_drain(&bars.kfull[t & 1], (t >> 1) & 1, wd, 210);
+        wait_drain(&bars.vfull[t & 1], (t >> 1) & 1, wd, 211);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f8(0, 0, 0, 0, kTile, kTile);   // Q K^T
       constexpr uint32_t kIdDP = idesc_f8(1, 0, 0, 0, kTile, kTile);  // dO^ (E5M2) V^T (E4M3)
-      bool ok = wait(&bars.q, 0, wd);
+      bool ok = wait(&bars.q, 0, wd, 203);
       tc_fence_after();
       const uint32_t sQ = smem_u32(sm + L::kQ), sDO = smem_u32(sm + L::kDO);
       for (int t = 0; t < nkv && ok; ++t) {
         const int s = t & 1;
         const uint32_t ph = (t >> 1) & 1;
-        ok = wait(&bars.tempty[s], ph ^ 1, wd) && wait(&bars.kfull[s], ph, wd);
+        ok = wait(&bars.tempty[s], ph ^ 1, wd, 204) && wait(&bars.kfull[s], ph, wd, 205);
         if (!ok) break;
         tc_fence_after();
         const uint32_t sK = smem_u32(sm + L::kK + s * L::kTileBytes);
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_f8(tmem + s * 128, SwTile<D>::kmajor(sQ, k), SwTile<D>::kmajor(sK, k), kIdS, k > 0);
         mma_commit(&bars.sfull[s]);
         mma_commit(&bars.kempty[s]);
-        ok = wait(&bars.vfull[s], ph, wd);
+        ok = wait(&bars.vfull[s], ph, wd, 206);
         if (!ok) break;
         tc_fence_after();
         const uint32_t sV = smem_u32(sm + L::kV + s * L::kTileBytes);
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&bars.vempty[s]);
       }
       mma_commit(&bars.mma_done);
-      wait_drain(&bars.mma_done, 0, a.wait_limit_ns);
+      wait_drain(&bars.mma_done, 0, wd, 212);
     }
   } else {
     const int wg = (warp - 2) >> 2;  // key-column half
@@ -164,11 +164,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int jlim = min(64, a.N - j0);
       if (a.causal) jlim = min(jlim, qi - j0 + 1);
       float sv[64], dp[64];
-      wait(&bars.sfull[s], ph, wd);
+      wait(&bars.sfull[s], ph, wd, 207);
       tc_fence_after();
       tmem_ld32(tl + s * 128, *reinterpret_cast<float(*)[32]>(&sv[0]));
       tmem_ld32(tl + s * 128 + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
-      wait(&bars.dpfull[s], ph, wd);
+      wait(&bars.dpfull[s], ph, wd, 208);
       tc_fence_after();
       tmem_ld32(tl + 256 + s * 128, *reinterpret_cast<float(*)[32]>(&dp[0]));
       tmem_ld32(tl + 256 + s * 128 + 32, *reinterpret_cast<float(*)[32]>(&dp[32]));

@@ -57,38 +57,50 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // device status word and raises the CTA's abort flag; from then on every wait
 // of the CTA returns immediately, so all roles run their (counted) loops to
 // the end without blocking and the kernel exits normally.
+// status[0] holds the status code, status[1] the site id (kernel * 100 + wait
+// number) of the first wait that expired.
 struct Watchdog {
   volatile int* abort_flag;  // shared memory
-  unsigned int* status;      // global status word
+  unsigned int* status;      // global status words [2]
   unsigned long long limit_ns;
 };
 
-static __device__ __noinline__ bool wait_slow(uint64_t* bar, uint32_t parity, const Watchdog& wd) {
+static __device__ __noinline__ void record_timeout(const Watchdog& wd, unsigned int site) {
+  *wd.abort_flag = 1;
+  atomicCAS(wd.status, 0u, (unsigned)DM_ERR_TIMEOUT);
+  atomicCAS(wd.status + 1, 0u, site);
+  __threadfence();
+}
+
+static __device__ __noinline__ bool wait_slow(uint64_t* bar, uint32_t parity, const Watchdog& wd,
+                                              unsigned int site) {
   const uint64_t t0 = globaltimer();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*wd.abort_flag) return false;
     if (globaltimer() - t0 > wd.limit_ns) {
-      *wd.abort_flag = 1;
-      atomicCAS(wd.status, 0u, (unsigned)DM_ERR_TIMEOUT);
-      __threadfence();
+      record_timeout(wd, site);
       return false;
     }
   }
 }
 
 // Returns true when the phase with `parity` completed, false on abort.
-__device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, const Watchdog& wd) {
+__device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, const Watchdog& wd, unsigned int site) {
   if (mbar_try_wait(bar, parity)) return true;
-  return wait_slow(bar, parity, wd);
+  return wait_slow(bar, parity, wd, site);
 }
 
 // Wait bounded only by time (not by the abort flag): used at teardown so that
 // a CTA never exits while its own TMA copies or MMAs are still in flight.
-static __device__ __noinline__ bool wait_drain(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
+static __device__ __noinline__ bool wait_drain(uint64_t* bar, uint32_t parity, const Watchdog& wd,
+                                               unsigned int site) {
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity))
-    if (globaltimer() - t0 > limit_ns) return false;
+    if (globaltimer() - t0 > wd.limit_ns) {
+      record_timeout(wd, site);
+      return false;
+    }
   return true;
 }
 

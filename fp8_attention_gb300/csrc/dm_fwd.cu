@@ -111,8 +111,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < nkv; ++t) {
         const int s = t & 1;
         const uint32_t ph = (t >> 1) & 1;
-        if (!wait(&bars.kempty[s], ph ^ 1, wd)) break;
-        if (!wait(&bars.vempty[s], ph ^ 1, wd)) break;
+        if (!wait(&bars.kempty[s], ph ^ 1, wd, 101)) break;
+        if (!wait(&bars.vempty[s], ph ^ 1, wd, 102)) break;
         mbar_arrive_expect_tx(&bars.kfull[s], L::kTileBytes);
         tma_load_3d(sm + L::kK + s * L::kTileBytes, &tmK, &bars.kfull[s], 0, t * kTile, bg);
         mbar_arrive_expect_tx(&bars.vfull[s], L::kTileBytes);
@@ -120,10 +120,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued = t + 1;
       }
       // every issued load has landed before the CTA may exit
-      wait_drain(&bars.q, 0, a.wait_limit_ns);
+      wait_drain(&bars.q, 0, wd, 116);
       for (int t = max(0, issued - 2); t < issued; ++t) {
-        wait_drain(&bars.kfull[t & 1], (t >> 1) & 1, a.wait_limit_ns);
-        wait_drain(&bars.vfull[t & 1], (t >> 1) & 1, a.wait_limit_ns);
+        wait_drain(&bars.kfull[t & 1], (t >> 1) & 1, wd, 117);
+        wait_drain(&bars.vfull[t & 1], (t >> 1) & 1, wd, 118);
       }
     }
   } else if (warp == 1) {
@@ -132,15 +132,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdS = idesc_f8(0, 0, 0, 0, kTile, kTile);  // Q K^T, both K-major
       constexpr uint32_t kIdO = idesc_f8(0, 0, 0, 1, kTile, D);      // P^ (K-major) V (MN-major)
       bool ok = true;
-      if (a.stall_test) ok = wait(&bars.stall, 0, wd);  // watchdog test: never signalled
-      ok = ok && wait(&bars.q, 0, wd);
+      if (a.stall_test) ok = wait(&bars.stall, 0, wd, 103);  // watchdog test: never signalled
+      ok = ok && wait(&bars.q, 0, wd, 104);
       tc_fence_after();
       const uint32_t sQ = smem_u32(sm + L::kQ);
       for (int t = 0; t <= nkv && ok; ++t) {
         if (t < nkv) {
           const int s = t & 1;
           const uint32_t ph = (t >> 1) & 1;
-          ok = wait(&bars.kfull[s], ph, wd) && wait(&bars.sempty[s], ph ^ 1, wd);
+          ok = wait(&bars.kfull[s], ph, wd, 105) && wait(&bars.sempty[s], ph ^ 1, wd, 106);
           if (!ok) break;
           tc_fence_after();
           const uint32_t sK = smem_u32(sm + L::kK + s * L::kTileBytes);
@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t >= 1) {
           const int u = t - 1, s = u & 1;
           const uint32_t ph = (u >> 1) & 1;
-          ok = wait(&bars.pfull[s], ph, wd) && wait(&bars.vfull[s], ph, wd) && wait(&bars.oempty[s], ph ^ 1, wd);
+          ok = wait(&bars.pfull[s], ph, wd, 107) && wait(&bars.vfull[s], ph, wd, 108) && wait(&bars.oempty[s], ph ^ 1, wd, 109);
           if (!ok) break;
           tc_fence_after();
           const uint32_t sP = smem_u32(sm + L::kP + s * kTile * kTile);
@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       mma_commit(&bars.mma_done);
-      wait_drain(&bars.mma_done, 0, a.wait_limit_ns);
+      wait_drain(&bars.mma_done, 0, wd, 119);
     }
   } else if (warp < 6) {
     // -------------------------------------------------------------- softmax
@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int jlim = min(kTile, a.N - j0);
       if (a.causal) jlim = min(jlim, qi - j0 + 1);
 
-      wait(&bars.sfull[s], ph, wd);
+      wait(&bars.sfull[s], ph, wd, 110);
       tc_fence_after();
       float v[kTile];
 #pragma unroll
@@ -226,8 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       m = m_new;
 
       if (t >= 2) {
-        wait(&bars.ofull[s], ph ^ 1, wd);   // PV(t-2) has read P buffer s
-        wait(&bars.oempty[s], ph ^ 1, wd);  // correction has read alpha/cs of t-2
+        wait(&bars.ofull[s], ph ^ 1, wd, 111);   // PV(t-2) has read P buffer s
+        wait(&bars.oempty[s], ph ^ 1, wd, 112);  // correction has read alpha/cs of t-2
       }
       uint8_t* sP = sm + L::kP + s * kTile * kTile;
 #pragma unroll
@@ -256,8 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < nkv; ++t) {
       const int s = t & 1;
       const uint32_t ph = (t >> 1) & 1;
-      wait(&bars.pfull[s], ph, wd);
-      wait(&bars.ofull[s], ph, wd);
+      wait(&bars.pfull[s], ph, wd, 113);
+      wait(&bars.ofull[s], ph, wd, 114);
       tc_fence_after();
       const float alpha = s_alpha[s][row];
       const float cs = s_cs[s];
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.oempty[s]);
     }
-    wait(&bars.fin, 0, wd);
+    wait(&bars.fin, 0, wd, 115);
     const float linv = s_linv[row];
     if (qi < a.N) {
       if (OUT_BF16) {

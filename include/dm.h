@@ -149,6 +149,11 @@ size_t dm_attn_bwd_workspace_size(const dm_attn_params* p);
  * reports an error, else DM_OK. */
 dm_status dm_get_status(void* stream);
 
+/* Where the last DM_ERR_TIMEOUT reported by dm_get_status came from:
+ * kernel * 100 + wait number (kernel 1 forward, 2 delta pass, 3 backward),
+ * 0 if no wait has expired.  A diagnostic for bug reports. */
+unsigned int dm_last_timeout_site(void);
+
 /* Human-readable name of a status code (static string). */
 const char* dm_status_string(dm_status s);
 
