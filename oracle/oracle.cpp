@@ -387,9 +387,13 @@ int or_attn_fwd(int B, int Hq, int Hkv, int N, int d, int causal, double sigma, 
 
 // ---------------------------------------------------------------------------
 // Softmax row correction delta (project page sections 01 and 03).
-//   matched      (section 03): delta_i = sum_j P_ij dP^_ij with P the FP32
-//                softmax before quantisation, P_ij = exp(S_ij - LSE_i), and
-//                dP^ = dO^ V^T accumulated exactly over the decoded operands;
+//   matched      (section 03): delta_i = sum_j P_ij dP^_ij / sum_j P_ij with
+//                P the FP32 softmax before quantisation, P_ij = exp(S_ij -
+//                LSE_i), and dP^ = dO^ V^T accumulated exactly over the decoded
+//                operands.  Section 03 cancels the row sum of dS "after using
+//                sum_j P_ij = 1"; P in FP32 with a stored FP32 LSE sums to
+//                1 + eta, and the division makes the cancellation hold for the
+//                P the backward uses (no change when P sums to 1 exactly);
 //   stale_dO     (section 01, "Why can we reuse the forward output?" and
 //                "What changes in FP8?"): delta_i = <dO_i, O_i>, dO before
 //                its FP8 cast, O as stored by the forward;
@@ -420,6 +424,7 @@ int or_attn_delta(int B, int Hq, int Hkv, int N, int d, int causal, double sigma
       } else if (mode == OR_DELTA_STALE_DOHAT) {
         dl = dot(dOhat + qo + (size_t)i * d, O + qo + (size_t)i * d, d);
       } else {
+        double psum = 0.0;
         for (int j = 0; j < N; ++j) {
           if (!visible(D, i, j)) continue;
           const double s = D.sigma * dot(Q + qo + (size_t)i * d, K + ko + (size_t)j * d, d);
@@ -427,7 +432,9 @@ int or_attn_delta(int B, int Hq, int Hkv, int N, int d, int causal, double sigma
           if (flags & OR_ROUND32) p = fl32(p);
           const double dp = dot(dOhat + qo + (size_t)i * d, V + ko + (size_t)j * d, d);
           dl += p * dp;
+          psum += p;
         }
+        dl /= psum;
       }
       delta[ro + i] = dl;
     }
