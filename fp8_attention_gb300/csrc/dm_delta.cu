@@ -1,7 +1,10 @@
 // Matched softmax row correction ("Delta-Matching for reliable FP8 attention
-// training", section 03): delta_i = sum_j P_ij * dP^_ij with P = exp(S - LSE)
-// the FP32 softmax before quantisation and dP^ = dO^ V^T the FP32 result of
-// the FP8 matmul.  This is the separate correction pass: one CTA per (batch,
+// training", section 03): delta_i = sum_j P_ij * dP^_ij / sum_j P_ij with
+// P = exp(S - LSE) the FP32 softmax before quantisation and dP^ = dO^ V^T the
+// FP32 result of the FP8 matmul.  Section 03 cancels the row sum of dS "after
+// using sum_j P_ij = 1"; with P held in FP32 (and LSE stored in FP32) that sum
+// is 1 + eta, and dividing by it makes the cancellation hold for the P the
+// backward actually uses (identical to the undivided form when P sums to 1).  This is the separate correction pass: one CTA per (batch,
 // query head, 128-row query tile), recomputing S = Q K^T and dP^ = dO^ V^T
 // on tcgen05 tile by tile.
 //
@@ -9,8 +12,8 @@
 //   warp 0      TMA: Q and dO tiles once, K/V tiles double-buffered
 //   warp 1      MMA: S(t) into TMEM S[t%2], dP(t) into TMEM dP[t%2]
 //   warps 2-9   two warpgroups, one thread per (query row, half of the key
-//               columns): P = exp2(S*c1 - LSE*log2e), sum P*dP, scaled by
-//               s_dO * s_V,t per key tile
+//               columns): P = exp2(S*c1 - LSE*log2e), sums of P*dP (scaled by
+//               s_dO * s_V,t per key tile) and of P
 // TMEM columns: S[0] 0, S[1] 128, dP[0] 256, dP[1] 384.
 #include <cudaTypedefs.h>
 
@@ -47,7 +50,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ DeltaBars bars;
-  __shared__ float s_part[kTile];
+  __shared__ float s_part[kTile], s_psum[kTile];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
@@ -154,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sq = a.q_scales[bh * a.T + qt];
     const float sdo = a.do_scales[bh * a.T + qt];
     const float lse2 = row_valid ? lse[(size_t)bh * a.N + qi] * kLog2e : 0.0f;
-    float dl = 0.0f;
+    float dl = 0.0f, psum = 0.0f;
     for (int t = 0; t < nkv; ++t) {
       const int s = t & 1;
       const uint32_t ph = (t >> 1) & 1;
@@ -176,19 +179,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.tempty[s]);
-      float part0 = 0.0f, part1 = 0.0f;
+      float part0 = 0.0f, part1 = 0.0f, ps0 = 0.0f, ps1 = 0.0f;
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
         const float p0 = (c < jlim) ? ex2(fmaf(sv[c], c1, -lse2)) : 0.0f;
         const float p1 = (c + 1 < jlim) ? ex2(fmaf(sv[c + 1], c1, -lse2)) : 0.0f;
         part0 = fmaf(p0, dp[c], part0);
         part1 = fmaf(p1, dp[c + 1], part1);
+        ps0 += p0;
+        ps1 += p1;
       }
       dl = fmaf(part0 + part1, c2, dl);
+      psum += ps0 + ps1;
     }
-    if (wg == 1) s_part[row] = dl;
+    if (wg == 1) {
+      s_part[row] = dl;
+      s_psum[row] = psum;
+    }
     named_bar_sync(1, 256);
-    if (wg == 0 && row_valid) delta[(size_t)bh * a.N + qi] = dl + s_part[row];
+    if (wg == 0 && row_valid) delta[(size_t)bh * a.N + qi] = (dl + s_part[row]) / (psum + s_psum[row]);
   }
 
   tc_fence_before();

@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const T* __restrict
   float r;
   const float s = tile_scale<FMT>(amax, r);
   if (threadIdx.x == 0) scales[tile] = s;
+  const bool flushed = (s == 0.0f);  // flushed tile: all codes +0 (x * 0 would give -0 for x < 0)
 
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
@@ -91,8 +92,9 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const T* __restrict
     uint32_t w[V / 4];
 #pragma unroll
     for (int k = 0; k < V / 4; ++k)
-      w[k] = pack4<FMT>(__fmul_rn(v[i][4 * k], r), __fmul_rn(v[i][4 * k + 1], r), __fmul_rn(v[i][4 * k + 2], r),
-                        __fmul_rn(v[i][4 * k + 3], r));
+      w[k] = flushed ? 0u
+                     : pack4<FMT>(__fmul_rn(v[i][4 * k], r), __fmul_rn(v[i][4 * k + 1], r),
+                                  __fmul_rn(v[i][4 * k + 2], r), __fmul_rn(v[i][4 * k + 3], r));
     uint8_t* dst = codes + base + (size_t)idx * V;
     if constexpr (V == 8) {
       *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
