@@ -42,14 +42,14 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic of one backward launch on the default workload, from the ncu
 # capture summarised in profiles/ (valid only for the kernel source it was
 # taken on; reported as null once dm_bwd.cu changes).
-BWD_TRAFFIC = {"sha1": None, "bytes": None}
+BWD_TRAFFIC = {"sha1": "c6cf319279dd6b864f5fc2ab10ec24bfac4feab6", "bytes": 167229056}
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
