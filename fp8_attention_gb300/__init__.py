@@ -23,7 +23,7 @@ import torch
 __all__ = [
     "AttnParams", "Fp8", "DMError", "lib", "dm_version", "dm_status_string", "dm_set_knob",
     "dm_get_status", "dm_last_timeout_site", "dm_quantize", "dm_attn_fwd", "dm_attn_delta", "dm_attn_bwd",
-    "dm_attn_bwd_workspace_size",
+    "dm_attn_bwd_workspace_size", "dm_attn_bwd_noalloc", "DM_NOALLOC_MAX_DELTA_ROWS",
     "DM_F32", "DM_BF16", "DM_E4M3", "DM_E5M2", "DM_DELTA_MATCHED", "DM_DELTA_STALE_DO",
     "DM_DELTA_STALE_DOHAT", "DM_KNOB_WAIT_LIMIT_NS", "DM_KNOB_STALL_TEST",
 ]
@@ -37,6 +37,7 @@ DM_E4M3, DM_E5M2 = 0, 1
 DM_DELTA_MATCHED, DM_DELTA_STALE_DO, DM_DELTA_STALE_DOHAT = 0, 1, 2
 DM_KNOB_WAIT_LIMIT_NS, DM_KNOB_STALL_TEST = 0, 1
 TILE = 128
+DM_NOALLOC_MAX_DELTA_ROWS = 1 << 21
 
 
 class DMError(RuntimeError):
@@ -115,6 +116,9 @@ def lib():
             L.dm_attn_bwd.restype = I
             L.dm_attn_bwd.argtypes = [PP, I, _Fp8, _Fp8, _Fp8, _Fp8, P, P, P, I, P, I, P, P, P,
                                       ctypes.POINTER(_Diag), P, S, P]
+            L.dm_attn_bwd_noalloc.restype = I
+            L.dm_attn_bwd_noalloc.argtypes = [PP, I, _Fp8, _Fp8, _Fp8, _Fp8, P, P, I, P, I, P, P, P,
+                                              ctypes.POINTER(_Diag), P]
             L.dm_attn_bwd_workspace_size.restype = S
             L.dm_attn_bwd_workspace_size.argtypes = [PP]
             _lib = L
@@ -258,3 +262,23 @@ def dm_attn_bwd(p: AttnParams, mode: int, q: Fp8, k: Fp8, v: Fp8, do_hat: Fp8, l
                            _stream(stream))
     _check(rc, "dm_attn_bwd")
     return out
+
+
+def dm_attn_bwd_noalloc(p: AttnParams, mode: int, q: Fp8, k: Fp8, v: Fp8, do_hat: Fp8, lse, dO=None, O=None,
+                        dQ=None, dK=None, dV=None, stream=None):
+    """Backward with delta computed for `mode` in the library's fixed device array (no
+    workspace, no allocation inside the call; the outputs here are allocated by torch only
+    when the caller passes none)."""
+    dev = lse.device
+    if dQ is None:
+        dQ = torch.empty((p.B, p.Hq, p.N, p.d), dtype=torch.float32, device=dev)
+    if dK is None:
+        dK = torch.empty((p.B, p.Hkv, p.N, p.d), dtype=torch.float32, device=dev)
+    if dV is None:
+        dV = torch.empty((p.B, p.Hkv, p.N, p.d), dtype=torch.float32, device=dev)
+    cp = p.c()
+    rc = lib().dm_attn_bwd_noalloc(ctypes.byref(cp), int(mode), _fp8(q), _fp8(k), _fp8(v), _fp8(do_hat),
+                                   _ptr(lse), _ptr(dO), _dtype(dO), _ptr(O), _dtype(O), _ptr(dQ), _ptr(dK),
+                                   _ptr(dV), None, _stream(stream))
+    _check(rc, "dm_attn_bwd_noalloc")
+    return {"dQ": dQ, "dK": dK, "dV": dV}

@@ -143,6 +143,31 @@ dm_status dm_attn_bwd(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor
 /* Bytes of workspace dm_attn_bwd needs when delta == NULL (0 on bad params). */
 size_t dm_attn_bwd_workspace_size(const dm_attn_params* p);
 
+/* dm_attn_bwd_noalloc -- dm_attn_bwd with delta computed for `mode`, for
+ * callers that cannot allocate device memory and so cannot hand
+ * dm_attn_bwd a workspace: a training runtime that plans every device byte
+ * ahead of the step and forbids allocations inside it, or a host program that
+ * reaches this library only through this C ABI with no device allocator of its
+ * own.  The method's pages have no counterpart to this call; it exists only
+ * for such callers.
+ *
+ * Arguments are those of dm_attn_bwd without delta and workspace.  delta is
+ * kept in a fixed device array of DM_NOALLOC_MAX_DELTA_ROWS floats (8 MiB),
+ * held on every GPU that loads the library until the process exits; problems
+ * with B*Hq*N above that limit are rejected with DM_ERR_SHAPE before anything
+ * is launched.  The call allocates nothing.  Its first call on a device looks
+ * up that array's device address (once per device, with the device current);
+ * make that first call before any stream capture.  All calls on a device
+ * share that device's array, which keeps the last call's contents: each call
+ * rewrites every delta row before reading it, so nothing needs clearing, but
+ * calls whose kernels overlap on the same GPU (for example on two streams)
+ * race on it and must be serialised by the caller. */
+#define DM_NOALLOC_MAX_DELTA_ROWS (1u << 21)
+dm_status dm_attn_bwd_noalloc(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor q, dm_fp8_tensor k,
+                              dm_fp8_tensor v, dm_fp8_tensor do_hat, const float* lse, const void* dO,
+                              dm_dtype do_dtype, const void* O, dm_dtype o_dtype, float* dQ, float* dK,
+                              float* dV, const dm_diag* diag, void* stream);
+
 /* Synchronises `stream`, then returns and clears the device status word of
  * the current device: DM_ERR_TIMEOUT if a kernel's bounded wait expired since
  * the last call (its outputs are then undefined), DM_ERR_CUDA if the stream

@@ -88,7 +88,12 @@ def rowsum_check(rs, ab, delta):
     dominant key) dS is rounding noise of delta and only |sum_j dS_ij| <= 2^-10 |delta_i| can hold.
     Returns (number of rows checked, number of noise rows)."""
     live = ab >= 1e-3 * np.abs(delta)
-    assert np.all(np.abs(rs[live]) <= ROWSUM_TOL * ab[live]), np.max(np.abs(rs[live]) / ab[live])
+    bad = live & (np.abs(rs) > ROWSUM_TOL * ab)
+    if bad.any():
+        print("row-sum violations:", int(bad.sum()), "of", int(live.sum()),
+              "|sum dS|/|delta|:", np.abs(rs[bad]) / np.abs(delta[bad]),
+              "sum|dS|/|delta|:", ab[bad] / np.abs(delta[bad]))
+    assert not bad.any(), np.max(np.abs(rs[live]) / ab[live])
     noise = ~live
     assert np.all(np.abs(rs[noise]) <= 2.0 ** -10 * np.abs(delta[noise]) + 1e-30)
     return int(live.sum()), int(noise.sum())
