@@ -83,20 +83,20 @@ def test_delta_computed_inside_backward():
 
 
 def rowsum_check(rs, ab, delta):
-    """Rows whose dS carries more than FP32 rounding noise of delta (sum_j |dS_ij| >= 1e-3 |delta_i|)
-    must satisfy |sum_j dS_ij| <= 1e-4 sum_j |dS_ij|; in the other rows (one visible key, or one
-    dominant key) dS is rounding noise of delta and only |sum_j dS_ij| <= 2^-10 |delta_i| can hold.
-    Returns (number of rows checked, number of noise rows)."""
-    live = ab >= 1e-3 * np.abs(delta)
-    bad = live & (np.abs(rs) > ROWSUM_TOL * ab)
-    if bad.any():
-        print("row-sum violations:", int(bad.sum()), "of", int(live.sum()),
-              "|sum dS|/|delta|:", np.abs(rs[bad]) / np.abs(delta[bad]),
-              "sum|dS|/|delta|:", ab[bad] / np.abs(delta[bad]))
-    assert not bad.any(), np.max(np.abs(rs[live]) / ab[live])
-    noise = ~live
-    assert np.all(np.abs(rs[noise]) <= 2.0 ** -10 * np.abs(delta[noise]) + 1e-30)
-    return int(live.sum()), int(noise.sum())
+    """Matched delta restores zero row sums of dS "up to FP32 rounding" (project page section 03):
+    every row must satisfy |sum_j dS_ij| <= 1e-4 * sum_j |dS_ij| + 2^-20 * |delta_i|.  The second
+    term is the FP32 resolution of delta (16 units in its last place): in near-one-hot rows
+    sum_j |dS_ij| is only ~1e-3 |delta_i| (one key carries P ~ 1 and dP ~ delta), and the relative
+    term alone would ask for less than one ulp of delta.
+    Returns (rows, rows that needed the FP32 term)."""
+    floor = 2.0 ** -20 * np.abs(delta)
+    ok = np.abs(rs) <= ROWSUM_TOL * ab + floor
+    needed = np.abs(rs) > ROWSUM_TOL * ab
+    if needed.any():
+        print("rows needing the FP32 term:", int(needed.sum()), "of", rs.size,
+              "max |sum dS|/|delta| there:", float(np.max(np.abs(rs[needed]) / np.abs(delta[needed]))))
+    assert ok.all(), float(np.max((np.abs(rs) - floor) / np.maximum(ab, 1e-38)))
+    return rs.size, int(needed.sum())
 
 
 def test_matched_rows_sum_to_zero_and_stale_do_not():
@@ -108,11 +108,12 @@ def test_matched_rows_sum_to_zero_and_stale_do_not():
         res[mode] = tuple(np32(g[n]) for n in ("rowsum_pre", "abssum_pre", "rowsum_post", "abssum_post",
                                                 "delta"))
     rs, ab, _, _, delta = res[dm.DM_DELTA_MATCHED]
-    checked, noise = rowsum_check(rs, ab, delta)
-    assert checked > 0.95 * rs.size
+    rows, needed = rowsum_check(rs, ab, delta)
+    assert needed <= 1e-3 * rows
+    # the stale correction leaves residuals far above both terms
     rs_s, ab_s = res[dm.DM_DELTA_STALE_DO][:2]
-    live = ab >= 1e-3 * np.abs(delta)
-    assert np.median(np.abs(rs_s[live]) / ab_s[live]) > 10 * np.median(np.abs(rs[live]) / ab[live])
+    live = ab_s > 0
+    assert np.median(np.abs(rs_s[live]) / ab_s[live]) > 100 * ROWSUM_TOL
 
 
 def test_diagnostics_match_oracle():
