@@ -75,6 +75,18 @@ dm_status encode_codes_map(CUtensorMap* m, const uint8_t* codes, int BH, int N, 
   return r == CUDA_SUCCESS ? DM_OK : DM_ERR_CUDA;
 }
 
+// fp32 [BH][N][d] (dQ), box = 128 rows x 32 columns with the 128-byte swizzle.
+dm_status encode_f32_rows_map(CUtensorMap* m, const float* x, int BH, int N, int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)d * 4 * (cuuint64_t)N};
+  cuuint32_t box[3] = {32, (cuuint32_t)kTileRows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(x), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DM_OK : DM_ERR_CUDA;
+}
+
 dm_status check_params(const dm_attn_params* p) {
   if (!p) return DM_ERR_INVALID_ARG;
   if (p->B < 0 || p->Hq <= 0 || p->Hkv <= 0 || p->N < 0) return DM_ERR_SHAPE;
@@ -327,6 +339,7 @@ dm_status dm_attn_bwd(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor
   DM_TRY(encode_codes_map(&f.tmK, k.codes, p->B * p->Hkv, p->N, p->d));
   DM_TRY(encode_codes_map(&f.tmV, v.codes, p->B * p->Hkv, p->N, p->d));
   DM_TRY(encode_codes_map(&f.tmDO, do_hat.codes, p->B * p->Hq, p->N, p->d));
+  DM_TRY(encode_f32_rows_map(&f.tmDQ, dQ, p->B * p->Hq, p->N, p->d));
   f.args = make_args(p, status);
   f.args.q_scales = q.scales, f.args.k_scales = k.scales, f.args.v_scales = v.scales;
   f.args.do_scales = do_hat.scales;

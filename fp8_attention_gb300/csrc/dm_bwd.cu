@@ -11,7 +11,8 @@
 //   dS   = P (dP - delta) in FP32, dS^ = E5M2 per 128x128 tile
 //   dV  += P^T dO          (MMA, TMEM cols 256..)
 //   dK  += dS^T Q          (MMA, TMEM cols 384..)
-//   dQ_i = dS^ K           (MMA into cols 128.., drained with vector atomics)
+//   dQ_i = dS^ K           (MMA into cols 128.., staged in shared memory and
+//                           added into global dQ with a TMA bulk reduce-add)
 // dV and dK accumulate in TMEM in units of the current iteration's scale
 // product (s_P * s_dO, resp. sigma * s_dS * s_Q): before each accumulation the
 // compute warps rescale the accumulator by old/new unit.  Iterations whose
@@ -41,18 +42,14 @@ struct BwdLayout {
   static constexpr int kDO = kQ + 2 * kTileBytes;   // 2 stages
   static constexpr int kPt = kDO + 2 * kTileBytes;  // P^T codes, [key row][128 query bytes]
   static constexpr int kDSt = kPt + kTile * kTile;  // dS^T codes
-  static constexpr int kBytes = kDSt + kTile * kTile;
+  static constexpr int kDQ = kDSt + kTile * kTile;   // dQ tile staging: D/32 boxes of [128 rows][32 fp32]
+  static constexpr int kBytes = kDQ + kTile * D * 4;
   static constexpr int kDynSmem = kBytes + 1024;
 };
 
 struct BwdBars {
   uint64_t kv, qfull[2], qempty[2], sfull, dpfull, pds, mma2, dqempty, mma_done;
 };
-
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
 
 // Column sums over the 32 lanes of a warp: on return lane l holds the sum over
 // all lanes of their v[l] (recursive halving, 31 shuffles).
@@ -100,8 +97,9 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                    const AttnArgs a, const float* __restrict__ lse, const float* __restrict__ delta,
-                    float* __restrict__ dQ, float* __restrict__ dK, float* __restrict__ dV, const dm_diag diag) {
+                    const __grid_constant__ CUtensorMap tmDQ, const AttnArgs a, const float* __restrict__ lse,
+                    const float* __restrict__ delta, float* __restrict__ dK, float* __restrict__ dV,
+                    const dm_diag diag) {
   using L = BwdLayout<D>;
   constexpr int DH = D / 2;  // d columns per compute warpgroup
   extern __shared__ uint8_t smem_raw[];
@@ -239,24 +237,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sk = a.k_scales[bg * a.T + kt];
     const float svv = a.v_scales[bg * a.T + kt];
     float unit_dv = 0.0f, unit_dk = 0.0f;
+    // Per-iteration global values are loaded one iteration ahead: this
+    // thread's element of the query tile's LSE (threads 0-127; +inf for absent
+    // rows) or delta (threads 128-255; 0 for absent rows), and the tile's Q and
+    // dO scales.
+    auto row_value = [&](int n) -> float {
+      const int bh_n = b * a.Hq + g * G + n / nq;
+      const int qi = (qt0 + n % nq) * kTile + (ct & 127);
+      if (ct < 128) return qi < a.N ? lse[(size_t)bh_n * a.N + qi] : INFINITY;
+      return qi < a.N ? delta[(size_t)bh_n * a.N + qi] : 0.0f;
+    };
+    auto tile_index = [&](int n) { return (b * a.Hq + g * G + n / nq) * a.T + qt0 + n % nq; };
+    float pre_row = row_value(0);
+    float pre_sq = a.q_scales[tile_index(0)], pre_sdo = a.do_scales[tile_index(0)];
 
     for (int n = 0; n < n_iter; ++n) {
       const int hh = n / nq, qt = qt0 + n % nq;
       const int bh = b * a.Hq + g * G + hh;
       const int qi0 = qt * kTile;
       const int buf = n & 1;
-      // row vectors of this query tile: LSE (log2 units; +inf for absent rows) and delta
-      {
-        const int idx = ct & 127;
-        const int qi = qi0 + idx;
-        if (ct < 128)
-          s_lse[buf][idx] = qi < a.N ? lse[(size_t)bh * a.N + qi] * kLog2e : INFINITY;
-        else
-          s_dl[buf][idx] = qi < a.N ? delta[(size_t)bh * a.N + qi] : 0.0f;
+      if (ct < 128)
+        s_lse[buf][ct] = pre_row * kLog2e;
+      else
+        s_dl[buf][ct - 128] = pre_row;
+      const float sq = pre_sq, sdo = pre_sdo;
+      if (n + 1 < n_iter) {
+        pre_row = row_value(n + 1);
+        pre_sq = a.q_scales[tile_index(n + 1)];
+        pre_sdo = a.do_scales[tile_index(n + 1)];
       }
+      // the previous iteration's dQ reduce has finished reading the staging tile
+      if (ct == 0) bulk_wait_read_all();
       named_bar_sync(1, 256);
-      const float sq = a.q_scales[bh * a.T + qt];
-      const float sdo = a.do_scales[bh * a.T + qt];
       const float c1 = a.sigma * sq * sk * kLog2e;
       const float cdp = sdo * svv;
       const int cmin = !kv_valid ? (1 << 30) : (a.causal && qt == kt) ? r - wg * 64 : 0;
@@ -385,29 +397,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 
-      // dQ tile (query rows on TMEM lanes): scale and reduce into global dQ.
-      // TMEM loads are warp-collective (.sync.aligned): every lane loads, and
-      // only the global reduction is guarded by the row bound.
+      // dQ tile (query rows on TMEM lanes): scaled, staged in shared memory with
+      // the 128-byte swizzle of the dQ tensor map, then added into global dQ
+      // by one bulk reduce per 32-column box.  TMEM loads are warp-collective:
+      // every lane loads; rows beyond N are clipped by the tensor map.
       wait(&bars.mma2, n & 1, wd, 312);
       tc_fence_after();
       {
         const float cdq = a.sigma * sds * sk;
-        const int qi = qi0 + r;
         float v[DH];
 #pragma unroll
         for (int c = 0; c < DH; c += 32) tmem_ld32(tl + 128 + wg * DH + c, *reinterpret_cast<float(*)[32]>(&v[c]));
         tmem_wait_ld();
-        if (qi < a.N && cdq != 0.0f) {
-          float* dst = dQ + ((size_t)bh * a.N + qi) * D + wg * DH;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.dqempty);
 #pragma unroll
-          for (int k = 0; k < DH; k += 4)
-            red_add_v4(dst + k, v[k] * cdq, v[k + 1] * cdq, v[k + 2] * cdq, v[k + 3] * cdq);
+        for (int c = 0; c < DH; c += 32) {
+          uint8_t* box = sm + L::kDQ + ((wg * DH + c) / 32) * (kTile * 128);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            *reinterpret_cast<float4*>(box + SwTile<128>::chunk_offset(r, e)) =
+                make_float4(v[c + 4 * e] * cdq, v[c + 4 * e + 1] * cdq, v[c + 4 * e + 2] * cdq,
+                            v[c + 4 * e + 3] * cdq);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(2, 256);
+        if (ct == 0 && cdq != 0.0f) {
+#pragma unroll
+          for (int bx = 0; bx < D / 32; ++bx)
+            tma_reduce_add_3d(&tmDQ, sm + L::kDQ + bx * (kTile * 128), bx * 32, qi0, bh);
+          bulk_commit();
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.dqempty);
     }
+
+    if (ct == 0) bulk_wait_all();
 
     // epilogue: dV and dK rows of this key tile, in true units (an
     // accumulator that never received a contribution holds garbage: write 0).
@@ -450,7 +475,7 @@ cudaError_t launch_t(const BwdLaunch& f, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(f.args.B * f.args.Hkv * f.args.T);
-  k<<<grid, kThreads, smem, st>>>(f.tmQ, f.tmK, f.tmV, f.tmDO, f.args, f.lse, f.delta, f.dQ, f.dK, f.dV, f.diag);
+  k<<<grid, kThreads, smem, st>>>(f.tmQ, f.tmK, f.tmV, f.tmDO, f.tmDQ, f.args, f.lse, f.delta, f.dK, f.dV, f.diag);
   return cudaGetLastError();
 }
 

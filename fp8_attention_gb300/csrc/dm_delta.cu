@@ -157,12 +157,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sq = a.q_scales[bh * a.T + qt];
     const float sdo = a.do_scales[bh * a.T + qt];
     const float lse2 = row_valid ? lse[(size_t)bh * a.N + qi] * kLog2e : 0.0f;
+    const float* ksc = a.k_scales + (size_t)bg * a.T;
+    const float* vsc = a.v_scales + (size_t)bg * a.T;
+    float sk_next = ksc[0], sv_next = vsc[0];  // per-tile scales, loaded one tile ahead
     float dl = 0.0f, psum = 0.0f;
     for (int t = 0; t < nkv; ++t) {
       const int s = t & 1;
       const uint32_t ph = (t >> 1) & 1;
-      const float c1 = a.sigma * sq * a.k_scales[bg * a.T + t] * kLog2e;
-      const float c2 = sdo * a.v_scales[bg * a.T + t];
+      const float c1 = a.sigma * sq * sk_next * kLog2e;
+      const float c2 = sdo * sv_next;
+      if (t + 1 < nkv) {
+        sk_next = ksc[t + 1];
+        sv_next = vsc[t + 1];
+      }
       const int j0 = t * kTile + wg * 64;
       int jlim = min(64, a.N - j0);
       if (a.causal) jlim = min(jlim, qi - j0 + 1);

@@ -25,6 +25,7 @@ struct DeltaLaunch {
 
 struct BwdLaunch {
   CUtensorMap tmQ, tmK, tmV, tmDO;
+  CUtensorMap tmDQ;  // fp32 [B*Hq][N][d], box 128 rows x 32 columns, 128-byte swizzle
   AttnArgs args;
   const float* lse;
   const float* delta;

@@ -109,7 +109,7 @@ def test_matched_rows_sum_to_zero_and_stale_do_not():
                                                 "delta"))
     rs, ab, _, _, delta = res[dm.DM_DELTA_MATCHED]
     rows, needed = rowsum_check(rs, ab, delta)
-    assert needed <= 1e-3 * rows
+    assert needed <= 1e-3 * rows + 4   # plus row 0 of each causal head: a single key, dS is pure rounding
     # the stale correction leaves residuals far above both terms
     rs_s, ab_s = res[dm.DM_DELTA_STALE_DO][:2]
     live = ab_s > 0

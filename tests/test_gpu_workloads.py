@@ -62,7 +62,7 @@ def test_long_workloads_sampled(name):
     _codes_match(g, r)
     errs = _compare_sampled(g, r, w)
     rows, needed = rowsum_check(np32(g["rowsum_pre"]), np32(g["abssum_pre"]), np32(g["delta"]))
-    assert needed <= 1e-3 * rows
+    assert needed <= 1e-3 * rows + w.B * w.Hq   # plus row 0 of each causal head (a single key)
     print(name, "errors", errs, "row-sum rows", rows, "needing the FP32 term", needed)
 
 
