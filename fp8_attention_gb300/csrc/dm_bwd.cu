@@ -2,21 +2,23 @@
 // ("Delta-Matching for reliable FP8 attention training", section 01, "Write
 // down softmax backward", and section 03 for delta).  One CTA per (batch, kv
 // head, 128-row key tile); it loops over the query heads of the kv head's
-// group and over the query tiles that see the key tile, so dK and dV are
-// summed over the group inside the CTA.  Computed transposed (key rows on
-// TMEM lanes) so that dV and dK accumulate in TMEM:
-//   S^T  = K Q^T           (MMA, TMEM cols 0..127)
-//   dP^T = V dO^T          (MMA, TMEM cols 128..255)
-//   P    = exp(S - LSE) in FP32, P^ = E4M3 per 128x128 tile
-//   dS   = P (dP - delta) in FP32, dS^ = E5M2 per 128x128 tile
-//   dV  += P^T dO          (MMA, TMEM cols 256..)
-//   dK  += dS^T Q          (MMA, TMEM cols 384..)
-//   dQ_i = dS^ K           (MMA into cols 128.., staged in shared memory and
-//                           added into global dQ with a TMA bulk reduce-add)
-// dV and dK accumulate in TMEM in units of the current iteration's scale
-// product (s_P * s_dO, resp. sigma * s_dS * s_Q): before each accumulation the
-// compute warps rescale the accumulator by old/new unit.  Iterations whose
-// product is below 2^-100 (a flushed or negligible tile) add nothing.
+// group and over the query tiles that see the key tile (iterations n), so dK
+// and dV are summed over the group inside the CTA.  Products are computed
+// transposed (key rows on TMEM lanes) so that dV and dK accumulate in TMEM:
+//   S^T  = K Q^T                 P  = exp(S - LSE) in FP32,   P^  = E4M3 per 128x128 tile
+//   dP^T = V dO^T                dS = P (dP - delta) in FP32, dS^ = E5M2 per 128x128 tile
+//   dV  += P^T dO     dK += dS^T Q     dQ_i = dS^ K (staged, then TMA bulk reduce-add into dQ)
+//
+// TMEM (512 columns): two 128-column work buffers and the two accumulators.
+// Iteration n uses work buffer n%2 three times in a row: S(n), then dP(n) once
+// S(n) has been read, then dQ(n) once dP(n) has been read.  The other buffer
+// meanwhile carries iteration n-1's dQ and n+1's S, so the tensor core runs
+// S(n+1), [dV dK dQ](n) and dP(n+1) while the compute warps work on n:
+//   cols 0-127 work buffer 0, 128-255 work buffer 1, 256.. dV, 384.. dK.
+// dV and dK accumulate in units of the current iteration's scale product
+// (s_P * s_dO, resp. sigma * s_dS * s_Q): before each accumulation the compute
+// warps rescale the accumulator by old/new unit.  Iterations whose product is
+// below 2^-100 (a flushed or negligible tile) add nothing.
 //
 // Warp roles (320 threads): warp 0 TMA, warp 1 MMA, warps 2-9 two compute
 // warpgroups; thread = key row, warpgroup = half of the query columns (and
@@ -33,22 +35,30 @@ constexpr int kThreads = 320;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMinUnit = 0x1p-100f;
 
+struct BwdBars {
+  uint64_t kv, qfull[2], qempty[2], sfull[2], sread[2], dpfull[2], bfree[2], pds, mma2, mma_done;
+};
+
+// Everything lives in dynamic shared memory (no static shared variables), so
+// the 1024-byte aligned tile region starts at the window's base.
 template <int D>
 struct BwdLayout {
   static constexpr int kTileBytes = kTile * D;
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTileBytes;
-  static constexpr int kQ = kV + kTileBytes;        // 2 stages
-  static constexpr int kDO = kQ + 2 * kTileBytes;   // 2 stages
-  static constexpr int kPt = kDO + 2 * kTileBytes;  // P^T codes, [key row][128 query bytes]
-  static constexpr int kDSt = kPt + kTile * kTile;  // dS^T codes
-  static constexpr int kDQ = kDSt + kTile * kTile;   // dQ tile staging: D/32 boxes of [128 rows][32 fp32]
-  static constexpr int kBytes = kDQ + kTile * D * 4;
-  static constexpr int kDynSmem = kBytes + 1024;
-};
-
-struct BwdBars {
-  uint64_t kv, qfull[2], qempty[2], sfull, dpfull, pds, mma2, dqempty, mma_done;
+  static constexpr int kQ = kV + kTileBytes;            // 2 stages
+  static constexpr int kDO = kQ + 2 * kTileBytes;       // 2 stages
+  static constexpr int kPt = kDO + 2 * kTileBytes;      // 2 x P^T codes, [key row][128 query bytes]
+  static constexpr int kDSt = kPt + 2 * kTile * kTile;  // 2 x dS^T codes
+  static constexpr int kDQ = kDSt + 2 * kTile * kTile;  // dQ staging: D/32 boxes of [128 rows][32 fp32]
+  static constexpr int kLse = kDQ + kTile * D * 4;      // float [2][128]
+  static constexpr int kDl = kLse + 2 * kTile * 4;      // float [2][128]
+  static constexpr int kRed = kDl + 2 * kTile * 4;      // float [2][2][8]
+  static constexpr int kMode = kRed + 2 * 2 * 8 * 4;    // int [2][2]
+  static constexpr int kBars = kMode + 16;              // BwdBars
+  static constexpr int kMisc = kBars + ((int)(sizeof(BwdBars) + 15) / 16) * 16;  // tmem address, abort flag
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kDynSmem = kBytes;
 };
 
 // Column sums over the 32 lanes of a warp: on return lane l holds the sum over
@@ -102,14 +112,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const dm_diag diag) {
   using L = BwdLayout<D>;
   constexpr int DH = D / 2;  // d columns per compute warpgroup
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ BwdBars bars;
-  __shared__ float s_lse[2][kTile], s_dl[2][kTile];
-  __shared__ float s_red[2][2][8];
-  __shared__ int s_mode[2];
-  __shared__ uint32_t s_tmem;
-  __shared__ int s_abort;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
+  BwdBars& bars = *reinterpret_cast<BwdBars*>(sm + L::kBars);
+  float(*s_lse)[kTile] = reinterpret_cast<float(*)[kTile]>(sm + L::kLse);
+  float(*s_dl)[kTile] = reinterpret_cast<float(*)[kTile]>(sm + L::kDl);
+  float(*s_red)[2][8] = reinterpret_cast<float(*)[2][8]>(sm + L::kRed);
+  int(*s_mode)[2] = reinterpret_cast<int(*)[2]>(sm + L::kMode);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + L::kMisc);
+  int* s_abort = reinterpret_cast<int*>(sm + L::kMisc + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int BG = a.B * a.Hkv;
@@ -122,30 +133,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_iter = G * nq;
   const bool want_diag = diag.rowsum_pre || diag.abssum_pre || diag.rowsum_post || diag.abssum_post;
 
-  Watchdog wd{&s_abort, a.status, a.wait_limit_ns};
+  // The swizzled tiles need a 1024-byte aligned base; the window is expected
+  // to start aligned (no static shared variables).  Checked uniformly before
+  // anything is initialised: a misaligned window reports an error instead.
+  if (smem_u32(smem_raw) & 1023u) {
+    if (tid == 0) atomicCAS(a.status, 0u, (unsigned)DM_ERR_UNSUPPORTED);
+    return;
+  }
+  Watchdog wd{s_abort, a.status, a.wait_limit_ns};
   if (tid == 0) {
-    s_abort = 0;
+    *s_abort = 0;
     mbar_init(&bars.kv, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars.qfull[s], 1);
       mbar_init(&bars.qempty[s], 1);
+      mbar_init(&bars.sfull[s], 1);
+      mbar_init(&bars.sread[s], 8);
+      mbar_init(&bars.dpfull[s], 1);
+      mbar_init(&bars.bfree[s], 8);
     }
-    mbar_init(&bars.sfull, 1);
-    mbar_init(&bars.dpfull, 1);
     mbar_init(&bars.pds, 8);
     mbar_init(&bars.mma2, 1);
-    mbar_init(&bars.dqempty, 8);
     mbar_init(&bars.mma_done, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(&s_tmem, 512);
+    tmem_alloc(s_tmem, 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = s_tmem;
+  const uint32_t tmem = *s_tmem;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -154,6 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmDO);
+      tma_prefetch_desc(&tmDQ);
       mbar_arrive_expect_tx(&bars.kv, 2 * L::kTileBytes);
       tma_load_3d(sm + L::kK, &tmK, &bars.kv, 0, kt * kTile, bg);
       tma_load_3d(sm + L::kV, &tmV, &bars.kv, 0, kt * kTile, bg);
@@ -169,9 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sm + L::kDO + s * L::kTileBytes, &tmDO, &bars.qfull[s], 0, qt * kTile, bh);
         issued = n + 1;
       }
-      wait_drain(&bars.kv, 0, wd, 309);
-      for (int n = max(0, issued - 2); n < issued; ++n)
-        wait_drain(&bars.qfull[n & 1], (n >> 1) & 1, wd, 310);
+      wait_drain(&bars.kv, 0, wd, 302);
+      for (int n = max(0, issued - 2); n < issued; ++n) wait_drain(&bars.qfull[n & 1], (n >> 1) & 1, wd, 303);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer
@@ -182,28 +201,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdDK = idesc_f8(1, 0, 0, 1, kTile, D);      // dS^T (K-major) Q (MN-major)
       constexpr uint32_t kIdDQ = idesc_f8(1, 0, 1, 1, kTile, D);      // dS (MN-major) K (MN-major)
       const uint32_t sK = smem_u32(sm + L::kK), sV = smem_u32(sm + L::kV);
-      const uint32_t sPt = smem_u32(sm + L::kPt), sDSt = smem_u32(sm + L::kDSt);
-      bool ok = wait(&bars.kv, 0, wd, 302);
-      for (int n = 0; n < n_iter && ok; ++n) {
-        const int s = n & 1;
-        const uint32_t ph = (n >> 1) & 1;
-        const uint32_t sQ = smem_u32(sm + L::kQ + s * L::kTileBytes);
-        const uint32_t sDO = smem_u32(sm + L::kDO + s * L::kTileBytes);
-        if (!(ok = wait(&bars.qfull[s], ph, wd, 303))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < D / 32; ++k)
-          mma_f8(tmem + 0, SwTile<D>::kmajor(sK, k), SwTile<D>::kmajor(sQ, k), kIdS, k > 0);
-        mma_commit(&bars.sfull);
-        if (n >= 1 && !(ok = wait(&bars.dqempty, (n - 1) & 1, wd, 304))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < D / 32; ++k)
-          mma_f8(tmem + 128, SwTile<D>::kmajor(sV, k), SwTile<D>::kmajor(sDO, k), kIdDP, k > 0);
-        mma_commit(&bars.dpfull);
-        if (!(ok = wait(&bars.pds, n & 1, wd, 305))) break;
-        tc_fence_after();
-        const int mode_dv = s_mode[0], mode_dk = s_mode[1];
+      // dV, dK and dQ of iteration m (its work buffer now takes dQ)
+      auto tail = [&](int m) {
+        const int bm = m & 1;
+        const uint32_t sQ = smem_u32(sm + L::kQ + bm * L::kTileBytes);
+        const uint32_t sDO = smem_u32(sm + L::kDO + bm * L::kTileBytes);
+        const uint32_t sPt = smem_u32(sm + L::kPt + bm * kTile * kTile);
+        const uint32_t sDSt = smem_u32(sm + L::kDSt + bm * kTile * kTile);
+        const int mode_dv = s_mode[bm][0], mode_dk = s_mode[bm][1];
         if (mode_dv) {
 #pragma unroll
           for (int k = 0; k < kTile / 32; ++k)
@@ -218,12 +223,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int k = 0; k < kTile / 32; ++k)
-          mma_f8(tmem + 128, SwTile<128>::mnmajor(sDSt, k), SwTile<D>::mnmajor(sK, k), kIdDQ, k > 0);
+          mma_f8(tmem + bm * 128, SwTile<128>::mnmajor(sDSt, k), SwTile<D>::mnmajor(sK, k), kIdDQ, k > 0);
         mma_commit(&bars.mma2);
-        mma_commit(&bars.qempty[s]);
+        mma_commit(&bars.qempty[bm]);
+      };
+      bool ok = wait(&bars.kv, 0, wd, 304);
+      for (int n = 0; n < n_iter && ok; ++n) {
+        const int bn = n & 1;
+        const uint32_t ph = (n >> 1) & 1;
+        const uint32_t sQ = smem_u32(sm + L::kQ + bn * L::kTileBytes);
+        const uint32_t sDO = smem_u32(sm + L::kDO + bn * L::kTileBytes);
+        if (!(ok = wait(&bars.qfull[bn], ph, wd, 305))) break;
+        if (n >= 2 && !(ok = wait(&bars.bfree[bn], ph ^ 1, wd, 306))) break;  // dQ(n-2) drained
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k)
+          mma_f8(tmem + bn * 128, SwTile<D>::kmajor(sK, k), SwTile<D>::kmajor(sQ, k), kIdS, k > 0);
+        mma_commit(&bars.sfull[bn]);
+        if (n >= 1) {
+          if (!(ok = wait(&bars.pds, (n - 1) & 1, wd, 307))) break;
+          tc_fence_after();
+          tail(n - 1);
+        }
+        if (!(ok = wait(&bars.sread[bn], ph, wd, 308))) break;  // S(n) read: the buffer takes dP(n)
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k)
+          mma_f8(tmem + bn * 128, SwTile<D>::kmajor(sV, k), SwTile<D>::kmajor(sDO, k), kIdDP, k > 0);
+        mma_commit(&bars.dpfull[bn]);
+      }
+      if (ok && n_iter > 0 && wait(&bars.pds, (n_iter - 1) & 1, wd, 309)) {
+        tc_fence_after();
+        tail(n_iter - 1);
       }
       mma_commit(&bars.mma_done);
-      wait_drain(&bars.mma_done, 0, wd, 311);
+      wait_drain(&bars.mma_done, 0, wd, 310);
     }
   } else {
     // -------------------------------------------------------------- compute
@@ -248,25 +282,66 @@ __global__ void __launch_bounds__(kThreads, 1)
       return qi < a.N ? delta[(size_t)bh_n * a.N + qi] : 0.0f;
     };
     auto tile_index = [&](int n) { return (b * a.Hq + g * G + n / nq) * a.T + qt0 + n % nq; };
-    float pre_row = row_value(0);
-    float pre_sq = a.q_scales[tile_index(0)], pre_sdo = a.do_scales[tile_index(0)];
+    float pre_row = n_iter > 0 ? row_value(0) : 0.0f;
+    float pre_sq = n_iter > 0 ? a.q_scales[tile_index(0)] : 0.0f;
+    float pre_sdo = n_iter > 0 ? a.do_scales[tile_index(0)] : 0.0f;
+    float prev_cdq = 0.0f;  // dQ scale of the previous iteration, drained one iteration late
+
+    // dQ(m) (query rows on TMEM lanes of buffer m%2): scaled, staged in shared
+    // memory with the 128-byte swizzle of the dQ tensor map, then added into
+    // global dQ by one bulk reduce per 32-column box.  TMEM loads are
+    // warp-collective: every lane loads; rows beyond N are clipped by the map.
+    // The caller guarantees that the previous reduce has read the staging tile.
+    auto drain_dq = [&](int m, float cdq) {
+      const int bm = m & 1;
+      const int bh_m = b * a.Hq + g * G + m / nq;
+      const int qi0_m = (qt0 + m % nq) * kTile;
+      wait(&bars.mma2, m & 1, wd, 311);
+      tc_fence_after();
+      float v[DH];
+#pragma unroll
+      for (int c = 0; c < DH; c += 32)
+        tmem_ld32(tl + bm * 128 + wg * DH + c, *reinterpret_cast<float(*)[32]>(&v[c]));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.bfree[bm]);
+#pragma unroll
+      for (int c = 0; c < DH; c += 32) {
+        uint8_t* box = sm + L::kDQ + ((wg * DH + c) / 32) * (kTile * 128);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          *reinterpret_cast<float4*>(box + SwTile<128>::chunk_offset(r, e)) =
+              make_float4(v[c + 4 * e] * cdq, v[c + 4 * e + 1] * cdq, v[c + 4 * e + 2] * cdq,
+                          v[c + 4 * e + 3] * cdq);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(2, 256);
+      if (ct == 0 && cdq != 0.0f) {
+#pragma unroll
+        for (int bx = 0; bx < D / 32; ++bx)
+          tma_reduce_add_3d(&tmDQ, sm + L::kDQ + bx * (kTile * 128), bx * 32, qi0_m, bh_m);
+        bulk_commit();
+      }
+    };
 
     for (int n = 0; n < n_iter; ++n) {
       const int hh = n / nq, qt = qt0 + n % nq;
       const int bh = b * a.Hq + g * G + hh;
       const int qi0 = qt * kTile;
-      const int buf = n & 1;
+      const int bn = n & 1;
+      const uint32_t ph = (n >> 1) & 1;
       if (ct < 128)
-        s_lse[buf][ct] = pre_row * kLog2e;
+        s_lse[bn][ct] = pre_row * kLog2e;
       else
-        s_dl[buf][ct - 128] = pre_row;
+        s_dl[bn][ct - 128] = pre_row;
       const float sq = pre_sq, sdo = pre_sdo;
       if (n + 1 < n_iter) {
         pre_row = row_value(n + 1);
         pre_sq = a.q_scales[tile_index(n + 1)];
         pre_sdo = a.do_scales[tile_index(n + 1)];
       }
-      // the previous iteration's dQ reduce has finished reading the staging tile
+      // the previous dQ reduce has finished reading the staging tile
       if (ct == 0) bulk_wait_read_all();
       named_bar_sync(1, 256);
       const float c1 = a.sigma * sq * sk * kLog2e;
@@ -275,27 +350,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // P = exp(S - LSE), its tile amax and E4M3 codes
       float p[64];
-      wait(&bars.sfull, n & 1, wd, 306);
+      wait(&bars.sfull[bn], ph, wd, 312);
       tc_fence_after();
-      tmem_ld32(tl + wg * 64, *reinterpret_cast<float(*)[32]>(&p[0]));
-      tmem_ld32(tl + wg * 64 + 32, *reinterpret_cast<float(*)[32]>(&p[32]));
+      tmem_ld32(tl + bn * 128 + wg * 64, *reinterpret_cast<float(*)[32]>(&p[0]));
+      tmem_ld32(tl + bn * 128 + wg * 64 + 32, *reinterpret_cast<float(*)[32]>(&p[32]));
       tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.sread[bn]);
       float pmax = 0.0f;
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        p[c] = (c >= cmin) ? ex2(fmaf(p[c], c1, -s_lse[buf][wg * 64 + c])) : 0.0f;
+        p[c] = (c >= cmin) ? ex2(fmaf(p[c], c1, -s_lse[bn][wg * 64 + c])) : 0.0f;
         pmax = fmaxf(pmax, p[c]);
       }
       pmax = warp_max(pmax);
-      if (lane == 0) s_red[buf][0][warp - 2] = pmax;
+      if (lane == 0) s_red[bn][0][warp - 2] = pmax;
       named_bar_sync(1, 256);
-      float amax = s_red[buf][0][0];
+      float amax = s_red[bn][0][0];
 #pragma unroll
-      for (int w = 1; w < 8; ++w) amax = fmaxf(amax, s_red[buf][0][w]);
+      for (int w = 1; w < 8; ++w) amax = fmaxf(amax, s_red[bn][0][w]);
       float rp;
       const float sp = tile_scale<0>(amax, rp);
       {
-        uint8_t* dst = sm + L::kPt;
+        uint8_t* dst = sm + L::kPt + bn * kTile * kTile;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t w4[4];
@@ -309,32 +387,35 @@ __global__ void __launch_bounds__(kThreads, 1)
               make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
       }
+
+      // previous iteration's dQ; its completion also means dV/dK(n-1) are done
+      if (n >= 1) drain_dq(n - 1, prev_cdq);
       const int mode_dv = next_unit(unit_dv, sp * sdo, tl + 256 + wg * DH, DH);
 
       // dS = P (dP - delta), its tile amax and E5M2 codes
       float ds[64];
-      wait(&bars.dpfull, n & 1, wd, 307);
+      wait(&bars.dpfull[bn], ph, wd, 313);
       tc_fence_after();
-      tmem_ld32(tl + 128 + wg * 64, *reinterpret_cast<float(*)[32]>(&ds[0]));
-      tmem_ld32(tl + 128 + wg * 64 + 32, *reinterpret_cast<float(*)[32]>(&ds[32]));
+      tmem_ld32(tl + bn * 128 + wg * 64, *reinterpret_cast<float(*)[32]>(&ds[0]));
+      tmem_ld32(tl + bn * 128 + wg * 64 + 32, *reinterpret_cast<float(*)[32]>(&ds[32]));
       tmem_wait_ld();
       float dmax = 0.0f;
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        ds[c] = p[c] * fmaf(ds[c], cdp, -s_dl[buf][wg * 64 + c]);
+        ds[c] = p[c] * fmaf(ds[c], cdp, -s_dl[bn][wg * 64 + c]);
         dmax = fmaxf(dmax, fabsf(ds[c]));
       }
       dmax = warp_max(dmax);
-      if (lane == 0) s_red[buf][1][warp - 2] = dmax;
+      if (lane == 0) s_red[bn][1][warp - 2] = dmax;
       named_bar_sync(1, 256);
-      amax = s_red[buf][1][0];
+      amax = s_red[bn][1][0];
 #pragma unroll
-      for (int w = 1; w < 8; ++w) amax = fmaxf(amax, s_red[buf][1][w]);
+      for (int w = 1; w < 8; ++w) amax = fmaxf(amax, s_red[bn][1][w]);
       float rs;
       const float sds = tile_scale<1>(amax, rs);
       uint32_t dcode[16];
       {
-        uint8_t* dst = sm + L::kDSt;
+        uint8_t* dst = sm + L::kDSt + bn * kTile * kTile;
 #pragma unroll
         for (int c = 0; c < 16; ++c)
           dcode[c] = pack4_e5m2(__fmul_rn(ds[4 * c], rs), __fmul_rn(ds[4 * c + 1], rs), __fmul_rn(ds[4 * c + 2], rs),
@@ -346,9 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int mode_dk = next_unit(unit_dk, a.sigma * sds * sq, tl + 384 + wg * DH, DH);
       if (ct == 0) {
-        s_mode[0] = mode_dv;
-        s_mode[1] = mode_dk;
+        s_mode[bn][0] = mode_dv;
+        s_mode[bn][1] = mode_dk;
       }
+      prev_cdq = a.sigma * sds * sk;
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -396,42 +478,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-
-      // dQ tile (query rows on TMEM lanes): scaled, staged in shared memory with
-      // the 128-byte swizzle of the dQ tensor map, then added into global dQ
-      // by one bulk reduce per 32-column box.  TMEM loads are warp-collective:
-      // every lane loads; rows beyond N are clipped by the tensor map.
-      wait(&bars.mma2, n & 1, wd, 312);
-      tc_fence_after();
-      {
-        const float cdq = a.sigma * sds * sk;
-        float v[DH];
-#pragma unroll
-        for (int c = 0; c < DH; c += 32) tmem_ld32(tl + 128 + wg * DH + c, *reinterpret_cast<float(*)[32]>(&v[c]));
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.dqempty);
-#pragma unroll
-        for (int c = 0; c < DH; c += 32) {
-          uint8_t* box = sm + L::kDQ + ((wg * DH + c) / 32) * (kTile * 128);
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            *reinterpret_cast<float4*>(box + SwTile<128>::chunk_offset(r, e)) =
-                make_float4(v[c + 4 * e] * cdq, v[c + 4 * e + 1] * cdq, v[c + 4 * e + 2] * cdq,
-                            v[c + 4 * e + 3] * cdq);
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(2, 256);
-        if (ct == 0 && cdq != 0.0f) {
-#pragma unroll
-          for (int bx = 0; bx < D / 32; ++bx)
-            tma_reduce_add_3d(&tmDQ, sm + L::kDQ + bx * (kTile * 128), bx * 32, qi0, bh);
-          bulk_commit();
-        }
-      }
     }
-
+    if (n_iter > 0) {
+      if (ct == 0) bulk_wait_read_all();
+      named_bar_sync(1, 256);
+      drain_dq(n_iter - 1, prev_cdq);
+    }
     if (ct == 0) bulk_wait_all();
 
     // epilogue: dV and dK rows of this key tile, in true units (an
@@ -472,6 +524,7 @@ template <int D>
 cudaError_t launch_t(const BwdLaunch& f, cudaStream_t st) {
   auto k = attn_bwd_kernel<D>;
   constexpr int smem = BwdLayout<D>::kDynSmem;
+  static_assert(smem <= 232448, "backward shared memory exceeds the per-block limit");
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(f.args.B * f.args.Hkv * f.args.T);
