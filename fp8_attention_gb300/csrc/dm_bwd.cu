@@ -298,23 +298,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qi0_m = (qt0 + m % nq) * kTile;
       wait(&bars.mma2, m & 1, wd, 311);
       tc_fence_after();
-      float v[DH];
+      // 32 columns at a time (the P registers of the current iteration are live)
 #pragma unroll
-      for (int c = 0; c < DH; c += 32)
-        tmem_ld32(tl + bm * 128 + wg * DH + c, *reinterpret_cast<float(*)[32]>(&v[c]));
-      tmem_wait_ld();
+      for (int c = 0; c < DH; c += 32) {
+        float v[32];
+        tmem_ld32(tl + bm * 128 + wg * DH + c, v);
+        tmem_wait_ld();
+        uint8_t* box = sm + L::kDQ + ((wg * DH + c) / 32) * (kTile * 128);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float2 a01 = __fmul2_rn(make_float2(v[4 * e], v[4 * e + 1]), make_float2(cdq, cdq));
+          const float2 a23 = __fmul2_rn(make_float2(v[4 * e + 2], v[4 * e + 3]), make_float2(cdq, cdq));
+          *reinterpret_cast<float4*>(box + SwTile<128>::chunk_offset(r, e)) = make_float4(a01.x, a01.y, a23.x, a23.y);
+        }
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.bfree[bm]);
-#pragma unroll
-      for (int c = 0; c < DH; c += 32) {
-        uint8_t* box = sm + L::kDQ + ((wg * DH + c) / 32) * (kTile * 128);
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          *reinterpret_cast<float4*>(box + SwTile<128>::chunk_offset(r, e)) =
-              make_float4(v[c + 4 * e] * cdq, v[c + 4 * e + 1] * cdq, v[c + 4 * e + 2] * cdq,
-                          v[c + 4 * e + 3] * cdq);
-      }
       fence_proxy_async_smem();
       named_bar_sync(2, 256);
       if (ct == 0 && cdq != 0.0f) {
@@ -332,9 +332,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int bn = n & 1;
       const uint32_t ph = (n >> 1) & 1;
       if (ct < 128)
-        s_lse[bn][ct] = pre_row * kLog2e;
+        s_lse[bn][ct] = -pre_row * kLog2e;  // stored negated: one packed FMA per pair below
       else
-        s_dl[bn][ct - 128] = pre_row;
+        s_dl[bn][ct - 128] = -pre_row;
       const float sq = pre_sq, sdo = pre_sdo;
       if (n + 1 < n_iter) {
         pre_row = row_value(n + 1);
@@ -358,12 +358,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.sread[bn]);
-      float pmax = 0.0f;
+      const float2 c1_2 = make_float2(c1, c1);
+      const float2* nlse2 = reinterpret_cast<const float2*>(&s_lse[bn][wg * 64]);
+      float pm0 = 0.0f, pm1 = 0.0f;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        p[c] = (c >= cmin) ? ex2(fmaf(p[c], c1, -s_lse[bn][wg * 64 + c])) : 0.0f;
-        pmax = fmaxf(pmax, p[c]);
+      for (int c = 0; c < 64; c += 2) {
+        const float2 x = __ffma2_rn(make_float2(p[c], p[c + 1]), c1_2, nlse2[c / 2]);
+        p[c] = ex2(x.x);
+        p[c + 1] = ex2(x.y);
       }
+      if (cmin > 0) {  // diagonal tile or absent key row: mask
+#pragma unroll
+        for (int c = 0; c < 64; ++c) p[c] = c >= cmin ? p[c] : 0.0f;
+      }
+#pragma unroll
+      for (int c = 0; c < 64; c += 2) {
+        pm0 = fmaxf(pm0, p[c]);
+        pm1 = fmaxf(pm1, p[c + 1]);
+      }
+      float pmax = fmaxf(pm0, pm1);
       pmax = warp_max(pmax);
       if (lane == 0) s_red[bn][0][warp - 2] = pmax;
       named_bar_sync(1, 256);
@@ -380,8 +393,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float* q4 = &p[16 * c + 4 * e];
-            w4[e] = pack4_e4m3(__fmul_rn(q4[0], rp), __fmul_rn(q4[1], rp), __fmul_rn(q4[2], rp),
-                               __fmul_rn(q4[3], rp));
+            const float2 a01 = __fmul2_rn(make_float2(q4[0], q4[1]), make_float2(rp, rp));
+            const float2 a23 = __fmul2_rn(make_float2(q4[2], q4[3]), make_float2(rp, rp));
+            w4[e] = pack4_e4m3(a01.x, a01.y, a23.x, a23.y);
           }
           *reinterpret_cast<uint4*>(dst + SwTile<128>::chunk_offset(r, wg * 4 + c)) =
               make_uint4(w4[0], w4[1], w4[2], w4[3]);
@@ -392,19 +406,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n >= 1) drain_dq(n - 1, prev_cdq);
       const int mode_dv = next_unit(unit_dv, sp * sdo, tl + 256 + wg * DH, DH);
 
-      // dS = P (dP - delta), its tile amax and E5M2 codes
-      float ds[64];
+      // dS = P (dP - delta), computed in place over p (P in FP32 is not needed
+      // once its codes are written), its tile amax and E5M2 codes
+      float* ds = p;
       wait(&bars.dpfull[bn], ph, wd, 313);
       tc_fence_after();
-      tmem_ld32(tl + bn * 128 + wg * 64, *reinterpret_cast<float(*)[32]>(&ds[0]));
-      tmem_ld32(tl + bn * 128 + wg * 64 + 32, *reinterpret_cast<float(*)[32]>(&ds[32]));
-      tmem_wait_ld();
-      float dmax = 0.0f;
+      const float2 cdp2 = make_float2(cdp, cdp);
+      const float2* ndl2 = reinterpret_cast<const float2*>(&s_dl[bn][wg * 64]);
+      float dm0 = 0.0f, dm1 = 0.0f;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        ds[c] = p[c] * fmaf(ds[c], cdp, -s_dl[bn][wg * 64 + c]);
-        dmax = fmaxf(dmax, fabsf(ds[c]));
+      for (int h = 0; h < 2; ++h) {
+        float dp[32];
+        tmem_ld32(tl + bn * 128 + wg * 64 + h * 32, dp);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const int cc = h * 32 + c;
+          const float2 d2 = __fmul2_rn(make_float2(p[cc], p[cc + 1]),
+                                       __ffma2_rn(make_float2(dp[c], dp[c + 1]), cdp2, ndl2[cc / 2]));
+          ds[cc] = d2.x;
+          ds[cc + 1] = d2.y;
+          dm0 = fmaxf(dm0, fabsf(d2.x));
+          dm1 = fmaxf(dm1, fabsf(d2.y));
+        }
       }
+      float dmax = fmaxf(dm0, dm1);
       dmax = warp_max(dmax);
       if (lane == 0) s_red[bn][1][warp - 2] = dmax;
       named_bar_sync(1, 256);
@@ -417,9 +443,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         uint8_t* dst = sm + L::kDSt + bn * kTile * kTile;
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          dcode[c] = pack4_e5m2(__fmul_rn(ds[4 * c], rs), __fmul_rn(ds[4 * c + 1], rs), __fmul_rn(ds[4 * c + 2], rs),
-                                __fmul_rn(ds[4 * c + 3], rs));
+        for (int c = 0; c < 16; ++c) {
+          const float2 a01 = __fmul2_rn(make_float2(ds[4 * c], ds[4 * c + 1]), make_float2(rs, rs));
+          const float2 a23 = __fmul2_rn(make_float2(ds[4 * c + 2], ds[4 * c + 3]), make_float2(rs, rs));
+          dcode[c] = pack4_e5m2(a01.x, a01.y, a23.x, a23.y);
+        }
 #pragma unroll
         for (int c = 0; c < 4; ++c)
           *reinterpret_cast<uint4*>(dst + SwTile<128>::chunk_offset(r, wg * 4 + c)) =

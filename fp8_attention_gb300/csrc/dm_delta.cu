@@ -186,18 +186,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.tempty[s]);
-      float part0 = 0.0f, part1 = 0.0f, ps0 = 0.0f, ps1 = 0.0f;
+      // P = exp2(S c1 - LSE log2e) on packed pairs; masks only on the
+      // diagonal or ragged tile
+      const bool full = jlim >= 64;
+      const float2 c1_2 = make_float2(c1, c1), nl2 = make_float2(-lse2, -lse2);
+      float2 acc0 = make_float2(0.0f, 0.0f), acc1 = acc0, ps0 = acc0, ps1 = acc0;
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        const float p0 = (c < jlim) ? ex2(fmaf(sv[c], c1, -lse2)) : 0.0f;
-        const float p1 = (c + 1 < jlim) ? ex2(fmaf(sv[c + 1], c1, -lse2)) : 0.0f;
-        part0 = fmaf(p0, dp[c], part0);
-        part1 = fmaf(p1, dp[c + 1], part1);
-        ps0 += p0;
-        ps1 += p1;
+      for (int c = 0; c < 64; c += 4) {
+        const float2 x0 = __ffma2_rn(make_float2(sv[c], sv[c + 1]), c1_2, nl2);
+        const float2 x1 = __ffma2_rn(make_float2(sv[c + 2], sv[c + 3]), c1_2, nl2);
+        float2 p0 = make_float2(ex2(x0.x), ex2(x0.y)), p1 = make_float2(ex2(x1.x), ex2(x1.y));
+        if (!full) {
+          p0.x = c < jlim ? p0.x : 0.0f;
+          p0.y = c + 1 < jlim ? p0.y : 0.0f;
+          p1.x = c + 2 < jlim ? p1.x : 0.0f;
+          p1.y = c + 3 < jlim ? p1.y : 0.0f;
+        }
+        acc0 = __ffma2_rn(p0, make_float2(dp[c], dp[c + 1]), acc0);
+        acc1 = __ffma2_rn(p1, make_float2(dp[c + 2], dp[c + 3]), acc1);
+        ps0 = __fadd2_rn(ps0, p0);
+        ps1 = __fadd2_rn(ps1, p1);
       }
-      dl = fmaf(part0 + part1, c2, dl);
-      psum += ps0 + ps1;
+      dl = fmaf((acc0.x + acc0.y) + (acc1.x + acc1.y), c2, dl);
+      psum += (ps0.x + ps0.y) + (ps1.x + ps1.y);
     }
     if (wg == 1) {
       s_part[row] = dl;

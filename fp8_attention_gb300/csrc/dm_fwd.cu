@@ -6,14 +6,17 @@
 //   warp 0      TMA producer: Q tile once, K/V tiles double-buffered
 //   warp 1      MMA issuer (+ TMEM owner): S(t) = Q K_t^T into TMEM S[t%2];
 //               O_t = P^_t V_t into TMEM O[t%2]
-//   warps 2-5   softmax: one thread per query row; online row max, P~ in FP32,
-//               per-tile amax -> E4M3 codes written to shared memory
-//   warps 6-9   correction: O accumulated in registers in true units,
-//               acc = alpha * acc + (s_P * s_V) * O_t, then O / l
+//   warps 2-9   two warpgroups; thread = query row (TMEM lane), warpgroup =
+//               half of the key columns for the softmax and half of the d
+//               columns for O.  Per key tile t: online row max (the halves
+//               exchange partial maxima through shared memory), P~ in FP32,
+//               the tile's amax -> E4M3 codes into shared memory; then, one
+//               tile behind, O_acc = alpha * O_acc + (s_P * s_V) * O_{t-1} in
+//               registers, in true units.
 //
-// Each key tile t brings its own FP32 scale product s_P,t * s_V,t, so the
-// tiles' products are summed outside the tensor core; the S/O double buffers
-// let S(t+1) run on the tensor core while the softmax works on S(t).
+// Each key tile brings its own FP32 scale product s_P,t * s_V,t, so the
+// tiles' products are summed outside the tensor core.  The O update lags one
+// tile: it runs while the tensor core computes the next S and P V products.
 //
 // TMEM columns (512 allocated): S[0] 0-127, S[1] 128-255, O[0] 256.., O[1] 384..
 #include <cuda_bf16.h>
@@ -29,20 +32,26 @@ constexpr int kThreads = 320;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+struct FwdBars {
+  uint64_t q, kfull[2], kempty[2], vfull[2], vempty[2], sfull[2], sempty[2], pfull[2], ofull[2], oempty[2],
+      stall, mma_done;
+};
+
+// Everything lives in dynamic shared memory (no static shared variables), so
+// the 1024-byte aligned tile region starts at the window's base.
 template <int D>
 struct FwdLayout {
   static constexpr int kTileBytes = kTile * D;  // one FP8 Q/K/V tile
   static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTileBytes;           // 2 stages
-  static constexpr int kV = kK + 2 * kTileBytes;       // 2 stages
-  static constexpr int kP = kV + 2 * kTileBytes;       // 2 x (128 x 128) P^ codes
-  static constexpr int kBytes = kP + 2 * kTile * kTile;
-  static constexpr int kDynSmem = kBytes + 1024;       // + alignment slack
-};
-
-struct FwdBars {
-  uint64_t q, kfull[2], kempty[2], vfull[2], vempty[2], sfull[2], sempty[2], pfull[2], ofull[2], oempty[2],
-      fin, stall, mma_done;
+  static constexpr int kK = kQ + kTileBytes;              // 2 stages
+  static constexpr int kV = kK + 2 * kTileBytes;          // 2 stages
+  static constexpr int kP = kV + 2 * kTileBytes;          // 2 x (128 x 128) P^ codes
+  static constexpr int kRmax = kP + 2 * kTile * kTile;    // float [2][2][128] partial row maxima
+  static constexpr int kRed = kRmax + 2 * 2 * kTile * 4;  // float [2][8] tile amax partials
+  static constexpr int kL = kRed + 2 * 8 * 4;             // float [128] row sums
+  static constexpr int kBars = kL + kTile * 4;
+  static constexpr int kMisc = kBars + ((int)(sizeof(FwdBars) + 15) / 16) * 16;  // tmem address, abort flag
+  static constexpr int kBytes = kMisc + 16;
 };
 
 template <int D, bool OUT_BF16>
@@ -51,15 +60,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tmV, const AttnArgs a, void* __restrict__ O,
                     float* __restrict__ lse) {
   using L = FwdLayout<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ FwdBars bars;
-  __shared__ float s_alpha[2][kTile];
-  __shared__ float s_cs[2];
-  __shared__ float s_linv[kTile];
-  __shared__ float s_red[2][4];
-  __shared__ uint32_t s_tmem;
-  __shared__ int s_abort;
+  constexpr int DH = D / 2;  // O columns per warpgroup
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
+  FwdBars& bars = *reinterpret_cast<FwdBars*>(sm + L::kBars);
+  float(*s_rmax)[2][kTile] = reinterpret_cast<float(*)[2][kTile]>(sm + L::kRmax);
+  float(*s_red)[8] = reinterpret_cast<float(*)[8]>(sm + L::kRed);
+  float* s_l = reinterpret_cast<float*>(sm + L::kL);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + L::kMisc);
+  int* s_abort = reinterpret_cast<int*>(sm + L::kMisc + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int BH = a.B * a.Hq;
@@ -70,9 +79,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q0 = qt * kTile;
   const int nkv = a.causal ? qt + 1 : a.T;
 
-  Watchdog wd{&s_abort, a.status, a.wait_limit_ns};
+  // the swizzled tiles need a 1024-byte aligned window (no static shared variables)
+  if (smem_u32(smem_raw) & 1023u) {
+    if (tid == 0) atomicCAS(a.status, 0u, (unsigned)DM_ERR_UNSUPPORTED);
+    return;
+  }
+  Watchdog wd{s_abort, a.status, a.wait_limit_ns};
   if (tid == 0) {
-    s_abort = 0;
+    *s_abort = 0;
     mbar_init(&bars.q, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars.kfull[s], 1);
@@ -80,24 +94,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.vfull[s], 1);
       mbar_init(&bars.vempty[s], 1);
       mbar_init(&bars.sfull[s], 1);
-      mbar_init(&bars.sempty[s], 4);
-      mbar_init(&bars.pfull[s], 4);
+      mbar_init(&bars.sempty[s], 8);
+      mbar_init(&bars.pfull[s], 8);
       mbar_init(&bars.ofull[s], 1);
-      mbar_init(&bars.oempty[s], 4);
+      mbar_init(&bars.oempty[s], 8);
     }
-    mbar_init(&bars.fin, 4);
     mbar_init(&bars.stall, 1);
     mbar_init(&bars.mma_done, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(&s_tmem, 512);
+    tmem_alloc(s_tmem, 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = s_tmem;
+  const uint32_t tmem = *s_tmem;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -153,7 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t >= 1) {
           const int u = t - 1, s = u & 1;
           const uint32_t ph = (u >> 1) & 1;
-          ok = wait(&bars.pfull[s], ph, wd, 107) && wait(&bars.vfull[s], ph, wd, 108) && wait(&bars.oempty[s], ph ^ 1, wd, 109);
+          ok = wait(&bars.pfull[s], ph, wd, 107) && wait(&bars.vfull[s], ph, wd, 108) &&
+               wait(&bars.oempty[s], ph ^ 1, wd, 109);
           if (!ok) break;
           tc_fence_after();
           const uint32_t sP = smem_u32(sm + L::kP + s * kTile * kTile);
@@ -168,8 +182,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bars.mma_done);
       wait_drain(&bars.mma_done, 0, wd, 119);
     }
-  } else if (warp < 6) {
-    // -------------------------------------------------------------- softmax
+  } else {
+    // ------------------------------------------------ softmax and O update
+    const int wg = (warp - 2) >> 2;  // key-column half and O-column half
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const int qi = q0 + row;
@@ -179,7 +194,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float* ksc = a.k_scales + (size_t)bg * a.T;
     const float* vsc = a.v_scales + (size_t)bg * a.T;
     float sk_next = ksc[0], sv_next = vsc[0];  // per-tile scales, loaded one tile ahead
-    float m = -INFINITY, l = 0.0f;  // running max (log2 units) and row sum
+    float m = -INFINITY, l = 0.0f;             // running max (log2 units), row sum of this half
+    float2 acc[DH / 2];                        // O in true units, packed pairs of d columns
+#pragma unroll
+    for (int k = 0; k < DH / 2; ++k) acc[k] = make_float2(0.0f, 0.0f);
+    float alpha_prev = 0.0f, c_prev = 0.0f;    // the previous tile's rescale and scale product
+
+    // O_acc = alpha * O_acc + c * O_u over this warpgroup's d columns
+    auto update_o = [&](int u, float alpha, float c) {
+      const int su = u & 1;
+      wait(&bars.ofull[su], (u >> 1) & 1, wd, 114);
+      tc_fence_after();
+      const float2 a2 = make_float2(alpha, alpha), c2 = make_float2(c, c);
+#pragma unroll
+      for (int cc = 0; cc < DH; cc += 32) {
+        float v[32];
+        tmem_ld32(tl + 256 + su * 128 + wg * DH + cc, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 32; k += 2)
+          acc[(cc + k) / 2] = __ffma2_rn(c2, make_float2(v[k], v[k + 1]), __fmul2_rn(a2, acc[(cc + k) / 2]));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.oempty[su]);
+    };
+
     for (int t = 0; t < nkv; ++t) {
       const int s = t & 1;
       const uint32_t ph = (t >> 1) & 1;
@@ -189,119 +229,122 @@ __global__ void __launch_bounds__(kThreads, 1)
         sk_next = ksc[t + 1];
         sv_next = vsc[t + 1];
       }
-      const int j0 = t * kTile;
-      int jlim = min(kTile, a.N - j0);
+      const int j0 = t * kTile + wg * 64;
+      int jlim = min(64, a.N - j0);
       if (a.causal) jlim = min(jlim, qi - j0 + 1);
 
       wait(&bars.sfull[s], ph, wd, 110);
       tc_fence_after();
-      float v[kTile];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tl + s * 128 + c * 32, *reinterpret_cast<float(*)[32]>(&v[c * 32]));
+      float v[64];
+      tmem_ld32(tl + s * 128 + wg * 64, *reinterpret_cast<float(*)[32]>(&v[0]));
+      tmem_ld32(tl + s * 128 + wg * 64 + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.sempty[s]);
 
+      // row max over both halves (raw units; c1 > 0 preserves the order)
+      const bool full = jlim >= 64;  // no masked column in this half (all but the diagonal/ragged tile)
       float mx = -INFINITY;
+      if (full) {
+        float m4[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
-      for (int c = 0; c < kTile; ++c)
-        if (c < jlim) mx = fmaxf(mx, v[c]);
-      const float tmax = mx * c1;
+        for (int c = 4; c < 64; ++c) m4[c & 3] = fmaxf(m4[c & 3], v[c]);
+        mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c < jlim) mx = fmaxf(mx, v[c]);
+      }
+      s_rmax[s][wg][row] = mx;
+      named_bar_sync(1, 256);
+      const float tmax = fmaxf(mx, s_rmax[s][wg ^ 1][row]) * c1;
       const float m_new = fmaxf(m, tmax);
       // amax of this tile of P~ = max over its rows of exp2(tile row max - running max)
       float arow = row_valid ? ex2(tmax - m_new) : 0.0f;
       arow = warp_max(arow);
-      if (lane == 0) s_red[s][quarter] = arow;
-      named_bar_sync(1, 128);
-      const float amax = fmaxf(fmaxf(s_red[s][0], s_red[s][1]), fmaxf(s_red[s][2], s_red[s][3]));
+      if (lane == 0) s_red[s][warp - 2] = arow;
+      named_bar_sync(1, 256);
+      float amax = s_red[s][0];
+#pragma unroll
+      for (int w = 1; w < 8; ++w) amax = fmaxf(amax, s_red[s][w]);
       float r;
       const float sp = tile_scale<0>(amax, r);
-
       const float alpha = ex2(m - m_new);
-      float rowsum = 0.0f;
-      uint32_t packed[kTile / 4];
-#pragma unroll
-      for (int c = 0; c < kTile; c += 4) {
-        float p[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) p[k] = (c + k < jlim) ? ex2(fmaf(v[c + k], c1, -m_new)) : 0.0f;
-        rowsum += (p[0] + p[1]) + (p[2] + p[3]);
-        packed[c / 4] = pack4_e4m3(__fmul_rn(p[0], r), __fmul_rn(p[1], r), __fmul_rn(p[2], r), __fmul_rn(p[3], r));
-      }
-      l = alpha * l + rowsum;
-      m = m_new;
 
-      if (t >= 2) {
-        wait(&bars.ofull[s], ph ^ 1, wd, 111);   // PV(t-2) has read P buffer s
-        wait(&bars.oempty[s], ph ^ 1, wd, 112);  // correction has read alpha/cs of t-2
-      }
+      // P~ r = exp2(S c1 - m + log2 r) straight into E4M3 codes (P buffer s;
+      // its last reader, the P V product of tile t-2, completed before this
+      // thread's O update of tile t-2); the unquantised row sum of this half
+      // is sum(P~ r) * s_P.  A flushed tile (r = 0) gives codes 0.
+      const float bias = (r > 0.0f ? __log2f(r) : -INFINITY) - m_new;
+      const float2 c1_2 = make_float2(c1, c1), b2 = make_float2(bias, bias);
+      float2 rs2 = make_float2(0.0f, 0.0f);
       uint8_t* sP = sm + L::kP + s * kTile * kTile;
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(sP + SwTile<128>::chunk_offset(row, c)) =
-            make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
-      s_alpha[s][row] = alpha;
-      if (row == 0) s_cs[s] = sp * sv;
+      for (int c = 0; c < 64; c += 16) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int cc = c + 4 * e;
+          const float2 x01 = __ffma2_rn(make_float2(v[cc], v[cc + 1]), c1_2, b2);
+          const float2 x23 = __ffma2_rn(make_float2(v[cc + 2], v[cc + 3]), c1_2, b2);
+          float2 q01 = make_float2(ex2(x01.x), ex2(x01.y)), q23 = make_float2(ex2(x23.x), ex2(x23.y));
+          if (!full) {
+            q01.x = cc < jlim ? q01.x : 0.0f;
+            q01.y = cc + 1 < jlim ? q01.y : 0.0f;
+            q23.x = cc + 2 < jlim ? q23.x : 0.0f;
+            q23.y = cc + 3 < jlim ? q23.y : 0.0f;
+          }
+          rs2 = __fadd2_rn(rs2, __fadd2_rn(q01, q23));
+          w4[e] = pack4_e4m3(q01.x, q01.y, q23.x, q23.y);
+        }
+        *reinterpret_cast<uint4*>(sP + SwTile<128>::chunk_offset(row, wg * 4 + c / 16)) =
+            make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      }
+      l = alpha * l + (rs2.x + rs2.y) * sp;
+      m = m_new;
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.pfull[s]);
+
+      // O update for the previous tile, while the tensor core works on this one
+      if (t >= 1) update_o(t - 1, alpha_prev, c_prev);
+      alpha_prev = alpha;
+      c_prev = sp * sv;
     }
-    if (row_valid) lse[(size_t)bh * a.N + qi] = m * kLn2 + logf(l);
-    s_linv[row] = 1.0f / l;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bars.fin);
-  } else {
-    // ----------------------------------------------------------- correction
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    const int qi = q0 + row;
-    const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-    float acc[D];
-#pragma unroll
-    for (int k = 0; k < D; ++k) acc[k] = 0.0f;
-    for (int t = 0; t < nkv; ++t) {
-      const int s = t & 1;
-      const uint32_t ph = (t >> 1) & 1;
-      wait(&bars.pfull[s], ph, wd, 113);
-      wait(&bars.ofull[s], ph, wd, 114);
-      tc_fence_after();
-      const float alpha = s_alpha[s][row];
-      const float cs = s_cs[s];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float v[32];
-        tmem_ld32(tl + 256 + s * 128 + c * 32, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 32; ++k) acc[c * 32 + k] = fmaf(cs, v[k], alpha * acc[c * 32 + k]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.oempty[s]);
+    update_o(nkv - 1, alpha_prev, c_prev);
+
+    // row sum over both halves, LSE, and O / l
+    if (wg == 1) s_l[row] = l;
+    named_bar_sync(1, 256);
+    if (wg == 0) {
+      const float lt = l + s_l[row];
+      s_l[row] = lt;
+      if (row_valid) lse[(size_t)bh * a.N + qi] = m * kLn2 + logf(lt);
     }
-    wait(&bars.fin, 0, wd, 115);
-    const float linv = s_linv[row];
-    if (qi < a.N) {
+    named_bar_sync(1, 256);
+    const float linv = 1.0f / s_l[row];
+    if (row_valid) {
       if (OUT_BF16) {
-        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(O) + ((size_t)bh * a.N + qi) * D;
+        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(O) + ((size_t)bh * a.N + qi) * D + wg * DH;
 #pragma unroll
-        for (int k = 0; k < D; k += 8) {
+        for (int k = 0; k < DH; k += 8) {
           uint4 w;
           uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[k + 2 * e] * linv, acc[k + 2 * e + 1] * linv);
+            const float2 x = acc[k / 2 + e];
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(x.x * linv, x.y * linv);
             wp[e] = *reinterpret_cast<uint32_t*>(&h2);
           }
           *reinterpret_cast<uint4*>(o + k) = w;
         }
       } else {
-        float* o = reinterpret_cast<float*>(O) + ((size_t)bh * a.N + qi) * D;
+        float* o = reinterpret_cast<float*>(O) + ((size_t)bh * a.N + qi) * D + wg * DH;
 #pragma unroll
-        for (int k = 0; k < D; k += 4)
-          *reinterpret_cast<float4*>(o + k) =
-              make_float4(acc[k] * linv, acc[k + 1] * linv, acc[k + 2] * linv, acc[k + 3] * linv);
+        for (int k = 0; k < DH; k += 4)
+          *reinterpret_cast<float4*>(o + k) = make_float4(acc[k / 2].x * linv, acc[k / 2].y * linv,
+                                                          acc[k / 2 + 1].x * linv, acc[k / 2 + 1].y * linv);
       }
     }
   }
@@ -317,7 +360,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, bool BF16>
 cudaError_t launch_fwd_t(const FwdLaunch& f, cudaStream_t st) {
   auto k = attn_fwd_kernel<D, BF16>;
-  constexpr int smem = FwdLayout<D>::kDynSmem;
+  constexpr int smem = FwdLayout<D>::kBytes;
+  static_assert(smem <= 232448, "forward shared memory exceeds the per-block limit");
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(f.args.B * f.args.Hq * f.args.T);
