@@ -84,7 +84,11 @@ __device__ __forceinline__ void tmem_scale(uint32_t taddr, int ncols, float f) {
     tmem_ld32(taddr + c, v);
     tmem_wait_ld();
 #pragma unroll
-    for (int k = 0; k < 32; ++k) v[k] *= f;
+    for (int k = 0; k < 32; k += 2) {
+      const float2 x = __fmul2_rn(make_float2(v[k], v[k + 1]), make_float2(f, f));
+      v[k] = x.x;
+      v[k + 1] = x.y;
+    }
     tmem_st32(taddr + c, v);
   }
   tmem_wait_st();
@@ -178,11 +182,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_3d(sm + L::kK, &tmK, &bars.kv, 0, kt * kTile, bg);
       tma_load_3d(sm + L::kV, &tmV, &bars.kv, 0, kt * kTile, bg);
       int issued = 0;
+      int bh = b * a.Hq + g * G, qt = qt0;  // (query head, query tile) of iteration n
       for (int n = 0; n < n_iter; ++n) {
         const int s = n & 1;
         const uint32_t ph = (n >> 1) & 1;
-        const int bh = b * a.Hq + g * G + n / nq;
-        const int qt = qt0 + n % nq;
+        if (n > 0 && ++qt == a.T) {
+          qt = qt0;
+          ++bh;
+        }
         if (!wait(&bars.qempty[s], ph ^ 1, wd, 301)) break;
         mbar_arrive_expect_tx(&bars.qfull[s], 2 * L::kTileBytes);
         tma_load_3d(sm + L::kQ + s * L::kTileBytes, &tmQ, &bars.qfull[s], 0, qt * kTile, bh);
@@ -275,27 +282,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     // thread's element of the query tile's LSE (threads 0-127; +inf for absent
     // rows) or delta (threads 128-255; 0 for absent rows), and the tile's Q and
     // dO scales.
-    auto row_value = [&](int n) -> float {
-      const int bh_n = b * a.Hq + g * G + n / nq;
-      const int qi = (qt0 + n % nq) * kTile + (ct & 127);
+    auto row_value = [&](int bh_n, int qt_n) -> float {
+      const int qi = qt_n * kTile + (ct & 127);
       if (ct < 128) return qi < a.N ? lse[(size_t)bh_n * a.N + qi] : INFINITY;
       return qi < a.N ? delta[(size_t)bh_n * a.N + qi] : 0.0f;
     };
-    auto tile_index = [&](int n) { return (b * a.Hq + g * G + n / nq) * a.T + qt0 + n % nq; };
-    float pre_row = n_iter > 0 ? row_value(0) : 0.0f;
-    float pre_sq = n_iter > 0 ? a.q_scales[tile_index(0)] : 0.0f;
-    float pre_sdo = n_iter > 0 ? a.do_scales[tile_index(0)] : 0.0f;
+    // (query head, query tile) of the current and of the next iteration
+    int bh = b * a.Hq + g * G, qt = qt0;
+    int bh_next = bh, qt_next = qt;
+    float pre_row = n_iter > 0 ? row_value(bh, qt) : 0.0f;
+    float pre_sq = n_iter > 0 ? a.q_scales[bh * a.T + qt] : 0.0f;
+    float pre_sdo = n_iter > 0 ? a.do_scales[bh * a.T + qt] : 0.0f;
     float prev_cdq = 0.0f;  // dQ scale of the previous iteration, drained one iteration late
+    int prev_bh = bh, prev_qi0 = qt * kTile;  // where the previous iteration's dQ goes
 
     // dQ(m) (query rows on TMEM lanes of buffer m%2): scaled, staged in shared
     // memory with the 128-byte swizzle of the dQ tensor map, then added into
     // global dQ by one bulk reduce per 32-column box.  TMEM loads are
     // warp-collective: every lane loads; rows beyond N are clipped by the map.
     // The caller guarantees that the previous reduce has read the staging tile.
-    auto drain_dq = [&](int m, float cdq) {
+    auto drain_dq = [&](int m, float cdq, int bh_m, int qi0_m) {
       const int bm = m & 1;
-      const int bh_m = b * a.Hq + g * G + m / nq;
-      const int qi0_m = (qt0 + m % nq) * kTile;
       wait(&bars.mma2, m & 1, wd, 311);
       tc_fence_after();
       // 32 columns at a time (the P registers of the current iteration are live)
@@ -326,8 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     for (int n = 0; n < n_iter; ++n) {
-      const int hh = n / nq, qt = qt0 + n % nq;
-      const int bh = b * a.Hq + g * G + hh;
+      bh = bh_next;
+      qt = qt_next;
       const int qi0 = qt * kTile;
       const int bn = n & 1;
       const uint32_t ph = (n >> 1) & 1;
@@ -337,9 +344,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_dl[bn][ct - 128] = -pre_row;
       const float sq = pre_sq, sdo = pre_sdo;
       if (n + 1 < n_iter) {
-        pre_row = row_value(n + 1);
-        pre_sq = a.q_scales[tile_index(n + 1)];
-        pre_sdo = a.do_scales[tile_index(n + 1)];
+        if (++qt_next == a.T) {
+          qt_next = qt0;
+          ++bh_next;
+        }
+        pre_row = row_value(bh_next, qt_next);
+        pre_sq = a.q_scales[bh_next * a.T + qt_next];
+        pre_sdo = a.do_scales[bh_next * a.T + qt_next];
       }
       // the previous dQ reduce has finished reading the staging tile
       if (ct == 0) bulk_wait_read_all();
@@ -372,9 +383,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 64; ++c) p[c] = c >= cmin ? p[c] : 0.0f;
       }
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        pm0 = fmaxf(pm0, p[c]);
-        pm1 = fmaxf(pm1, p[c + 1]);
+      for (int c = 0; c < 64; c += 4) {
+        pm0 = max3(pm0, p[c], p[c + 1]);
+        pm1 = max3(pm1, p[c + 2], p[c + 3]);
       }
       float pmax = fmaxf(pm0, pm1);
       pmax = warp_max(pmax);
@@ -384,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int w = 1; w < 8; ++w) amax = fmaxf(amax, s_red[bn][0][w]);
       float rp;
-      const float sp = tile_scale<0>(amax, rp);
+      const float sp = tile_scale_fast<0>(amax, rp);
       {
         uint8_t* dst = sm + L::kPt + bn * kTile * kTile;
 #pragma unroll
@@ -403,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
       // previous iteration's dQ; its completion also means dV/dK(n-1) are done
-      if (n >= 1) drain_dq(n - 1, prev_cdq);
+      if (n >= 1) drain_dq(n - 1, prev_cdq, prev_bh, prev_qi0);
       const int mode_dv = next_unit(unit_dv, sp * sdo, tl + 256 + wg * DH, DH);
 
       // dS = P (dP - delta), computed in place over p (P in FP32 is not needed
@@ -426,8 +437,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        __ffma2_rn(make_float2(dp[c], dp[c + 1]), cdp2, ndl2[cc / 2]));
           ds[cc] = d2.x;
           ds[cc + 1] = d2.y;
-          dm0 = fmaxf(dm0, fabsf(d2.x));
-          dm1 = fmaxf(dm1, fabsf(d2.y));
+          if (c & 2)
+            dm1 = max3(dm1, fabsf(d2.x), fabsf(d2.y));
+          else
+            dm0 = max3(dm0, fabsf(d2.x), fabsf(d2.y));
         }
       }
       float dmax = fmaxf(dm0, dm1);
@@ -438,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int w = 1; w < 8; ++w) amax = fmaxf(amax, s_red[bn][1][w]);
       float rs;
-      const float sds = tile_scale<1>(amax, rs);
+      const float sds = tile_scale_fast<1>(amax, rs);
       uint32_t dcode[16];
       {
         uint8_t* dst = sm + L::kDSt + bn * kTile * kTile;
@@ -459,6 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_mode[bn][1] = mode_dk;
       }
       prev_cdq = a.sigma * sds * sk;
+      prev_bh = bh;
+      prev_qi0 = qi0;
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -510,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (n_iter > 0) {
       if (ct == 0) bulk_wait_read_all();
       named_bar_sync(1, 256);
-      drain_dq(n_iter - 1, prev_cdq);
+      drain_dq(n_iter - 1, prev_cdq, prev_bh, prev_qi0);
     }
     if (ct == 0) bulk_wait_all();
 

@@ -318,6 +318,27 @@ __device__ __forceinline__ float tile_scale(float amax, float& r) {
   return __fdiv_rn(amax, kFmax);
 }
 
+// Scale rule for tiles that stay on chip (P^, dS^): the same rule with a
+// hardware reciprocal instead of IEEE divisions.  The codes only feed the
+// tensor core, so a last-place difference in r moves a code only when P r
+// sits within one ulp of a rounding boundary.
+template <int FMT>
+__device__ __forceinline__ float tile_scale_fast(float amax, float& r) {
+  constexpr float kFmax = FMT == 0 ? 448.0f : 57344.0f;
+  if (!(amax >= 0x1p-96f)) {
+    r = 0.0f;
+    return 0.0f;
+  }
+  r = __fdividef(kFmax, amax);
+  return amax * (1.0f / kFmax);
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -249,7 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (full) {
         float m4[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
-        for (int c = 4; c < 64; ++c) m4[c & 3] = fmaxf(m4[c & 3], v[c]);
+        for (int c = 4; c < 64; c += 8) {
+          m4[0] = max3(m4[0], v[c], v[c + 1]);
+          m4[1] = max3(m4[1], v[c + 2], v[c + 3]);
+          m4[2] = max3(m4[2], v[c + 4], v[c + 5]);
+          m4[3] = max3(m4[3], v[c + 6], v[c + 7]);
+        }
         mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       } else {
 #pragma unroll
@@ -269,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int w = 1; w < 8; ++w) amax = fmaxf(amax, s_red[s][w]);
       float r;
-      const float sp = tile_scale<0>(amax, r);
+      const float sp = tile_scale_fast<0>(amax, r);
       const float alpha = ex2(m - m_new);
 
       // P~ r = exp2(S c1 - m + log2 r) straight into E4M3 codes (P buffer s;
