@@ -169,7 +169,7 @@ def run_native(args, rank, world, local_rank):
             times.append(marks)
         return g
 
-    launches_per_step = 4 + 1 + 1 + 2  # quantise x4, forward, delta, dQ zero fill + backward
+    launches_per_step = 4 + 1 + 1 + 2  # quantise x4, forward, delta, zero fill of dQ/dK/dV + backward
     inputs = (qd, kd, vd, dod)
     with torch.cuda.stream(st):
         for _ in range(args.warmup):

@@ -330,16 +330,22 @@ dm_status dm_attn_bwd(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor
     DM_TRY(delta_impl(p, mode, q, k, v, do_hat, lse, dO, do_dtype, O, o_dtype, ws, status, st));
     dl = ws;
   }
-  DM_TRY(cuda_status(dm::launch_zero(dQ, (size_t)p->B * p->Hq * p->N * p->d, st)));
+  // dQ, dK and dV are sums of bulk reduce-adds; the diagnostics sums of atomics
+  dm::ZeroList z{};
+  z.add(dQ, (size_t)p->B * p->Hq * p->N * p->d);
+  z.add(dK, (size_t)p->B * p->Hkv * p->N * p->d);
+  z.add(dV, (size_t)p->B * p->Hkv * p->N * p->d);
   const size_t nrow = (size_t)p->B * p->Hq * p->N;
-  for (float* ptr : {dg.rowsum_pre, dg.abssum_pre, dg.rowsum_post, dg.abssum_post})
-    if (ptr) DM_TRY(cuda_status(dm::launch_zero(ptr, nrow, st)));
+  for (float* ptr : {dg.rowsum_pre, dg.abssum_pre, dg.rowsum_post, dg.abssum_post}) z.add(ptr, nrow);
+  DM_TRY(cuda_status(dm::launch_zero(z, st)));
   dm::BwdLaunch f{};
   DM_TRY(encode_codes_map(&f.tmQ, q.codes, p->B * p->Hq, p->N, p->d));
   DM_TRY(encode_codes_map(&f.tmK, k.codes, p->B * p->Hkv, p->N, p->d));
   DM_TRY(encode_codes_map(&f.tmV, v.codes, p->B * p->Hkv, p->N, p->d));
   DM_TRY(encode_codes_map(&f.tmDO, do_hat.codes, p->B * p->Hq, p->N, p->d));
   DM_TRY(encode_f32_rows_map(&f.tmDQ, dQ, p->B * p->Hq, p->N, p->d));
+  DM_TRY(encode_f32_rows_map(&f.tmDK, dK, p->B * p->Hkv, p->N, p->d));
+  DM_TRY(encode_f32_rows_map(&f.tmDV, dV, p->B * p->Hkv, p->N, p->d));
   f.args = make_args(p, status);
   f.args.q_scales = q.scales, f.args.k_scales = k.scales, f.args.v_scales = v.scales;
   f.args.do_scales = do_hat.scales;

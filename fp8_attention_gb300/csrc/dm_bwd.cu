@@ -1,13 +1,14 @@
 // Backward: dQ, dK, dV with the five backward matmuls on tcgen05 FP8 MMAs
 // ("Delta-Matching for reliable FP8 attention training", section 01, "Write
-// down softmax backward", and section 03 for delta).  One CTA per (batch, kv
-// head, 128-row key tile); it loops over the query heads of the kv head's
-// group and over the query tiles that see the key tile (iterations n), so dK
-// and dV are summed over the group inside the CTA.  Products are computed
-// transposed (key rows on TMEM lanes) so that dV and dK accumulate in TMEM:
+// down softmax backward", and section 03 for delta).  One CTA per (batch,
+// query head, 128-row key tile), launched longest first; it loops over the
+// query tiles that see the key tile (iterations n).  Its dK and dV tiles (the
+// head's share of the kv head's gradients) are added into global dK and dV
+// with TMA bulk reduce-adds, like dQ.  Products are computed transposed (key
+// rows on TMEM lanes) so that dV and dK accumulate in TMEM:
 //   S^T  = K Q^T                 P  = exp(S - LSE) in FP32,   P^  = E4M3 per 128x128 tile
 //   dP^T = V dO^T                dS = P (dP - delta) in FP32, dS^ = E5M2 per 128x128 tile
-//   dV  += P^T dO     dK += dS^T Q     dQ_i = dS^ K (staged, then TMA bulk reduce-add into dQ)
+//   dV  += P^T dO     dK += dS^T Q     dQ_i = dS^ K (each staged, then bulk reduce-added)
 //
 // TMEM (512 columns): two 128-column work buffers and the two accumulators.
 // Iteration n uses work buffer n%2 three times in a row: S(n), then dP(n) once
@@ -111,9 +112,9 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                    const __grid_constant__ CUtensorMap tmDQ, const AttnArgs a, const float* __restrict__ lse,
-                    const float* __restrict__ delta, float* __restrict__ dK, float* __restrict__ dV,
-                    const dm_diag diag) {
+                    const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ CUtensorMap tmDK,
+                    const __grid_constant__ CUtensorMap tmDV, const AttnArgs a, const float* __restrict__ lse,
+                    const float* __restrict__ delta, const dm_diag diag) {
   using L = BwdLayout<D>;
   constexpr int DH = D / 2;  // d columns per compute warpgroup
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -127,14 +128,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* s_abort = reinterpret_cast<int*>(sm + L::kMisc + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int BG = a.B * a.Hkv;
-  const int kt = (int)(blockIdx.x / BG);  // key tile 0 sees the most query tiles: first
-  const int bg = (int)(blockIdx.x % BG);
-  const int b = bg / a.Hkv, g = bg % a.Hkv;
-  const int G = a.Hq / a.Hkv;
+  const int BH = a.B * a.Hq;
+  const int kt = (int)(blockIdx.x / BH);  // key tile 0 sees the most query tiles: first
+  const int bh0 = (int)(blockIdx.x % BH);
+  const int bg = (bh0 / a.Hq) * a.Hkv + (bh0 % a.Hq) / (a.Hq / a.Hkv);
   const int qt0 = a.causal ? kt : 0;
-  const int nq = a.T - qt0;
-  const int n_iter = G * nq;
+  const int n_iter = a.T - qt0;
   const bool want_diag = diag.rowsum_pre || diag.abssum_pre || diag.rowsum_post || diag.abssum_post;
 
   // The swizzled tiles need a 1024-byte aligned base; the window is expected
@@ -178,18 +177,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmDO);
       tma_prefetch_desc(&tmDQ);
+      tma_prefetch_desc(&tmDK);
+      tma_prefetch_desc(&tmDV);
       mbar_arrive_expect_tx(&bars.kv, 2 * L::kTileBytes);
       tma_load_3d(sm + L::kK, &tmK, &bars.kv, 0, kt * kTile, bg);
       tma_load_3d(sm + L::kV, &tmV, &bars.kv, 0, kt * kTile, bg);
       int issued = 0;
-      int bh = b * a.Hq + g * G, qt = qt0;  // (query head, query tile) of iteration n
+      const int bh = bh0;
+      int qt = qt0;  // query tile of iteration n
       for (int n = 0; n < n_iter; ++n) {
         const int s = n & 1;
         const uint32_t ph = (n >> 1) & 1;
-        if (n > 0 && ++qt == a.T) {
-          qt = qt0;
-          ++bh;
-        }
+        if (n > 0) ++qt;
         if (!wait(&bars.qempty[s], ph ^ 1, wd, 301)) break;
         mbar_arrive_expect_tx(&bars.qfull[s], 2 * L::kTileBytes);
         tma_load_3d(sm + L::kQ + s * L::kTileBytes, &tmQ, &bars.qfull[s], 0, qt * kTile, bh);
@@ -271,8 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wg = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // key row within the tile (TMEM lane)
-    const int kj = kt * kTile + r;
-    const bool kv_valid = kj < a.N;
+    const bool kv_valid = kt * kTile + r < a.N;
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
     const int ct = tid - 64;  // 0..255
     const float sk = a.k_scales[bg * a.T + kt];
@@ -287,9 +285,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ct < 128) return qi < a.N ? lse[(size_t)bh_n * a.N + qi] : INFINITY;
       return qi < a.N ? delta[(size_t)bh_n * a.N + qi] : 0.0f;
     };
-    // (query head, query tile) of the current and of the next iteration
-    int bh = b * a.Hq + g * G, qt = qt0;
-    int bh_next = bh, qt_next = qt;
+    // query tile of the current and of the next iteration (one query head)
+    const int bh = bh0;
+    int qt = qt0, qt_next = qt0;
     float pre_row = n_iter > 0 ? row_value(bh, qt) : 0.0f;
     float pre_sq = n_iter > 0 ? a.q_scales[bh * a.T + qt] : 0.0f;
     float pre_sdo = n_iter > 0 ? a.do_scales[bh * a.T + qt] : 0.0f;
@@ -333,7 +331,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     for (int n = 0; n < n_iter; ++n) {
-      bh = bh_next;
       qt = qt_next;
       const int qi0 = qt * kTile;
       const int bn = n & 1;
@@ -344,13 +341,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_dl[bn][ct - 128] = -pre_row;
       const float sq = pre_sq, sdo = pre_sdo;
       if (n + 1 < n_iter) {
-        if (++qt_next == a.T) {
-          qt_next = qt0;
-          ++bh_next;
-        }
-        pre_row = row_value(bh_next, qt_next);
-        pre_sq = a.q_scales[bh_next * a.T + qt_next];
-        pre_sdo = a.do_scales[bh_next * a.T + qt_next];
+        ++qt_next;
+        pre_row = row_value(bh, qt_next);
+        pre_sq = a.q_scales[bh * a.T + qt_next];
+        pre_sdo = a.do_scales[bh * a.T + qt_next];
       }
       // the previous dQ reduce has finished reading the staging tile
       if (ct == 0) bulk_wait_read_all();
@@ -527,32 +521,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(1, 256);
       drain_dq(n_iter - 1, prev_cdq, prev_bh, prev_qi0);
     }
-    if (ct == 0) bulk_wait_all();
-
-    // epilogue: dV and dK rows of this key tile, in true units (an
-    // accumulator that never received a contribution holds garbage: write 0).
-    // All lanes load (warp-collective); only the stores are guarded.
+    // epilogue: this head's dV and dK tiles in true units, staged like dQ
+    // (after the last dQ reduce has read the staging tile) and added into
+    // global dV and dK.  An accumulator that never received a contribution
+    // holds garbage and is skipped.  TMEM loads are warp-collective.
+    auto reduce_acc = [&](uint32_t col, float unit, const CUtensorMap* map) {
+      if (ct == 0) bulk_wait_read_all();
+      named_bar_sync(1, 256);
+      if (unit != 0.0f) {
 #pragma unroll
-    for (int c = 0; c < DH; c += 32) {
-      float v[32], u[32];
-      tmem_ld32(tl + 256 + wg * DH + c, v);
-      tmem_ld32(tl + 384 + wg * DH + c, u);
-      tmem_wait_ld();
-      if (kv_valid) {
-        float* dv = dV + ((size_t)bg * a.N + kj) * D + wg * DH + c;
-        float* dk = dK + ((size_t)bg * a.N + kj) * D + wg * DH + c;
-        const float fv = unit_dv, fk = unit_dk;
+        for (int c = 0; c < DH; c += 32) {
+          float v[32];
+          tmem_ld32(tl + col + wg * DH + c, v);
+          tmem_wait_ld();
+          uint8_t* box = sm + L::kDQ + ((wg * DH + c) / 32) * (kTile * 128);
 #pragma unroll
-        for (int k = 0; k < 32; k += 4) {
-          *reinterpret_cast<float4*>(dv + k) =
-              fv == 0.0f ? make_float4(0.f, 0.f, 0.f, 0.f)
-                         : make_float4(v[k] * fv, v[k + 1] * fv, v[k + 2] * fv, v[k + 3] * fv);
-          *reinterpret_cast<float4*>(dk + k) =
-              fk == 0.0f ? make_float4(0.f, 0.f, 0.f, 0.f)
-                         : make_float4(u[k] * fk, u[k + 1] * fk, u[k + 2] * fk, u[k + 3] * fk);
+          for (int e = 0; e < 8; ++e) {
+            const float2 a01 = __fmul2_rn(make_float2(v[4 * e], v[4 * e + 1]), make_float2(unit, unit));
+            const float2 a23 = __fmul2_rn(make_float2(v[4 * e + 2], v[4 * e + 3]), make_float2(unit, unit));
+            *reinterpret_cast<float4*>(box + SwTile<128>::chunk_offset(r, e)) =
+                make_float4(a01.x, a01.y, a23.x, a23.y);
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(2, 256);
+        if (ct == 0) {
+#pragma unroll
+          for (int bx = 0; bx < D / 32; ++bx)
+            tma_reduce_add_3d(map, sm + L::kDQ + bx * (kTile * 128), bx * 32, kt * kTile, bg);
+          bulk_commit();
         }
       }
-    }
+    };
+    reduce_acc(256, unit_dv, &tmDV);
+    reduce_acc(384, unit_dk, &tmDK);
+    if (ct == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -570,8 +573,9 @@ cudaError_t launch_t(const BwdLaunch& f, cudaStream_t st) {
   static_assert(smem <= 232448, "backward shared memory exceeds the per-block limit");
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)(f.args.B * f.args.Hkv * f.args.T);
-  k<<<grid, kThreads, smem, st>>>(f.tmQ, f.tmK, f.tmV, f.tmDO, f.tmDQ, f.args, f.lse, f.delta, f.dK, f.dV, f.diag);
+  const unsigned grid = (unsigned)(f.args.B * f.args.Hq * f.args.T);
+  k<<<grid, kThreads, smem, st>>>(f.tmQ, f.tmK, f.tmV, f.tmDO, f.tmDQ, f.tmDK, f.tmDV, f.args, f.lse, f.delta,
+                                  f.diag);
   return cudaGetLastError();
 }
 

@@ -203,13 +203,23 @@ cudaError_t stale_d(const AttnArgs& a, dm_delta_mode mode, const void* dO, dm_dt
                               delta, st);
 }
 
-__global__ void zero_kernel(float* __restrict__ p, size_t n) {
-  const size_t n4 = n / 4;
+// Zero fill of several FP32 buffers in one launch.  Each buffer is written
+// with 16-byte stores between its first and last 16-byte boundary and with
+// scalar stores at its ragged ends, so any 4-byte aligned pointer works.
+__global__ void zero_kernel(const ZeroList z) {
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   const size_t i0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  float4* p4 = reinterpret_cast<float4*>(p);
-  for (size_t i = i0; i < n4; i += stride) p4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (size_t i = 4 * n4 + i0; i < n; i += stride) p[i] = 0.0f;
+  for (int s = 0; s < z.count; ++s) {
+    float* p = z.p[s];
+    const size_t n = z.n[s];
+    size_t head = ((16 - ((uintptr_t)p & 15)) & 15) / 4;
+    if (head > n) head = n;
+    const size_t n4 = (n - head) / 4;
+    float4* p4 = reinterpret_cast<float4*>(p + head);
+    for (size_t i = i0; i < n4; i += stride) p4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i0 < head) p[i0] = 0.0f;
+    for (size_t i = head + 4 * n4 + i0; i < n; i += stride) p[i] = 0.0f;
+  }
 }
 
 }  // namespace
@@ -234,12 +244,13 @@ cudaError_t launch_delta_stale(const AttnArgs& a, int d, dm_delta_mode mode, con
                   : stale_d<64>(a, mode, dO, do_t, do_codes, O, o_t, delta, st);
 }
 
-// p must be 16-byte aligned.
-cudaError_t launch_zero(float* p, size_t n, cudaStream_t st) {
-  if (n == 0) return cudaSuccess;
-  size_t blocks = (n / 4 + 255) / 256 + 1;
+cudaError_t launch_zero(const ZeroList& z, cudaStream_t st) {
+  size_t total = 0;
+  for (int s = 0; s < z.count; ++s) total += z.n[s];
+  if (total == 0) return cudaSuccess;
+  size_t blocks = (total / 4 + 255) / 256 + 1;
   if (blocks > 152 * 16) blocks = 152 * 16;
-  zero_kernel<<<(unsigned)blocks, 256, 0, st>>>(p, n);
+  zero_kernel<<<(unsigned)blocks, 256, 0, st>>>(z);
   return cudaGetLastError();
 }
 

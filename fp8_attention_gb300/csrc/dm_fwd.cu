@@ -22,6 +22,8 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <type_traits>
+
 #include "dm_device.cuh"
 #include "dm_internal.h"
 
@@ -195,25 +197,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float* vsc = a.v_scales + (size_t)bg * a.T;
     float sk_next = ksc[0], sv_next = vsc[0];  // per-tile scales, loaded one tile ahead
     float m = -INFINITY, l = 0.0f;             // running max (log2 units), row sum of this half
-    float2 acc[DH / 2];                        // O in true units, packed pairs of d columns
+    float2 acc[DH / 2];                        // O / unit, packed pairs of d columns
 #pragma unroll
     for (int k = 0; k < DH / 2; ++k) acc[k] = make_float2(0.0f, 0.0f);
+    float unit = 0.0f;                         // O in true units = unit * acc (0: nothing added yet)
     float alpha_prev = 0.0f, c_prev = 0.0f;    // the previous tile's rescale and scale product
 
-    // O_acc = alpha * O_acc + c * O_u over this warpgroup's d columns
+    // O_true = alpha * O_true + c * O_u over this warpgroup's d columns, kept
+    // in units of the latest scale product: acc = acc * (alpha * unit / c) + O_u
+    // (one packed FMA per pair).  When c is zero (a flushed P or V tile) or
+    // so small that the factor would exceed 2^64, the unit stays and the
+    // general form acc = acc * alpha + O_u * (c / unit) is used.
     auto update_o = [&](int u, float alpha, float c) {
       const int su = u & 1;
       wait(&bars.ofull[su], (u >> 1) & 1, wd, 114);
       tc_fence_after();
-      const float2 a2 = make_float2(alpha, alpha), c2 = make_float2(c, c);
+      const float f_fast = __fdividef(alpha * unit, c);
+      const bool fast = c != 0.0f && f_fast <= 0x1p64f;  // false for NaN
+      const float f = fast ? f_fast : alpha;
+      const float g = fast || c == 0.0f ? 0.0f : __fdividef(c, unit);
+      if (fast) unit = c;
+      const float2 f2 = make_float2(f, f), g2 = make_float2(g, g);
 #pragma unroll
       for (int cc = 0; cc < DH; cc += 32) {
         float v[32];
-        tmem_ld32(tl + 256 + su * 128 + wg * DH + cc, v);
+        tmem_ld32(tl + 256 + su * 128 + wg * DH + cc, v);  // warp-collective: before any branch
         tmem_wait_ld();
+        if (fast) {
 #pragma unroll
-        for (int k = 0; k < 32; k += 2)
-          acc[(cc + k) / 2] = __ffma2_rn(c2, make_float2(v[k], v[k + 1]), __fmul2_rn(a2, acc[(cc + k) / 2]));
+          for (int k = 0; k < 32; k += 2)
+            acc[(cc + k) / 2] = __ffma2_rn(acc[(cc + k) / 2], f2, make_float2(v[k], v[k + 1]));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; k += 2)
+            acc[(cc + k) / 2] = __ffma2_rn(make_float2(v[k], v[k + 1]), g2, __fmul2_rn(acc[(cc + k) / 2], f2));
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -285,27 +303,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float2 c1_2 = make_float2(c1, c1), b2 = make_float2(bias, bias);
       float2 rs2 = make_float2(0.0f, 0.0f);
       uint8_t* sP = sm + L::kP + s * kTile * kTile;
+      // two instances: full tiles carry no masking selects
+      auto p_codes = [&](auto full_tile) {
 #pragma unroll
-      for (int c = 0; c < 64; c += 16) {
-        uint32_t w4[4];
+        for (int c = 0; c < 64; c += 16) {
+          uint32_t w4[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int cc = c + 4 * e;
-          const float2 x01 = __ffma2_rn(make_float2(v[cc], v[cc + 1]), c1_2, b2);
-          const float2 x23 = __ffma2_rn(make_float2(v[cc + 2], v[cc + 3]), c1_2, b2);
-          float2 q01 = make_float2(ex2(x01.x), ex2(x01.y)), q23 = make_float2(ex2(x23.x), ex2(x23.y));
-          if (!full) {
-            q01.x = cc < jlim ? q01.x : 0.0f;
-            q01.y = cc + 1 < jlim ? q01.y : 0.0f;
-            q23.x = cc + 2 < jlim ? q23.x : 0.0f;
-            q23.y = cc + 3 < jlim ? q23.y : 0.0f;
+          for (int e = 0; e < 4; ++e) {
+            const int cc = c + 4 * e;
+            const float2 x01 = __ffma2_rn(make_float2(v[cc], v[cc + 1]), c1_2, b2);
+            const float2 x23 = __ffma2_rn(make_float2(v[cc + 2], v[cc + 3]), c1_2, b2);
+            float2 q01 = make_float2(ex2(x01.x), ex2(x01.y)), q23 = make_float2(ex2(x23.x), ex2(x23.y));
+            if (!decltype(full_tile)::value) {
+              q01.x = cc < jlim ? q01.x : 0.0f;
+              q01.y = cc + 1 < jlim ? q01.y : 0.0f;
+              q23.x = cc + 2 < jlim ? q23.x : 0.0f;
+              q23.y = cc + 3 < jlim ? q23.y : 0.0f;
+            }
+            rs2 = __fadd2_rn(rs2, __fadd2_rn(q01, q23));
+            w4[e] = pack4_e4m3(q01.x, q01.y, q23.x, q23.y);
           }
-          rs2 = __fadd2_rn(rs2, __fadd2_rn(q01, q23));
-          w4[e] = pack4_e4m3(q01.x, q01.y, q23.x, q23.y);
+          *reinterpret_cast<uint4*>(sP + SwTile<128>::chunk_offset(row, wg * 4 + c / 16)) =
+              make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
-        *reinterpret_cast<uint4*>(sP + SwTile<128>::chunk_offset(row, wg * 4 + c / 16)) =
-            make_uint4(w4[0], w4[1], w4[2], w4[3]);
-      }
+      };
+      if (full)
+        p_codes(std::true_type{});
+      else
+        p_codes(std::false_type{});
       l = alpha * l + (rs2.x + rs2.y) * sp;
       m = m_new;
       fence_proxy_async_smem();
@@ -328,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (row_valid) lse[(size_t)bh * a.N + qi] = m * kLn2 + logf(lt);
     }
     named_bar_sync(1, 256);
-    const float linv = 1.0f / s_l[row];
+    const float linv = unit / s_l[row];
     if (row_valid) {
       if (OUT_BF16) {
         __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(O) + ((size_t)bh * a.N + qi) * D + wg * DH;

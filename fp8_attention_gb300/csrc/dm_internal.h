@@ -25,7 +25,8 @@ struct DeltaLaunch {
 
 struct BwdLaunch {
   CUtensorMap tmQ, tmK, tmV, tmDO;
-  CUtensorMap tmDQ;  // fp32 [B*Hq][N][d], box 128 rows x 32 columns, 128-byte swizzle
+  CUtensorMap tmDQ;       // fp32 [B*Hq][N][d], box 128 rows x 32 columns, 128-byte swizzle
+  CUtensorMap tmDK, tmDV;  // fp32 [B*Hkv][N][d], same boxes
   AttnArgs args;
   const float* lse;
   const float* delta;
@@ -40,7 +41,22 @@ cudaError_t launch_delta_matched(const DeltaLaunch& f, int d, cudaStream_t st);
 cudaError_t launch_delta_stale(const AttnArgs& a, int d, dm_delta_mode mode, const void* dO, dm_dtype do_t,
                                const uint8_t* do_codes, const void* O, dm_dtype o_t, float* delta,
                                cudaStream_t st);
-cudaError_t launch_zero(float* p, size_t n, cudaStream_t st);
+// FP32 buffers (4-byte aligned) that one launch sets to zero.
+struct ZeroList {
+  static constexpr int kMax = 8;
+  float* p[kMax];
+  size_t n[kMax];
+  int count;
+  void add(float* ptr, size_t len) {
+    if (ptr && len) {
+      p[count] = ptr;
+      n[count] = len;
+      ++count;
+    }
+  }
+};
+
+cudaError_t launch_zero(const ZeroList& z, cudaStream_t st);
 cudaError_t launch_attn_bwd(const BwdLaunch& f, int d, cudaStream_t st);
 
 }  // namespace dm
