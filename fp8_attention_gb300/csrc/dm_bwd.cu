@@ -21,7 +21,8 @@
 // warps rescale the accumulator by old/new unit.  Iterations whose product is
 // below 2^-100 (a flushed or negligible tile) add nothing.
 //
-// Warp roles (320 threads): warp 0 TMA, warp 1 MMA, warps 2-9 two compute
+// Warp roles (384 threads): warp 0 TMA, warp 1 MMA, warps 2-3 idle (each
+// warpgroup starts at a multiple of four warps), warps 4-11 two compute
 // warpgroups; thread = key row, warpgroup = half of the query columns (and
 // half of the d columns for the dV/dK/dQ epilogues).
 #include <cudaTypedefs.h>
@@ -32,7 +33,7 @@
 namespace dm {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;  // warps 0-3: TMA, MMA, two idle; warps 4-11: compute
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMinUnit = 0x1p-100f;
 
@@ -82,17 +83,15 @@ __device__ __forceinline__ float lane_column_sum(float (&v)[32], int lane) {
 __device__ __forceinline__ void tmem_scale(uint32_t taddr, int ncols, float f) {
   for (int c = 0; c < ncols; c += 32) {
     float v[32];
-    tmem_ld32(taddr + c, v);
-    tmem_wait_ld();
+    tmem_load32(taddr + c, v);
 #pragma unroll
     for (int k = 0; k < 32; k += 2) {
       const float2 x = __fmul2_rn(make_float2(v[k], v[k + 1]), make_float2(f, f));
       v[k] = x.x;
       v[k + 1] = x.y;
     }
-    tmem_st32(taddr + c, v);
+    tmem_store32(taddr + c, v);
   }
-  tmem_wait_st();
 }
 
 // Unit bookkeeping for one TMEM accumulator; every compute thread holds an
@@ -265,14 +264,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bars.mma_done);
       wait_drain(&bars.mma_done, 0, wd, 310);
     }
-  } else {
+  } else if (warp >= 4) {
     // -------------------------------------------------------------- compute
-    const int wg = (warp - 2) >> 2;
+    const int wg = (warp - 4) >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // key row within the tile (TMEM lane)
     const bool kv_valid = kt * kTile + r < a.N;
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-    const int ct = tid - 64;  // 0..255
+    const int ct = tid - 128;  // 0..255
     const float sk = a.k_scales[bg * a.T + kt];
     const float svv = a.v_scales[bg * a.T + kt];
     float unit_dv = 0.0f, unit_dk = 0.0f;
@@ -307,8 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < DH; c += 32) {
         float v[32];
-        tmem_ld32(tl + bm * 128 + wg * DH + c, v);
-        tmem_wait_ld();
+        tmem_load32(tl + bm * 128 + wg * DH + c, v);
         uint8_t* box = sm + L::kDQ + ((wg * DH + c) / 32) * (kTile * 128);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -357,9 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float p[64];
       wait(&bars.sfull[bn], ph, wd, 312);
       tc_fence_after();
-      tmem_ld32(tl + bn * 128 + wg * 64, *reinterpret_cast<float(*)[32]>(&p[0]));
-      tmem_ld32(tl + bn * 128 + wg * 64 + 32, *reinterpret_cast<float(*)[32]>(&p[32]));
-      tmem_wait_ld();
+      tmem_load64(tl + bn * 128 + wg * 64, tl + bn * 128 + wg * 64 + 32, p);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.sread[bn]);
@@ -383,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float pmax = fmaxf(pm0, pm1);
       pmax = warp_max(pmax);
-      if (lane == 0) s_red[bn][0][warp - 2] = pmax;
+      if (lane == 0) s_red[bn][0][warp - 4] = pmax;
       named_bar_sync(1, 256);
       float amax = s_red[bn][0][0];
 #pragma unroll
@@ -422,8 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float dp[32];
-        tmem_ld32(tl + bn * 128 + wg * 64 + h * 32, dp);
-        tmem_wait_ld();
+        tmem_load32(tl + bn * 128 + wg * 64 + h * 32, dp);
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           const int cc = h * 32 + c;
@@ -439,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float dmax = fmaxf(dm0, dm1);
       dmax = warp_max(dmax);
-      if (lane == 0) s_red[bn][1][warp - 2] = dmax;
+      if (lane == 0) s_red[bn][1][warp - 4] = dmax;
       named_bar_sync(1, 256);
       amax = s_red[bn][1][0];
 #pragma unroll
@@ -532,8 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < DH; c += 32) {
           float v[32];
-          tmem_ld32(tl + col + wg * DH + c, v);
-          tmem_wait_ld();
+          tmem_load32(tl + col + wg * DH + c, v);
           uint8_t* box = sm + L::kDQ + ((wg * DH + c) / 32) * (kTile * 128);
 #pragma unroll
           for (int e = 0; e < 8; ++e) {

@@ -8,14 +8,19 @@
 // query head, 128-row query tile), recomputing S = Q K^T and dP^ = dO^ V^T
 // on tcgen05 tile by tile.
 //
-// Warp roles (320 threads):
+// Warp roles (640 threads):
 //   warp 0      TMA: Q and dO tiles once, K/V tiles double-buffered
 //   warp 1      MMA: S(t) into TMEM S[t%2], dP(t) into TMEM dP[t%2]
-//   warps 2-9   two warpgroups, one thread per (query row, half of the key
-//               columns): P = exp2(S*c1 - LSE*log2e), sums of P*dP (scaled by
-//               s_dO * s_V,t per key tile) and of P
+//   warps 2-3   idle (each warpgroup starts at a multiple of four warps)
+//   warps 4-19  four warpgroups, one thread per (query row, quarter of the
+//               key columns): P = exp2(S*c1 - LSE*log2e), sums of P*dP
+//               (scaled by s_dO * s_V,t per key tile) and of P.  Sixteen
+//               compute warps (four per SM sub-partition) hide the TMEM load
+//               latency of each other.
 // TMEM columns: S[0] 0, S[1] 128, dP[0] 256, dP[1] 384.
 #include <cudaTypedefs.h>
+
+#include <type_traits>
 
 #include "dm_device.cuh"
 #include "dm_internal.h"
@@ -23,7 +28,9 @@
 namespace dm {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kGroups = 4;            // compute warpgroups
+constexpr int kThreads = 128 + 128 * kGroups;  // warps 0-3: TMA, MMA, two idle; then the compute warpgroups
+constexpr int kCols = kTile / kGroups;  // key columns per thread
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
@@ -50,7 +57,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ DeltaBars bars;
-  __shared__ float s_part[kTile], s_psum[kTile];
+  __shared__ float s_part[kGroups][kTile], s_psum[kGroups][kTile];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
@@ -74,7 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.vempty[s], 1);
       mbar_init(&bars.sfull[s], 1);
       mbar_init(&bars.dpfull[s], 1);
-      mbar_init(&bars.tempty[s], 8);
+      mbar_init(&bars.tempty[s], 4 * kGroups);
     }
     mbar_init(&bars.mma_done, 1);
     fence_barrier_init();
@@ -147,13 +154,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bars.mma_done);
       wait_drain(&bars.mma_done, 0, wd, 212);
     }
-  } else {
-    const int wg = (warp - 2) >> 2;  // key-column half
+  } else if (warp >= 4) {
+    const int wg = (warp - 4) >> 2;  // key-column quarter
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const int qi = q0 + row;
     const bool row_valid = qi < a.N;
-    const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16) + wg * 64;
+    const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16) + wg * kCols;
     const float sq = a.q_scales[bh * a.T + qt];
     const float sdo = a.do_scales[bh * a.T + qt];
     const float lse2 = row_valid ? lse[(size_t)bh * a.N + qi] * kLog2e : 0.0f;
@@ -170,52 +177,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         sk_next = ksc[t + 1];
         sv_next = vsc[t + 1];
       }
-      const int j0 = t * kTile + wg * 64;
-      int jlim = min(64, a.N - j0);
+      const int j0 = t * kTile + wg * kCols;
+      int jlim = min(kCols, a.N - j0);
       if (a.causal) jlim = min(jlim, qi - j0 + 1);
-      float sv[64], dp[64];
+      float x[2 * kCols];  // S then dP of this thread's columns
+      const float* sv = x;
+      const float* dp = x + kCols;
       wait(&bars.sfull[s], ph, wd, 207);
-      tc_fence_after();
-      tmem_ld32(tl + s * 128, *reinterpret_cast<float(*)[32]>(&sv[0]));
-      tmem_ld32(tl + s * 128 + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
       wait(&bars.dpfull[s], ph, wd, 208);
       tc_fence_after();
-      tmem_ld32(tl + 256 + s * 128, *reinterpret_cast<float(*)[32]>(&dp[0]));
-      tmem_ld32(tl + 256 + s * 128 + 32, *reinterpret_cast<float(*)[32]>(&dp[32]));
-      tmem_wait_ld();
+      tmem_load64(tl + s * 128, tl + 256 + s * 128, x);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.tempty[s]);
       // P = exp2(S c1 - LSE log2e) on packed pairs; masks only on the
-      // diagonal or ragged tile
-      const bool full = jlim >= 64;
+      // diagonal or ragged tile (a separate instance without selects)
       const float2 c1_2 = make_float2(c1, c1), nl2 = make_float2(-lse2, -lse2);
       float2 acc0 = make_float2(0.0f, 0.0f), acc1 = acc0, ps0 = acc0, ps1 = acc0;
+      auto accumulate = [&](auto full_tile) {
 #pragma unroll
-      for (int c = 0; c < 64; c += 4) {
-        const float2 x0 = __ffma2_rn(make_float2(sv[c], sv[c + 1]), c1_2, nl2);
-        const float2 x1 = __ffma2_rn(make_float2(sv[c + 2], sv[c + 3]), c1_2, nl2);
-        float2 p0 = make_float2(ex2(x0.x), ex2(x0.y)), p1 = make_float2(ex2(x1.x), ex2(x1.y));
-        if (!full) {
-          p0.x = c < jlim ? p0.x : 0.0f;
-          p0.y = c + 1 < jlim ? p0.y : 0.0f;
-          p1.x = c + 2 < jlim ? p1.x : 0.0f;
-          p1.y = c + 3 < jlim ? p1.y : 0.0f;
+        for (int c = 0; c < kCols; c += 4) {
+          const float2 x0 = __ffma2_rn(make_float2(sv[c], sv[c + 1]), c1_2, nl2);
+          const float2 x1 = __ffma2_rn(make_float2(sv[c + 2], sv[c + 3]), c1_2, nl2);
+          float2 p0 = make_float2(ex2(x0.x), ex2(x0.y)), p1 = make_float2(ex2(x1.x), ex2(x1.y));
+          if (!decltype(full_tile)::value) {
+            p0.x = c < jlim ? p0.x : 0.0f;
+            p0.y = c + 1 < jlim ? p0.y : 0.0f;
+            p1.x = c + 2 < jlim ? p1.x : 0.0f;
+            p1.y = c + 3 < jlim ? p1.y : 0.0f;
+          }
+          acc0 = __ffma2_rn(p0, make_float2(dp[c], dp[c + 1]), acc0);
+          acc1 = __ffma2_rn(p1, make_float2(dp[c + 2], dp[c + 3]), acc1);
+          ps0 = __fadd2_rn(ps0, p0);
+          ps1 = __fadd2_rn(ps1, p1);
         }
-        acc0 = __ffma2_rn(p0, make_float2(dp[c], dp[c + 1]), acc0);
-        acc1 = __ffma2_rn(p1, make_float2(dp[c + 2], dp[c + 3]), acc1);
-        ps0 = __fadd2_rn(ps0, p0);
-        ps1 = __fadd2_rn(ps1, p1);
-      }
+      };
+      if (jlim >= kCols)
+        accumulate(std::true_type{});
+      else
+        accumulate(std::false_type{});
       dl = fmaf((acc0.x + acc0.y) + (acc1.x + acc1.y), c2, dl);
       psum += (ps0.x + ps0.y) + (ps1.x + ps1.y);
     }
-    if (wg == 1) {
-      s_part[row] = dl;
-      s_psum[row] = psum;
+    s_part[wg][row] = dl;
+    s_psum[wg][row] = psum;
+    named_bar_sync(1, 4 * kGroups * 32);
+    if (wg == 0 && row_valid) {
+      float num = 0.0f, den = 0.0f;
+#pragma unroll
+      for (int g = 0; g < kGroups; ++g) {
+        num += s_part[g][row];
+        den += s_psum[g][row];
+      }
+      delta[(size_t)bh * a.N + qi] = num / den;
     }
-    named_bar_sync(1, 256);
-    if (wg == 0 && row_valid) delta[(size_t)bh * a.N + qi] = (dl + s_part[row]) / (psum + s_psum[row]);
   }
 
   tc_fence_before();

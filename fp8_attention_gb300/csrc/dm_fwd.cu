@@ -2,17 +2,19 @@
 // tile), with both matmuls on tcgen05 FP8 MMAs ("Delta-Matching for reliable
 // FP8 attention training", section 01: "What changes in FP8?").
 //
-// Warp roles (320 threads):
+// Warp roles (640 threads):
 //   warp 0      TMA producer: Q tile once, K/V tiles double-buffered
 //   warp 1      MMA issuer (+ TMEM owner): S(t) = Q K_t^T into TMEM S[t%2];
 //               O_t = P^_t V_t into TMEM O[t%2]
-//   warps 2-9   two warpgroups; thread = query row (TMEM lane), warpgroup =
-//               half of the key columns for the softmax and half of the d
-//               columns for O.  Per key tile t: online row max (the halves
-//               exchange partial maxima through shared memory), P~ in FP32,
-//               the tile's amax -> E4M3 codes into shared memory; then, one
-//               tile behind, O_acc = alpha * O_acc + (s_P * s_V) * O_{t-1} in
-//               registers, in true units.
+//   warps 2-3   idle (each warpgroup starts at a multiple of four warps)
+//   warps 4-19  four warpgroups; thread = query row (TMEM lane), warpgroup =
+//               a quarter of the key columns for the softmax and a quarter
+//               of the d columns for O.  Per key tile t: online row max (the
+//               quarters exchange partial maxima through shared memory), P~
+//               in FP32, the tile's amax -> E4M3 codes into shared memory;
+//               then, one tile behind, O_acc = alpha * O_acc + (s_P * s_V) *
+//               O_{t-1} in registers.  Four compute warps per SM
+//               sub-partition hide each other's TMEM and MUFU latency.
 //
 // Each key tile brings its own FP32 scale product s_P,t * s_V,t, so the
 // tiles' products are summed outside the tensor core.  The O update lags one
@@ -30,7 +32,10 @@
 namespace dm {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kGroups = 2;                // compute warpgroups
+constexpr int kWarps = 4 * kGroups;      // compute warps
+constexpr int kThreads = 128 + 32 * kWarps;  // warps 0-3: TMA, MMA, two idle; then the compute warpgroups
+constexpr int kCols = kTile / kGroups;    // key columns per thread
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -48,10 +53,10 @@ struct FwdLayout {
   static constexpr int kK = kQ + kTileBytes;              // 2 stages
   static constexpr int kV = kK + 2 * kTileBytes;          // 2 stages
   static constexpr int kP = kV + 2 * kTileBytes;          // 2 x (128 x 128) P^ codes
-  static constexpr int kRmax = kP + 2 * kTile * kTile;    // float [2][2][128] partial row maxima
-  static constexpr int kRed = kRmax + 2 * 2 * kTile * 4;  // float [2][8] tile amax partials
-  static constexpr int kL = kRed + 2 * 8 * 4;             // float [128] row sums
-  static constexpr int kBars = kL + kTile * 4;
+  static constexpr int kRmax = kP + 2 * kTile * kTile;          // float [2][kGroups][128] partial row maxima
+  static constexpr int kRed = kRmax + 2 * kGroups * kTile * 4;  // float [2][kWarps] tile amax partials
+  static constexpr int kL = kRed + 2 * kWarps * 4;              // float [kGroups][128] row sums
+  static constexpr int kBars = kL + kGroups * kTile * 4;
   static constexpr int kMisc = kBars + ((int)(sizeof(FwdBars) + 15) / 16) * 16;  // tmem address, abort flag
   static constexpr int kBytes = kMisc + 16;
 };
@@ -62,13 +67,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tmV, const AttnArgs a, void* __restrict__ O,
                     float* __restrict__ lse) {
   using L = FwdLayout<D>;
-  constexpr int DH = D / 2;  // O columns per warpgroup
+  constexpr int DH = D / kGroups;  // O columns per warpgroup
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   FwdBars& bars = *reinterpret_cast<FwdBars*>(sm + L::kBars);
-  float(*s_rmax)[2][kTile] = reinterpret_cast<float(*)[2][kTile]>(sm + L::kRmax);
-  float(*s_red)[8] = reinterpret_cast<float(*)[8]>(sm + L::kRed);
-  float* s_l = reinterpret_cast<float*>(sm + L::kL);
+  float(*s_rmax)[kGroups][kTile] = reinterpret_cast<float(*)[kGroups][kTile]>(sm + L::kRmax);
+  float(*s_red)[kWarps] = reinterpret_cast<float(*)[kWarps]>(sm + L::kRed);
+  float(*s_l)[kTile] = reinterpret_cast<float(*)[kTile]>(sm + L::kL);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + L::kMisc);
   int* s_abort = reinterpret_cast<int*>(sm + L::kMisc + 4);
 
@@ -96,10 +101,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.vfull[s], 1);
       mbar_init(&bars.vempty[s], 1);
       mbar_init(&bars.sfull[s], 1);
-      mbar_init(&bars.sempty[s], 8);
-      mbar_init(&bars.pfull[s], 8);
+      mbar_init(&bars.sempty[s], kWarps);
+      mbar_init(&bars.pfull[s], kWarps);
       mbar_init(&bars.ofull[s], 1);
-      mbar_init(&bars.oempty[s], 8);
+      mbar_init(&bars.oempty[s], kWarps);
     }
     mbar_init(&bars.stall, 1);
     mbar_init(&bars.mma_done, 1);
@@ -147,7 +152,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdS = idesc_f8(0, 0, 0, 0, kTile, kTile);  // Q K^T, both K-major
       constexpr uint32_t kIdO = idesc_f8(0, 0, 0, 1, kTile, D);      // P^ (K-major) V (MN-major)
       bool ok = true;
-      if (a.stall_test) ok = wait(&bars.stall, 0, wd, 103);  // watchdog test: never signalled
+      if (a.stall_test) {
+        // watchdog test: a barrier nothing signals, with half the limit so
+        // that it expires before the waits that depend on it
+        const Watchdog wd_half{wd.abort_flag, wd.status, wd.limit_ns / 2};
+        ok = wait(&bars.stall, 0, wd_half, 103);
+      }
       ok = ok && wait(&bars.q, 0, wd, 104);
       tc_fence_after();
       const uint32_t sQ = smem_u32(sm + L::kQ);
@@ -184,9 +194,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bars.mma_done);
       wait_drain(&bars.mma_done, 0, wd, 119);
     }
-  } else {
+  } else if (warp >= 4) {
     // ------------------------------------------------ softmax and O update
-    const int wg = (warp - 2) >> 2;  // key-column half and O-column half
+    constexpr int kCT = 32 * kWarps;  // compute threads
+    const int wg = (warp - 4) >> 2;   // key-column and O-column quarter
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const int qi = q0 + row;
@@ -196,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float* ksc = a.k_scales + (size_t)bg * a.T;
     const float* vsc = a.v_scales + (size_t)bg * a.T;
     float sk_next = ksc[0], sv_next = vsc[0];  // per-tile scales, loaded one tile ahead
-    float m = -INFINITY, l = 0.0f;             // running max (log2 units), row sum of this half
+    float m = -INFINITY, l = 0.0f;             // running max (log2 units), row sum of this quarter
     float2 acc[DH / 2];                        // O / unit, packed pairs of d columns
 #pragma unroll
     for (int k = 0; k < DH / 2; ++k) acc[k] = make_float2(0.0f, 0.0f);
@@ -218,24 +229,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float g = fast || c == 0.0f ? 0.0f : __fdividef(c, unit);
       if (fast) unit = c;
       const float2 f2 = make_float2(f, f), g2 = make_float2(g, g);
-#pragma unroll
-      for (int cc = 0; cc < DH; cc += 32) {
-        float v[32];
-        tmem_ld32(tl + 256 + su * 128 + wg * DH + cc, v);  // warp-collective: before any branch
-        tmem_wait_ld();
-        if (fast) {
-#pragma unroll
-          for (int k = 0; k < 32; k += 2)
-            acc[(cc + k) / 2] = __ffma2_rn(acc[(cc + k) / 2], f2, make_float2(v[k], v[k + 1]));
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; k += 2)
-            acc[(cc + k) / 2] = __ffma2_rn(make_float2(v[k], v[k + 1]), g2, __fmul2_rn(acc[(cc + k) / 2], f2));
-        }
-      }
+      float v[DH];  // warp-collective load: before any branch
+      tmem_load_cols<DH>(tl + 256 + su * 128 + wg * DH, v);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.oempty[su]);
+      if (fast) {
+#pragma unroll
+        for (int k = 0; k < DH; k += 2) acc[k / 2] = __ffma2_rn(acc[k / 2], f2, make_float2(v[k], v[k + 1]));
+      } else {
+#pragma unroll
+        for (int k = 0; k < DH; k += 2)
+          acc[k / 2] = __ffma2_rn(make_float2(v[k], v[k + 1]), g2, __fmul2_rn(acc[k / 2], f2));
+      }
     };
 
     for (int t = 0; t < nkv; ++t) {
@@ -247,27 +253,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         sk_next = ksc[t + 1];
         sv_next = vsc[t + 1];
       }
-      const int j0 = t * kTile + wg * 64;
-      int jlim = min(64, a.N - j0);
+      const int j0 = t * kTile + wg * kCols;
+      int jlim = min(kCols, a.N - j0);
       if (a.causal) jlim = min(jlim, qi - j0 + 1);
 
       wait(&bars.sfull[s], ph, wd, 110);
       tc_fence_after();
-      float v[64];
-      tmem_ld32(tl + s * 128 + wg * 64, *reinterpret_cast<float(*)[32]>(&v[0]));
-      tmem_ld32(tl + s * 128 + wg * 64 + 32, *reinterpret_cast<float(*)[32]>(&v[32]));
-      tmem_wait_ld();
+      float v[kCols];
+      tmem_load_cols<kCols>(tl + s * 128 + wg * kCols, v);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.sempty[s]);
 
-      // row max over both halves (raw units; c1 > 0 preserves the order)
-      const bool full = jlim >= 64;  // no masked column in this half (all but the diagonal/ragged tile)
+      // row max over the four quarters (raw units; c1 > 0 preserves the order)
+      const bool full = jlim >= kCols;  // no masked column here (all but the diagonal/ragged tile)
       float mx = -INFINITY;
       if (full) {
         float m4[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
-        for (int c = 4; c < 64; c += 8) {
+        for (int c = 4; c < kCols; c += 8) {
           m4[0] = max3(m4[0], v[c], v[c + 1]);
           m4[1] = max3(m4[1], v[c + 2], v[c + 3]);
           m4[2] = max3(m4[2], v[c + 4], v[c + 5]);
@@ -276,29 +280,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       } else {
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
+        for (int c = 0; c < kCols; ++c)
           if (c < jlim) mx = fmaxf(mx, v[c]);
       }
       s_rmax[s][wg][row] = mx;
-      named_bar_sync(1, 256);
-      const float tmax = fmaxf(mx, s_rmax[s][wg ^ 1][row]) * c1;
+      named_bar_sync(1, kCT);
+      float tmax = s_rmax[s][0][row];
+#pragma unroll
+      for (int g = 1; g < kGroups; ++g) tmax = fmaxf(tmax, s_rmax[s][g][row]);
+      tmax *= c1;
       const float m_new = fmaxf(m, tmax);
       // amax of this tile of P~ = max over its rows of exp2(tile row max - running max)
       float arow = row_valid ? ex2(tmax - m_new) : 0.0f;
       arow = warp_max(arow);
-      if (lane == 0) s_red[s][warp - 2] = arow;
-      named_bar_sync(1, 256);
+      if (lane == 0) s_red[s][warp - 4] = arow;
+      named_bar_sync(1, kCT);
       float amax = s_red[s][0];
 #pragma unroll
-      for (int w = 1; w < 8; ++w) amax = fmaxf(amax, s_red[s][w]);
+      for (int w = 1; w < kWarps; ++w) amax = fmaxf(amax, s_red[s][w]);
       float r;
       const float sp = tile_scale_fast<0>(amax, r);
       const float alpha = ex2(m - m_new);
 
       // P~ r = exp2(S c1 - m + log2 r) straight into E4M3 codes (P buffer s;
       // its last reader, the P V product of tile t-2, completed before this
-      // thread's O update of tile t-2); the unquantised row sum of this half
-      // is sum(P~ r) * s_P.  A flushed tile (r = 0) gives codes 0.
+      // thread's O update of tile t-2); the unquantised row sum of this
+      // quarter is sum(P~ r) * s_P.  A flushed tile (r = 0) gives codes 0.
       const float bias = (r > 0.0f ? __log2f(r) : -INFINITY) - m_new;
       const float2 c1_2 = make_float2(c1, c1), b2 = make_float2(bias, bias);
       float2 rs2 = make_float2(0.0f, 0.0f);
@@ -306,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // two instances: full tiles carry no masking selects
       auto p_codes = [&](auto full_tile) {
 #pragma unroll
-        for (int c = 0; c < 64; c += 16) {
+        for (int c = 0; c < kCols; c += 16) {
           uint32_t w4[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -323,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             rs2 = __fadd2_rn(rs2, __fadd2_rn(q01, q23));
             w4[e] = pack4_e4m3(q01.x, q01.y, q23.x, q23.y);
           }
-          *reinterpret_cast<uint4*>(sP + SwTile<128>::chunk_offset(row, wg * 4 + c / 16)) =
+          *reinterpret_cast<uint4*>(sP + SwTile<128>::chunk_offset(row, (wg * kCols + c) / 16)) =
               make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
       };
@@ -344,16 +351,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     update_o(nkv - 1, alpha_prev, c_prev);
 
-    // row sum over both halves, LSE, and O / l
-    if (wg == 1) s_l[row] = l;
-    named_bar_sync(1, 256);
-    if (wg == 0) {
-      const float lt = l + s_l[row];
-      s_l[row] = lt;
-      if (row_valid) lse[(size_t)bh * a.N + qi] = m * kLn2 + logf(lt);
-    }
-    named_bar_sync(1, 256);
-    const float linv = unit / s_l[row];
+    // row sum over the quarters, LSE, and O / l
+    s_l[wg][row] = l;
+    named_bar_sync(1, kCT);
+    float lt = s_l[0][row];
+#pragma unroll
+    for (int g = 1; g < kGroups; ++g) lt += s_l[g][row];
+    if (wg == 0 && row_valid) lse[(size_t)bh * a.N + qi] = m * kLn2 + logf(lt);
+    const float linv = unit / lt;
     if (row_valid) {
       if (OUT_BF16) {
         __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(O) + ((size_t)bh * a.N + qi) * D + wg * DH;
