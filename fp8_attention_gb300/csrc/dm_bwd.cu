@@ -38,7 +38,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMinUnit = 0x1p-100f;
 
 struct BwdBars {
-  uint64_t kv, qfull[2], qempty[2], sfull[2], sread[2], dpfull[2], bfree[2], pds, mma2, mma_done;
+  uint64_t kv, qfull[2], qempty[2], sfull[2], sread[2], dpfull[2], bfree[2], pds, mma2, mma_done, dq_staged,
+      dq_free;
 };
 
 // Everything lives in dynamic shared memory (no static shared variables), so
@@ -79,32 +80,45 @@ __device__ __forceinline__ float lane_column_sum(float (&v)[32], int lane) {
   return v[0];
 }
 
-// Rescale `ncols` (multiple of 32) TMEM columns of this warp's lanes by f.
-__device__ __forceinline__ void tmem_scale(uint32_t taddr, int ncols, float f) {
-  for (int c = 0; c < ncols; c += 32) {
-    float v[32];
-    tmem_load32(taddr + c, v);
-#pragma unroll
-    for (int k = 0; k < 32; k += 2) {
-      const float2 x = __fmul2_rn(make_float2(v[k], v[k + 1]), make_float2(f, f));
-      v[k] = x.x;
-      v[k + 1] = x.y;
-    }
-    tmem_store32(taddr + c, v);
-  }
-}
-
 // Unit bookkeeping for one TMEM accumulator; every compute thread holds an
-// identical copy.  Returns the MMA mode: 0 skip, 1 overwrite, 2 accumulate.
-__device__ __forceinline__ int next_unit(float& unit, float c, uint32_t taddr, int ncols) {
+// identical copy.  Sets f to the factor the accumulator must be multiplied by
+// (1 when it stays) and returns the MMA mode: 0 skip, 1 overwrite,
+// 2 accumulate.
+__device__ __forceinline__ int unit_step(float& unit, float c, float& f) {
+  f = 1.0f;
   if (!(c >= kMinUnit)) return 0;
   if (unit == 0.0f) {
     unit = c;
     return 1;
   }
-  if (unit != c) tmem_scale(taddr, ncols, unit / c);
+  f = unit / c;
   unit = c;
   return 2;
+}
+
+// dV *= fv and dK *= fk over this warp's lanes and this warpgroup's DH
+// columns of each, with one TMEM load and one store of both.
+template <int DH>
+__device__ __forceinline__ void rescale_pair(uint32_t tdv, float fv, uint32_t tdk, float fk) {
+  static_assert(DH == 32 || DH == 64, "unsupported column split");
+  float v[2 * DH];
+  if constexpr (DH == 64)
+    tmem_load128(tdv, tdv + 32, tdk, tdk + 32, v);
+  else
+    tmem_load64(tdv, tdk, v);
+#pragma unroll
+  for (int k = 0; k < 2 * DH; k += 2) {
+    const float f = k < DH ? fv : fk;
+    const float2 x = __fmul2_rn(make_float2(v[k], v[k + 1]), make_float2(f, f));
+    v[k] = x.x;
+    v[k + 1] = x.y;
+  }
+  if constexpr (DH == 64) {
+    tmem_store128(tdv, tdv + 32, tdk, tdk + 32, v);
+  } else {
+    tmem_store32(tdv, *reinterpret_cast<const float(*)[32]>(&v[0]));
+    tmem_store32(tdk, *reinterpret_cast<const float(*)[32]>(&v[32]));
+  }
 }
 
 template <int D>
@@ -157,6 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars.pds, 8);
     mbar_init(&bars.mma2, 1);
     mbar_init(&bars.mma_done, 1);
+    mbar_init(&bars.dq_staged, 8);
+    mbar_init(&bars.dq_free, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -264,6 +280,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bars.mma_done);
       wait_drain(&bars.mma_done, 0, wd, 310);
     }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ dQ reducer
+    // Adds each staged dQ tile into global dQ (one bulk reduce per 32-column
+    // box) and frees the staging tile once the copies have read it, so that
+    // no compute thread waits on the bulk copies.
+    if (lane == 0) {
+      for (int m = 0; m < n_iter; ++m) {
+        if (!wait(&bars.dq_staged, m & 1, wd, 314)) break;
+#pragma unroll
+        for (int bx = 0; bx < D / 32; ++bx)
+          tma_reduce_add_3d(&tmDQ, sm + L::kDQ + bx * (kTile * 128), bx * 32, (qt0 + m) * kTile, bh0);
+        bulk_commit();
+        bulk_wait_read_all();
+        mbar_arrive(&bars.dq_free);
+      }
+      bulk_wait_all();
+    }
   } else if (warp >= 4) {
     // -------------------------------------------------------------- compute
     const int wg = (warp - 4) >> 2;
@@ -284,23 +317,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ct < 128) return qi < a.N ? lse[(size_t)bh_n * a.N + qi] : INFINITY;
       return qi < a.N ? delta[(size_t)bh_n * a.N + qi] : 0.0f;
     };
-    // query tile of the current and of the next iteration (one query head)
+    // Stores this thread's element of iteration m's LSE (negated, log2
+    // units) or delta (negated) into the double-buffered shared copy.  The
+    // copy for m + 1 is written during m, before m's dS barrier, which orders
+    // it before every read in m + 1 (and after every read of the same buffer
+    // in m - 1).
+    auto stage_row = [&](int m, float value) {
+      if (ct < 128)
+        s_lse[m & 1][ct] = -value * kLog2e;  // one packed FMA per pair below
+      else
+        s_dl[m & 1][ct - 128] = -value;
+    };
     const int bh = bh0;
-    int qt = qt0, qt_next = qt0;
-    float pre_row = n_iter > 0 ? row_value(bh, qt) : 0.0f;
+    int qt = qt0;  // query tile of the current iteration (one query head)
+    if (n_iter > 0) stage_row(0, row_value(bh, qt0));
+    float row_next = n_iter > 1 ? row_value(bh, qt0 + 1) : 0.0f;  // staged during iteration 0
     float pre_sq = n_iter > 0 ? a.q_scales[bh * a.T + qt] : 0.0f;
     float pre_sdo = n_iter > 0 ? a.do_scales[bh * a.T + qt] : 0.0f;
     float prev_cdq = 0.0f;  // dQ scale of the previous iteration, drained one iteration late
-    int prev_bh = bh, prev_qi0 = qt * kTile;  // where the previous iteration's dQ goes
+    named_bar_sync(1, 256);
 
     // dQ(m) (query rows on TMEM lanes of buffer m%2): scaled, staged in shared
     // memory with the 128-byte swizzle of the dQ tensor map, then added into
     // global dQ by one bulk reduce per 32-column box.  TMEM loads are
     // warp-collective: every lane loads; rows beyond N are clipped by the map.
-    // The caller guarantees that the previous reduce has read the staging tile.
-    auto drain_dq = [&](int m, float cdq, int bh_m, int qi0_m) {
+    // The reducer warp adds the staged tile into global dQ; drain m waits
+    // until it has read the tile of m - 1.
+    auto drain_dq = [&](int m, float cdq) {
       const int bm = m & 1;
       wait(&bars.mma2, m & 1, wd, 311);
+      if (m >= 1) wait(&bars.dq_free, (m - 1) & 1, wd, 315);
       tc_fence_after();
       // 32 columns at a time (the P registers of the current iteration are live)
 #pragma unroll
@@ -316,37 +362,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.bfree[bm]);
       fence_proxy_async_smem();
-      named_bar_sync(2, 256);
-      if (ct == 0 && cdq != 0.0f) {
-#pragma unroll
-        for (int bx = 0; bx < D / 32; ++bx)
-          tma_reduce_add_3d(&tmDQ, sm + L::kDQ + bx * (kTile * 128), bx * 32, qi0_m, bh_m);
-        bulk_commit();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars.bfree[bm]);
+        mbar_arrive(&bars.dq_staged);
       }
     };
 
-    for (int n = 0; n < n_iter; ++n) {
-      qt = qt_next;
+    for (int n = 0; n < n_iter; ++n, ++qt) {
       const int qi0 = qt * kTile;
       const int bn = n & 1;
       const uint32_t ph = (n >> 1) & 1;
-      if (ct < 128)
-        s_lse[bn][ct] = -pre_row * kLog2e;  // stored negated: one packed FMA per pair below
-      else
-        s_dl[bn][ct - 128] = -pre_row;
       const float sq = pre_sq, sdo = pre_sdo;
       if (n + 1 < n_iter) {
-        ++qt_next;
-        pre_row = row_value(bh, qt_next);
-        pre_sq = a.q_scales[bh * a.T + qt_next];
-        pre_sdo = a.do_scales[bh * a.T + qt_next];
+        pre_sq = a.q_scales[bh * a.T + qt + 1];
+        pre_sdo = a.do_scales[bh * a.T + qt + 1];
       }
-      // the previous dQ reduce has finished reading the staging tile
-      if (ct == 0) bulk_wait_read_all();
-      named_bar_sync(1, 256);
       const float c1 = a.sigma * sq * sk * kLog2e;
       const float cdp = sdo * svv;
       const int cmin = !kv_valid ? (1 << 30) : (a.causal && qt == kt) ? r - wg * 64 : 0;
@@ -403,9 +435,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 
+      // LSE / delta of the next iteration (read after this iteration's dS barrier)
+      if (n + 1 < n_iter) {
+        stage_row(n + 1, row_next);
+        if (n + 2 < n_iter) row_next = row_value(bh, qt + 2);
+      }
+
       // previous iteration's dQ; its completion also means dV/dK(n-1) are done
-      if (n >= 1) drain_dq(n - 1, prev_cdq, prev_bh, prev_qi0);
-      const int mode_dv = next_unit(unit_dv, sp * sdo, tl + 256 + wg * DH, DH);
+      if (n >= 1) drain_dq(n - 1, prev_cdq);
 
       // dS = P (dP - delta), computed in place over p (P in FP32 is not needed
       // once its codes are written), its tile amax and E5M2 codes
@@ -455,19 +492,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(dst + SwTile<128>::chunk_offset(r, wg * 4 + c)) =
               make_uint4(dcode[4 * c], dcode[4 * c + 1], dcode[4 * c + 2], dcode[4 * c + 3]);
       }
-      const int mode_dk = next_unit(unit_dk, a.sigma * sds * sq, tl + 384 + wg * DH, DH);
-      if (ct == 0) {
-        s_mode[bn][0] = mode_dv;
-        s_mode[bn][1] = mode_dk;
-      }
-      prev_cdq = a.sigma * sds * sk;
-      prev_bh = bh;
-      prev_qi0 = qi0;
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.pds);
-
       // per-query-row diagnostics (column sums over the key rows)
       if (want_diag) {
         const size_t rowbase = (size_t)bh * a.N + qi0 + wg * 64;
@@ -510,11 +534,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+
+      // both accumulators into the units of this iteration's products (dV/dK
+      // of n - 1 completed before the drain above)
+      float fv, fk;
+      const int mode_dv = unit_step(unit_dv, sp * sdo, fv);
+      const int mode_dk = unit_step(unit_dk, a.sigma * sds * sq, fk);
+      if (fv != 1.0f || fk != 1.0f) rescale_pair<DH>(tl + 256 + wg * DH, fv, tl + 384 + wg * DH, fk);
+      if (ct == 0) {
+        s_mode[bn][0] = mode_dv;
+        s_mode[bn][1] = mode_dk;
+      }
+      prev_cdq = a.sigma * sds * sk;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.pds);
+
     }
     if (n_iter > 0) {
-      if (ct == 0) bulk_wait_read_all();
-      named_bar_sync(1, 256);
-      drain_dq(n_iter - 1, prev_cdq, prev_bh, prev_qi0);
+      drain_dq(n_iter - 1, prev_cdq);
+      wait(&bars.dq_free, (n_iter - 1) & 1, wd, 316);  // the last dQ tile has been read
     }
     // epilogue: this head's dV and dK tiles in true units, staged like dQ
     // (after the last dQ reduce has read the staging tile) and added into
