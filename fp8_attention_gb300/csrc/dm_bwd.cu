@@ -392,13 +392,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.sread[bn]);
       const float2 c1_2 = make_float2(c1, c1);
-      const float2* nlse2 = reinterpret_cast<const float2*>(&s_lse[bn][wg * 64]);
+      const float4* nlse4 = reinterpret_cast<const float4*>(&s_lse[bn][wg * 64]);  // broadcast reads
       float pm0 = 0.0f, pm1 = 0.0f;
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        const float2 x = __ffma2_rn(make_float2(p[c], p[c + 1]), c1_2, nlse2[c / 2]);
-        p[c] = ex2(x.x);
-        p[c + 1] = ex2(x.y);
+      for (int c = 0; c < 64; c += 4) {
+        const float4 l4 = nlse4[c / 4];
+        const float2 x01 = __ffma2_rn(make_float2(p[c], p[c + 1]), c1_2, make_float2(l4.x, l4.y));
+        const float2 x23 = __ffma2_rn(make_float2(p[c + 2], p[c + 3]), c1_2, make_float2(l4.z, l4.w));
+        p[c] = ex2(x01.x);
+        p[c + 1] = ex2(x01.y);
+        p[c + 2] = ex2(x23.x);
+        p[c + 3] = ex2(x23.y);
       }
       if (cmin > 0) {  // diagonal tile or absent key row: mask
 #pragma unroll
@@ -450,23 +454,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait(&bars.dpfull[bn], ph, wd, 313);
       tc_fence_after();
       const float2 cdp2 = make_float2(cdp, cdp);
-      const float2* ndl2 = reinterpret_cast<const float2*>(&s_dl[bn][wg * 64]);
+      const float4* ndl4 = reinterpret_cast<const float4*>(&s_dl[bn][wg * 64]);  // broadcast reads
       float dm0 = 0.0f, dm1 = 0.0f;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float dp[32];
         tmem_load32(tl + bn * 128 + wg * 64 + h * 32, dp);
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
+        for (int c = 0; c < 32; c += 4) {
           const int cc = h * 32 + c;
-          const float2 d2 = __fmul2_rn(make_float2(p[cc], p[cc + 1]),
-                                       __ffma2_rn(make_float2(dp[c], dp[c + 1]), cdp2, ndl2[cc / 2]));
-          ds[cc] = d2.x;
-          ds[cc + 1] = d2.y;
-          if (c & 2)
-            dm1 = max3(dm1, fabsf(d2.x), fabsf(d2.y));
-          else
-            dm0 = max3(dm0, fabsf(d2.x), fabsf(d2.y));
+          const float4 l4 = ndl4[cc / 4];
+          const float2 d01 = __fmul2_rn(make_float2(p[cc], p[cc + 1]),
+                                        __ffma2_rn(make_float2(dp[c], dp[c + 1]), cdp2, make_float2(l4.x, l4.y)));
+          const float2 d23 = __fmul2_rn(make_float2(p[cc + 2], p[cc + 3]),
+                                        __ffma2_rn(make_float2(dp[c + 2], dp[c + 3]), cdp2, make_float2(l4.z, l4.w)));
+          ds[cc] = d01.x;
+          ds[cc + 1] = d01.y;
+          ds[cc + 2] = d23.x;
+          ds[cc + 3] = d23.y;
+          dm0 = max3(dm0, fabsf(d01.x), fabsf(d01.y));
+          dm1 = max3(dm1, fabsf(d23.x), fabsf(d23.y));
         }
       }
       float dmax = fmaxf(dm0, dm1);
