@@ -42,7 +42,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic of one backward launch on the default workload, from the ncu
 # capture summarised in profiles/ (valid only for the kernel source it was
 # taken on; reported as null once dm_bwd.cu changes).
-BWD_TRAFFIC = {"sha1": "c6cf319279dd6b864f5fc2ab10ec24bfac4feab6", "bytes": 167229056}
+BWD_TRAFFIC = {"sha1": "74f18abf8ff85862185339247be5b64e7a2f28bd", "bytes": 268921344}
 
 
 def parse():
@@ -267,6 +267,12 @@ def run_native(args, rank, world, local_rank):
             "fwd": round(fl["fwd"] / (kernel_ms["fwd"] * 1e-3) / 1e12, 1),
             "delta": round(fl["delta"] / (kernel_ms["delta"] * 1e-3) / 1e12, 1),
             "bwd": round(bwd_tflops, 1)},
+        # the flash-attention convention: fwd + bwd = 7U over the attention
+        # kernels' time (the delta pass counted as part of the backward)
+        "tflops_7U": round((fl["fwd"] + fl["bwd"]) / ((kernel_ms["fwd"] + kernel_ms["delta"] + kernel_ms["bwd"]) * 1e-3)
+                           / 1e12, 1),
+        # quantisation of Q, K, V, dO: 2 B read + 1 B code written per element, plus the tile scales
+        "quantize_gbs": round(quant_bytes(w) / (kernel_ms["quantize"] * 1e-3) / 1e9, 1),
         "roofline": {"kernel": "attn_bwd_kernel<128>", "bound": "tensor", "achieved": round(bwd_tflops, 1),
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(bwd_tflops / fp8_peak, 4),
                      "peak_source": f"{src} bf16 burst x {FP8_PER_BF16} (fp8/bf16 nominal ratio)",
@@ -282,6 +288,17 @@ def run_native(args, rank, world, local_rank):
     if dist:
         dist.destroy_process_group()
     return line
+
+
+def quant_bytes(w):
+    """Algorithmic HBM bytes of quantising Q, K, V and dO (bf16 in, FP8 codes and FP32 tile scales out)."""
+    el_q = w.B * w.Hq * w.N * w.d
+    el_kv = w.B * w.Hkv * w.N * w.d
+    tiles = (w.N + 127) // 128
+    in_bytes = 2 if w.storage == "bf16" else 4
+    elements = 2 * el_q + 2 * el_kv
+    scales = 4 * tiles * (2 * w.B * w.Hq + 2 * w.B * w.Hkv)
+    return elements * (in_bytes + 1) + scales
 
 
 # ------------------------------------------------------------------ oracle
