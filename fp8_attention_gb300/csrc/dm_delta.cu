@@ -1,11 +1,12 @@
 // Matched softmax row correction ("Delta-Matching for reliable FP8 attention
 // training", section 03): delta_i = sum_j P_ij * dP^_ij / sum_j P_ij with
 // P = exp(S - LSE) the FP32 softmax before quantisation and dP^ = dO^ V^T the
-// FP32 result of the FP8 matmul.  Section 03 cancels the row sum of dS "after
-// using sum_j P_ij = 1"; with P held in FP32 (and LSE stored in FP32) that sum
-// is 1 + eta, and dividing by it makes the cancellation hold for the P the
-// backward actually uses (identical to the undivided form when P sums to 1).  This is the separate correction pass: one CTA per (batch,
-// query head, 128-row query tile), recomputing S = Q K^T and dP^ = dO^ V^T
+// FP32 result of the FP8 matmul.  Section 03 cancels the row sum of dS by
+// using that each row of P sums to one; with P held in FP32 (and LSE stored
+// in FP32) that sum is 1 + eta, and dividing by it makes the cancellation
+// hold for the P the backward actually uses (identical to the undivided form
+// when P sums to 1).  This is the separate correction pass: one CTA per
+// (batch, query head, 128-row query tile), recomputing S = Q K^T and dP^ = dO^ V^T
 // on tcgen05 tile by tile.
 //
 // Warp roles (640 threads):

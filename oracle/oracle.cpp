@@ -107,8 +107,8 @@ uint8_t fp8_encode(float x, int f) {
 }
 
 // Tile quantiser Qz: one FP32 scale per tile, derived from the tile's amax.
-// The pages only say "block scales" (project page, section 01, "What changes
-// in FP8?"); the rule used here is the plain amax rule:
+// The pages name per-block scales but give no rule (project page, section 01,
+// "What changes in FP8?"); the rule used here is the plain amax rule:
 //   amax = max |x| over the tile (exact),
 //   if amax < 2^-96 (zero, subnormal or tiny tile): scale 0, all codes +0,
 //   else s = fl32(amax / FMAX), r = fl32(FMAX / amax), code = enc(fl32(x * r)).
@@ -261,8 +261,8 @@ void or_dequantize(const uint8_t* codes, const float* scales, int B, int H, int 
 //
 // Without OR_QUANT_P_FWD this is the plain definition, row by row, in FP64.
 // With it, the probabilities are quantised the only way a one-pass kernel can
-// (the pages leave this step open and assume P normalised "to isolate operand
-// rounding"): key tiles t = 0, 1, ... in ascending order, running row max
+// (the pages leave this step open; their analysis takes P as normalised so
+// that only the rounding of the operands enters): key tiles t = 0, 1, ... in ascending order, running row max
 // m^(t), P~_ij = exp(S_ij - m^(t)_i) (rounded to FP32 under OR_ROUND32),
 // P~ quantised per 128x128 tile (E4M3), l_i accumulated from the unquantised
 // P~, and earlier partial sums rescaled by exp(m^(t-1) - m^(t)).  Then
@@ -390,8 +390,8 @@ int or_attn_fwd(int B, int Hq, int Hkv, int N, int d, int causal, double sigma, 
 //   matched      (section 03): delta_i = sum_j P_ij dP^_ij / sum_j P_ij with
 //                P the FP32 softmax before quantisation, P_ij = exp(S_ij -
 //                LSE_i), and dP^ = dO^ V^T accumulated exactly over the decoded
-//                operands.  Section 03 cancels the row sum of dS "after using
-//                sum_j P_ij = 1"; P in FP32 with a stored FP32 LSE sums to
+//                operands.  Section 03 cancels the row sum of dS by using that
+//                each row of P sums to one; P in FP32 with a stored FP32 LSE sums to
 //                1 + eta, and the division makes the cancellation hold for the
 //                P the backward uses (no change when P sums to 1 exactly);
 //   stale_dO     (section 01, "Why can we reuse the forward output?" and

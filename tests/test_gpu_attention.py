@@ -83,7 +83,7 @@ def test_delta_computed_inside_backward():
 
 
 def rowsum_check(rs, ab, delta):
-    """Matched delta restores zero row sums of dS "up to FP32 rounding" (project page section 03):
+    """Matched delta brings the row sums of dS back to zero within FP32 rounding (project page section 03):
     every row must satisfy |sum_j dS_ij| <= 1e-4 * sum_j |dS_ij| + 2^-20 * |delta_i|.  The second
     term is the FP32 resolution of delta (16 units in its last place): in near-one-hot rows
     sum_j |dS_ij| is only ~1e-3 |delta_i| (one key carries P ~ 1 and dP ~ delta), and the relative
