@@ -127,24 +127,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmV);
       mbar_arrive_expect_tx(&bars.q, L::kTileBytes);
       tma_load_3d(sm + L::kQ, &tmQ, &bars.q, 0, q0, bh);
-      int issued = 0;  // K/V tiles whose loads were issued (stops early on abort)
-      for (int t = 0; t < nkv; ++t) {
-        const int s = t & 1;
-        const uint32_t ph = (t >> 1) & 1;
-        if (!wait(&bars.kempty[s], ph ^ 1, wd, 101)) break;
-        if (!wait(&bars.vempty[s], ph ^ 1, wd, 102)) break;
-        mbar_arrive_expect_tx(&bars.kfull[s], L::kTileBytes);
-        tma_load_3d(sm + L::kK + s * L::kTileBytes, &tmK, &bars.kfull[s], 0, t * kTile, bg);
-        mbar_arrive_expect_tx(&bars.vfull[s], L::kTileBytes);
-        tma_load_3d(sm + L::kV + s * L::kTileBytes, &tmV, &bars.vfull[s], 0, t * kTile, bg);
-        issued = t + 1;
+      // K runs one tile ahead of V: K(t) needs only S(t-2) to have finished
+      // with its stage, V(t) needs P V(t-2), which completes a tile later.
+      int k_issued = 0, v_issued = 0;  // loads issued (both stop early on abort)
+      for (int t = 0; t <= nkv; ++t) {
+        if (t < nkv) {
+          const int s = t & 1;
+          if (!wait(&bars.kempty[s], ((t >> 1) & 1) ^ 1, wd, 101)) break;
+          mbar_arrive_expect_tx(&bars.kfull[s], L::kTileBytes);
+          tma_load_3d(sm + L::kK + s * L::kTileBytes, &tmK, &bars.kfull[s], 0, t * kTile, bg);
+          k_issued = t + 1;
+        }
+        if (t >= 1) {
+          const int u = t - 1, s = u & 1;
+          if (!wait(&bars.vempty[s], ((u >> 1) & 1) ^ 1, wd, 102)) break;
+          mbar_arrive_expect_tx(&bars.vfull[s], L::kTileBytes);
+          tma_load_3d(sm + L::kV + s * L::kTileBytes, &tmV, &bars.vfull[s], 0, u * kTile, bg);
+          v_issued = u + 1;
+        }
       }
       // every issued load has landed before the CTA may exit
       wait_drain(&bars.q, 0, wd, 116);
-      for (int t = max(0, issued - 2); t < issued; ++t) {
-        wait_drain(&bars.kfull[t & 1], (t >> 1) & 1, wd, 117);
-        wait_drain(&bars.vfull[t & 1], (t >> 1) & 1, wd, 118);
-      }
+      for (int t = max(0, k_issued - 2); t < k_issued; ++t) wait_drain(&bars.kfull[t & 1], (t >> 1) & 1, wd, 117);
+      for (int t = max(0, v_issued - 2); t < v_issued; ++t) wait_drain(&bars.vfull[t & 1], (t >> 1) & 1, wd, 118);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer
