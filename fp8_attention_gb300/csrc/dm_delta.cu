@@ -33,6 +33,9 @@ constexpr int kGroups = 4;            // compute warpgroups
 constexpr int kThreads = 128 + 128 * kGroups;  // warps 0-3: TMA, MMA, two idle; then the compute warpgroups
 constexpr int kCols = kTile / kGroups;  // key columns per thread
 constexpr float kLog2e = 1.4426950408889634f;
+// K/V shared-memory stages: loads run up to kKV - 1 tiles ahead of the
+// products, which covers the L2 latency of a tile load.
+constexpr int kKV = 2;
 
 template <int D>
 struct DeltaLayout {
@@ -40,13 +43,13 @@ struct DeltaLayout {
   static constexpr int kQ = 0;
   static constexpr int kDO = kQ + kTileBytes;
   static constexpr int kK = kDO + kTileBytes;      // 2 stages
-  static constexpr int kV = kK + 2 * kTileBytes;   // 2 stages
-  static constexpr int kBytes = kV + 2 * kTileBytes;
+  static constexpr int kV = kK + kKV * kTileBytes;  // kKV stages
+  static constexpr int kBytes = kV + kKV * kTileBytes;
   static constexpr int kDynSmem = kBytes + 1024;
 };
 
 struct DeltaBars {
-  uint64_t q, kfull[2], kempty[2], vfull[2], vempty[2], sfull[2], dpfull[2], tempty[2], mma_done;
+  uint64_t q, kfull[kKV], kempty[kKV], vfull[kKV], vempty[kKV], sfull[2], dpfull[2], tempty[2], mma_done;
 };
 
 template <int D>
@@ -75,11 +78,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     s_abort = 0;
     mbar_init(&bars.q, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kKV; ++s) {
       mbar_init(&bars.kfull[s], 1);
       mbar_init(&bars.kempty[s], 1);
       mbar_init(&bars.vfull[s], 1);
       mbar_init(&bars.vempty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&bars.sfull[s], 1);
       mbar_init(&bars.dpfull[s], 1);
       mbar_init(&bars.tempty[s], 4 * kGroups);
@@ -107,8 +112,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_3d(sm + L::kDO, &tmDO, &bars.q, 0, q0, bh);
       int issued = 0;
       for (int t = 0; t < nkv; ++t) {
-        const int s = t & 1;
-        const uint32_t ph = (t >> 1) & 1;
+        const int s = t % kKV;
+        const uint32_t ph = (t / kKV) & 1;
         if (!wait(&bars.kempty[s], ph ^ 1, wd, 201)) break;
         if (!wait(&bars.vempty[s], ph ^ 1, wd, 202)) break;
         mbar_arrive_expect_tx(&bars.kfull[s], L::kTileBytes);
@@ -118,9 +123,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued = t + 1;
       }
       wait_drain(&bars.q, 0, wd, 209);
-      for (int t = max(0, issued - 2); t < issued; ++t) {
-        wait_drain(&bars.kfull[t & 1], (t >> 1) & 1, wd, 210);
-        wait_drain(&bars.vfull[t & 1], (t >> 1) & 1, wd, 211);
+      for (int t = max(0, issued - kKV); t < issued; ++t) {
+        wait_drain(&bars.kfull[t % kKV], (t / kKV) & 1, wd, 210);
+        wait_drain(&bars.vfull[t % kKV], (t / kKV) & 1, wd, 211);
       }
     }
   } else if (warp == 1) {
@@ -131,26 +136,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t sQ = smem_u32(sm + L::kQ), sDO = smem_u32(sm + L::kDO);
       for (int t = 0; t < nkv && ok; ++t) {
-        const int s = t & 1;
+        const int s = t & 1;  // TMEM buffers
         const uint32_t ph = (t >> 1) & 1;
-        ok = wait(&bars.tempty[s], ph ^ 1, wd, 204) && wait(&bars.kfull[s], ph, wd, 205);
+        const int ks = t % kKV;  // K/V stage
+        const uint32_t kph = (t / kKV) & 1;
+        ok = wait(&bars.tempty[s], ph ^ 1, wd, 204) && wait(&bars.kfull[ks], kph, wd, 205);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t sK = smem_u32(sm + L::kK + s * L::kTileBytes);
+        const uint32_t sK = smem_u32(sm + L::kK + ks * L::kTileBytes);
 #pragma unroll
         for (int k = 0; k < D / 32; ++k)
           mma_f8(tmem + s * 128, SwTile<D>::kmajor(sQ, k), SwTile<D>::kmajor(sK, k), kIdS, k > 0);
         mma_commit(&bars.sfull[s]);
-        mma_commit(&bars.kempty[s]);
-        ok = wait(&bars.vfull[s], ph, wd, 206);
+        mma_commit(&bars.kempty[ks]);
+        ok = wait(&bars.vfull[ks], kph, wd, 206);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t sV = smem_u32(sm + L::kV + s * L::kTileBytes);
+        const uint32_t sV = smem_u32(sm + L::kV + ks * L::kTileBytes);
 #pragma unroll
         for (int k = 0; k < D / 32; ++k)
           mma_f8(tmem + 256 + s * 128, SwTile<D>::kmajor(sDO, k), SwTile<D>::kmajor(sV, k), kIdDP, k > 0);
         mma_commit(&bars.dpfull[s]);
-        mma_commit(&bars.vempty[s]);
+        mma_commit(&bars.vempty[ks]);
       }
       mma_commit(&bars.mma_done);
       wait_drain(&bars.mma_done, 0, wd, 212);

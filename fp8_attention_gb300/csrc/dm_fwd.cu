@@ -36,11 +36,12 @@ constexpr int kGroups = 2;                // compute warpgroups
 constexpr int kWarps = 4 * kGroups;      // compute warps
 constexpr int kThreads = 128 + 32 * kWarps;  // warps 0-3: TMA, MMA, two idle; then the compute warpgroups
 constexpr int kCols = kTile / kGroups;    // key columns per thread
+constexpr int kKV = 4;                    // K and V shared-memory stages (loads run ahead of the products)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct FwdBars {
-  uint64_t q, kfull[2], kempty[2], vfull[2], vempty[2], sfull[2], sempty[2], pfull[2], ofull[2], oempty[2],
+  uint64_t q, kfull[kKV], kempty[kKV], vfull[kKV], vempty[kKV], sfull[2], sempty[2], pfull[2], ofull[2], oempty[2],
       stall, mma_done;
 };
 
@@ -50,9 +51,9 @@ template <int D>
 struct FwdLayout {
   static constexpr int kTileBytes = kTile * D;  // one FP8 Q/K/V tile
   static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTileBytes;              // 2 stages
-  static constexpr int kV = kK + 2 * kTileBytes;          // 2 stages
-  static constexpr int kP = kV + 2 * kTileBytes;          // 2 x (128 x 128) P^ codes
+  static constexpr int kK = kQ + kTileBytes;              // kKV stages
+  static constexpr int kV = kK + kKV * kTileBytes;        // kKV stages
+  static constexpr int kP = kV + kKV * kTileBytes;        // 2 x (128 x 128) P^ codes
   static constexpr int kRmax = kP + 2 * kTile * kTile;          // float [2][kGroups][128] partial row maxima
   static constexpr int kRed = kRmax + 2 * kGroups * kTile * 4;  // float [2][kWarps] tile amax partials
   static constexpr int kL = kRed + 2 * kWarps * 4;              // float [kGroups][128] row sums
@@ -96,15 +97,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     *s_abort = 0;
     mbar_init(&bars.q, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars.kfull[s], 1);
-      mbar_init(&bars.kempty[s], 1);
-      mbar_init(&bars.vfull[s], 1);
-      mbar_init(&bars.vempty[s], 1);
       mbar_init(&bars.sfull[s], 1);
       mbar_init(&bars.sempty[s], kWarps);
       mbar_init(&bars.pfull[s], kWarps);
       mbar_init(&bars.ofull[s], 1);
       mbar_init(&bars.oempty[s], kWarps);
+    }
+    for (int s = 0; s < kKV; ++s) {
+      mbar_init(&bars.kfull[s], 1);
+      mbar_init(&bars.kempty[s], 1);
+      mbar_init(&bars.vfull[s], 1);
+      mbar_init(&bars.vempty[s], 1);
     }
     mbar_init(&bars.stall, 1);
     mbar_init(&bars.mma_done, 1);
@@ -132,15 +135,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       int k_issued = 0, v_issued = 0;  // loads issued (both stop early on abort)
       for (int t = 0; t <= nkv; ++t) {
         if (t < nkv) {
-          const int s = t & 1;
-          if (!wait(&bars.kempty[s], ((t >> 1) & 1) ^ 1, wd, 101)) break;
+          const int s = t % kKV;
+          if (!wait(&bars.kempty[s], ((t / kKV) & 1) ^ 1, wd, 101)) break;
           mbar_arrive_expect_tx(&bars.kfull[s], L::kTileBytes);
           tma_load_3d(sm + L::kK + s * L::kTileBytes, &tmK, &bars.kfull[s], 0, t * kTile, bg);
           k_issued = t + 1;
         }
         if (t >= 1) {
-          const int u = t - 1, s = u & 1;
-          if (!wait(&bars.vempty[s], ((u >> 1) & 1) ^ 1, wd, 102)) break;
+          const int u = t - 1, s = u % kKV;
+          if (!wait(&bars.vempty[s], ((u / kKV) & 1) ^ 1, wd, 102)) break;
           mbar_arrive_expect_tx(&bars.vfull[s], L::kTileBytes);
           tma_load_3d(sm + L::kV + s * L::kTileBytes, &tmV, &bars.vfull[s], 0, u * kTile, bg);
           v_issued = u + 1;
@@ -148,8 +151,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // every issued load has landed before the CTA may exit
       wait_drain(&bars.q, 0, wd, 116);
-      for (int t = max(0, k_issued - 2); t < k_issued; ++t) wait_drain(&bars.kfull[t & 1], (t >> 1) & 1, wd, 117);
-      for (int t = max(0, v_issued - 2); t < v_issued; ++t) wait_drain(&bars.vfull[t & 1], (t >> 1) & 1, wd, 118);
+      for (int t = max(0, k_issued - kKV); t < k_issued; ++t)
+        wait_drain(&bars.kfull[t % kKV], (t / kKV) & 1, wd, 117);
+      for (int t = max(0, v_issued - kKV); t < v_issued; ++t)
+        wait_drain(&bars.vfull[t % kKV], (t / kKV) & 1, wd, 118);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer
@@ -170,30 +175,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t < nkv) {
           const int s = t & 1;
           const uint32_t ph = (t >> 1) & 1;
-          ok = wait(&bars.kfull[s], ph, wd, 105) && wait(&bars.sempty[s], ph ^ 1, wd, 106);
+          const int ks = t % kKV;
+          ok = wait(&bars.kfull[ks], (t / kKV) & 1, wd, 105) && wait(&bars.sempty[s], ph ^ 1, wd, 106);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t sK = smem_u32(sm + L::kK + s * L::kTileBytes);
+          const uint32_t sK = smem_u32(sm + L::kK + ks * L::kTileBytes);
 #pragma unroll
           for (int k = 0; k < D / 32; ++k)
             mma_f8(tmem + s * 128, SwTile<D>::kmajor(sQ, k), SwTile<D>::kmajor(sK, k), kIdS, k > 0);
           mma_commit(&bars.sfull[s]);
-          mma_commit(&bars.kempty[s]);
+          mma_commit(&bars.kempty[ks]);
         }
         if (t >= 1) {
           const int u = t - 1, s = u & 1;
           const uint32_t ph = (u >> 1) & 1;
-          ok = wait(&bars.pfull[s], ph, wd, 107) && wait(&bars.vfull[s], ph, wd, 108) &&
+          const int vs = u % kKV;
+          ok = wait(&bars.pfull[s], ph, wd, 107) && wait(&bars.vfull[vs], (u / kKV) & 1, wd, 108) &&
                wait(&bars.oempty[s], ph ^ 1, wd, 109);
           if (!ok) break;
           tc_fence_after();
           const uint32_t sP = smem_u32(sm + L::kP + s * kTile * kTile);
-          const uint32_t sV = smem_u32(sm + L::kV + s * L::kTileBytes);
+          const uint32_t sV = smem_u32(sm + L::kV + vs * L::kTileBytes);
 #pragma unroll
           for (int k = 0; k < kTile / 32; ++k)
             mma_f8(tmem + 256 + s * 128, SwTile<128>::kmajor(sP, k), SwTile<D>::mnmajor(sV, k), kIdO, k > 0);
           mma_commit(&bars.ofull[s]);
-          mma_commit(&bars.vempty[s]);
+          mma_commit(&bars.vempty[vs]);
         }
       }
       mma_commit(&bars.mma_done);
