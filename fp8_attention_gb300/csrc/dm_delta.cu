@@ -11,8 +11,8 @@
 //
 // Warp roles (640 threads):
 //   warp 0      TMA: Q and dO tiles once, K/V tiles double-buffered
-//   warp 1      MMA: S(t) into TMEM S[t%2], dP(t) into TMEM dP[t%2]
-//   warps 2-3   idle (each warpgroup starts at a multiple of four warps)
+//   warps 1, 3  MMA issuers: S(t) into TMEM S[t%2] (warp 1), dP(t) into TMEM dP[t%2] (warp 3)
+//   warp 2      idle (each warpgroup starts at a multiple of four warps)
 //   warps 4-19  four warpgroups, one thread per (query row, quarter of the
 //               key columns): P = exp2(S*c1 - LSE*log2e), sums of P*dP
 //               (scaled by s_dO * s_V,t per key tile) and of P.  Sixteen
@@ -30,7 +30,7 @@ namespace dm {
 namespace {
 
 constexpr int kGroups = 4;            // compute warpgroups
-constexpr int kThreads = 128 + 128 * kGroups;  // warps 0-3: TMA, MMA, two idle; then the compute warpgroups
+constexpr int kThreads = 128 + 128 * kGroups;  // warps 0-3: TMA, S issuer, idle, dP issuer; then compute
 constexpr int kCols = kTile / kGroups;  // key columns per thread
 constexpr float kLog2e = 1.4426950408889634f;
 // K/V shared-memory stages: loads run up to kKV - 1 tiles ahead of the
@@ -49,7 +49,7 @@ struct DeltaLayout {
 };
 
 struct DeltaBars {
-  uint64_t q, kfull[kKV], kempty[kKV], vfull[kKV], vempty[kKV], sfull[2], dpfull[2], tempty[2], mma_done;
+  uint64_t q, kfull[kKV], kempty[kKV], vfull[kKV], vempty[kKV], sfull[2], dpfull[2], tempty[2], mma_done, mma_done2;
 };
 
 template <int D>
@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.tempty[s], 4 * kGroups);
     }
     mbar_init(&bars.mma_done, 1);
+    mbar_init(&bars.mma_done2, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -128,39 +129,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_drain(&bars.vfull[t % kKV], (t / kKV) & 1, wd, 211);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 3) {
+    // Two MMA issuers: warp 1 issues S = Q K^T, warp 3 dP = dO^ V^T.  A
+    // thread that issues tcgen05.mma stalls on its own mbarrier operations;
+    // with two issuers one keeps the tensor pipe fed while the other waits.
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_f8(0, 0, 0, 0, kTile, kTile);   // Q K^T
-      constexpr uint32_t kIdDP = idesc_f8(1, 0, 0, 0, kTile, kTile);  // dO^ (E5M2) V^T (E4M3)
+      const bool is_s = warp == 1;
+      const uint32_t idesc = is_s ? idesc_f8(0, 0, 0, 0, kTile, kTile)   // Q K^T
+                                  : idesc_f8(1, 0, 0, 0, kTile, kTile);  // dO^ (E5M2) V^T (E4M3)
+      uint64_t* full = is_s ? bars.sfull : bars.dpfull;
+      uint64_t* operand_full = is_s ? bars.kfull : bars.vfull;
+      uint64_t* operand_empty = is_s ? bars.kempty : bars.vempty;
+      const uint32_t dcol = is_s ? 0u : 256u;
       bool ok = wait(&bars.q, 0, wd, 203);
       tc_fence_after();
-      const uint32_t sQ = smem_u32(sm + L::kQ), sDO = smem_u32(sm + L::kDO);
+      const uint32_t sA = smem_u32(sm + (is_s ? L::kQ : L::kDO));
+      const uint32_t sB0 = smem_u32(sm + (is_s ? L::kK : L::kV));
       for (int t = 0; t < nkv && ok; ++t) {
         const int s = t & 1;  // TMEM buffers
         const uint32_t ph = (t >> 1) & 1;
         const int ks = t % kKV;  // K/V stage
         const uint32_t kph = (t / kKV) & 1;
-        ok = wait(&bars.tempty[s], ph ^ 1, wd, 204) && wait(&bars.kfull[ks], kph, wd, 205);
+        ok = wait(&bars.tempty[s], ph ^ 1, wd, 204) && wait(&operand_full[ks], kph, wd, is_s ? 205 : 206);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t sK = smem_u32(sm + L::kK + ks * L::kTileBytes);
+        const uint32_t sB = sB0 + ks * L::kTileBytes;
 #pragma unroll
         for (int k = 0; k < D / 32; ++k)
-          mma_f8(tmem + s * 128, SwTile<D>::kmajor(sQ, k), SwTile<D>::kmajor(sK, k), kIdS, k > 0);
-        mma_commit(&bars.sfull[s]);
-        mma_commit(&bars.kempty[ks]);
-        ok = wait(&bars.vfull[ks], kph, wd, 206);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t sV = smem_u32(sm + L::kV + ks * L::kTileBytes);
-#pragma unroll
-        for (int k = 0; k < D / 32; ++k)
-          mma_f8(tmem + 256 + s * 128, SwTile<D>::kmajor(sDO, k), SwTile<D>::kmajor(sV, k), kIdDP, k > 0);
-        mma_commit(&bars.dpfull[s]);
-        mma_commit(&bars.vempty[ks]);
+          mma_f8(tmem + dcol + s * 128, SwTile<D>::kmajor(sA, k), SwTile<D>::kmajor(sB, k), idesc, k > 0);
+        mma_commit(&full[s]);
+        mma_commit(&operand_empty[ks]);
       }
-      mma_commit(&bars.mma_done);
-      wait_drain(&bars.mma_done, 0, wd, 212);
+      uint64_t* done = is_s ? &bars.mma_done : &bars.mma_done2;
+      mma_commit(done);
+      wait_drain(done, 0, wd, is_s ? 212 : 213);
     }
   } else if (warp >= 4) {
     const int wg = (warp - 4) >> 2;  // key-column quarter
