@@ -2,19 +2,19 @@
 // tile), with both matmuls on tcgen05 FP8 MMAs ("Delta-Matching for reliable
 // FP8 attention training", section 01: "What changes in FP8?").
 //
-// Warp roles (640 threads):
-//   warp 0      TMA producer: Q tile once, K/V tiles double-buffered
-//   warp 1      MMA issuer (+ TMEM owner): S(t) = Q K_t^T into TMEM S[t%2];
-//               O_t = P^_t V_t into TMEM O[t%2]
-//   warps 2-3   idle (each warpgroup starts at a multiple of four warps)
-//   warps 4-19  four warpgroups; thread = query row (TMEM lane), warpgroup =
-//               a quarter of the key columns for the softmax and a quarter
-//               of the d columns for O.  Per key tile t: online row max (the
-//               quarters exchange partial maxima through shared memory), P~
-//               in FP32, the tile's amax -> E4M3 codes into shared memory;
-//               then, one tile behind, O_acc = alpha * O_acc + (s_P * s_V) *
-//               O_{t-1} in registers.  Four compute warps per SM
-//               sub-partition hide each other's TMEM and MUFU latency.
+// Warp roles (384 threads):
+//   warp 0      TMA producer: Q tile once, K/V tiles in kKV stages (K one
+//               tile ahead of V)
+//   warp 1      S issuer (+ TMEM owner): S(t) = Q K_t^T into TMEM S[t%2]
+//   warp 3      O issuer: O_t = P^_t V_t into TMEM O[t%2]
+//   warp 2      idle (each warpgroup starts at a multiple of four warps)
+//   warps 4-11  two warpgroups; thread = query row (TMEM lane), warpgroup =
+//               half of the key columns for the softmax and half of the d
+//               columns for O.  Per key tile t: online row max (the halves
+//               exchange partial maxima through shared memory), P~ in FP32,
+//               the tile's amax -> E4M3 codes into shared memory; then, one
+//               tile behind, O_acc = alpha * O_acc + (s_P * s_V) * O_{t-1} in
+//               registers.
 //
 // Each key tile brings its own FP32 scale product s_P,t * s_V,t, so the
 // tiles' products are summed outside the tensor core.  The O update lags one
@@ -42,7 +42,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 struct FwdBars {
   uint64_t q, kfull[kKV], kempty[kKV], vfull[kKV], vempty[kKV], sfull[2], sempty[2], pfull[2], ofull[2], oempty[2],
-      stall, mma_done;
+      stall, mma_done, mma_done2;
 };
 
 // Everything lives in dynamic shared memory (no static shared variables), so
@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bars.stall, 1);
     mbar_init(&bars.mma_done, 1);
+    mbar_init(&bars.mma_done2, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -157,10 +158,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_drain(&bars.vfull[t % kKV], (t / kKV) & 1, wd, 118);
     }
   } else if (warp == 1) {
-    // ----------------------------------------------------------- MMA issuer
+    // ------------------------------------------------------- S = Q K^T issuer
+    // (two issuing threads: one thread's barrier waits stall its own
+    // tcgen05.mma stream, and the other keeps the tensor pipe fed meanwhile)
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f8(0, 0, 0, 0, kTile, kTile);  // Q K^T, both K-major
-      constexpr uint32_t kIdO = idesc_f8(0, 0, 0, 1, kTile, D);      // P^ (K-major) V (MN-major)
       bool ok = true;
       if (a.stall_test) {
         // watchdog test: a barrier nothing signals, with half the limit so
@@ -171,40 +173,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = ok && wait(&bars.q, 0, wd, 104);
       tc_fence_after();
       const uint32_t sQ = smem_u32(sm + L::kQ);
-      for (int t = 0; t <= nkv && ok; ++t) {
-        if (t < nkv) {
-          const int s = t & 1;
-          const uint32_t ph = (t >> 1) & 1;
-          const int ks = t % kKV;
-          ok = wait(&bars.kfull[ks], (t / kKV) & 1, wd, 105) && wait(&bars.sempty[s], ph ^ 1, wd, 106);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t sK = smem_u32(sm + L::kK + ks * L::kTileBytes);
+      for (int t = 0; t < nkv && ok; ++t) {
+        const int s = t & 1;
+        const uint32_t ph = (t >> 1) & 1;
+        const int ks = t % kKV;
+        ok = wait(&bars.kfull[ks], (t / kKV) & 1, wd, 105) && wait(&bars.sempty[s], ph ^ 1, wd, 106);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sK = smem_u32(sm + L::kK + ks * L::kTileBytes);
 #pragma unroll
-          for (int k = 0; k < D / 32; ++k)
-            mma_f8(tmem + s * 128, SwTile<D>::kmajor(sQ, k), SwTile<D>::kmajor(sK, k), kIdS, k > 0);
-          mma_commit(&bars.sfull[s]);
-          mma_commit(&bars.kempty[ks]);
-        }
-        if (t >= 1) {
-          const int u = t - 1, s = u & 1;
-          const uint32_t ph = (u >> 1) & 1;
-          const int vs = u % kKV;
-          ok = wait(&bars.pfull[s], ph, wd, 107) && wait(&bars.vfull[vs], (u / kKV) & 1, wd, 108) &&
-               wait(&bars.oempty[s], ph ^ 1, wd, 109);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t sP = smem_u32(sm + L::kP + s * kTile * kTile);
-          const uint32_t sV = smem_u32(sm + L::kV + vs * L::kTileBytes);
-#pragma unroll
-          for (int k = 0; k < kTile / 32; ++k)
-            mma_f8(tmem + 256 + s * 128, SwTile<128>::kmajor(sP, k), SwTile<D>::mnmajor(sV, k), kIdO, k > 0);
-          mma_commit(&bars.ofull[s]);
-          mma_commit(&bars.vempty[vs]);
-        }
+        for (int k = 0; k < D / 32; ++k)
+          mma_f8(tmem + s * 128, SwTile<D>::kmajor(sQ, k), SwTile<D>::kmajor(sK, k), kIdS, k > 0);
+        mma_commit(&bars.sfull[s]);
+        mma_commit(&bars.kempty[ks]);
       }
       mma_commit(&bars.mma_done);
       wait_drain(&bars.mma_done, 0, wd, 119);
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------------- O_u = P^ V issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdO = idesc_f8(0, 0, 0, 1, kTile, D);  // P^ (K-major) V (MN-major)
+      bool ok = true;
+      for (int u = 0; u < nkv && ok; ++u) {
+        const int s = u & 1;
+        const uint32_t ph = (u >> 1) & 1;
+        const int vs = u % kKV;
+        ok = wait(&bars.pfull[s], ph, wd, 107) && wait(&bars.vfull[vs], (u / kKV) & 1, wd, 108) &&
+             wait(&bars.oempty[s], ph ^ 1, wd, 109);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sP = smem_u32(sm + L::kP + s * kTile * kTile);
+        const uint32_t sV = smem_u32(sm + L::kV + vs * L::kTileBytes);
+#pragma unroll
+        for (int k = 0; k < kTile / 32; ++k)
+          mma_f8(tmem + 256 + s * 128, SwTile<128>::kmajor(sP, k), SwTile<D>::mnmajor(sV, k), kIdO, k > 0);
+        mma_commit(&bars.ofull[s]);
+        mma_commit(&bars.vempty[vs]);
+      }
+      mma_commit(&bars.mma_done2);
+      wait_drain(&bars.mma_done2, 0, wd, 120);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------ softmax and O update
