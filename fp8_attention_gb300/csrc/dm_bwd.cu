@@ -422,7 +422,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int w = 1; w < 8; ++w) amax = fmaxf(amax, s_red[bn][0][w]);
       float rp;
       const float sp = tile_scale_fast<0>(amax, rp);
-      {
+      // P^T codes and the next iteration's LSE / delta (read after this
+      // iteration's dS barrier), and the previous iteration's dQ (its
+      // completion also means dV/dK(n-1) are done).  The two warpgroups take
+      // the two in opposite order, so that on every SM sub-partition one
+      // warp's code conversion overlaps the other's TMEM loads and staging.
+      auto write_p = [&]() {
         uint8_t* dst = sm + L::kPt + bn * kTile * kTile;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -437,16 +442,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(dst + SwTile<128>::chunk_offset(r, wg * 4 + c)) =
               make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
+        if (n + 1 < n_iter) {
+          stage_row(n + 1, row_next);
+          if (n + 2 < n_iter) row_next = row_value(bh, qt + 2);
+        }
+      };
+      if (wg == 0) {
+        write_p();
+        if (n >= 1) drain_dq(n - 1, prev_cdq);
+      } else {
+        if (n >= 1) drain_dq(n - 1, prev_cdq);
+        write_p();
       }
-
-      // LSE / delta of the next iteration (read after this iteration's dS barrier)
-      if (n + 1 < n_iter) {
-        stage_row(n + 1, row_next);
-        if (n + 2 < n_iter) row_next = row_value(bh, qt + 2);
-      }
-
-      // previous iteration's dQ; its completion also means dV/dK(n-1) are done
-      if (n >= 1) drain_dq(n - 1, prev_cdq);
 
       // dS = P (dP - delta), computed in place over p (P in FP32 is not needed
       // once its codes are written), its tile amax and E5M2 codes
@@ -485,68 +492,70 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int w = 1; w < 8; ++w) amax = fmaxf(amax, s_red[bn][1][w]);
       float rs;
       const float sds = tile_scale_fast<1>(amax, rs);
-      uint32_t dcode[16];
-      {
-        uint8_t* dst = sm + L::kDSt + bn * kTile * kTile;
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float2 a01 = __fmul2_rn(make_float2(ds[4 * c], ds[4 * c + 1]), make_float2(rs, rs));
-          const float2 a23 = __fmul2_rn(make_float2(ds[4 * c + 2], ds[4 * c + 3]), make_float2(rs, rs));
-          dcode[c] = pack4_e5m2(a01.x, a01.y, a23.x, a23.y);
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          *reinterpret_cast<uint4*>(dst + SwTile<128>::chunk_offset(r, wg * 4 + c)) =
-              make_uint4(dcode[4 * c], dcode[4 * c + 1], dcode[4 * c + 2], dcode[4 * c + 3]);
-      }
-      // per-query-row diagnostics (column sums over the key rows)
-      if (want_diag) {
-        const size_t rowbase = (size_t)bh * a.N + qi0 + wg * 64;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int col = half * 32 + lane;
-          const bool col_ok = qi0 + wg * 64 + col < a.N;
-          float v[32];
-          if (diag.rowsum_pre) {
-#pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] = ds[half * 32 + k];
-            const float sum = lane_column_sum(v, lane);
-            if (col_ok) atomicAdd(diag.rowsum_pre + rowbase + col, sum);
-          }
-          if (diag.abssum_pre) {
-#pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] = fabsf(ds[half * 32 + k]);
-            const float sum = lane_column_sum(v, lane);
-            if (col_ok) atomicAdd(diag.abssum_pre + rowbase + col, sum);
-          }
-          if (diag.rowsum_post || diag.abssum_post) {
-            float w2[32];
-#pragma unroll
-            for (int k = 0; k < 32; k += 4) {
-              const uint32_t w = dcode[(half * 32 + k) / 4];
-              const float2 lo = unpack2<1>((uint16_t)(w & 0xFFFF));
-              const float2 hi = unpack2<1>((uint16_t)(w >> 16));
-              v[k] = lo.x * sds, v[k + 1] = lo.y * sds, v[k + 2] = hi.x * sds, v[k + 3] = hi.y * sds;
-            }
-#pragma unroll
-            for (int k = 0; k < 32; ++k) w2[k] = fabsf(v[k]);
-            if (diag.rowsum_post) {
-              const float sum = lane_column_sum(v, lane);
-              if (col_ok) atomicAdd(diag.rowsum_post + rowbase + col, sum);
-            }
-            if (diag.abssum_post) {
-              const float sum = lane_column_sum(w2, lane);
-              if (col_ok) atomicAdd(diag.abssum_post + rowbase + col, sum);
-            }
-          }
-        }
-      }
-
       // both accumulators into the units of this iteration's products (dV/dK
-      // of n - 1 completed before the drain above)
+      // of n - 1 completed before the drain above), after the dS codes
       float fv, fk;
       const int mode_dv = unit_step(unit_dv, sp * sdo, fv);
       const int mode_dk = unit_step(unit_dk, a.sigma * sds * sq, fk);
+      auto write_ds = [&]() {
+        uint32_t dcode[16];
+        {
+          uint8_t* dst = sm + L::kDSt + bn * kTile * kTile;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float2 a01 = __fmul2_rn(make_float2(ds[4 * c], ds[4 * c + 1]), make_float2(rs, rs));
+            const float2 a23 = __fmul2_rn(make_float2(ds[4 * c + 2], ds[4 * c + 3]), make_float2(rs, rs));
+            dcode[c] = pack4_e5m2(a01.x, a01.y, a23.x, a23.y);
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4*>(dst + SwTile<128>::chunk_offset(r, wg * 4 + c)) =
+                make_uint4(dcode[4 * c], dcode[4 * c + 1], dcode[4 * c + 2], dcode[4 * c + 3]);
+        }
+        // per-query-row diagnostics (column sums over the key rows)
+        if (want_diag) {
+          const size_t rowbase = (size_t)bh * a.N + qi0 + wg * 64;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const int col = half * 32 + lane;
+            const bool col_ok = qi0 + wg * 64 + col < a.N;
+            float v[32];
+            if (diag.rowsum_pre) {
+#pragma unroll
+              for (int k = 0; k < 32; ++k) v[k] = ds[half * 32 + k];
+              const float sum = lane_column_sum(v, lane);
+              if (col_ok) atomicAdd(diag.rowsum_pre + rowbase + col, sum);
+            }
+            if (diag.abssum_pre) {
+#pragma unroll
+              for (int k = 0; k < 32; ++k) v[k] = fabsf(ds[half * 32 + k]);
+              const float sum = lane_column_sum(v, lane);
+              if (col_ok) atomicAdd(diag.abssum_pre + rowbase + col, sum);
+            }
+            if (diag.rowsum_post || diag.abssum_post) {
+              float w2[32];
+#pragma unroll
+              for (int k = 0; k < 32; k += 4) {
+                const uint32_t w = dcode[(half * 32 + k) / 4];
+                const float2 lo = unpack2<1>((uint16_t)(w & 0xFFFF));
+                const float2 hi = unpack2<1>((uint16_t)(w >> 16));
+                v[k] = lo.x * sds, v[k + 1] = lo.y * sds, v[k + 2] = hi.x * sds, v[k + 3] = hi.y * sds;
+              }
+#pragma unroll
+              for (int k = 0; k < 32; ++k) w2[k] = fabsf(v[k]);
+              if (diag.rowsum_post) {
+                const float sum = lane_column_sum(v, lane);
+                if (col_ok) atomicAdd(diag.rowsum_post + rowbase + col, sum);
+              }
+              if (diag.abssum_post) {
+                const float sum = lane_column_sum(w2, lane);
+                if (col_ok) atomicAdd(diag.abssum_post + rowbase + col, sum);
+              }
+            }
+          }
+        }
+      };
+      write_ds();
       if (fv != 1.0f || fk != 1.0f) rescale_pair<DH>(tl + 256 + wg * DH, fv, tl + 384 + wg * DH, fk);
       if (ct == 0) {
         s_mode[bn][0] = mode_dv;
