@@ -22,7 +22,7 @@ import torch
 
 __all__ = [
     "AttnParams", "Fp8", "DMError", "lib", "dm_version", "dm_status_string", "dm_set_knob",
-    "dm_get_status", "dm_last_timeout_site", "dm_quantize", "dm_attn_fwd", "dm_attn_delta", "dm_attn_bwd",
+    "dm_get_status", "dm_last_timeout_site", "dm_quantize", "dm_quantize_batch", "dm_attn_fwd", "dm_attn_delta", "dm_attn_bwd",
     "dm_attn_bwd_workspace_size", "dm_attn_bwd_noalloc", "DM_NOALLOC_MAX_DELTA_ROWS",
     "DM_F32", "DM_BF16", "DM_E4M3", "DM_E5M2", "DM_DELTA_MATCHED", "DM_DELTA_STALE_DO",
     "DM_DELTA_STALE_DOHAT", "DM_KNOB_WAIT_LIMIT_NS", "DM_KNOB_STALL_TEST",
@@ -109,6 +109,8 @@ def lib():
             L.dm_last_timeout_site.restype = ctypes.c_uint
             L.dm_quantize.restype = I
             L.dm_quantize.argtypes = [P, I, I, I, I, I, I, P, P, P, P]
+            L.dm_quantize_batch.restype = I
+            L.dm_quantize_batch.argtypes = [P, I, I, P]
             L.dm_attn_fwd.restype = I
             L.dm_attn_fwd.argtypes = [PP, _Fp8, _Fp8, _Fp8, P, I, P, P]
             L.dm_attn_delta.restype = I
@@ -195,6 +197,34 @@ def dm_quantize(x: torch.Tensor, fmt: int, codes=None, scales=None, codes_t=None
     _check(rc, "dm_quantize")
     out = Fp8(codes, scales)
     return (out, codes_t) if codes_t is not None else out
+
+
+class _QuantJob(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("B", ctypes.c_int), ("H", ctypes.c_int), ("N", ctypes.c_int),
+                ("d", ctypes.c_int), ("fmt", ctypes.c_int), ("codes", ctypes.c_void_p),
+                ("scales", ctypes.c_void_p), ("codes_t", ctypes.c_void_p)]
+
+
+def dm_quantize_batch(tensors, stream=None):
+    """dm_quantize of several tensors in one launch: tensors is a sequence of (x, fmt) with x [B][H][N][d]
+    (all of one dtype and one d); returns one Fp8 per tensor."""
+    jobs, outs = [], []
+    for x, fmt in tensors:
+        B, H, N, d = x.shape
+        T = (N + TILE - 1) // TILE
+        codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+        scales = torch.empty((B, H, T), dtype=torch.float32, device=x.device)
+        jobs.append(_QuantJob(_ptr(x), B, H, N, d, int(fmt), _ptr(codes), _ptr(scales), None))
+        outs.append(Fp8(codes, scales))
+    if not jobs:
+        return []
+    dtype = _dtype(tensors[0][0])
+    if any(_dtype(x) != dtype for x, _ in tensors):
+        raise DMError(DM_ERR_DTYPE, "dm_quantize_batch: tensors of different dtypes")
+    arr = (_QuantJob * len(jobs))(*jobs)
+    rc = lib().dm_quantize_batch(arr, len(jobs), dtype, _stream(stream))
+    _check(rc, "dm_quantize_batch")
+    return outs
 
 
 def dm_attn_fwd(p: AttnParams, q: Fp8, k: Fp8, v: Fp8, O=None, o_dtype=torch.float32, lse=None, stream=None):

@@ -230,20 +230,59 @@ unsigned int dm_last_timeout_site(void) {
   return g_last_site;
 }
 
-dm_status dm_quantize(const void* x, dm_dtype x_dtype, int B, int H, int N, int d, dm_fp8 fmt, uint8_t* codes,
-                      float* scales, uint8_t* codes_t, void* stream) {
+static_assert(DM_QUANTIZE_MAX_JOBS == dm::QuantBatch::kMaxJobs, "quantiser batch size");
+
+namespace {
+dm_status check_quantize_job(const dm_quantize_job& j, int d) {
+  if (j.fmt != DM_E4M3 && j.fmt != DM_E5M2) return DM_ERR_INVALID_ARG;
+  if (j.B < 0 || j.H <= 0 || j.N < 0 || j.d != d) return DM_ERR_SHAPE;
+  if ((long long)j.B * j.H * j.N * j.d >= (1ll << 31)) return DM_ERR_SHAPE;
+  if (j.B == 0 || j.N == 0) return DM_OK;  // empty tensor: pointers may be NULL
+  DM_TRY(check_ptr(j.x));
+  DM_TRY(check_ptr(j.codes));
+  DM_TRY(check_ptr(j.scales));
+  if (j.codes_t && !aligned16(j.codes_t)) return DM_ERR_ALIGNMENT;
+  return DM_OK;
+}
+}  // namespace
+
+dm_status dm_quantize_batch(const dm_quantize_job* jobs, int njobs, dm_dtype x_dtype, void* stream) {
   if (!valid_dtype(x_dtype)) return DM_ERR_DTYPE;
-  if (fmt != DM_E4M3 && fmt != DM_E5M2) return DM_ERR_INVALID_ARG;
-  if (B < 0 || H <= 0 || N < 0 || (d != 64 && d != 128)) return DM_ERR_SHAPE;
-  if ((long long)B * H * N * d >= (1ll << 31)) return DM_ERR_SHAPE;
-  if (B == 0 || N == 0) return DM_OK;  // empty input: nothing to do, pointers may be NULL
-  DM_TRY(check_ptr(x));
-  DM_TRY(check_ptr(codes));
-  DM_TRY(check_ptr(scales));
-  if (codes_t && !aligned16(codes_t)) return DM_ERR_ALIGNMENT;
+  if (njobs < 0 || njobs > DM_QUANTIZE_MAX_JOBS) return DM_ERR_INVALID_ARG;
+  if (njobs == 0) return DM_OK;
+  if (!jobs) return DM_ERR_INVALID_ARG;
+  const int d = jobs[0].d;
+  if (d != 64 && d != 128) return DM_ERR_SHAPE;
+  dm::QuantBatch b{};
+  long long tiles = 0;
+  for (int i = 0; i < njobs; ++i) {
+    DM_TRY(check_quantize_job(jobs[i], d));
+    if (jobs[i].B == 0 || jobs[i].N == 0) continue;
+    dm::QuantJob& q = b.job[b.count];
+    q.x = jobs[i].x;
+    q.N = jobs[i].N;
+    q.T_tiles = (jobs[i].N + 127) / 128;
+    q.fmt = jobs[i].fmt == DM_E5M2 ? 1 : 0;
+    q.codes = jobs[i].codes;
+    q.scales = jobs[i].scales;
+    q.codes_t = jobs[i].codes_t;
+    b.first_tile[b.count] = (int)tiles;
+    tiles += (long long)jobs[i].B * jobs[i].H * q.T_tiles;
+    ++b.count;
+  }
+  if (b.count == 0) return DM_OK;  // every tensor empty
+  if (tiles >= (1ll << 31)) return DM_ERR_SHAPE;
+  b.first_tile[b.count] = (int)tiles;
   unsigned int* status = nullptr;
   DM_TRY(device_state(&status));
-  return cuda_status(dm::launch_quantize(x, x_dtype, B, H, N, d, fmt, codes, scales, codes_t, as_stream(stream)));
+  return cuda_status(dm::launch_quantize(b, x_dtype, d, as_stream(stream)));
+}
+
+dm_status dm_quantize(const void* x, dm_dtype x_dtype, int B, int H, int N, int d, dm_fp8 fmt, uint8_t* codes,
+                      float* scales, uint8_t* codes_t, void* stream) {
+  const dm_quantize_job job{x, B, H, N, d, fmt, codes, scales, codes_t};
+  if (d != 64 && d != 128) return valid_dtype(x_dtype) ? DM_ERR_SHAPE : DM_ERR_DTYPE;
+  return dm_quantize_batch(&job, 1, x_dtype, stream);
 }
 
 dm_status dm_attn_fwd(const dm_attn_params* p, dm_fp8_tensor q, dm_fp8_tensor k, dm_fp8_tensor v, void* O,

@@ -42,19 +42,23 @@ struct Vec<__nv_bfloat16> {
   }
 };
 
-// One CTA per (b*h, tile).  Supports d in {64, 128}.
-template <typename T, int FMT, int D>
-__global__ void __launch_bounds__(kQThreads) quantize_kernel(const T* __restrict__ x, int N, int T_tiles,
-                                                             uint8_t* __restrict__ codes,
-                                                             float* __restrict__ scales,
-                                                             uint8_t* __restrict__ codes_t) {
+// One CTA per 128-row x D tile of one of up to kMaxJobs tensors (one launch
+// quantises Q, K, V and dO together); the CTA finds its tensor from the
+// running tile counts.  fmt is per tensor (0 E4M3, 1 E5M2).
+template <typename T, int D>
+__global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantBatch batch) {
   constexpr int V = Vec<T>::kElems;
   constexpr int kVecs = kTile * D / V;     // vectors in a full tile
   constexpr int kPer = kVecs / kQThreads;  // per thread
   __shared__ float s_red[kQThreads / 32];
-  __shared__ __align__(16) uint8_t s_codes[kTile * D];
+  extern __shared__ __align__(16) uint8_t s_codes[];  // [kTile * D] when a transposed copy is wanted
 
-  const int tile = blockIdx.x;
+  int j = 0;
+  while (j + 1 < batch.count && (int)blockIdx.x >= batch.first_tile[j + 1]) ++j;
+  const QuantJob& job = batch.job[j];
+  const T* __restrict__ x = static_cast<const T*>(job.x);
+  const int N = job.N, T_tiles = job.T_tiles;
+  const int tile = (int)blockIdx.x - batch.first_tile[j];
   const int bh = tile / T_tiles, t = tile % T_tiles;
   const int rows = min(kTile, N - t * kTile);
   const size_t base = ((size_t)bh * N + (size_t)t * kTile) * D;
@@ -80,10 +84,12 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const T* __restrict
   amax = s_red[0];
 #pragma unroll
   for (int w = 1; w < kQThreads / 32; ++w) amax = fmaxf(amax, s_red[w]);
+  const bool e5m2 = job.fmt != 0;  // uniform over the CTA
   float r;
-  const float s = tile_scale<FMT>(amax, r);
-  if (threadIdx.x == 0) scales[tile] = s;
+  const float s = e5m2 ? tile_scale<1>(amax, r) : tile_scale<0>(amax, r);
+  if (threadIdx.x == 0) job.scales[tile] = s;
   const bool flushed = (s == 0.0f);  // flushed tile: all codes +0 (x * 0 would give -0 for x < 0)
+  uint8_t* codes_t = job.codes_t;
 
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
@@ -91,11 +97,12 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const T* __restrict
     if (idx >= nvec) continue;
     uint32_t w[V / 4];
 #pragma unroll
-    for (int k = 0; k < V / 4; ++k)
-      w[k] = flushed ? 0u
-                     : pack4<FMT>(__fmul_rn(v[i][4 * k], r), __fmul_rn(v[i][4 * k + 1], r),
-                                  __fmul_rn(v[i][4 * k + 2], r), __fmul_rn(v[i][4 * k + 3], r));
-    uint8_t* dst = codes + base + (size_t)idx * V;
+    for (int k = 0; k < V / 4; ++k) {
+      const float x0 = __fmul_rn(v[i][4 * k], r), x1 = __fmul_rn(v[i][4 * k + 1], r);
+      const float x2 = __fmul_rn(v[i][4 * k + 2], r), x3 = __fmul_rn(v[i][4 * k + 3], r);
+      w[k] = flushed ? 0u : (e5m2 ? pack4<1>(x0, x1, x2, x3) : pack4<0>(x0, x1, x2, x3));
+    }
+    uint8_t* dst = job.codes + base + (size_t)idx * V;
     if constexpr (V == 8) {
       *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
       if (codes_t) *reinterpret_cast<uint2*>(s_codes + idx * V) = make_uint2(w[0], w[1]);
@@ -115,15 +122,16 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(const T* __restrict
   }
 }
 
-template <typename T, int FMT>
-cudaError_t quantize_t(const T* x, int BH, int N, int d, uint8_t* codes, float* scales, uint8_t* codes_t,
-                       cudaStream_t st) {
-  const int T_tiles = (N + kTile - 1) / kTile;
-  const unsigned grid = (unsigned)(BH * T_tiles);
+template <typename T>
+cudaError_t quantize_t(const QuantBatch& b, int d, cudaStream_t st) {
+  bool any_t = false;
+  for (int j = 0; j < b.count; ++j) any_t = any_t || b.job[j].codes_t;
+  const int smem = any_t ? kTile * d : 0;
+  const unsigned grid = (unsigned)b.first_tile[b.count];
   if (d == 128)
-    quantize_kernel<T, FMT, 128><<<grid, kQThreads, 0, st>>>(x, N, T_tiles, codes, scales, codes_t);
+    quantize_kernel<T, 128><<<grid, kQThreads, smem, st>>>(b);
   else
-    quantize_kernel<T, FMT, 64><<<grid, kQThreads, 0, st>>>(x, N, T_tiles, codes, scales, codes_t);
+    quantize_kernel<T, 64><<<grid, kQThreads, smem, st>>>(b);
   return cudaGetLastError();
 }
 
@@ -224,17 +232,9 @@ __global__ void zero_kernel(const ZeroList z) {
 
 }  // namespace
 
-cudaError_t launch_quantize(const void* x, dm_dtype xt, int B, int H, int N, int d, dm_fp8 fmt, uint8_t* codes,
-                            float* scales, uint8_t* codes_t, cudaStream_t st) {
-  const int BH = B * H;
-  if (xt == DM_BF16) {
-    auto p = reinterpret_cast<const __nv_bfloat16*>(x);
-    return fmt == DM_E4M3 ? quantize_t<__nv_bfloat16, 0>(p, BH, N, d, codes, scales, codes_t, st)
-                          : quantize_t<__nv_bfloat16, 1>(p, BH, N, d, codes, scales, codes_t, st);
-  }
-  auto p = reinterpret_cast<const float*>(x);
-  return fmt == DM_E4M3 ? quantize_t<float, 0>(p, BH, N, d, codes, scales, codes_t, st)
-                        : quantize_t<float, 1>(p, BH, N, d, codes, scales, codes_t, st);
+cudaError_t launch_quantize(const QuantBatch& b, dm_dtype xt, int d, cudaStream_t st) {
+  if (b.count == 0 || b.first_tile[b.count] == 0) return cudaSuccess;
+  return xt == DM_BF16 ? quantize_t<__nv_bfloat16>(b, d, st) : quantize_t<float>(b, d, st);
 }
 
 cudaError_t launch_delta_stale(const AttnArgs& a, int d, dm_delta_mode mode, const void* dO, dm_dtype do_t,

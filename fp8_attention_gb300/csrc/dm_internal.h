@@ -34,8 +34,22 @@ struct BwdLaunch {
   dm_diag diag;
 };
 
-cudaError_t launch_quantize(const void* x, dm_dtype xt, int B, int H, int N, int d, dm_fp8 fmt, uint8_t* codes,
-                            float* scales, uint8_t* codes_t, cudaStream_t st);
+// Tensors one quantiser launch processes (same input dtype and d).
+struct QuantJob {
+  const void* x;
+  int N, T_tiles, fmt;
+  uint8_t* codes;
+  float* scales;
+  uint8_t* codes_t;
+};
+struct QuantBatch {
+  static constexpr int kMaxJobs = 8;
+  QuantJob job[kMaxJobs];
+  int first_tile[kMaxJobs + 1];  // running tile counts; first_tile[count] = total
+  int count;
+};
+
+cudaError_t launch_quantize(const QuantBatch& b, dm_dtype xt, int d, cudaStream_t st);
 cudaError_t launch_attn_fwd(const FwdLaunch& f, int d, bool o_bf16, cudaStream_t st);
 cudaError_t launch_delta_matched(const DeltaLaunch& f, int d, cudaStream_t st);
 cudaError_t launch_delta_stale(const AttnArgs& a, int d, dm_delta_mode mode, const void* dO, dm_dtype do_t,

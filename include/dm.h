@@ -107,6 +107,25 @@ typedef struct {
 dm_status dm_quantize(const void* x, dm_dtype x_dtype, int B, int H, int N, int d, dm_fp8 fmt,
                       uint8_t* codes, float* scales, uint8_t* codes_t, void* stream);
 
+/* dm_quantize_batch -- dm_quantize of up to DM_QUANTIZE_MAX_JOBS tensors in one
+ * launch (the pages quantise Q, K, V and dO with the same rule; one launch
+ * avoids a short kernel per tensor).  All jobs share x_dtype and d; fmt,
+ * shapes and buffers are per job, with the meaning, layout and ownership of
+ * dm_quantize.  Every job is validated before the launch (DM_ERR_SHAPE if the
+ * jobs' d differ, DM_ERR_INVALID_ARG for njobs outside 0..MAX or jobs == NULL
+ * with njobs > 0); empty tensors are skipped.  Results are bit-identical to
+ * separate dm_quantize calls. */
+#define DM_QUANTIZE_MAX_JOBS 8
+typedef struct {
+  const void* x;
+  int B, H, N, d;
+  dm_fp8 fmt;
+  uint8_t* codes;
+  float* scales;
+  uint8_t* codes_t; /* nullable */
+} dm_quantize_job;
+dm_status dm_quantize_batch(const dm_quantize_job* jobs, int njobs, dm_dtype x_dtype, void* stream);
+
 /* dm_attn_fwd -- O = P^ V^ and LSE (section 01).  q, k, v: E4M3 tensors of
  * shapes [B][Hq][N][d], [B][Hkv][N][d], [B][Hkv][N][d].  O: [B][Hq][N][d] of
  * o_dtype (DM_F32 or DM_BF16).  lse: float [B][Hq][N], natural log of the

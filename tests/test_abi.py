@@ -78,6 +78,17 @@ def test_validation_without_gpu(lib):
     assert lib.dm_quantize(A, 2, 1, 2, 128, 64, 0, A, A, None, None) == dm.DM_ERR_DTYPE
     assert lib.dm_quantize(A, 0, 1, 2, 128, 64, 2, A, A, None, None) == dm.DM_ERR_INVALID_ARG
     assert lib.dm_quantize(A, 0, 1, 2, 128, 32, 0, A, A, None, None) == dm.DM_ERR_SHAPE
+    J = dm._QuantJob
+    two = (J * 2)(J(A, 1, 2, 128, 64, 0, A, A, None), J(A, 1, 2, 128, 128, 1, A, A, None))
+    assert lib.dm_quantize_batch(two, 2, 0, None) == dm.DM_ERR_SHAPE           # d differs between jobs
+    assert lib.dm_quantize_batch(two, 9, 0, None) == dm.DM_ERR_INVALID_ARG     # more than 8 jobs
+    assert lib.dm_quantize_batch(None, 1, 0, None) == dm.DM_ERR_INVALID_ARG
+    assert lib.dm_quantize_batch(two, 1, 5, None) == dm.DM_ERR_DTYPE
+    bad = (J * 1)(J(A + 4, 1, 2, 128, 64, 0, A, A, None))
+    assert lib.dm_quantize_batch(bad, 1, 0, None) == dm.DM_ERR_ALIGNMENT
+    empty = (J * 1)(J(None, 0, 2, 128, 64, 0, None, None, None))
+    assert lib.dm_quantize_batch(empty, 1, 0, None) == 0
+    assert lib.dm_quantize_batch(None, 0, 0, None) == 0
     assert lib.dm_attn_delta(ctypes.byref(_p()), 3, f, f, f, f, A, A, 0, A, 0, A, None) == dm.DM_ERR_INVALID_ARG
     assert lib.dm_attn_delta(ctypes.byref(_p()), 1, f, f, f, f, A, None, 0, A, 0, A, None) \
         == dm.DM_ERR_INVALID_ARG

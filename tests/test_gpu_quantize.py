@@ -34,6 +34,29 @@ def test_quantize_bit_exact(dtype, fmt, shape):
     assert np.array_equal(codes_t.cpu().numpy(), codes.transpose(0, 1, 3, 2))
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_quantize_batch_matches_oracle(dtype):
+    """One launch for Q, K, V (E4M3) and dO (E5M2) of different head counts and a ragged N, plus an empty
+    tensor: every tensor's codes and scales bit-exact with the oracle."""
+    g = torch.Generator().manual_seed(7)
+    shapes = [((2, 4, 333, 128), dm.DM_E4M3), ((2, 1, 333, 128), dm.DM_E4M3), ((2, 1, 333, 128), dm.DM_E4M3),
+              ((2, 4, 333, 128), dm.DM_E5M2), ((0, 4, 333, 128), dm.DM_E4M3)]
+    xs = []
+    for shape, fmt in shapes:
+        x = torch.randn(shape, generator=g) * torch.exp(torch.randn(shape[:3] + (1,), generator=g) * 3)
+        if fmt == dm.DM_E5M2:
+            x *= 1e-3
+        xs.append((x.to(dtype), fmt))
+    outs = dm.dm_quantize_batch([(x.to(DEV), fmt) for x, fmt in xs])
+    for (x, fmt), got in zip(xs, outs):
+        if x.numel() == 0:
+            assert got.codes.numel() == 0
+            continue
+        codes, scales = oracle.quantize(x.float().numpy(), fmt)
+        assert np.array_equal(got.scales.cpu().numpy(), scales)
+        assert np.array_equal(got.codes.cpu().numpy(), codes)
+
+
 def test_quantize_empty_is_noop():
     x = torch.empty((0, 2, 128, 64), device=DEV)
     out = dm.dm_quantize(x, dm.DM_E4M3)
