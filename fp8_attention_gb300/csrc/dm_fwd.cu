@@ -37,13 +37,13 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr int kCTAsPerSM = 2;
-constexpr int kKV = 2;  // K and V shared-memory stages
+constexpr int kKV = 2;  // K shared-memory stages (V has one: it is needed a whole tile later than K)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint32_t kColS = 0, kColO = 128;
 
 struct FwdBars {
-  uint64_t q, kfull[kKV], kempty[kKV], vfull[kKV], vempty[kKV], sfull, sempty, pready, ofull, stall, mma_done;
+  uint64_t q, kfull[kKV], kempty[kKV], vfull, vempty, sfull, sempty, pready, ofull, stall, mma_done;
 };
 
 // Everything lives in dynamic shared memory (no static shared variables), so
@@ -53,9 +53,9 @@ struct FwdLayout {
   static constexpr int kTileBytes = kTile * D;  // one FP8 Q/K/V tile
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTileBytes;          // kKV stages
-  static constexpr int kV = kK + kKV * kTileBytes;    // kKV stages
-  static constexpr int kP = kV + kKV * kTileBytes;    // 128 x 128 P^ codes
-  static constexpr int kRed = kP + kTile * kTile;     // float [2][4] per-warp amax exponents
+  static constexpr int kV = kK + kKV * kTileBytes;    // one stage
+  static constexpr int kP = kV + kTileBytes;          // 2 x (128 x 128) P^ codes
+  static constexpr int kRed = kP + 2 * kTile * kTile;  // float [2][4] per-warp amax exponents
   static constexpr int kMode = kRed + 2 * 4 * 4;      // int [2] per-tile P V mode
   static constexpr int kBars = kMode + 16;
   static constexpr int kMisc = kBars + ((int)(sizeof(FwdBars) + 15) / 16) * 16;  // tmem address, abort flag
@@ -116,9 +116,9 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
     for (int s = 0; s < kKV; ++s) {
       mbar_init(&bars.kfull[s], 1);
       mbar_init(&bars.kempty[s], 1);
-      mbar_init(&bars.vfull[s], 1);
-      mbar_init(&bars.vempty[s], 1);
     }
+    mbar_init(&bars.vfull, 1);
+    mbar_init(&bars.vempty, 1);
     mbar_init(&bars.sfull, 1);
     mbar_init(&bars.sempty, 4);
     mbar_init(&bars.pready, 4);
@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
       mbar_arrive_expect_tx(&bars.q, L::kTileBytes);
       tma_load_3d(sm + L::kQ, &tmQ, &bars.q, 0, q0, bh);
       // K runs one tile ahead of V: K(t) needs only S(t-2) to have finished
-      // with its stage, V(t) needs P V(t-2), which completes later.
+      // with its stage, V(t) needs P V(t-1), which completes a tile later.
       int k_issued = 0, v_issued = 0;  // loads issued (both stop early on abort)
       for (int t = 0; t <= nkv; ++t) {
         if (t < nkv) {
@@ -156,10 +156,10 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
           k_issued = t + 1;
         }
         if (t >= 1) {
-          const int u = t - 1, s = u % kKV;
-          if (!wait(&bars.vempty[s], ((u / kKV) & 1) ^ 1, wd, 102)) break;
-          mbar_arrive_expect_tx(&bars.vfull[s], L::kTileBytes);
-          tma_load_3d(sm + L::kV + s * L::kTileBytes, &tmV, &bars.vfull[s], 0, u * kTile, bg);
+          const int u = t - 1;
+          if (!wait(&bars.vempty, (u & 1) ^ 1, wd, 102)) break;
+          mbar_arrive_expect_tx(&bars.vfull, L::kTileBytes);
+          tma_load_3d(sm + L::kV, &tmV, &bars.vfull, 0, u * kTile, bg);
           v_issued = u + 1;
         }
       }
@@ -167,8 +167,7 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
       wait_drain(&bars.q, 0, wd, 116);
       for (int t = max(0, k_issued - kKV); t < k_issued; ++t)
         wait_drain(&bars.kfull[t % kKV], (t / kKV) & 1, wd, 117);
-      for (int t = max(0, v_issued - kKV); t < v_issued; ++t)
-        wait_drain(&bars.vfull[t % kKV], (t / kKV) & 1, wd, 118);
+      if (v_issued > 0) wait_drain(&bars.vfull, (v_issued - 1) & 1, wd, 118);
     }
   } else if (warp == 5) {
     // ----------------------------------------------------------- MMA issuer
@@ -185,7 +184,6 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
       ok = ok && wait(&bars.q, 0, wd, 104);
       tc_fence_after();
       const uint32_t sQ = smem_u32(sm + L::kQ);
-      const uint32_t sP = smem_u32(sm + L::kP);
       for (int t = 0; t <= nkv && ok; ++t) {
         if (t < nkv) {
           // S(t) once K(t) has landed and the warpgroup has read S(t-1)
@@ -203,20 +201,21 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
         }
         if (t >= 1) {
           // O += P^(u) V(u) once the codes are written and O is rescaled
-          const int u = t - 1, vs = u % kKV;
-          ok = wait(&bars.pready, u & 1, wd, 107) && wait(&bars.vfull[vs], (u / kKV) & 1, wd, 108);
+          const int u = t - 1;
+          ok = wait(&bars.pready, u & 1, wd, 107) && wait(&bars.vfull, u & 1, wd, 108);
           if (!ok) break;
           tc_fence_after();
           const int mode = s_mode[u & 1];  // 0 skip, 1 overwrite, 2 accumulate
           if (mode) {
-            const uint32_t sV = smem_u32(sm + L::kV + vs * L::kTileBytes);
+            const uint32_t sV = smem_u32(sm + L::kV);
+            const uint32_t sP = smem_u32(sm + L::kP + (u & 1) * kTile * kTile);
 #pragma unroll
             for (int k = 0; k < kTile / 32; ++k)
               mma_f8(tmem + kColO, SwTile<128>::kmajor(sP, k), SwTile<D>::mnmajor(sV, k), kIdO,
                      (k > 0 || mode == 2) ? 1u : 0u);
           }
           mma_commit(&bars.ofull);
-          mma_commit(&bars.vempty[vs]);
+          mma_commit(&bars.vempty);
         }
       }
       mma_commit(&bars.mma_done);
@@ -234,7 +233,6 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
     float sk_next = ksc[0], sv_next = vsc[0];  // per-tile scales, loaded one tile ahead
     float m = -INFINITY, l = 0.0f;             // running max (log2 units), row sum
     float unit = 0.0f;                         // O in true units = unit * O_tmem
-    uint8_t* sP = sm + L::kP;
 
     for (int t = 0; t < nkv; ++t) {
       const float c1 = a.sigma * sq * sk_next * kLog2e;
@@ -287,16 +285,15 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
       const float sp = tile_scale_fast<0>(amax, r);
       const float alpha = ex2(m - m_new);
 
-      // the P tile was last read by P V(t-1)
-      if (t >= 1) wait(&bars.ofull, (t - 1) & 1, wd, 114);
-      tc_fence_after();
-
-      // P~ r = exp2(S c1 - m + log2 r) straight into E4M3 codes; the
+      // P~ r = exp2(S c1 - m + log2 r) straight into E4M3 codes (P buffer
+      // t%2, last read by P V(t-2), whose completion this thread saw before
+      // its rescale of tile t-1); the
       // unquantised row sum is sum(P~ r) * s_P.  A flushed tile (r = 0)
       // gives codes 0.
       const float bias = (r > 0.0f ? __log2f(r) : -INFINITY) - m_new;
       const float2 c1_2 = make_float2(c1, c1), b2 = make_float2(bias, bias);
       float2 rs2 = make_float2(0.0f, 0.0f);
+      uint8_t* sP = sm + L::kP + (t & 1) * kTile * kTile;
       auto p_codes = [&](auto full_tile) {
 #pragma unroll
         for (int c = 0; c < kTile; c += 16) {
@@ -330,6 +327,10 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
       // O into the units of this tile's product (uniform decisions over the
       // CTA: c and unit are the same for every row, only alpha differs)
       const float c = sp * sv;
+      if (t >= 1) {
+        wait(&bars.ofull, (t - 1) & 1, wd, 114);  // P V(t-1) has been added into O
+        tc_fence_after();
+      }
       int mode;
       if (t == 0 || unit == 0.0f) {
         mode = 1;  // O holds nothing yet (or only zeros): overwrite
