@@ -244,32 +244,36 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
       const int j0 = t * kTile;
       int jlim = min(kTile, a.N - j0);
       if (a.causal) jlim = min(jlim, qi - j0 + 1);
-      const bool full = jlim >= kTile;  // no masked column (all but the diagonal/ragged tile)
+      // no masked column in this warp's rows (all but the diagonal/ragged
+      // tile); warp-uniform, because the masked and unmasked paths both issue
+      // warp-collective TMEM loads
+      const bool full = __all_sync(0xffffffffu, jlim >= kTile);
 
       wait(&bars.sfull, t & 1, wd, 110);
       tc_fence_after();
-      float v[kTile];
-      tmem_load128(tl + kColS, tl + kColS + 32, tl + kColS + 64, tl + kColS + 96, v);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.sempty);
 
-      // row max (raw units; c1 > 0 preserves the order)
+      // row max (raw units; c1 > 0 preserves the order), S read in halves
+      // (S is read again for the codes: half a row of registers each time)
       float mx = -INFINITY;
-      if (full) {
-        float m4[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
-        for (int c = 4; c < kTile; c += 8) {
-          m4[0] = max3(m4[0], v[c], v[c + 1]);
-          m4[1] = max3(m4[1], v[c + 2], v[c + 3]);
-          m4[2] = max3(m4[2], v[c + 4], v[c + 5]);
-          m4[3] = max3(m4[3], v[c + 6], v[c + 7]);
+      for (int hh = 0; hh < 2; ++hh) {
+        float v[64];
+        tmem_load64(tl + kColS + 64 * hh, tl + kColS + 64 * hh + 32, v);
+        if (full) {
+          float m4[4] = {v[0], v[1], v[2], v[3]};
+#pragma unroll
+          for (int c = 4; c < 64; c += 8) {
+            m4[0] = max3(m4[0], v[c], v[c + 1]);
+            m4[1] = max3(m4[1], v[c + 2], v[c + 3]);
+            m4[2] = max3(m4[2], v[c + 4], v[c + 5]);
+            m4[3] = max3(m4[3], v[c + 6], v[c + 7]);
+          }
+          mx = max3(mx, fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (64 * hh + c < jlim) mx = fmaxf(mx, v[c]);
         }
-        mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      } else {
-#pragma unroll
-        for (int c = 0; c < kTile; ++c)
-          if (c < jlim) mx = fmaxf(mx, v[c]);
       }
       // The tile amax of P~ = max over rows of exp2(tmax_i - m_new_i) =
       // exp2(min(0, max over rows of (tmax_i - m_i))): one exchange.
@@ -296,31 +300,40 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
       uint8_t* sP = sm + L::kP + (t & 1) * kTile * kTile;
       auto p_codes = [&](auto full_tile) {
 #pragma unroll
-        for (int c = 0; c < kTile; c += 16) {
-          uint32_t w4[4];
+        for (int hh = 0; hh < 2; ++hh) {
+          float v[64];
+          tmem_load64(tl + kColS + 64 * hh, tl + kColS + 64 * hh + 32, v);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int cc = c + 4 * e;
-            const float2 x01 = __ffma2_rn(make_float2(v[cc], v[cc + 1]), c1_2, b2);
-            const float2 x23 = __ffma2_rn(make_float2(v[cc + 2], v[cc + 3]), c1_2, b2);
-            float2 q01 = make_float2(ex2(x01.x), ex2(x01.y)), q23 = make_float2(ex2(x23.x), ex2(x23.y));
-            if (!decltype(full_tile)::value) {
-              q01.x = cc < jlim ? q01.x : 0.0f;
-              q01.y = cc + 1 < jlim ? q01.y : 0.0f;
-              q23.x = cc + 2 < jlim ? q23.x : 0.0f;
-              q23.y = cc + 3 < jlim ? q23.y : 0.0f;
+          for (int c = 0; c < 64; c += 16) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int cc = c + 4 * e, col = 64 * hh + cc;
+              const float2 x01 = __ffma2_rn(make_float2(v[cc], v[cc + 1]), c1_2, b2);
+              const float2 x23 = __ffma2_rn(make_float2(v[cc + 2], v[cc + 3]), c1_2, b2);
+              float2 q01 = make_float2(ex2(x01.x), ex2(x01.y)), q23 = make_float2(ex2(x23.x), ex2(x23.y));
+              if (!decltype(full_tile)::value) {
+                q01.x = col < jlim ? q01.x : 0.0f;
+                q01.y = col + 1 < jlim ? q01.y : 0.0f;
+                q23.x = col + 2 < jlim ? q23.x : 0.0f;
+                q23.y = col + 3 < jlim ? q23.y : 0.0f;
+              }
+              rs2 = __fadd2_rn(rs2, __fadd2_rn(q01, q23));
+              w4[e] = pack4_e4m3(q01.x, q01.y, q23.x, q23.y);
             }
-            rs2 = __fadd2_rn(rs2, __fadd2_rn(q01, q23));
-            w4[e] = pack4_e4m3(q01.x, q01.y, q23.x, q23.y);
+            *reinterpret_cast<uint4*>(sP + SwTile<128>::chunk_offset(row, (64 * hh + c) / 16)) =
+                make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
-          *reinterpret_cast<uint4*>(sP + SwTile<128>::chunk_offset(row, c / 16)) =
-              make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
       };
       if (full)
         p_codes(std::true_type{});
       else
         p_codes(std::false_type{});
+      // S has been read: the tensor core may write S(t+1)
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.sempty);
       l = alpha * l + (rs2.x + rs2.y) * sp;
       m = m_new;
 
