@@ -303,6 +303,12 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
         for (int hh = 0; hh < 2; ++hh) {
           float v[64];
           tmem_load64(tl + kColS + 64 * hh, tl + kColS + 64 * hh + 32, v);
+          if (hh == 1) {
+            // S has been read: the tensor core may write S(t+1)
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.sempty);
+          }
 #pragma unroll
           for (int c = 0; c < 64; c += 16) {
             uint32_t w4[4];
@@ -330,10 +336,6 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
         p_codes(std::true_type{});
       else
         p_codes(std::false_type{});
-      // S has been read: the tensor core may write S(t+1)
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.sempty);
       l = alpha * l + (rs2.x + rs2.y) * sp;
       m = m_new;
 
