@@ -41,8 +41,17 @@ FALLBACK_BF16_TFLOPS = 1900.0
 
 # DRAM traffic of one backward launch on the default workload, from the ncu
 # capture summarised in profiles/ (valid only for the kernel source it was
-# taken on; reported as null once dm_bwd.cu changes).
-BWD_TRAFFIC = {"sha1": "74f18abf8ff85862185339247be5b64e7a2f28bd", "bytes": 268921344}
+# taken on; reported as null once dm_bwd.cu or dm_device.cuh changes).
+BWD_TRAFFIC = {"sha1": "813d88a94fca956d469708df1d9ecba95e243e56", "bytes": 271275264}
+
+
+def bwd_source_hash():
+    """SHA-1 over the backward kernel's sources (the kernel and its device helpers)."""
+    h = hashlib.sha1()
+    for name in ("dm_bwd.cu", "dm_device.cuh"):
+        with open(os.path.join(ROOT, "fp8_attention_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def parse():
@@ -241,7 +250,7 @@ def run_native(args, rank, world, local_rank):
     kernel_ms = {name: statistics.mean(x[i] for x in per)
                  for i, name in enumerate(("quantize", "fwd", "delta", "bwd"))}
     bwd_tflops = fl["bwd"] / (kernel_ms["bwd"] * 1e-3) / 1e12
-    src_hash = hashlib.sha1(open(os.path.join(ROOT, "fp8_attention_gb300", "csrc", "dm_bwd.cu"), "rb").read()).hexdigest()
+    src_hash = bwd_source_hash()
     traffic = BWD_TRAFFIC["bytes"] if BWD_TRAFFIC["sha1"] == src_hash else None
     line = {
         "metric": METRIC,
