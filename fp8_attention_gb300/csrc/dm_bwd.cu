@@ -302,6 +302,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wg = (warp - 4) >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // key row within the tile (TMEM lane)
+    // swizzled offsets of this thread's row in 128-byte row tiles: chunk c at
+    // (tile + rsw) ^ 16 c; rsw_wg starts at this warpgroup's 64-byte half
+    const uint32_t rsw = SwTile<128>::row_base(r);
+    const uint32_t rsw_wg = rsw ^ (64u * wg);
     const bool kv_valid = kt * kTile + r < a.N;
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
     const int ct = tid - 128;  // 0..255
@@ -353,12 +357,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < DH; c += 32) {
         float v[32];
         tmem_load32(tl + bm * 128 + wg * DH + c, v);
-        uint8_t* box = sm + L::kDQ + ((wg * DH + c) / 32) * (kTile * 128);
+        const uint32_t box = L::kDQ + ((wg * DH + c) / 32) * (kTile * 128) + rsw;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float2 a01 = __fmul2_rn(make_float2(v[4 * e], v[4 * e + 1]), make_float2(cdq, cdq));
           const float2 a23 = __fmul2_rn(make_float2(v[4 * e + 2], v[4 * e + 3]), make_float2(cdq, cdq));
-          *reinterpret_cast<float4*>(box + SwTile<128>::chunk_offset(r, e)) = make_float4(a01.x, a01.y, a23.x, a23.y);
+          *reinterpret_cast<float4*>(sm + (box ^ (16u * e))) = make_float4(a01.x, a01.y, a23.x, a23.y);
         }
       }
       tc_fence_before();
@@ -428,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the two in opposite order, so that on every SM sub-partition one
       // warp's code conversion overlaps the other's TMEM loads and staging.
       auto write_p = [&]() {
-        uint8_t* dst = sm + L::kPt + bn * kTile * kTile;
+        const uint32_t dst = L::kPt + bn * kTile * kTile + rsw_wg;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t w4[4];
@@ -439,8 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 a23 = __fmul2_rn(make_float2(q4[2], q4[3]), make_float2(rp, rp));
             w4[e] = pack4_e4m3(a01.x, a01.y, a23.x, a23.y);
           }
-          *reinterpret_cast<uint4*>(dst + SwTile<128>::chunk_offset(r, wg * 4 + c)) =
-              make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          *reinterpret_cast<uint4*>(sm + (dst ^ (16u * c))) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
         if (n + 1 < n_iter) {
           stage_row(n + 1, row_next);
@@ -500,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto write_ds = [&]() {
         uint32_t dcode[16];
         {
-          uint8_t* dst = sm + L::kDSt + bn * kTile * kTile;
+          const uint32_t dst = L::kDSt + bn * kTile * kTile + rsw_wg;
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             const float2 a01 = __fmul2_rn(make_float2(ds[4 * c], ds[4 * c + 1]), make_float2(rs, rs));
@@ -509,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int c = 0; c < 4; ++c)
-            *reinterpret_cast<uint4*>(dst + SwTile<128>::chunk_offset(r, wg * 4 + c)) =
+            *reinterpret_cast<uint4*>(sm + (dst ^ (16u * c))) =
                 make_uint4(dcode[4 * c], dcode[4 * c + 1], dcode[4 * c + 2], dcode[4 * c + 3]);
         }
         // per-query-row diagnostics (column sums over the key rows)
@@ -584,12 +587,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < DH; c += 32) {
           float v[32];
           tmem_load32(tl + col + wg * DH + c, v);
-          uint8_t* box = sm + L::kDQ + ((wg * DH + c) / 32) * (kTile * 128);
+          const uint32_t box = L::kDQ + ((wg * DH + c) / 32) * (kTile * 128) + rsw;
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const float2 a01 = __fmul2_rn(make_float2(v[4 * e], v[4 * e + 1]), make_float2(unit, unit));
             const float2 a23 = __fmul2_rn(make_float2(v[4 * e + 2], v[4 * e + 3]), make_float2(unit, unit));
-            *reinterpret_cast<float4*>(box + SwTile<128>::chunk_offset(r, e)) =
+            *reinterpret_cast<float4*>(sm + (box ^ (16u * e))) =
                 make_float4(a01.x, a01.y, a23.x, a23.y);
           }
         }

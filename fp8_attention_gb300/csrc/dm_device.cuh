@@ -231,6 +231,14 @@ struct SwTile {
     constexpr uint32_t kMask = ROW_BYTES == 128 ? 7u : 3u;
     return a ^ (((a >> 7) & kMask) << 4);
   }
+  // The same with the row part hoisted: chunk c of row r sits at
+  // row_base(r) ^ 16 c, also after adding a 1024-byte aligned tile offset to
+  // row_base (which leaves bits [4, 7) alone), so a thread writing its row
+  // pays one XOR per chunk.
+  __device__ static uint32_t row_base(int r) {
+    constexpr uint32_t kMask = ROW_BYTES == 128 ? 7u : 3u;
+    return (uint32_t)r * ROW_BYTES | (((uint32_t)r & kMask) << 4);
+  }
 };
 
 // 32 lanes x 32 consecutive 32-bit columns.  Lane quarter of the warp is

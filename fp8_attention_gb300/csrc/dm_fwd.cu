@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
       const float bias = (r > 0.0f ? __log2f(r) : -INFINITY) - m_new;
       const float2 c1_2 = make_float2(c1, c1), b2 = make_float2(bias, bias);
       float2 rs2 = make_float2(0.0f, 0.0f);
-      uint8_t* sP = sm + L::kP + (t & 1) * kTile * kTile;
+      const uint32_t sP = L::kP + (t & 1) * kTile * kTile + SwTile<128>::row_base(row);  // chunk c at sP ^ 16 c
       auto p_codes = [&](auto full_tile) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
               rs2 = __fadd2_rn(rs2, __fadd2_rn(q01, q23));
               w4[e] = pack4_e4m3(q01.x, q01.y, q23.x, q23.y);
             }
-            *reinterpret_cast<uint4*>(sP + SwTile<128>::chunk_offset(row, (64 * hh + c) / 16)) =
+            *reinterpret_cast<uint4*>(sm + (sP ^ (uint32_t)(4 * hh + c / 16) * 16u)) =
                 make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
         }
