@@ -81,6 +81,9 @@ def _load():
             lib.or_attn_bwd.restype = I
             lib.or_attn_bwd.argtypes = [I, I, I, I, I, I, D, I, P, P, P, P, P, P,
                                         P, I, P, I, P, I, P, P, P, P, P, P, P]
+            lib.or_rope_table.argtypes = [I, I, D, P, P]
+            lib.or_qk_prologue.restype = I
+            lib.or_qk_prologue.argtypes = [P, I, I, I, I, P, D, I, D, P]
             lib.or_num_threads.restype = I
             _lib = lib
     return _lib
@@ -299,3 +302,41 @@ def _delta_tiles(q_tiles, kv_tiles, N, causal):
     for kt in (kv_tiles if kv_tiles is not None else range(T)):
         need.update(range(int(kt) if causal else 0, T))
     return sorted(need)
+
+
+# ------------------------------------------------------------------ prologue
+ROPE_BASE = 10000.0
+RMS_EPS = 1e-6
+
+
+def rope_table(N: int, d: int, base: float = ROPE_BASE):
+    """cos and sin of the rotary angles n * base^(-2i/d), each [N][d/2] float64."""
+    lib = _load()
+    if d <= 0 or d % 2 or N < 0:
+        raise ValueError("rope_table: need N >= 0 and an even d > 0")
+    c = np.empty((N, d // 2), dtype=np.float64)
+    s = np.empty((N, d // 2), dtype=np.float64)
+    lib.or_rope_table(N, d, float(base), _p(c), _p(s))
+    return c, s
+
+
+def qk_prologue(x, gain=None, eps: float = RMS_EPS, rope: bool = True, base: float = ROPE_BASE) -> np.ndarray:
+    """rotary(RMSNorm(x) * gain) of a [B][H][N][d] tensor, in FP64 (positions n = row index)."""
+    lib = _load()
+    xa = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    if xa.ndim != 4:
+        raise ValueError("x must be [B][H][N][d]")
+    B, H, N, d = xa.shape
+    g = None if gain is None else np.ascontiguousarray(np.asarray(gain, dtype=np.float64).reshape(d))
+    y = np.empty(xa.shape, dtype=np.float64)
+    if lib.or_qk_prologue(_p(xa), B, H, N, d, _p(g), float(eps), int(bool(rope)), float(base), _p(y)) != 0:
+        raise ValueError("or_qk_prologue: bad arguments")
+    return y
+
+
+def qk_prologue_quantized(x, gain=None, eps: float = RMS_EPS, rope: bool = True, base: float = ROPE_BASE):
+    """The prologue's E4M3 tile quantisation: (codes, scales, y) with codes and
+    scales = quantize(fl32(y), E4M3) and y the FP64 prologue output."""
+    y = qk_prologue(x, gain, eps, rope, base)
+    codes, scales = quantize(y.astype(np.float32), E4M3)
+    return codes, scales, y

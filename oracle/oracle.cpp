@@ -21,7 +21,10 @@
 // float8 casts and exhaustive decode; exact-mode forward/backward against
 // central finite differences and torch autograd in FP64; the identities of
 // sections 01-03 (saved-output shortcut, zero row sum, shift invariance, the
-// two-term split of the stale residual, dS_stale = dS_centered + eps*P).
+// two-term split of the stale residual, dS_stale = dS_centered + eps*P); the
+// attention-input prologue against textbook rotary values, the rotation as
+// complex multiplication, the relative-position property and the RMSNorm
+// invariants (tests/test_oracle_prologue.py).
 
 #include <cmath>
 #include <cstdint>
@@ -601,6 +604,66 @@ int or_attn_bwd(int B, int Hq, int Hkv, int N, int d, int causal, double sigma, 
                 for (int k = 0; k < d; ++k) dk[k] += D.sigma * ds * qr[k];
             }
         }
+      }
+    }
+  }
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
+// Attention-input prologue of a QK-normalised rotary model.  The models on the
+// project page normalise queries and keys with RMSNorm and learned per-channel
+// gains ("Delta-Matching for reliable FP8 attention training", section 02:
+// the gains are the RMSNorm scales on query and key channels, and one of them
+// grows to about 5.4 under stale delta) and use rotary position embedding
+// (section 05, "Attention variants change when failure appears": QK
+// normalisation can be removed, and removing RoPE gives the NoPE variant).
+// The pages give no epsilon, rotary layout or base; readings:
+//   RMSNorm  y_k = x_k / sqrt(mean_k x_k^2 + eps) * g_k   (g shared by heads)
+//   rotary   channel i < d/2 pairs with channel i + d/2 ("rotate half"), at
+//            the row's sequence position n, angle theta = n * base^(-2i/d):
+//            (a, b) <- (a cos theta - b sin theta, b cos theta + a sin theta).
+// Everything in FP64; the quantised result is or_quantize of fl32(y).
+
+// cos and sin of the rotary angles, [N][d/2] each.
+void or_rope_table(int N, int d, double base, double* cosv, double* sinv) {
+  const int h = d / 2;
+  for (int n = 0; n < N; ++n)
+    for (int i = 0; i < h; ++i) {
+      const double theta = (double)n * std::pow(base, -2.0 * i / d);
+      cosv[(size_t)n * h + i] = std::cos(theta);
+      sinv[(size_t)n * h + i] = std::sin(theta);
+    }
+}
+
+// y = rotary(RMSNorm(x) * gain) for every row of a [B][H][N][d] tensor.
+// gain: [d] or NULL (all ones); rope = 0 skips the rotation.
+int or_qk_prologue(const float* x, int B, int H, int N, int d, const double* gain, double eps, int rope,
+                   double base, double* y) {
+  if (B < 0 || H < 0 || N < 0 || d <= 0 || (d % 2) || !(eps >= 0.0)) return 1;
+  const int h = d / 2;
+  std::vector<double> cosv, sinv;
+  if (rope) {
+    cosv.resize((size_t)N * h);
+    sinv.resize((size_t)N * h);
+    or_rope_table(N, d, base, cosv.data(), sinv.data());
+  }
+  const int64_t rows = (int64_t)B * H * N;
+#pragma omp parallel for schedule(static)
+  for (int64_t row = 0; row < rows; ++row) {
+    const float* xr = x + (size_t)row * d;
+    double* yr = y + (size_t)row * d;
+    double ss = 0.0;
+    for (int k = 0; k < d; ++k) ss += (double)xr[k] * (double)xr[k];
+    const double inv = 1.0 / std::sqrt(ss / d + eps);
+    for (int k = 0; k < d; ++k) yr[k] = (double)xr[k] * inv * (gain ? gain[k] : 1.0);
+    if (rope) {
+      const int n = (int)(row % N);
+      for (int i = 0; i < h; ++i) {
+        const double c = cosv[(size_t)n * h + i], sn = sinv[(size_t)n * h + i];
+        const double a = yr[i], b = yr[i + h];
+        yr[i] = a * c - b * sn;
+        yr[i + h] = b * c + a * sn;
       }
     }
   }
