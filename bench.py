@@ -241,6 +241,36 @@ def run_native(args, rank, world, local_rank):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
 
+    # ---- attention-input prologue of Q and K (RMSNorm with the workload's
+    # gains, rotary embedding, E4M3 tile quantisation; one launch), timed on
+    # its own from the pre-normalisation draws: it is not part of the step
+    from fp8_attention_gb300.inputs import make_prologue_inputs
+    xq, xk, gain = make_prologue_inputs(w)
+    xqd, xkd, gd = xq.to(dev), xk.to(dev), gain.to(dev)
+    pro_marks, pro_clean = [], []
+    with torch.cuda.stream(st):
+        table = dm.dm_rope_table(w.N, w.d, device=dev, stream=st)
+        for i in range(3 + 2 * max(3, min(args.steps, 20))):
+            # alternately after the write flush (whose dirty lines the launch
+            # then writes back) and after a read sweep (which leaves L2 clean)
+            clean = i >= 3 and i % 2 == 1
+            if clean:
+                flush.sum()
+            else:
+                flush.zero_()
+            a, b = ev(), ev()
+            a.record(st)
+            dm.dm_qk_prologue_batch([(xqd, gd), (xkd, gd)], rope=table, stream=st)
+            b.record(st)
+            if i >= 3:
+                (pro_clean if clean else pro_marks).append((a, b))
+    torch.cuda.synchronize(dev)
+    if dm.dm_get_status(st) != 0:
+        raise RuntimeError("device status error in the prologue")
+    pro_ms = statistics.mean(a.elapsed_time(b) for a, b in pro_marks)
+    pro_clean_ms = statistics.mean(a.elapsed_time(b) for a, b in pro_clean)
+    del xqd, xkd, table
+
     fl = flops_of(w)
     step_flops = fl["fwd"] + fl["delta"] + fl["bwd"]
     ms_per_step = total_ms / args.steps
@@ -286,6 +316,15 @@ def run_native(args, rank, world, local_rank):
                      "traffic": traffic},
         "e2e": {"value": round(world * step_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        # Q and K prologue: x read + 1 B code per element, tile scales, the
+        # rotary table (read once; every head shares it) and the gains
+        "prologue": {"ms": round(pro_ms, 4), "gbs": round(prologue_bytes(w) / (pro_ms * 1e-3) / 1e9, 1),
+                     "bytes": prologue_bytes(w),
+                     "hbm_frac": round(prologue_bytes(w) / (pro_ms * 1e-3) / 1e9 / float(mp.get("hbm_gbs", 6800.0)), 3),
+                     "ms_clean_l2": round(pro_clean_ms, 4),
+                     "gbs_clean_l2": round(prologue_bytes(w) / (pro_clean_ms * 1e-3) / 1e9, 1),
+                     "timed": "alone, after the step's timed region; ms after the 256 MiB write flush, "
+                              "ms_clean_l2 after a 256 MiB read sweep"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed": round(wall, 3),
@@ -306,6 +345,15 @@ def quant_bytes(w):
     elements = 2 * el_q + 2 * el_kv
     scales = 4 * tiles * (2 * w.B * w.Hq + 2 * w.B * w.Hkv)
     return elements * (in_bytes + 1) + scales
+
+
+def prologue_bytes(w):
+    """Algorithmic HBM bytes of the Q and K prologue: x in, FP8 codes and tile
+    scales out, the [N][d/2] cos and sin tables and the gains read once."""
+    el = w.B * (w.Hq + w.Hkv) * w.N * w.d
+    tiles = (w.N + 127) // 128
+    in_bytes = 2 if w.storage == "bf16" else 4
+    return el * (in_bytes + 1) + 4 * tiles * w.B * (w.Hq + w.Hkv) + 2 * 4 * w.N * (w.d // 2) + 4 * w.d
 
 
 # ------------------------------------------------------------------ oracle

@@ -22,7 +22,8 @@ import torch
 
 __all__ = [
     "AttnParams", "Fp8", "DMError", "lib", "dm_version", "dm_status_string", "dm_set_knob",
-    "dm_get_status", "dm_last_timeout_site", "dm_quantize", "dm_quantize_batch", "dm_attn_fwd", "dm_attn_delta", "dm_attn_bwd",
+    "dm_get_status", "dm_last_timeout_site", "dm_quantize", "dm_quantize_batch", "dm_rope_table",
+    "dm_qk_prologue_batch", "ROPE_BASE", "RMS_EPS", "DM_PROLOGUE_MAX_JOBS", "dm_attn_fwd", "dm_attn_delta", "dm_attn_bwd",
     "dm_attn_bwd_workspace_size", "dm_attn_bwd_noalloc", "DM_NOALLOC_MAX_DELTA_ROWS",
     "DM_F32", "DM_BF16", "DM_E4M3", "DM_E5M2", "DM_DELTA_MATCHED", "DM_DELTA_STALE_DO",
     "DM_DELTA_STALE_DOHAT", "DM_KNOB_WAIT_LIMIT_NS", "DM_KNOB_STALL_TEST",
@@ -111,6 +112,10 @@ def lib():
             L.dm_quantize.argtypes = [P, I, I, I, I, I, I, P, P, P, P]
             L.dm_quantize_batch.restype = I
             L.dm_quantize_batch.argtypes = [P, I, I, P]
+            L.dm_rope_table.restype = I
+            L.dm_rope_table.argtypes = [I, I, ctypes.c_double, P, P, P]
+            L.dm_qk_prologue_batch.restype = I
+            L.dm_qk_prologue_batch.argtypes = [P, I, I, ctypes.c_float, P]
             L.dm_attn_fwd.restype = I
             L.dm_attn_fwd.argtypes = [PP, _Fp8, _Fp8, _Fp8, P, I, P, P]
             L.dm_attn_delta.restype = I
@@ -224,6 +229,52 @@ def dm_quantize_batch(tensors, stream=None):
     arr = (_QuantJob * len(jobs))(*jobs)
     rc = lib().dm_quantize_batch(arr, len(jobs), dtype, _stream(stream))
     _check(rc, "dm_quantize_batch")
+    return outs
+
+
+ROPE_BASE = 10000.0
+RMS_EPS = 1e-6
+DM_PROLOGUE_MAX_JOBS = 4
+
+
+def dm_rope_table(N: int, d: int, base: float = ROPE_BASE, device="cuda", stream=None):
+    """cos and sin of the rotary angles n * base^(-2i/d): two float32 tensors [N][d/2] on the device."""
+    cos = torch.empty((N, d // 2), dtype=torch.float32, device=device)
+    sin = torch.empty((N, d // 2), dtype=torch.float32, device=device)
+    rc = lib().dm_rope_table(int(N), int(d), float(base), _ptr(cos), _ptr(sin), _stream(stream))
+    _check(rc, "dm_rope_table")
+    return cos, sin
+
+
+class _PrologueJob(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("B", ctypes.c_int), ("H", ctypes.c_int), ("N", ctypes.c_int),
+                ("d", ctypes.c_int), ("gain", ctypes.c_void_p), ("rope_cos", ctypes.c_void_p),
+                ("rope_sin", ctypes.c_void_p), ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
+
+
+def dm_qk_prologue_batch(tensors, rope=None, eps: float = RMS_EPS, stream=None):
+    """RMSNorm with channel gains, rotary embedding and E4M3 tile quantisation of
+    several [B][H][N][d] tensors in one launch.  tensors: sequence of (x, gain)
+    with gain a float32 [d] device tensor or None; rope: (cos, sin) from
+    dm_rope_table (covering every position) or None.  Returns one Fp8 each."""
+    jobs, outs = [], []
+    cos, sin = rope if rope is not None else (None, None)
+    for x, gain in tensors:
+        B, H, N, d = x.shape
+        T = (N + TILE - 1) // TILE
+        codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+        scales = torch.empty((B, H, T), dtype=torch.float32, device=x.device)
+        jobs.append(_PrologueJob(_ptr(x), B, H, N, d, _ptr(gain), _ptr(cos), _ptr(sin), _ptr(codes),
+                                 _ptr(scales)))
+        outs.append(Fp8(codes, scales))
+    if not jobs:
+        return []
+    dtype = _dtype(tensors[0][0])
+    if any(_dtype(x) != dtype for x, _ in tensors):
+        raise DMError(DM_ERR_DTYPE, "dm_qk_prologue_batch: tensors of different dtypes")
+    arr = (_PrologueJob * len(jobs))(*jobs)
+    rc = lib().dm_qk_prologue_batch(arr, len(jobs), dtype, float(eps), _stream(stream))
+    _check(rc, "dm_qk_prologue_batch")
     return outs
 
 

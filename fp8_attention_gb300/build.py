@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdm.so")
-SOURCES = ["dm_api.cu", "dm_elementwise.cu", "dm_fwd.cu", "dm_delta.cu", "dm_bwd.cu", "dm_noalloc.cu"]
+SOURCES = ["dm_api.cu", "dm_elementwise.cu", "dm_prologue.cu", "dm_fwd.cu", "dm_delta.cu", "dm_bwd.cu", "dm_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", CSRC, "-I", INCLUDE]
 

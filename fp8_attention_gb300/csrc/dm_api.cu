@@ -231,6 +231,7 @@ unsigned int dm_last_timeout_site(void) {
 }
 
 static_assert(DM_QUANTIZE_MAX_JOBS == dm::QuantBatch::kMaxJobs, "quantiser batch size");
+static_assert(DM_PROLOGUE_MAX_JOBS == dm::PrologueBatch::kMaxJobs, "prologue batch size");
 
 namespace {
 dm_status check_quantize_job(const dm_quantize_job& j, int d) {
@@ -283,6 +284,67 @@ dm_status dm_quantize(const void* x, dm_dtype x_dtype, int B, int H, int N, int 
   const dm_quantize_job job{x, B, H, N, d, fmt, codes, scales, codes_t};
   if (d != 64 && d != 128) return valid_dtype(x_dtype) ? DM_ERR_SHAPE : DM_ERR_DTYPE;
   return dm_quantize_batch(&job, 1, x_dtype, stream);
+}
+
+namespace {
+dm_status check_prologue_job(const dm_prologue_job& j, int d) {
+  if (j.B < 0 || j.H <= 0 || j.N < 0 || j.d != d) return DM_ERR_SHAPE;
+  if ((long long)j.B * j.H * j.N * j.d >= (1ll << 31)) return DM_ERR_SHAPE;
+  if ((j.rope_cos == nullptr) != (j.rope_sin == nullptr)) return DM_ERR_INVALID_ARG;
+  if (j.B == 0 || j.N == 0) return DM_OK;  // empty tensor: pointers may be NULL
+  DM_TRY(check_ptr(j.x));
+  DM_TRY(check_ptr(j.codes));
+  DM_TRY(check_ptr(j.scales));
+  if (j.gain && !aligned16(j.gain)) return DM_ERR_ALIGNMENT;
+  if (j.rope_cos && (!aligned16(j.rope_cos) || !aligned16(j.rope_sin))) return DM_ERR_ALIGNMENT;
+  return DM_OK;
+}
+}  // namespace
+
+dm_status dm_qk_prologue_batch(const dm_prologue_job* jobs, int njobs, dm_dtype x_dtype, float eps, void* stream) {
+  if (!valid_dtype(x_dtype)) return DM_ERR_DTYPE;
+  if (njobs < 0 || njobs > DM_PROLOGUE_MAX_JOBS) return DM_ERR_INVALID_ARG;
+  if (!(eps > 0.0f) || !(eps < INFINITY)) return DM_ERR_INVALID_ARG;
+  if (njobs == 0) return DM_OK;
+  if (!jobs) return DM_ERR_INVALID_ARG;
+  const int d = jobs[0].d;
+  if (d != 64 && d != 128) return DM_ERR_SHAPE;
+  dm::PrologueBatch b{};
+  long long tiles = 0;
+  for (int i = 0; i < njobs; ++i) {
+    DM_TRY(check_prologue_job(jobs[i], d));
+    if (jobs[i].B == 0 || jobs[i].N == 0) continue;
+    dm::PrologueJob& q = b.job[b.count];
+    q.x = jobs[i].x;
+    q.N = jobs[i].N;
+    q.T_tiles = (jobs[i].N + 127) / 128;
+    q.gain = jobs[i].gain;
+    q.rope_cos = jobs[i].rope_cos;
+    q.rope_sin = jobs[i].rope_sin;
+    q.codes = jobs[i].codes;
+    q.scales = jobs[i].scales;
+    b.first_tile[b.count] = (int)tiles;
+    tiles += (long long)jobs[i].B * jobs[i].H * q.T_tiles;
+    ++b.count;
+  }
+  if (b.count == 0) return DM_OK;
+  if (tiles >= (1ll << 31)) return DM_ERR_SHAPE;
+  b.first_tile[b.count] = (int)tiles;
+  unsigned int* status = nullptr;
+  DM_TRY(device_state(&status));
+  return cuda_status(dm::launch_prologue(b, x_dtype, d, eps, as_stream(stream)));
+}
+
+dm_status dm_rope_table(int N, int d, double base, float* cos_table, float* sin_table, void* stream) {
+  if (N < 0 || d <= 0 || (d % 8)) return DM_ERR_SHAPE;
+  if ((long long)N * (d / 2) >= (1ll << 31)) return DM_ERR_SHAPE;
+  if (!(base > 1.0) || !(base < INFINITY)) return DM_ERR_INVALID_ARG;
+  if (N == 0) return DM_OK;
+  DM_TRY(check_ptr(cos_table));
+  DM_TRY(check_ptr(sin_table));
+  unsigned int* status = nullptr;
+  DM_TRY(device_state(&status));
+  return cuda_status(dm::launch_rope_table(N, d, base, cos_table, sin_table, as_stream(stream)));
 }
 
 dm_status dm_attn_fwd(const dm_attn_params* p, dm_fp8_tensor q, dm_fp8_tensor k, dm_fp8_tensor v, void* O,

@@ -50,6 +50,25 @@ struct QuantBatch {
 };
 
 cudaError_t launch_quantize(const QuantBatch& b, dm_dtype xt, int d, cudaStream_t st);
+
+// Tensors one prologue launch processes (same input dtype, d and eps).
+struct PrologueJob {
+  const void* x;
+  int N, T_tiles;
+  const float* gain;      // nullable
+  const float* rope_cos;  // nullable (no rotary embedding)
+  const float* rope_sin;
+  uint8_t* codes;
+  float* scales;
+};
+struct PrologueBatch {
+  static constexpr int kMaxJobs = 4;
+  PrologueJob job[kMaxJobs];
+  int first_tile[kMaxJobs + 1];
+  int count;
+};
+cudaError_t launch_prologue(const PrologueBatch& b, dm_dtype xt, int d, float eps, cudaStream_t st);
+cudaError_t launch_rope_table(int N, int d, double base, float* cos_t, float* sin_t, cudaStream_t st);
 cudaError_t launch_attn_fwd(const FwdLaunch& f, int d, bool o_bf16, cudaStream_t st);
 cudaError_t launch_delta_matched(const DeltaLaunch& f, int d, cudaStream_t st);
 cudaError_t launch_delta_stale(const AttnArgs& a, int d, dm_delta_mode mode, const void* dO, dm_dtype do_t,

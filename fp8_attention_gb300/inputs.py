@@ -83,3 +83,24 @@ def make_inputs(w: Workload):
         k = _rms_norm(k, w.gains)
     dt = torch.bfloat16 if w.storage == "bf16" else torch.float32
     return tuple(t.to(dt).contiguous() for t in (q, k, v, do))
+
+
+def gain_vector(w: Workload) -> torch.Tensor:
+    """The workload's per-channel gains as a float32 [d] vector (1.0 where unset)."""
+    g = torch.ones(w.d, dtype=torch.float32)
+    for ch, val in w.gains.items():
+        if ch < w.d:
+            g[ch] = float(val)
+    return g
+
+
+def make_prologue_inputs(w: Workload):
+    """Return (xq, xk, gain): the workload's Q and K draws before any
+    normalisation (same generator order as make_inputs), in its storage dtype,
+    and its gain vector, as inputs for the attention-input prologue."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(w.seed)
+    xq = torch.randn(w.B, w.Hq, w.N, w.d, generator=gen, dtype=torch.float32)
+    xk = torch.randn(w.B, w.Hkv, w.N, w.d, generator=gen, dtype=torch.float32)
+    dt = torch.bfloat16 if w.storage == "bf16" else torch.float32
+    return xq.to(dt).contiguous(), xk.to(dt).contiguous(), gain_vector(w)

@@ -126,6 +126,51 @@ typedef struct {
 } dm_quantize_job;
 dm_status dm_quantize_batch(const dm_quantize_job* jobs, int njobs, dm_dtype x_dtype, void* stream);
 
+/* dm_rope_table -- cos and sin of the rotary angles theta(n, i) = n *
+ * base^(-2i/d), n < N, i < d/2, written as float [N][d/2] each (row n = the
+ * sequence position), computed in FP64 on the device and rounded to FP32.
+ * The pages' models use RoPE (project page, section 05, "Attention variants
+ * change when failure appears", where removing it is the NoPE variant) but
+ * give no base; 10000 is the usual one.  d must be a multiple of 8 (so rows
+ * stay 16-byte aligned), base > 1; the caller owns both tables (16-byte
+ * aligned).  DM_ERR_SHAPE / DM_ERR_INVALID_ARG / DM_ERR_ALIGNMENT on bad
+ * arguments, before any launch. */
+dm_status dm_rope_table(int N, int d, double base, float* cos_table, float* sin_table, void* stream);
+
+/* dm_qk_prologue_batch -- the attention-input prologue of a QK-normalised
+ * rotary model fused with the tile quantiser, for up to
+ * DM_PROLOGUE_MAX_JOBS tensors (typically Q and K) in one launch.  The pages'
+ * models normalise queries and keys with RMSNorm and learned per-channel
+ * gains (project page, section 02: the gains are the quantity that drifts
+ * under stale delta) before attention.  Per row of x ([B][H][N][d] of x_dtype,
+ * DM_F32 or DM_BF16, row n = sequence position n):
+ *   y_k = x_k / sqrt(mean_k x_k^2 + eps) * gain_k     (gain [d] float shared by
+ *                                                      the heads; NULL = ones)
+ *   if rope_cos: channel i < d/2 and channel i + d/2 rotate by theta(n, i):
+ *     (a, b) <- (a cos - b sin, b cos + a sin), cos/sin from rope_cos/rope_sin
+ *     ([N][d/2] float, e.g. from dm_rope_table; both or neither)
+ * then y is quantised to E4M3 with the rule of dm_quantize (one FP32 scale per
+ * 128-row x d tile): codes [B][H][N][d], scales [B][H][ceil(N/128)], ready
+ * for dm_attn_fwd.  All arithmetic is FP32 (IEEE divide and square root), so
+ * codes can differ from an exact evaluation only where y * (448 / amax) lies
+ * within FP32 rounding of a code boundary.  All jobs share x_dtype, d (64 or
+ * 128) and eps (finite, > 0); x, codes, scales, gain and the tables are
+ * 16-byte aligned.  Every job is validated before the launch;
+ * empty tensors are skipped.  Errors: DM_ERR_DTYPE, DM_ERR_SHAPE,
+ * DM_ERR_INVALID_ARG (njobs out of range, bad eps, one table without the
+ * other), DM_ERR_ALIGNMENT. */
+#define DM_PROLOGUE_MAX_JOBS 4
+typedef struct {
+  const void* x;
+  int B, H, N, d;
+  const float* gain;     /* nullable */
+  const float* rope_cos; /* nullable */
+  const float* rope_sin; /* nullable */
+  uint8_t* codes;
+  float* scales;
+} dm_prologue_job;
+dm_status dm_qk_prologue_batch(const dm_prologue_job* jobs, int njobs, dm_dtype x_dtype, float eps, void* stream);
+
 /* dm_attn_fwd -- O = P^ V^ and LSE (section 01).  q, k, v: E4M3 tensors of
  * shapes [B][Hq][N][d], [B][Hkv][N][d], [B][Hkv][N][d].  O: [B][Hq][N][d] of
  * o_dtype (DM_F32 or DM_BF16).  lse: float [B][Hq][N], natural log of the

@@ -100,3 +100,33 @@ def test_validation_without_gpu(lib):
 def test_workspace_size(lib):
     assert dm.dm_attn_bwd_workspace_size(dm.AttnParams(2, 4, 2, 1000, 64)) == ((2 * 4 * 1000 * 4 + 255) // 256) * 256
     assert dm.dm_attn_bwd_workspace_size(dm.AttnParams(2, 4, 3, 1000, 64)) == 0
+
+
+def test_prologue_validation_without_gpu(lib):
+    """dm_qk_prologue_batch and dm_rope_table reject bad arguments before any CUDA call."""
+    A = 0x10000
+    J = dm._PrologueJob
+    ok = J(A, 1, 2, 256, 128, A, A, A, A, A)
+    one = (J * 1)(ok)
+    pro = lib.dm_qk_prologue_batch
+    assert pro(one, 1, 5, 1e-6, None) == dm.DM_ERR_DTYPE
+    assert pro(one, 5, 0, 1e-6, None) == dm.DM_ERR_INVALID_ARG          # more than 4 jobs
+    assert pro(one, 1, 0, 0.0, None) == dm.DM_ERR_INVALID_ARG           # eps must be > 0
+    assert pro(one, 1, 0, float("inf"), None) == dm.DM_ERR_INVALID_ARG
+    assert pro(None, 1, 0, 1e-6, None) == dm.DM_ERR_INVALID_ARG
+    assert pro((J * 1)(J(A, 1, 2, 256, 96, A, A, A, A, A)), 1, 0, 1e-6, None) == dm.DM_ERR_SHAPE
+    two = (J * 2)(ok, J(A, 1, 2, 256, 64, A, A, A, A, A))
+    assert pro(two, 2, 0, 1e-6, None) == dm.DM_ERR_SHAPE                # d differs between jobs
+    assert pro((J * 1)(J(A, 1, 2, 256, 128, A, A, None, A, A)), 1, 0, 1e-6, None) == dm.DM_ERR_INVALID_ARG
+    assert pro((J * 1)(J(A + 8, 1, 2, 256, 128, A, A, A, A, A)), 1, 0, 1e-6, None) == dm.DM_ERR_ALIGNMENT
+    assert pro((J * 1)(J(A, 1, 2, 256, 128, A + 4, A, A, A, A)), 1, 0, 1e-6, None) == dm.DM_ERR_ALIGNMENT
+    assert pro((J * 1)(J(A, 1, 2, 256, 128, A, A + 4, A + 4, A, A)), 1, 0, 1e-6, None) == dm.DM_ERR_ALIGNMENT
+    assert pro((J * 1)(J(None, 0, 2, 256, 128, None, None, None, None, None)), 1, 0, 1e-6, None) == 0
+    assert pro(None, 0, 0, 1e-6, None) == 0
+    rt = lib.dm_rope_table
+    assert rt(16, 12, 1e4, A, A, None) == dm.DM_ERR_SHAPE               # d not a multiple of 8
+    assert rt(-1, 64, 1e4, A, A, None) == dm.DM_ERR_SHAPE
+    assert rt(16, 64, 1.0, A, A, None) == dm.DM_ERR_INVALID_ARG         # base must exceed 1
+    assert rt(16, 64, 1e4, None, A, None) == dm.DM_ERR_INVALID_ARG
+    assert rt(16, 64, 1e4, A + 4, A, None) == dm.DM_ERR_ALIGNMENT
+    assert rt(0, 64, 1e4, None, None, None) == 0
