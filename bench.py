@@ -62,6 +62,7 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of the captured step")
     return ap.parse_args()
 
 
@@ -186,8 +187,27 @@ def run_native(args, rank, world, local_rank):
     if dm.dm_get_status(st) != 0:
         raise RuntimeError("device status error during warm-up")
 
+    # ---- the step captured once as a CUDA graph (the same launches, replayed
+    # without host work between them), so that host-side launch latency
+    # cannot leave the GPU idle inside the timed region
+    graph = None
+    if not args.no_graph:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=st):
+                step(inputs, st)
+            with torch.cuda.stream(st):
+                for _ in range(3):     # warm replays
+                    flush.zero_()
+                    graph.replay()
+            torch.cuda.synchronize(dev)
+        except RuntimeError as exc:  # capture unsupported: time the eager launches
+            print(f"graph capture failed ({exc}); timing eager launches", file=sys.stderr)
+            graph = None
+            torch.cuda.synchronize(dev)
+
     # ---- device-resident timed region
-    marks = []
+    marks, gmarks = [], []
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -196,7 +216,14 @@ def run_native(args, rank, world, local_rank):
         with torch.cuda.stream(st):
             for _ in range(args.steps):
                 flush.zero_()          # L2 flush between timed steps (outside the events)
-                step(inputs, st, marks)
+                if graph is not None:
+                    a, b = ev(), ev()
+                    a.record(st)
+                    graph.replay()
+                    b.record(st)
+                    gmarks.append((a, b))
+                else:
+                    step(inputs, st, marks)
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - wall0
     if dist:
@@ -204,8 +231,17 @@ def run_native(args, rank, world, local_rank):
     status = dm.dm_get_status(st)
     if status != 0:
         raise RuntimeError(f"device status {dm.dm_status_string(status)}")
+    if graph is not None:
+        # per-kernel split from separately timed eager steps (events between the launches)
+        with torch.cuda.stream(st):
+            for _ in range(max(3, min(args.steps, 50))):
+                flush.zero_()
+                step(inputs, st, marks)
+        torch.cuda.synchronize(dev)
+        step_ms = [a.elapsed_time(b) for a, b in gmarks]
     per = [[m[i].elapsed_time(m[i + 1]) for i in range(4)] for m in marks]
-    step_ms = [sum(x) for x in per]
+    if graph is None:
+        step_ms = [sum(x) for x in per]
     total_ms = sum(step_ms)
     if dist:
         t = torch.tensor([total_ms], device=dev)
@@ -250,6 +286,15 @@ def run_native(args, rank, world, local_rank):
     pro_marks, pro_clean = [], []
     with torch.cuda.stream(st):
         table = dm.dm_rope_table(w.N, w.d, device=dev, stream=st)
+    torch.cuda.synchronize(dev)
+    prologue = lambda: dm.dm_qk_prologue_batch([(xqd, gd), (xkd, gd)], rope=table, stream=st)
+    pro_graph = None
+    if graph is not None:
+        pro_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(pro_graph, stream=st):
+            prologue()
+        torch.cuda.synchronize(dev)
+    with torch.cuda.stream(st):
         for i in range(3 + 2 * max(3, min(args.steps, 20))):
             # alternately after the write flush (whose dirty lines the launch
             # then writes back) and after a read sweep (which leaves L2 clean)
@@ -260,7 +305,10 @@ def run_native(args, rank, world, local_rank):
                 flush.zero_()
             a, b = ev(), ev()
             a.record(st)
-            dm.dm_qk_prologue_batch([(xqd, gd), (xkd, gd)], rope=table, stream=st)
+            if pro_graph is not None:
+                pro_graph.replay()
+            else:
+                prologue()
             b.record(st)
             if i >= 3:
                 (pro_clean if clean else pro_marks).append((a, b))
@@ -297,7 +345,8 @@ def run_native(args, rank, world, local_rank):
         "data": "synthetic (seeded randn, RMS-normalised Q/K, bf16 storage)",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d, "causal": w.causal,
                    "delta_mode": "matched", "flop_accounting": "issued, causal-halved, 9U per step",
-                   "l2": "flushed between timed steps (256 MiB write)", "parallelism": f"independent x{world}"},
+                   "l2": "flushed between timed steps (256 MiB write)", "parallelism": f"independent x{world}",
+                   "launch": "CUDA graph of the step, replayed" if graph is not None else "eager launches"},
         "pct_of_fp8_peak": round(100.0 * value / (world * fp8_peak), 2),
         "per_kernel_ms": {k2: round(v2, 4) for k2, v2 in kernel_ms.items()},
         "per_kernel_tflops": {
@@ -323,8 +372,8 @@ def run_native(args, rank, world, local_rank):
                      "hbm_frac": round(prologue_bytes(w) / (pro_ms * 1e-3) / 1e9 / float(mp.get("hbm_gbs", 6800.0)), 3),
                      "ms_clean_l2": round(pro_clean_ms, 4),
                      "gbs_clean_l2": round(prologue_bytes(w) / (pro_clean_ms * 1e-3) / 1e9, 1),
-                     "timed": "alone, after the step's timed region; ms after the 256 MiB write flush, "
-                              "ms_clean_l2 after a 256 MiB read sweep"},
+                     "timed": "alone (one launch, replayed as a CUDA graph), after the step's timed region; "
+                              "ms after the 256 MiB write flush, ms_clean_l2 after a 256 MiB read sweep"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed": round(wall, 3),

@@ -332,6 +332,8 @@ dm_status dm_qk_prologue_batch(const dm_prologue_job* jobs, int njobs, dm_dtype 
   b.first_tile[b.count] = (int)tiles;
   unsigned int* status = nullptr;
   DM_TRY(device_state(&status));
+  b.status = status;
+  b.wait_limit_ns = g_wait_limit_ns ? g_wait_limit_ns : kDefaultWaitLimitNs;
   return cuda_status(dm::launch_prologue(b, x_dtype, d, eps, as_stream(stream)));
 }
 

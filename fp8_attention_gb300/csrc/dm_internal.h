@@ -66,6 +66,8 @@ struct PrologueBatch {
   PrologueJob job[kMaxJobs];
   int first_tile[kMaxJobs + 1];
   int count;
+  unsigned int* status;  // device status word (bounded waits)
+  unsigned long long wait_limit_ns;
 };
 cudaError_t launch_prologue(const PrologueBatch& b, dm_dtype xt, int d, float eps, cudaStream_t st);
 cudaError_t launch_rope_table(int N, int d, double base, float* cos_t, float* sin_t, cudaStream_t st);

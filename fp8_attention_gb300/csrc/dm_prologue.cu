@@ -9,10 +9,11 @@
 // y_k = x_k / sqrt(mean x^2 + eps) * g_k; rotate-half rotary, channel i < d/2
 // paired with i + d/2, angle n * base^(-2i/d) at sequence position n.
 //
-// HBM-bound: one CTA per 128-row x d tile, d/16 threads per row.  Thread p
-// of a row holds channels [8p, 8p + 8) and the same range shifted by d/2, so
-// each rotary pair sits in one thread and the row's sum of squares needs a
-// few shuffles; every load (row and angles) is issued before any arithmetic.
+// HBM-bound: one persistent CTA per SM streams 128-row x d tiles through a
+// shared-memory ring filled by bulk copies; d/32 threads per row.  Thread p
+// of a row holds channels [16p, 16p + 16) and the same range shifted by d/2,
+// so each rotary pair sits in one thread and the row's sum of squares needs a
+// shuffle or two.
 // The rotary table ([N][d/2] cos and sin, FP32) is shared by every head and
 // stays in L2.
 #include <cuda_bf16.h>
@@ -23,10 +24,11 @@
 namespace dm {
 namespace {
 
-// One 128-row tile per CTA, D / 16 threads per row: every thread holds 8
-// channels of each half of its row (16-byte loads of bf16 rows).
+// D / 32 threads per row: every thread holds 16 channels of each half of its
+// row, so that the per-tile fixed work (waits, cursor, scale) is shared by 32
+// elements per thread.
 template <int D>
-__host__ __device__ constexpr int row_threads() { return D / 16; }
+__host__ __device__ constexpr int row_threads() { return D / 32; }
 template <int D>
 __host__ __device__ constexpr int tile_threads() { return kTile * row_threads<D>(); }
 
@@ -34,7 +36,8 @@ template <typename T>
 struct RowLoad;
 template <>
 struct RowLoad<float> {
-  // n consecutive values (n a multiple of 4, 16-byte aligned)
+  // n consecutive values (n a multiple of 4, 16-byte aligned), from global
+  // memory through the read-only path, or from shared memory
   template <int n>
   __device__ static void load(const float* p, float* out) {
 #pragma unroll
@@ -43,14 +46,22 @@ struct RowLoad<float> {
       out[k] = v.x, out[k + 1] = v.y, out[k + 2] = v.z, out[k + 3] = v.w;
     }
   }
+  template <int n>
+  __device__ static void load_shared(const float* p, float* out) {
+#pragma unroll
+    for (int k = 0; k < n; k += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(p + k);
+      out[k] = v.x, out[k + 1] = v.y, out[k + 2] = v.z, out[k + 3] = v.w;
+    }
+  }
 };
 template <>
 struct RowLoad<__nv_bfloat16> {
   template <int n>
-  __device__ static void load(const __nv_bfloat16* p, float* out) {
+  __device__ static void load_shared(const __nv_bfloat16* p, float* out) {
 #pragma unroll
     for (int k = 0; k < n; k += 8) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(p + k));
+      const uint4 v = *reinterpret_cast<const uint4*>(p + k);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -61,99 +72,195 @@ struct RowLoad<__nv_bfloat16> {
   }
 };
 
+// Where tile g (over all jobs) lives: job index j, tile index in the job,
+// (b, h) and row tile t.  Fields are read from the kernel parameters by
+// index, never through a pointer, which would copy the whole batch to local
+// memory.  A CTA walks its tiles with a stride of gridDim.x, so the cursor is
+// advanced by subtraction instead of a division per tile.
+struct TileRef {
+  int j, tile, bh, t, rows;
+};
+__device__ __forceinline__ void tile_set(const PrologueBatch& batch, int g, TileRef& r) {
+  r.j = 0;
+  while (r.j + 1 < batch.count && g >= batch.first_tile[r.j + 1]) ++r.j;
+  r.tile = g - batch.first_tile[r.j];
+  const int T_tiles = batch.job[r.j].T_tiles;
+  r.bh = r.tile / T_tiles;
+  r.t = r.tile - r.bh * T_tiles;
+  r.rows = min(kTile, batch.job[r.j].N - r.t * kTile);
+}
+__device__ __forceinline__ void tile_advance(const PrologueBatch& batch, int g, int step, TileRef& r) {
+  if (r.j + 1 < batch.count && g >= batch.first_tile[r.j + 1]) {  // crossed into a later job
+    tile_set(batch, g, r);
+    return;
+  }
+  r.tile += step;
+  r.t += step;
+  const int T_tiles = batch.job[r.j].T_tiles;
+  while (r.t >= T_tiles) r.t -= T_tiles, ++r.bh;
+  r.rows = min(kTile, batch.job[r.j].N - r.t * kTile);
+}
+
+template <typename T, int D>
+struct PrologueCfg {
+  static constexpr int kRowThreads = row_threads<D>(), kThreads = tile_threads<D>();
+  static constexpr int Q = D / (2 * kRowThreads);  // channels per thread and half-row
+  static constexpr int kTileBytes = kTile * D * (int)sizeof(T);
+  static constexpr int kStages = 4 * kTileBytes <= 160 * 1024 ? 4 : 2;
+  static constexpr int kSmem = kStages * kTileBytes;
+};
+
+// Persistent: CTA c takes tiles c, c + grid, ...; thread 0 keeps the next
+// kStages tiles in flight as bulk copies into a shared-memory ring (each tile
+// of one head is one contiguous block of rows), so the SM always has loads
+// outstanding while it normalises, rotates and encodes the current tile.
 template <typename T, int D>
 __global__ void __launch_bounds__(tile_threads<D>(), 1) prologue_kernel(const PrologueBatch batch, float eps) {
-  constexpr int kRowThreads = row_threads<D>(), kPThreads = tile_threads<D>();
-  constexpr int Q = D / (2 * kRowThreads);  // channels per thread and half-row
-  static_assert(Q == 8, "eight channels per thread and half-row");
-  __shared__ float s_red[kPThreads / 32];
+  using C = PrologueCfg<T, D>;
+  constexpr int Q = C::Q, kRowThreads = C::kRowThreads;
+  static_assert(Q == 16, "sixteen channels per thread and half-row");
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ float s_red[2][C::kThreads / 32];
+  __shared__ uint64_t full[C::kStages];
+  __shared__ int s_abort;
 
-  int j = 0;
-  while (j + 1 < batch.count && (int)blockIdx.x >= batch.first_tile[j + 1]) ++j;
-  const PrologueJob& job = batch.job[j];
-  const int N = job.N, T_tiles = job.T_tiles;
-  const int tile = (int)blockIdx.x - batch.first_tile[j];
-  const int bh = tile / T_tiles, t = tile % T_tiles;
-  const int row = threadIdx.x / kRowThreads, part = threadIdx.x % kRowThreads;
-  const int n = t * kTile + row;  // sequence position
-  const bool valid = n < N;
-  const int ca = part * Q, cb = D / 2 + part * Q;  // first channel of each half-row
-  const size_t off = ((size_t)bh * N + n) * D;
-  const bool rope = job.rope_cos != nullptr;
-
-  // every load first: the row's channels and, with rope, its angles
-  float a[Q], b[Q], c[Q], sn[Q];
-  if (valid) {
-    RowLoad<T>::template load<Q>(static_cast<const T*>(job.x) + off + ca, a);
-    RowLoad<T>::template load<Q>(static_cast<const T*>(job.x) + off + cb, b);
-    if (rope) {
-      RowLoad<float>::template load<Q>(job.rope_cos + (size_t)n * (D / 2) + ca, c);
-      RowLoad<float>::template load<Q>(job.rope_sin + (size_t)n * (D / 2) + ca, sn);
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < Q; ++k) a[k] = b[k] = 0.0f;
+  const int total = batch.first_tile[batch.count];
+  Watchdog wd{&s_abort, batch.status, batch.wait_limit_ns};
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int s = 0; s < C::kStages; ++s) mbar_init(&full[s], 1);
+    fence_barrier_init();
   }
-  // RMSNorm: the row's sum of squares over its kRowThreads threads
-  float ss = 0.0f;
-#pragma unroll
-  for (int k = 0; k < Q; ++k) ss = fmaf(a[k], a[k], ss);
-#pragma unroll
-  for (int k = 0; k < Q; ++k) ss = fmaf(b[k], b[k], ss);
-#pragma unroll
-  for (int o = 1; o < kRowThreads; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  // eps > 0 (checked by the API), so an all-zero row normalises to zeros
-  const float inv = valid ? __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ss * (1.0f / D), eps))) : 0.0f;
-  if (job.gain) {
-    float ga[Q], gb[Q];
-    RowLoad<float>::template load<Q>(job.gain + ca, ga);
-    RowLoad<float>::template load<Q>(job.gain + cb, gb);
-#pragma unroll
-    for (int k = 0; k < Q; ++k) {
-      a[k] = __fmul_rn(a[k], inv) * ga[k];
-      b[k] = __fmul_rn(b[k], inv) * gb[k];
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < Q; ++k) a[k] = __fmul_rn(a[k], inv), b[k] = __fmul_rn(b[k], inv);
-  }
-  // rotary embedding: channel ca + k pairs with cb + k, angle index ca + k
-  if (rope && valid) {
-#pragma unroll
-    for (int k = 0; k < Q; ++k) {
-      const float x0 = a[k], x1 = b[k];
-      a[k] = fmaf(x0, c[k], -__fmul_rn(x1, sn[k]));
-      b[k] = fmaf(x1, c[k], __fmul_rn(x0, sn[k]));
-    }
-  }
-  // tile amax, scale and E4M3 codes (the rule of dm_quantize)
-  float amax = 0.0f;
-#pragma unroll
-  for (int k = 0; k < Q; ++k) amax = max3(amax, fabsf(a[k]), fabsf(b[k]));
-  amax = warp_max(amax);
-  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = amax;
   __syncthreads();
-  amax = s_red[0];
+  auto issue = [&](int g, int stage) {
+    TileRef r;
+    tile_set(batch, g, r);
+    const uint32_t bytes = (uint32_t)(r.rows * D * (int)sizeof(T));
+    const T* src = static_cast<const T*>(batch.job[r.j].x) + ((size_t)r.bh * batch.job[r.j].N + (size_t)r.t * kTile) * D;
+    mbar_arrive_expect_tx(&full[stage], bytes);
+    bulk_load(ring + stage * C::kTileBytes, src, bytes, &full[stage]);
+  };
+  if (threadIdx.x == 0)
+    for (int k = 0; k < C::kStages; ++k)
+      if ((int)blockIdx.x + k * (int)gridDim.x < total) issue((int)blockIdx.x + k * (int)gridDim.x, k);
+
+  const int row = threadIdx.x / kRowThreads, part = threadIdx.x % kRowThreads;
+  const int ca = part * Q, cb = D / 2 + part * Q;  // first channel of each half-row
+  // this thread's channel gains (ones without gains), reloaded when the job changes
+  float ga[Q], gb[Q];
+  int gain_job = -1;
+  int it = 0;
+  TileRef r;
+  tile_set(batch, blockIdx.x, r);
+  for (int g = blockIdx.x; g < total; g += gridDim.x, ++it) {
+    if (it > 0) tile_advance(batch, g, gridDim.x, r);
+    const int stage = it % C::kStages;
+    const float* gain = batch.job[r.j].gain;
+    const float* rope_cos = batch.job[r.j].rope_cos;
+    const float* rope_sin = batch.job[r.j].rope_sin;
+    const int N = batch.job[r.j].N;
+    if (r.j != gain_job) {
+      gain_job = r.j;
+      if (gain) {
+        RowLoad<float>::template load<Q>(gain + ca, ga);
+        RowLoad<float>::template load<Q>(gain + cb, gb);
+      } else {
 #pragma unroll
-  for (int w = 1; w < kPThreads / 32; ++w) amax = fmaxf(amax, s_red[w]);
-  float r;
-  const float sc = tile_scale<0>(amax, r);
-  if (threadIdx.x == 0) job.scales[tile] = sc;
-  if (!valid) return;
-  const bool flushed = sc == 0.0f;  // all codes +0
-  uint32_t wa[Q / 4], wb[Q / 4];
+        for (int k = 0; k < Q; ++k) ga[k] = gb[k] = 1.0f;
+      }
+    }
+    const int n = r.t * kTile + row;  // sequence position
+    const bool valid = row < r.rows;
+    const bool rope = rope_cos != nullptr;
+    // the row's angles (L2) while the rows arrive
+    float c[Q], sn[Q];
+    if (rope && valid) {
+      RowLoad<float>::template load<Q>(rope_cos + (size_t)n * (D / 2) + ca, c);
+      RowLoad<float>::template load<Q>(rope_sin + (size_t)n * (D / 2) + ca, sn);
+    }
+    wait(&full[stage], (uint32_t)(it / C::kStages) & 1, wd, 401);
+    float a[Q], b[Q];
+    if (valid) {
+      const T* xr = reinterpret_cast<const T*>(ring + stage * C::kTileBytes) + row * D;
+      RowLoad<T>::template load_shared<Q>(xr + ca, a);
+      RowLoad<T>::template load_shared<Q>(xr + cb, b);
+    } else {
 #pragma unroll
-  for (int k = 0; k < Q / 4; ++k) {
-    wa[k] = flushed ? 0u
-                    : pack4<0>(__fmul_rn(a[4 * k], r), __fmul_rn(a[4 * k + 1], r), __fmul_rn(a[4 * k + 2], r),
-                               __fmul_rn(a[4 * k + 3], r));
-    wb[k] = flushed ? 0u
-                    : pack4<0>(__fmul_rn(b[4 * k], r), __fmul_rn(b[4 * k + 1], r), __fmul_rn(b[4 * k + 2], r),
-                               __fmul_rn(b[4 * k + 3], r));
+      for (int k = 0; k < Q; ++k) a[k] = b[k] = 0.0f;
+    }
+    // RMSNorm: the row's sum of squares over its kRowThreads threads (pairs of
+    // adjacent channels in packed FP32x2 arithmetic throughout)
+    float2 ss2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int k = 0; k < Q; k += 2) {
+      ss2 = __ffma2_rn(make_float2(a[k], a[k + 1]), make_float2(a[k], a[k + 1]), ss2);
+      ss2 = __ffma2_rn(make_float2(b[k], b[k + 1]), make_float2(b[k], b[k + 1]), ss2);
+    }
+    float ss = ss2.x + ss2.y;
+#pragma unroll
+    for (int o = 1; o < kRowThreads; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    // eps > 0 (checked by the API), so an all-zero row normalises to zeros
+    const float inv = valid ? __frsqrt_rn(__fadd_rn(ss * (1.0f / D), eps)) : 0.0f;
+    const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+    for (int k = 0; k < Q; k += 2) {
+      const float2 ya = __fmul2_rn(__fmul2_rn(make_float2(a[k], a[k + 1]), inv2), make_float2(ga[k], ga[k + 1]));
+      const float2 yb = __fmul2_rn(__fmul2_rn(make_float2(b[k], b[k + 1]), inv2), make_float2(gb[k], gb[k + 1]));
+      a[k] = ya.x, a[k + 1] = ya.y, b[k] = yb.x, b[k + 1] = yb.y;
+    }
+    // rotary embedding: channel ca + k pairs with cb + k, angle index ca + k
+    if (rope && valid) {
+#pragma unroll
+      for (int k = 0; k < Q; k += 2) {
+        const float2 x0 = make_float2(a[k], a[k + 1]), x1 = make_float2(b[k], b[k + 1]);
+        const float2 c2 = make_float2(c[k], c[k + 1]), s2 = make_float2(sn[k], sn[k + 1]);
+        const float2 t1 = __fmul2_rn(x1, s2), t0 = __fmul2_rn(x0, s2);
+        const float2 ra = __ffma2_rn(x0, c2, make_float2(-t1.x, -t1.y));
+        const float2 rb = __ffma2_rn(x1, c2, t0);
+        a[k] = ra.x, a[k + 1] = ra.y, b[k] = rb.x, b[k + 1] = rb.y;
+      }
+    }
+    // tile amax, scale and E4M3 codes (the rule of dm_quantize)
+    float amax = 0.0f;
+#pragma unroll
+    for (int k = 0; k < Q; ++k) amax = max3(amax, fabsf(a[k]), fabsf(b[k]));
+    amax = warp_max(amax);
+    if ((threadIdx.x & 31) == 0) s_red[it & 1][threadIdx.x >> 5] = amax;
+    __syncthreads();
+    // every thread has its rows in registers: the stage takes a later tile
+    if (threadIdx.x == 0 && g + C::kStages * (int)gridDim.x < total) issue(g + C::kStages * (int)gridDim.x, stage);
+    {  // every warp reduces the warp maxima itself (one per lane)
+      const int lane = threadIdx.x & 31;
+      amax = warp_max(lane < C::kThreads / 32 ? s_red[it & 1][lane] : 0.0f);
+    }
+    float rr;
+    const float sc = tile_scale<0>(amax, rr);
+    if (threadIdx.x == 0) batch.job[r.j].scales[r.tile] = sc;
+    if (valid) {
+      const bool flushed = sc == 0.0f;  // all codes +0
+      const float2 r2 = make_float2(rr, rr);
+      uint32_t wa[Q / 4], wb[Q / 4];
+#pragma unroll
+      for (int k = 0; k < Q / 4; ++k) {
+        const float2 a01 = __fmul2_rn(make_float2(a[4 * k], a[4 * k + 1]), r2);
+        const float2 a23 = __fmul2_rn(make_float2(a[4 * k + 2], a[4 * k + 3]), r2);
+        const float2 b01 = __fmul2_rn(make_float2(b[4 * k], b[4 * k + 1]), r2);
+        const float2 b23 = __fmul2_rn(make_float2(b[4 * k + 2], b[4 * k + 3]), r2);
+        wa[k] = flushed ? 0u : pack4<0>(a01.x, a01.y, a23.x, a23.y);
+        wb[k] = flushed ? 0u : pack4<0>(b01.x, b01.y, b23.x, b23.y);
+      }
+      uint8_t* dst = batch.job[r.j].codes + ((size_t)r.bh * N + n) * D;
+      *reinterpret_cast<uint4*>(dst + ca) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+      *reinterpret_cast<uint4*>(dst + cb) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+    }
   }
-  uint8_t* dst = job.codes + off;
-  *reinterpret_cast<uint2*>(dst + ca) = make_uint2(wa[0], wa[1]);
-  *reinterpret_cast<uint2*>(dst + cb) = make_uint2(wb[0], wb[1]);
+  // after a timeout the loop ran on without the data: wait (bounded by time
+  // alone) for copies still landing in this CTA's shared memory
+  if (threadIdx.x == 0 && s_abort) {
+    const int issued = (total - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+    for (int k = max(0, issued - C::kStages); k < issued; ++k)
+      wait_drain(&full[k % C::kStages], (uint32_t)(k / C::kStages) & 1, wd, 402);
+  }
 }
 
 // cos and sin of n * base^(-2i/d) in FP64, rounded to FP32; one thread per entry.
@@ -169,14 +276,23 @@ __global__ void rope_table_kernel(int N, int d, double base, float* __restrict__
   sin_t[e] = (float)s;
 }
 
+template <typename T, int D>
+cudaError_t prologue_d(const PrologueBatch& b, float eps, cudaStream_t st) {
+  using C = PrologueCfg<T, D>;
+  auto k = prologue_kernel<T, D>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const unsigned grid = (unsigned)min(b.first_tile[b.count], sms);
+  k<<<grid, C::kThreads, C::kSmem, st>>>(b, eps);
+  return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t prologue_t(const PrologueBatch& b, int d, float eps, cudaStream_t st) {
-  const unsigned grid = (unsigned)b.first_tile[b.count];
-  if (d == 128)
-    prologue_kernel<T, 128><<<grid, tile_threads<128>(), 0, st>>>(b, eps);
-  else
-    prologue_kernel<T, 64><<<grid, tile_threads<64>(), 0, st>>>(b, eps);
-  return cudaGetLastError();
+  return d == 128 ? prologue_d<T, 128>(b, eps, st) : prologue_d<T, 64>(b, eps, st);
 }
 
 }  // namespace

@@ -151,7 +151,7 @@ dm_status dm_rope_table(int N, int d, double base, float* cos_table, float* sin_
  *     ([N][d/2] float, e.g. from dm_rope_table; both or neither)
  * then y is quantised to E4M3 with the rule of dm_quantize (one FP32 scale per
  * 128-row x d tile): codes [B][H][N][d], scales [B][H][ceil(N/128)], ready
- * for dm_attn_fwd.  All arithmetic is FP32 (IEEE divide and square root), so
+ * for dm_attn_fwd.  All arithmetic is FP32 (correctly rounded 1/sqrt), so
  * codes can differ from an exact evaluation only where y * (448 / amax) lies
  * within FP32 rounding of a code boundary.  All jobs share x_dtype, d (64 or
  * 128) and eps (finite, > 0); x, codes, scales, gain and the tables are
