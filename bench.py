@@ -42,7 +42,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic of one backward launch on the default workload, from the ncu
 # capture summarised in profiles/ (valid only for the kernel source it was
 # taken on; reported as null once dm_bwd.cu or dm_device.cuh changes).
-BWD_TRAFFIC = {"sha1": "813d88a94fca956d469708df1d9ecba95e243e56", "bytes": 271275264}
+BWD_TRAFFIC = {"sha1": "c1fe4ef6b42638a21a60c3a2691890574a428ab2", "bytes": 277838848}
 
 
 def bwd_source_hash():
@@ -187,27 +187,48 @@ def run_native(args, rank, world, local_rank):
     if dm.dm_get_status(st) != 0:
         raise RuntimeError("device status error during warm-up")
 
-    # ---- the step captured once as a CUDA graph (the same launches, replayed
-    # without host work between them), so that host-side launch latency
-    # cannot leave the GPU idle inside the timed region
-    graph = None
+    # ---- the step captured once as four CUDA graphs (quantise, forward, delta,
+    # zero fill + backward), replayed back to back with events between them:
+    # the same launches, without host work between them, so that host-side
+    # launch latency cannot leave the GPU idle inside the timed region
+    graphs = None
     if not args.no_graph:
         try:
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=st):
+            graphs = [torch.cuda.CUDAGraph() for _ in range(4)]
+            pool = None
+            cap = {}
+            stages = [
+                lambda: cap.update(zip(("qq", "kk", "vv", "dd"), dm.dm_quantize_batch(
+                    [(qd, dm.DM_E4M3), (kd, dm.DM_E4M3), (vd, dm.DM_E4M3), (dod, dm.DM_E5M2)], stream=st))),
+                lambda: cap.update(zip(("O", "lse"), dm.dm_attn_fwd(p, cap["qq"], cap["kk"], cap["vv"], stream=st))),
+                lambda: cap.update(delta=dm.dm_attn_delta(p, dm.DM_DELTA_MATCHED, cap["qq"], cap["kk"], cap["vv"],
+                                                          cap["dd"], cap["lse"], stream=st)),
+                lambda: cap.update(g=dm.dm_attn_bwd(p, dm.DM_DELTA_MATCHED, cap["qq"], cap["kk"], cap["vv"],
+                                                    cap["dd"], cap["lse"], cap["delta"], stream=st)),
+            ]
+            for gph, fn in zip(graphs, stages):
+                with torch.cuda.graph(gph, stream=st, pool=pool):
+                    fn()
+                pool = gph.pool()
+            # the whole step as one graph: the timed region
+            step_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(step_graph, stream=st):
                 step(inputs, st)
             with torch.cuda.stream(st):
                 for _ in range(3):     # warm replays
                     flush.zero_()
-                    graph.replay()
+                    step_graph.replay()
+                    flush.zero_()
+                    for gph in graphs:
+                        gph.replay()
             torch.cuda.synchronize(dev)
         except RuntimeError as exc:  # capture unsupported: time the eager launches
             print(f"graph capture failed ({exc}); timing eager launches", file=sys.stderr)
-            graph = None
+            graphs = None
             torch.cuda.synchronize(dev)
 
     # ---- device-resident timed region
-    marks, gmarks = [], []
+    marks, smarks = [], []
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -216,12 +237,12 @@ def run_native(args, rank, world, local_rank):
         with torch.cuda.stream(st):
             for _ in range(args.steps):
                 flush.zero_()          # L2 flush between timed steps (outside the events)
-                if graph is not None:
+                if graphs is not None:
                     a, b = ev(), ev()
                     a.record(st)
-                    graph.replay()
+                    step_graph.replay()
                     b.record(st)
-                    gmarks.append((a, b))
+                    smarks.append((a, b))
                 else:
                     step(inputs, st, marks)
         torch.cuda.synchronize(dev)
@@ -231,16 +252,21 @@ def run_native(args, rank, world, local_rank):
     status = dm.dm_get_status(st)
     if status != 0:
         raise RuntimeError(f"device status {dm.dm_status_string(status)}")
-    if graph is not None:
-        # per-kernel split from separately timed eager steps (events between the launches)
+    if graphs is not None:
+        step_ms = [a.elapsed_time(b) for a, b in smarks]
+        # per-kernel split: the four stage graphs with events between them
         with torch.cuda.stream(st):
-            for _ in range(max(3, min(args.steps, 50))):
+            for _ in range(max(3, min(args.steps, 100))):
                 flush.zero_()
-                step(inputs, st, marks)
+                m = [ev() for _ in range(5)]
+                m[0].record(st)
+                for i, gph in enumerate(graphs):
+                    gph.replay()
+                    m[i + 1].record(st)
+                marks.append(m)
         torch.cuda.synchronize(dev)
-        step_ms = [a.elapsed_time(b) for a, b in gmarks]
     per = [[m[i].elapsed_time(m[i + 1]) for i in range(4)] for m in marks]
-    if graph is None:
+    if graphs is None:
         step_ms = [sum(x) for x in per]
     total_ms = sum(step_ms)
     if dist:
@@ -289,7 +315,7 @@ def run_native(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     prologue = lambda: dm.dm_qk_prologue_batch([(xqd, gd), (xkd, gd)], rope=table, stream=st)
     pro_graph = None
-    if graph is not None:
+    if graphs is not None:
         pro_graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(pro_graph, stream=st):
             prologue()
@@ -346,7 +372,8 @@ def run_native(args, rank, world, local_rank):
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d, "causal": w.causal,
                    "delta_mode": "matched", "flop_accounting": "issued, causal-halved, 9U per step",
                    "l2": "flushed between timed steps (256 MiB write)", "parallelism": f"independent x{world}",
-                   "launch": "CUDA graph of the step, replayed" if graph is not None else "eager launches"},
+                   "launch": "CUDA graph of the step, replayed (per-kernel split: one graph per stage)"
+                   if graphs is not None else "eager launches"},
         "pct_of_fp8_peak": round(100.0 * value / (world * fp8_peak), 2),
         "per_kernel_ms": {k2: round(v2, 4) for k2, v2 in kernel_ms.items()},
         "per_kernel_tflops": {
