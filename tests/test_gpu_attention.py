@@ -65,6 +65,26 @@ def test_shapes(shape, causal):
     _compare(g, r)
 
 
+@pytest.mark.parametrize("shape,causal", [
+    ((1, 2, 1, 127, 128), True),      # one row short of a tile
+    ((1, 2, 1, 129, 128), True),      # one row past a tile
+    ((1, 2, 2, 255, 64), False),      # multi-head (G = 1), one short of two tiles
+    ((1, 2, 2, 257, 64), True),
+    ((3, 8, 1, 96, 64), True),        # G = 8, several batches, a single partial tile
+    ((1, 4, 2, 513, 128), True),      # five key tiles, the last one row long
+])
+def test_tile_boundaries_and_group_sizes(shape, causal):
+    """Sequence lengths at tile edges (every kernel's ragged path), group sizes
+    1 and 8 and several batches: codes bit-exact, results within the bar."""
+    B, Hq, Hkv, N, d = shape
+    w = custom(B, Hq, Hkv, N, d, causal=causal, seed=7 * N + d)
+    q, k, v, do = make_inputs(w)
+    g = gpu_pipeline(q, k, v, do, causal=causal)
+    r = oracle_pipeline(q, k, v, do, causal=causal)
+    _codes_match(g, r)
+    _compare(g, r)
+
+
 def test_bf16_output_and_explicit_scale():
     w = custom(1, 4, 2, 256, 128, seed=3)
     q, k, v, do = make_inputs(w)
