@@ -80,6 +80,12 @@ __device__ __forceinline__ float lane_column_sum(float (&v)[32], int lane) {
   return v[0];
 }
 
+// Largest of the eight warp maxima (16-byte aligned): two vector loads.
+__device__ __forceinline__ float max8(const float (&v)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(v)[0], b = reinterpret_cast<const float4*>(v)[1];
+  return fmaxf(max3(a.x, a.y, a.z), max3(a.w, b.x, max3(b.y, b.z, b.w)));
+}
+
 // Unit bookkeeping for one TMEM accumulator; every compute thread holds an
 // identical copy.  Sets f to the factor the accumulator must be multiplied by
 // (1 when it stays) and returns the MMA mode: 0 skip, 1 overwrite,
@@ -421,9 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       pmax = warp_max(pmax);
       if (lane == 0) s_red[bn][0][warp - 4] = pmax;
       named_bar_sync(1, 256);
-      float amax = s_red[bn][0][0];
-#pragma unroll
-      for (int w = 1; w < 8; ++w) amax = fmaxf(amax, s_red[bn][0][w]);
+      float amax = max8(s_red[bn][0]);
       float rp;
       const float sp = tile_scale_fast<0>(amax, rp);
       // P^T codes and the next iteration's LSE / delta (read after this
@@ -482,17 +486,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           ds[cc + 1] = d01.y;
           ds[cc + 2] = d23.x;
           ds[cc + 3] = d23.y;
-          dm0 = max3(dm0, fabsf(d01.x), fabsf(d01.y));
-          dm1 = max3(dm1, fabsf(d23.x), fabsf(d23.y));
+          // plain fmaxf: |x| folds into the max (the three-input asm max cannot take it)
+          dm0 = fmaxf(dm0, fmaxf(fabsf(d01.x), fabsf(d01.y)));
+          dm1 = fmaxf(dm1, fmaxf(fabsf(d23.x), fabsf(d23.y)));
         }
       }
       float dmax = fmaxf(dm0, dm1);
       dmax = warp_max(dmax);
       if (lane == 0) s_red[bn][1][warp - 4] = dmax;
       named_bar_sync(1, 256);
-      amax = s_red[bn][1][0];
-#pragma unroll
-      for (int w = 1; w < 8; ++w) amax = fmaxf(amax, s_red[bn][1][w]);
+      amax = max8(s_red[bn][1]);
       float rs;
       const float sds = tile_scale_fast<1>(amax, rs);
       // both accumulators into the units of this iteration's products (dV/dK

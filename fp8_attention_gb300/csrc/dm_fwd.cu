@@ -283,7 +283,8 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
       if (lane == 0) s_red[t & 1][warp] = x;
       named_bar_sync(1, 128);
       const float m_new = fmaxf(m, tmax);
-      const float xmax = fmaxf(fmaxf(s_red[t & 1][0], s_red[t & 1][1]), fmaxf(s_red[t & 1][2], s_red[t & 1][3]));
+      const float4 x4 = *reinterpret_cast<const float4*>(s_red[t & 1]);  // 16-byte aligned row
+      const float xmax = fmaxf(max3(x4.x, x4.y, x4.z), x4.w);
       const float amax = ex2(fminf(xmax, 0.0f));
       float r;
       const float sp = tile_scale_fast<0>(amax, r);

@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(tile_threads<D>(), 1) prologue_kernel(const Pr
     // tile amax, scale and E4M3 codes (the rule of dm_quantize)
     float amax = 0.0f;
 #pragma unroll
-    for (int k = 0; k < Q; ++k) amax = max3(amax, fabsf(a[k]), fabsf(b[k]));
+    for (int k = 0; k < Q; ++k) amax = fmaxf(amax, fmaxf(fabsf(a[k]), fabsf(b[k])));  // |x| folds into the max
     amax = warp_max(amax);
     if ((threadIdx.x & 31) == 0) s_red[it & 1][threadIdx.x >> 5] = amax;
     __syncthreads();
