@@ -265,15 +265,6 @@ __device__ __forceinline__ void tmem_load32(uint32_t taddr, float (&v)[32]) {
       : "r"(taddr)
       : "memory");
 }
-__device__ __forceinline__ void tmem_load16(uint32_t taddr, float (&v)[16]) {
-  uint32_t* r = reinterpret_cast<uint32_t*>(v);
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-}
 // Two 32-column loads (v[0..31] from taddr0, v[32..63] from taddr1), one wait.
 __device__ __forceinline__ void tmem_load64(uint32_t taddr0, uint32_t taddr1, float (&v)[64]) {
   uint32_t* r = reinterpret_cast<uint32_t*>(v);
@@ -284,17 +275,6 @@ __device__ __forceinline__ void tmem_load64(uint32_t taddr0, uint32_t taddr1, fl
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
       : "r"(taddr0), "r"(taddr1)
       : "memory");
-}
-// N consecutive columns (N = 16, 32 or 64) from taddr.
-template <int N>
-__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&v)[N]) {
-  static_assert(N == 16 || N == 32 || N == 64, "unsupported TMEM load width");
-  if constexpr (N == 16)
-    tmem_load16(taddr, v);
-  else if constexpr (N == 32)
-    tmem_load32(taddr, v);
-  else
-    tmem_load64(taddr, taddr + 32, v);
 }
 // Four 32-column loads (v[32k..32k+31] from taddr_k), one wait.
 __device__ __forceinline__ void tmem_load128(uint32_t t0, uint32_t t1, uint32_t t2, uint32_t t3, float (&v)[128]) {
