@@ -286,7 +286,7 @@ def run_native(args, rank, world, local_rank):
     d2h = sum(t.numel() * t.element_size() for t in outs[0].values())
     slots = [tuple(torch.empty(t.shape, dtype=t.dtype, device=dev) for t in (qh, kh, vh, doh)) for _ in range(2)]
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    e2e_steps = max(4, min(args.steps, 20))
+    e2e_steps = max(4, min(args.steps, 50))
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
