@@ -42,7 +42,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic of one backward launch on the default workload, from the ncu
 # capture summarised in profiles/ (valid only for the kernel source it was
 # taken on; reported as null once dm_bwd.cu or dm_device.cuh changes).
-BWD_TRAFFIC = {"sha1": "c1fe4ef6b42638a21a60c3a2691890574a428ab2", "bytes": 277838848}
+BWD_TRAFFIC = {"sha1": "faa32ffecdab728c23d83ed0649b38cae0928fec", "bytes": 268227072}
 
 
 def bwd_source_hash():
