@@ -130,3 +130,26 @@ def test_prologue_validation_without_gpu(lib):
     assert rt(16, 64, 1e4, None, A, None) == dm.DM_ERR_INVALID_ARG
     assert rt(16, 64, 1e4, A + 4, A, None) == dm.DM_ERR_ALIGNMENT
     assert rt(0, 64, 1e4, None, None, None) == 0
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """include/dm.h compiles as strict C99 (no C++ or torch types) and a C
+    program links against libdm.so and calls host-only entry points."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    src = tmp_path / "abi.c"
+    src.write_text(
+        '#include "dm.h"\n#include <stdio.h>\n'
+        "int main(void) {\n"
+        "  dm_quantize_job qj = {0};\n  dm_prologue_job pj = {0};\n  (void)qj; (void)pj;\n"
+        '  printf("%d %s\\n", dm_version(), dm_status_string(DM_ERR_SHAPE));\n'
+        "  return dm_quantize_batch(NULL, 0, DM_BF16, NULL) == DM_OK ? 0 : 1;\n}\n")
+    libdir = os.path.dirname(dm.LIB_PATH)
+    exe = tmp_path / "abi"
+    cmd = ["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+           str(src), "-L", libdir, "-ldm", f"-Wl,-rpath,{libdir}", "-o", str(exe)]
+    subprocess.run(cmd, check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    assert out.split() == ["100", "DM_ERR_SHAPE"]
