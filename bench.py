@@ -54,6 +54,17 @@ def bwd_source_hash():
     return h.hexdigest()
 
 
+def max_over_ranks(value, dist, device):
+    """The largest of every rank's value (a job's time is its slowest rank's);
+    value itself when not distributed."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -268,11 +279,7 @@ def run_native(args, rank, world, local_rank):
     per = [[m[i].elapsed_time(m[i + 1]) for i in range(4)] for m in marks]
     if graphs is None:
         step_ms = [sum(x) for x in per]
-    total_ms = sum(step_ms)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dist, dev)
 
     # ---- end to end through the public API from pinned host buffers: every
     # step copies its inputs in, computes, and copies dQ, dK, dV out.  The
@@ -316,11 +323,7 @@ def run_native(args, rank, world, local_rank):
     s_out.wait_event(done[-1])
     t_end.record(s_out)
     torch.cuda.synchronize(dev)
-    e2e_ms = t_start.elapsed_time(t_end) / e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(t_start.elapsed_time(t_end) / e2e_steps, dist, dev)
 
     # ---- attention-input prologue of Q and K (RMSNorm with the workload's
     # gains, rotary embedding, E4M3 tile quantisation; one launch), timed on
