@@ -103,3 +103,19 @@ def test_long_64k_sampled_and_invariants():
         :, :, :w.N, None]
     want = dohat.reshape(w.B, w.Hkv, G, w.N, w.d).sum(dim=(2, 3))
     assert float((dV.sum(dim=2) - want).norm() / want.norm()) < 0.05
+
+
+@pytest.mark.parametrize("mode,omode", [(dm.DM_DELTA_MATCHED, oracle.DELTA_MATCHED),
+                                        (dm.DM_DELTA_STALE_DOHAT, oracle.DELTA_STALE_DOHAT)])
+def test_non_causal_1k_groups(mode, omode):
+    """Non-causal attention at a size where every CTA loops over eight key or
+    query tiles, two whole kv groups checked, in the matched and one stale mode."""
+    from fp8_attention_gb300.inputs import custom
+    w = custom(2, 8, 2, 1024, 128, causal=False, seed=11)
+    q, k, v, do = make_inputs(w)
+    g = gpu_pipeline(q, k, v, do, causal=False, mode=mode)
+    r = oracle_pipeline(q, k, v, do, causal=False, mode=omode, groups=[(0, 0), (1, 1)],
+                        q_tiles=list(range(8)), kv_tiles=list(range(8)))
+    _codes_match(g, r)
+    errs = _compare_sampled(g, r, w)
+    print("non-causal 1k errors", errs)
