@@ -252,12 +252,15 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
       wait(&bars.sfull, t & 1, wd, 110);
       tc_fence_after();
 
-      // row max (raw units; c1 > 0 preserves the order), S read in halves
-      // (S is read again for the codes: half a row of registers each time)
+      // row max (raw units; c1 > 0 preserves the order), S read in halves;
+      // the second half stays in registers for its codes, the first is read
+      // again (half a row of registers live at a time)
       float mx = -INFINITY;
+      float v1[64];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        float v[64];
+        float v0[64];
+        float(&v)[64] = hh == 0 ? v0 : v1;
         tmem_load64(tl + kColS + 64 * hh, tl + kColS + 64 * hh + 32, v);
         if (full) {
           float m4[4] = {v[0], v[1], v[2], v[3]};
@@ -301,10 +304,12 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
       const uint32_t sP = L::kP + (t & 1) * kTile * kTile + SwTile<128>::row_base(row);  // chunk c at sP ^ 16 c
       auto p_codes = [&](auto full_tile) {
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float v[64];
-          tmem_load64(tl + kColS + 64 * hh, tl + kColS + 64 * hh + 32, v);
-          if (hh == 1) {
+        for (int i = 0; i < 2; ++i) {
+          const int hh = 1 - i;  // the kept second half first
+          float v0[64];
+          float(&v)[64] = hh == 1 ? v1 : v0;
+          if (hh == 0) {
+            tmem_load64(tl + kColS, tl + kColS + 32, v);
             // S has been read: the tensor core may write S(t+1)
             tc_fence_before();
             __syncwarp();
