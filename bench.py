@@ -39,10 +39,14 @@ L2_BYTES = 129 * 1024 * 1024
 FP8_PER_BF16 = 2.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
-# DRAM traffic of one backward launch on the default workload, from the ncu
-# capture summarised in profiles/ (valid only for the kernel source it was
-# taken on; reported as null once dm_bwd.cu or dm_device.cuh changes).
-BWD_TRAFFIC = {"sha1": "faa32ffecdab728c23d83ed0649b38cae0928fec", "bytes": 268227072}
+# DRAM traffic of one backward launch per workload, from the ncu captures
+# summarised in profiles/ (valid only for the kernel source it was taken on;
+# reported as null once dm_bwd.cu or dm_device.cuh changes).
+BWD_TRAFFIC = {
+    "gqa_b1_n8192_d128": {"sha1": "faa32ffecdab728c23d83ed0649b38cae0928fec", "bytes": 268227072},
+}
+# head dimensions the Q/K prologue is built for
+PROLOGUE_DIMS = (64, 128)
 
 
 def bwd_source_hash():
@@ -328,44 +332,8 @@ def run_native(args, rank, world, local_rank):
     # ---- attention-input prologue of Q and K (RMSNorm with the workload's
     # gains, rotary embedding, E4M3 tile quantisation; one launch), timed on
     # its own from the pre-normalisation draws: it is not part of the step
-    from fp8_attention_gb300.inputs import make_prologue_inputs
-    xq, xk, gain = make_prologue_inputs(w)
-    xqd, xkd, gd = xq.to(dev), xk.to(dev), gain.to(dev)
-    pro_marks, pro_clean = [], []
-    with torch.cuda.stream(st):
-        table = dm.dm_rope_table(w.N, w.d, device=dev, stream=st)
-    torch.cuda.synchronize(dev)
-    prologue = lambda: dm.dm_qk_prologue_batch([(xqd, gd), (xkd, gd)], rope=table, stream=st)
-    pro_graph = None
-    if graphs is not None:
-        pro_graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(pro_graph, stream=st):
-            prologue()
-        torch.cuda.synchronize(dev)
-    with torch.cuda.stream(st):
-        for i in range(3 + 2 * max(3, min(args.steps, 20))):
-            # alternately after the write flush (whose dirty lines the launch
-            # then writes back) and after a read sweep (which leaves L2 clean)
-            clean = i >= 3 and i % 2 == 1
-            if clean:
-                flush.sum()
-            else:
-                flush.zero_()
-            a, b = ev(), ev()
-            a.record(st)
-            if pro_graph is not None:
-                pro_graph.replay()
-            else:
-                prologue()
-            b.record(st)
-            if i >= 3:
-                (pro_clean if clean else pro_marks).append((a, b))
-    torch.cuda.synchronize(dev)
-    if dm.dm_get_status(st) != 0:
-        raise RuntimeError("device status error in the prologue")
-    pro_ms = statistics.mean(a.elapsed_time(b) for a, b in pro_marks)
-    pro_clean_ms = statistics.mean(a.elapsed_time(b) for a, b in pro_clean)
-    del xqd, xkd, table
+    prologue_line = timed_prologue(args, w, dm, dev, st, flush, graphs is not None) \
+        if w.d in PROLOGUE_DIMS else {"skipped": f"the prologue is built for d in {PROLOGUE_DIMS}"}
 
     fl = flops_of(w)
     step_flops = fl["fwd"] + fl["delta"] + fl["bwd"]
@@ -377,7 +345,8 @@ def run_native(args, rank, world, local_rank):
                  for i, name in enumerate(("quantize", "fwd", "delta", "bwd"))}
     bwd_tflops = fl["bwd"] / (kernel_ms["bwd"] * 1e-3) / 1e12
     src_hash = bwd_source_hash()
-    traffic = BWD_TRAFFIC["bytes"] if BWD_TRAFFIC["sha1"] == src_hash else None
+    known = BWD_TRAFFIC.get(w.name)
+    traffic = known["bytes"] if known and known["sha1"] == src_hash else None
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -408,7 +377,7 @@ def run_native(args, rank, world, local_rank):
                            / 1e12, 1),
         # quantisation of Q, K, V, dO: 2 B read + 1 B code written per element, plus the tile scales
         "quantize_gbs": round(quant_bytes(w) / (kernel_ms["quantize"] * 1e-3) / 1e9, 1),
-        "roofline": {"kernel": "attn_bwd_kernel<128>", "bound": "tensor", "achieved": round(bwd_tflops, 1),
+        "roofline": {"kernel": f"attn_bwd_kernel<{w.d}>", "bound": "tensor", "achieved": round(bwd_tflops, 1),
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(bwd_tflops / fp8_peak, 4),
                      "peak_source": f"{src} bf16 burst x {FP8_PER_BF16} (fp8/bf16 nominal ratio)",
                      "traffic": traffic},
@@ -419,13 +388,7 @@ def run_native(args, rank, world, local_rank):
                        "D2H on three streams, two input slots, copies overlapped with neighbouring steps"},
         # Q and K prologue: x read + 1 B code per element, tile scales, the
         # rotary table (read once; every head shares it) and the gains
-        "prologue": {"ms": round(pro_ms, 4), "gbs": round(prologue_bytes(w) / (pro_ms * 1e-3) / 1e9, 1),
-                     "bytes": prologue_bytes(w),
-                     "hbm_frac": round(prologue_bytes(w) / (pro_ms * 1e-3) / 1e9 / float(mp.get("hbm_gbs", 6800.0)), 3),
-                     "ms_clean_l2": round(pro_clean_ms, 4),
-                     "gbs_clean_l2": round(prologue_bytes(w) / (pro_clean_ms * 1e-3) / 1e9, 1),
-                     "timed": "alone (one launch, replayed as a CUDA graph), after the step's timed region; "
-                              "ms after the 256 MiB write flush, ms_clean_l2 after a 256 MiB read sweep"},
+        "prologue": prologue_line,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed": round(wall, 3),
@@ -435,6 +398,60 @@ def run_native(args, rank, world, local_rank):
     if dist:
         dist.destroy_process_group()
     return line
+
+
+def timed_prologue(args, w, dm, dev, st, flush, use_graph):
+    """Times the Q/K prologue alone (one launch, replayed as a CUDA graph when
+    the step is), alternately after the write flush and after a read sweep."""
+    import torch
+
+    from fp8_attention_gb300.inputs import make_prologue_inputs
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    xq, xk, gain = make_prologue_inputs(w)
+    xqd, xkd, gd = xq.to(dev), xk.to(dev), gain.to(dev)
+    pro_marks, pro_clean = [], []
+    with torch.cuda.stream(st):
+        table = dm.dm_rope_table(w.N, w.d, device=dev, stream=st)
+    torch.cuda.synchronize(dev)
+    prologue = lambda: dm.dm_qk_prologue_batch([(xqd, gd), (xkd, gd)], rope=table, stream=st)
+    pro_graph = None
+    if use_graph:
+        pro_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(pro_graph, stream=st):
+            prologue()
+        torch.cuda.synchronize(dev)
+    with torch.cuda.stream(st):
+        for i in range(3 + 2 * max(3, min(args.steps, 20))):
+            # alternately after the write flush (whose dirty lines the launch
+            # then writes back) and after a read sweep (which leaves L2 clean)
+            clean = i >= 3 and i % 2 == 1
+            if clean:
+                flush.sum()
+            else:
+                flush.zero_()
+            a, b = ev(), ev()
+            a.record(st)
+            if pro_graph is not None:
+                pro_graph.replay()
+            else:
+                prologue()
+            b.record(st)
+            if i >= 3:
+                (pro_clean if clean else pro_marks).append((a, b))
+    torch.cuda.synchronize(dev)
+    if dm.dm_get_status(st) != 0:
+        raise RuntimeError("device status error in the prologue")
+    pro_ms = statistics.mean(a.elapsed_time(b) for a, b in pro_marks)
+    pro_clean_ms = statistics.mean(a.elapsed_time(b) for a, b in pro_clean)
+    del xqd, xkd, table
+    mp, _ = peaks()
+    gbs = prologue_bytes(w) / (pro_ms * 1e-3) / 1e9
+    return {"ms": round(pro_ms, 4), "gbs": round(gbs, 1), "bytes": prologue_bytes(w),
+            "hbm_frac": round(gbs / float(mp.get("hbm_gbs", 6800.0)), 3),
+            "ms_clean_l2": round(pro_clean_ms, 4),
+            "gbs_clean_l2": round(prologue_bytes(w) / (pro_clean_ms * 1e-3) / 1e9, 1),
+            "timed": "alone (one launch, replayed as a CUDA graph), after the step's timed region; "
+                     "ms after the 256 MiB write flush, ms_clean_l2 after a 256 MiB read sweep"}
 
 
 def quant_bytes(w):

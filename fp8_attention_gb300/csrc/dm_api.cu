@@ -62,15 +62,17 @@ dm_status device_state(unsigned int** status) {
   return DM_OK;
 }
 
-// FP8 codes viewed as [BH][N][d]; box = 128 rows x d, hardware swizzle of width d.
+// FP8 codes viewed as [BH][N][d]; box = 128 rows x min(d, 128) bytes with the
+// hardware swizzle of that width (d = 256 rows are loaded as two boxes).
 dm_status encode_codes_map(CUtensorMap* m, const uint8_t* codes, int BH, int N, int d) {
+  const int box_x = d < 128 ? d : 128;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d, (cuuint64_t)d * (cuuint64_t)N};
-  cuuint32_t box[3] = {(cuuint32_t)d, (cuuint32_t)kTileRows, 1};
+  cuuint32_t box[3] = {(cuuint32_t)box_x, (cuuint32_t)kTileRows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(codes), dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                        box_x == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DM_OK : DM_ERR_CUDA;
 }
@@ -90,7 +92,7 @@ dm_status encode_f32_rows_map(CUtensorMap* m, const float* x, int BH, int N, int
 dm_status check_params(const dm_attn_params* p) {
   if (!p) return DM_ERR_INVALID_ARG;
   if (p->B < 0 || p->Hq <= 0 || p->Hkv <= 0 || p->N < 0) return DM_ERR_SHAPE;
-  if (p->d != 64 && p->d != 128) return DM_ERR_SHAPE;
+  if (p->d != 64 && p->d != 128 && p->d != 256) return DM_ERR_SHAPE;
   if (p->Hq % p->Hkv != 0) return DM_ERR_SHAPE;
   if ((long long)p->B * p->Hq * p->N * p->d >= (1ll << 31)) return DM_ERR_SHAPE;
   if (!std::isfinite(p->softmax_scale)) return DM_ERR_INVALID_ARG;
@@ -253,7 +255,7 @@ dm_status dm_quantize_batch(const dm_quantize_job* jobs, int njobs, dm_dtype x_d
   if (njobs == 0) return DM_OK;
   if (!jobs) return DM_ERR_INVALID_ARG;
   const int d = jobs[0].d;
-  if (d != 64 && d != 128) return DM_ERR_SHAPE;
+  if (d != 64 && d != 128 && d != 256) return DM_ERR_SHAPE;
   dm::QuantBatch b{};
   long long tiles = 0;
   for (int i = 0; i < njobs; ++i) {
@@ -282,7 +284,7 @@ dm_status dm_quantize_batch(const dm_quantize_job* jobs, int njobs, dm_dtype x_d
 dm_status dm_quantize(const void* x, dm_dtype x_dtype, int B, int H, int N, int d, dm_fp8 fmt, uint8_t* codes,
                       float* scales, uint8_t* codes_t, void* stream) {
   const dm_quantize_job job{x, B, H, N, d, fmt, codes, scales, codes_t};
-  if (d != 64 && d != 128) return valid_dtype(x_dtype) ? DM_ERR_SHAPE : DM_ERR_DTYPE;
+  if (d != 64 && d != 128 && d != 256) return valid_dtype(x_dtype) ? DM_ERR_SHAPE : DM_ERR_DTYPE;
   return dm_quantize_batch(&job, 1, x_dtype, stream);
 }
 

@@ -21,10 +21,21 @@
 // warps rescale the accumulator by old/new unit.  Iterations whose product is
 // below 2^-100 (a flushed or negligible tile) add nothing.
 //
-// Warp roles (384 threads): warp 0 TMA, warp 1 MMA, warps 2-3 idle (each
-// warpgroup starts at a multiple of four warps), warps 4-11 two compute
-// warpgroups; thread = key row, warpgroup = half of the query columns (and
-// half of the d columns for the dV/dK/dQ epilogues).
+// Warp roles (384 threads): warp 0 TMA, warp 1 MMA, warp 2 the dQ reducer,
+// warp 3 idle (each warpgroup starts at a multiple of four warps), warps 4-11
+// two compute warpgroups; thread = key row, warpgroup = half of the query
+// columns (and half of the d columns for the dV/dK/dQ epilogues).
+//
+// d = 256 splits the head dimension over two CTAs per key tile ("halves"):
+// dV, dK and dQ of 128 key/query rows x 256 columns, plus the work buffers,
+// do not fit one SM's 512 TMEM columns.  Each half owns 128 of the d columns
+// of dV, dK and dQ (its accumulators take the same TMEM columns as d = 128)
+// and computes S and dP itself over the full d (two K steps per sub-tile, the
+// products dV, dK, dQ only over its columns).  Shared memory (227 KB) holds K
+// and V whole, this half's columns of Q and dO in two stages, the other
+// columns in one stage (needed only by S and dP, which finish early in an
+// iteration), one P^ and one dS^ code tile, and a 64-column dQ staging tile
+// drained in two passes.
 #include <cudaTypedefs.h>
 
 #include "dm_device.cuh"
@@ -39,22 +50,37 @@ constexpr float kMinUnit = 0x1p-100f;
 
 struct BwdBars {
   uint64_t kv, qfull[2], qempty[2], sfull[2], sread[2], dpfull[2], bfree[2], pds, mma2, mma_done, dq_staged,
-      dq_free;
+      dq_free, ofull, oempty;
+};
+
+template <int D>
+struct BwdCfg {
+  static constexpr bool kSplit = D > 128;            // two CTAs per key tile, one per 128 d columns
+  static constexpr int kDC = kSplit ? 128 : D;       // d columns of dV, dK, dQ this CTA accumulates
+  static constexpr int kDH = kDC / 2;                // ... per compute warpgroup
+  static constexpr int kCodeBufs = kSplit ? 1 : 2;   // P^T and dS^T code tiles
+  static constexpr int kStageCols = kSplit ? 64 : kDC;  // fp32 columns per staged dQ/dK/dV pass
+  static constexpr int kPasses = kDC / kStageCols;
 };
 
 // Everything lives in dynamic shared memory (no static shared variables), so
 // the 1024-byte aligned tile region starts at the window's base.
 template <int D>
 struct BwdLayout {
-  static constexpr int kTileBytes = kTile * D;
+  using C = BwdCfg<D>;
+  static constexpr int kTileBytes = kTile * D;    // K, V (OpTile<D>)
+  static constexpr int kOwnBytes = kTile * C::kDC;  // this CTA's columns of a Q or dO tile
+  static constexpr int kOtherBytes = C::kSplit ? kTile * 128 : 0;
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTileBytes;
-  static constexpr int kQ = kV + kTileBytes;            // 2 stages
-  static constexpr int kDO = kQ + 2 * kTileBytes;       // 2 stages
-  static constexpr int kPt = kDO + 2 * kTileBytes;      // 2 x P^T codes, [key row][128 query bytes]
-  static constexpr int kDSt = kPt + 2 * kTile * kTile;  // 2 x dS^T codes
-  static constexpr int kDQ = kDSt + 2 * kTile * kTile;  // dQ staging: D/32 boxes of [128 rows][32 fp32]
-  static constexpr int kLse = kDQ + kTile * D * 4;      // float [2][128]
+  static constexpr int kQ = kV + kTileBytes;             // 2 stages
+  static constexpr int kDO = kQ + 2 * kOwnBytes;         // 2 stages
+  static constexpr int kQo = kDO + 2 * kOwnBytes;        // split: the other half's Q columns, one stage
+  static constexpr int kDOo = kQo + kOtherBytes;         // split: ... and dO columns
+  static constexpr int kPt = kDOo + kOtherBytes;         // P^T codes, [key row][128 query bytes]
+  static constexpr int kDSt = kPt + C::kCodeBufs * kTile * kTile;  // dS^T codes
+  static constexpr int kDQ = kDSt + C::kCodeBufs * kTile * kTile;  // staging: boxes of [128 rows][32 fp32]
+  static constexpr int kLse = kDQ + kTile * C::kStageCols * 4;      // float [2][128]
   static constexpr int kDl = kLse + 2 * kTile * 4;      // float [2][128]
   static constexpr int kRed = kDl + 2 * kTile * 4;      // float [2][2][8]
   static constexpr int kMode = kRed + 2 * 2 * 8 * 4;    // int [2][2]
@@ -135,7 +161,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tmDV, const AttnArgs a, const float* __restrict__ lse,
                     const float* __restrict__ delta, const dm_diag diag) {
   using L = BwdLayout<D>;
-  constexpr int DH = D / 2;  // d columns per compute warpgroup
+  using C = BwdCfg<D>;
+  constexpr int DH = C::kDH;  // d columns per compute warpgroup
+  constexpr int SH = C::kStageCols / 2;  // ... per staging pass
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   BwdBars& bars = *reinterpret_cast<BwdBars*>(sm + L::kBars);
@@ -148,12 +176,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int BH = a.B * a.Hq;
-  const int kt = (int)(blockIdx.x / BH);  // key tile 0 sees the most query tiles: first
-  const int bh0 = (int)(blockIdx.x % BH);
+  // split: the two halves of a key tile are neighbouring CTAs
+  const int hf = C::kSplit ? (int)(blockIdx.x & 1u) : 0;
+  const unsigned blk = C::kSplit ? blockIdx.x >> 1 : blockIdx.x;
+  const int kt = (int)(blk / BH);  // key tile 0 sees the most query tiles: first
+  const int bh0 = (int)(blk % BH);
+  const int col0 = hf * C::kDC;  // this CTA's first d column
   const int bg = (bh0 / a.Hq) * a.Hkv + (bh0 % a.Hq) / (a.Hq / a.Hkv);
   const int qt0 = a.causal ? kt : 0;
   const int n_iter = a.T - qt0;
-  const bool want_diag = diag.rowsum_pre || diag.abssum_pre || diag.rowsum_post || diag.abssum_post;
+  // the halves of a split key tile compute the same dS: one adds the diagnostics
+  const bool want_diag =
+      hf == 0 && (diag.rowsum_pre || diag.abssum_pre || diag.rowsum_post || diag.abssum_post);
 
   // The swizzled tiles need a 1024-byte aligned base; the window is expected
   // to start aligned (no static shared variables).  Checked uniformly before
@@ -179,6 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars.mma_done, 1);
     mbar_init(&bars.dq_staged, 8);
     mbar_init(&bars.dq_free, 1);
+    mbar_init(&bars.ofull, 1);
+    mbar_init(&bars.oempty, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -201,71 +237,108 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmDK);
       tma_prefetch_desc(&tmDV);
       mbar_arrive_expect_tx(&bars.kv, 2 * L::kTileBytes);
-      tma_load_3d(sm + L::kK, &tmK, &bars.kv, 0, kt * kTile, bg);
-      tma_load_3d(sm + L::kV, &tmV, &bars.kv, 0, kt * kTile, bg);
-      int issued = 0;
+      tma_load_tile<D>(sm + L::kK, &tmK, &bars.kv, kt * kTile, bg);
+      tma_load_tile<D>(sm + L::kV, &tmV, &bars.kv, kt * kTile, bg);
+      int issued = 0, o_issued = 0;
       const int bh = bh0;
       int qt = qt0;  // query tile of iteration n
       for (int n = 0; n < n_iter; ++n) {
         const int s = n & 1;
         const uint32_t ph = (n >> 1) & 1;
         if (n > 0) ++qt;
+        // this CTA's columns: stage s, free once dV/dK(n-2) have read it
         if (!wait(&bars.qempty[s], ph ^ 1, wd, 301)) break;
-        mbar_arrive_expect_tx(&bars.qfull[s], 2 * L::kTileBytes);
-        tma_load_3d(sm + L::kQ + s * L::kTileBytes, &tmQ, &bars.qfull[s], 0, qt * kTile, bh);
-        tma_load_3d(sm + L::kDO + s * L::kTileBytes, &tmDO, &bars.qfull[s], 0, qt * kTile, bh);
+        mbar_arrive_expect_tx(&bars.qfull[s], 2 * L::kOwnBytes);
+        if constexpr (C::kSplit) {
+          tma_load_3d(sm + L::kQ + s * L::kOwnBytes, &tmQ, &bars.qfull[s], col0, qt * kTile, bh);
+          tma_load_3d(sm + L::kDO + s * L::kOwnBytes, &tmDO, &bars.qfull[s], col0, qt * kTile, bh);
+        } else {
+          tma_load_tile<D>(sm + L::kQ + s * L::kOwnBytes, &tmQ, &bars.qfull[s], qt * kTile, bh);
+          tma_load_tile<D>(sm + L::kDO + s * L::kOwnBytes, &tmDO, &bars.qfull[s], qt * kTile, bh);
+        }
         issued = n + 1;
+        if constexpr (C::kSplit) {
+          // the other half's columns: one stage, free once S(n-1) and dP(n-1) are done
+          if (n >= 1 && !wait(&bars.oempty, (n - 1) & 1, wd, 317)) break;
+          mbar_arrive_expect_tx(&bars.ofull, 2 * L::kOtherBytes);
+          tma_load_3d(sm + L::kQo, &tmQ, &bars.ofull, 128 - col0, qt * kTile, bh);
+          tma_load_3d(sm + L::kDOo, &tmDO, &bars.ofull, 128 - col0, qt * kTile, bh);
+          o_issued = n + 1;
+        }
       }
       wait_drain(&bars.kv, 0, wd, 302);
       for (int n = max(0, issued - 2); n < issued; ++n) wait_drain(&bars.qfull[n & 1], (n >> 1) & 1, wd, 303);
+      if (o_issued > 0) wait_drain(&bars.ofull, (o_issued - 1) & 1, wd, 318);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f8(0, 0, 0, 0, kTile, kTile);   // K Q^T
       constexpr uint32_t kIdDP = idesc_f8(0, 1, 0, 0, kTile, kTile);  // V (E4M3) dO^T (E5M2)
-      constexpr uint32_t kIdDV = idesc_f8(0, 1, 0, 1, kTile, D);      // P^T (K-major) dO (MN-major)
-      constexpr uint32_t kIdDK = idesc_f8(1, 0, 0, 1, kTile, D);      // dS^T (K-major) Q (MN-major)
-      constexpr uint32_t kIdDQ = idesc_f8(1, 0, 1, 1, kTile, D);      // dS (MN-major) K (MN-major)
+      constexpr int DC = C::kDC;
+      constexpr uint32_t kIdDV = idesc_f8(0, 1, 0, 1, kTile, DC);     // P^T (K-major) dO (MN-major)
+      constexpr uint32_t kIdDK = idesc_f8(1, 0, 0, 1, kTile, DC);     // dS^T (K-major) Q (MN-major)
+      constexpr uint32_t kIdDQ = idesc_f8(1, 0, 1, 1, kTile, DC);     // dS (MN-major) K (MN-major)
       const uint32_t sK = smem_u32(sm + L::kK), sV = smem_u32(sm + L::kV);
+      // this CTA's columns of K (split: its sub-tile) for dQ
+      const uint32_t sKown = sK + (C::kSplit ? (uint32_t)hf * OpTile<D>::kSubBytes : 0u);
       // dV, dK and dQ of iteration m (its work buffer now takes dQ)
       auto tail = [&](int m) {
-        const int bm = m & 1;
-        const uint32_t sQ = smem_u32(sm + L::kQ + bm * L::kTileBytes);
-        const uint32_t sDO = smem_u32(sm + L::kDO + bm * L::kTileBytes);
-        const uint32_t sPt = smem_u32(sm + L::kPt + bm * kTile * kTile);
-        const uint32_t sDSt = smem_u32(sm + L::kDSt + bm * kTile * kTile);
+        const int bm = m & 1, cb = C::kCodeBufs == 2 ? bm : 0;
+        const uint32_t sQ = smem_u32(sm + L::kQ + bm * L::kOwnBytes);
+        const uint32_t sDO = smem_u32(sm + L::kDO + bm * L::kOwnBytes);
+        const uint32_t sPt = smem_u32(sm + L::kPt + cb * kTile * kTile);
+        const uint32_t sDSt = smem_u32(sm + L::kDSt + cb * kTile * kTile);
         const int mode_dv = s_mode[bm][0], mode_dk = s_mode[bm][1];
         if (mode_dv) {
 #pragma unroll
           for (int k = 0; k < kTile / 32; ++k)
-            mma_f8(tmem + 256, SwTile<128>::kmajor(sPt, k), SwTile<D>::mnmajor(sDO, k), kIdDV,
+            mma_f8(tmem + 256, SwTile<128>::kmajor(sPt, k), SwTile<DC>::mnmajor(sDO, k), kIdDV,
                    (k > 0 || mode_dv == 2) ? 1u : 0u);
         }
         if (mode_dk) {
 #pragma unroll
           for (int k = 0; k < kTile / 32; ++k)
-            mma_f8(tmem + 384, SwTile<128>::kmajor(sDSt, k), SwTile<D>::mnmajor(sQ, k), kIdDK,
+            mma_f8(tmem + 384, SwTile<128>::kmajor(sDSt, k), SwTile<DC>::mnmajor(sQ, k), kIdDK,
                    (k > 0 || mode_dk == 2) ? 1u : 0u);
         }
 #pragma unroll
         for (int k = 0; k < kTile / 32; ++k)
-          mma_f8(tmem + bm * 128, SwTile<128>::mnmajor(sDSt, k), SwTile<D>::mnmajor(sK, k), kIdDQ, k > 0);
+          mma_f8(tmem + bm * 128, SwTile<128>::mnmajor(sDSt, k), SwTile<DC>::mnmajor(sKown, k), kIdDQ, k > 0);
         mma_commit(&bars.mma2);
         mma_commit(&bars.qempty[bm]);
       };
+      // A (key rows) x B (query rows) over the full d: split, this half's
+      // sub-tile of A with its own columns of B, then the other sub-tile with
+      // the other half's columns
+      auto full_d = [&](uint32_t d_tmem, uint32_t sA, uint32_t sBown, uint32_t sBother, uint32_t idesc) {
+        if constexpr (C::kSplit) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f8(d_tmem, SwTile<128>::kmajor(sA + (uint32_t)hf * OpTile<D>::kSubBytes, k),
+                   SwTile<128>::kmajor(sBown, k), idesc, k > 0);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f8(d_tmem, SwTile<128>::kmajor(sA + (uint32_t)(1 - hf) * OpTile<D>::kSubBytes, k),
+                   SwTile<128>::kmajor(sBother, k), idesc, 1u);
+        } else {
+#pragma unroll
+          for (int k = 0; k < D / 32; ++k)
+            mma_f8(d_tmem, SwTile<D>::kmajor(sA, k), SwTile<D>::kmajor(sBown, k), idesc, k > 0);
+        }
+      };
+      const uint32_t sQo = smem_u32(sm + L::kQo), sDOo = smem_u32(sm + L::kDOo);
       bool ok = wait(&bars.kv, 0, wd, 304);
       for (int n = 0; n < n_iter && ok; ++n) {
         const int bn = n & 1;
         const uint32_t ph = (n >> 1) & 1;
-        const uint32_t sQ = smem_u32(sm + L::kQ + bn * L::kTileBytes);
-        const uint32_t sDO = smem_u32(sm + L::kDO + bn * L::kTileBytes);
+        const uint32_t sQ = smem_u32(sm + L::kQ + bn * L::kOwnBytes);
+        const uint32_t sDO = smem_u32(sm + L::kDO + bn * L::kOwnBytes);
         if (!(ok = wait(&bars.qfull[bn], ph, wd, 305))) break;
+        if (C::kSplit && !(ok = wait(&bars.ofull, n & 1, wd, 319))) break;
         if (n >= 2 && !(ok = wait(&bars.bfree[bn], ph ^ 1, wd, 306))) break;  // dQ(n-2) drained
         tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < D / 32; ++k)
-          mma_f8(tmem + bn * 128, SwTile<D>::kmajor(sK, k), SwTile<D>::kmajor(sQ, k), kIdS, k > 0);
+        full_d(tmem + bn * 128, sK, sQ, sQo, kIdS);
         mma_commit(&bars.sfull[bn]);
         if (n >= 1) {
           if (!(ok = wait(&bars.pds, (n - 1) & 1, wd, 307))) break;
@@ -274,10 +347,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!(ok = wait(&bars.sread[bn], ph, wd, 308))) break;  // S(n) read: the buffer takes dP(n)
         tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < D / 32; ++k)
-          mma_f8(tmem + bn * 128, SwTile<D>::kmajor(sV, k), SwTile<D>::kmajor(sDO, k), kIdDP, k > 0);
+        full_d(tmem + bn * 128, sV, sDO, sDOo, kIdDP);
         mma_commit(&bars.dpfull[bn]);
+        if (C::kSplit) mma_commit(&bars.oempty);  // S(n) and dP(n) have read the other half's columns
       }
       if (ok && n_iter > 0 && wait(&bars.pds, (n_iter - 1) & 1, wd, 309)) {
         tc_fence_after();
@@ -288,15 +360,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ dQ reducer
-    // Adds each staged dQ tile into global dQ (one bulk reduce per 32-column
+    // Adds each staged dQ pass into global dQ (one bulk reduce per 32-column
     // box) and frees the staging tile once the copies have read it, so that
     // no compute thread waits on the bulk copies.
     if (lane == 0) {
-      for (int m = 0; m < n_iter; ++m) {
-        if (!wait(&bars.dq_staged, m & 1, wd, 314)) break;
+      for (int g = 0; g < n_iter * C::kPasses; ++g) {
+        if (!wait(&bars.dq_staged, g & 1, wd, 314)) break;
+        const int m = g / C::kPasses, ps = g % C::kPasses;
 #pragma unroll
-        for (int bx = 0; bx < D / 32; ++bx)
-          tma_reduce_add_3d(&tmDQ, sm + L::kDQ + bx * (kTile * 128), bx * 32, (qt0 + m) * kTile, bh0);
+        for (int bx = 0; bx < C::kStageCols / 32; ++bx)
+          tma_reduce_add_3d(&tmDQ, sm + L::kDQ + bx * (kTile * 128), col0 + ps * C::kStageCols + bx * 32,
+                            (qt0 + m) * kTile, bh0);
         bulk_commit();
         bulk_wait_read_all();
         mbar_arrive(&bars.dq_free);
@@ -351,32 +425,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     // memory with the 128-byte swizzle of the dQ tensor map, then added into
     // global dQ by one bulk reduce per 32-column box.  TMEM loads are
     // warp-collective: every lane loads; rows beyond N are clipped by the map.
-    // The reducer warp adds the staged tile into global dQ; drain m waits
-    // until it has read the tile of m - 1.
+    // The reducer warp adds each staged pass into global dQ; a pass waits
+    // until it has read the one before.  Pass ps stages columns
+    // [ps * kStageCols, (ps + 1) * kStageCols) of this CTA's, each warpgroup
+    // half of them.
     auto drain_dq = [&](int m, float cdq) {
       const int bm = m & 1;
       wait(&bars.mma2, m & 1, wd, 311);
-      if (m >= 1) wait(&bars.dq_free, (m - 1) & 1, wd, 315);
-      tc_fence_after();
-      // 32 columns at a time (the P registers of the current iteration are live)
 #pragma unroll
-      for (int c = 0; c < DH; c += 32) {
-        float v[32];
-        tmem_load32(tl + bm * 128 + wg * DH + c, v);
-        const uint32_t box = L::kDQ + ((wg * DH + c) / 32) * (kTile * 128) + rsw;
+      for (int ps = 0; ps < C::kPasses; ++ps) {
+        const int g = m * C::kPasses + ps;
+        if (g >= 1) wait(&bars.dq_free, (g - 1) & 1, wd, 315);
+        tc_fence_after();
+        // 32 columns at a time (the P registers of the current iteration are live)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float2 a01 = __fmul2_rn(make_float2(v[4 * e], v[4 * e + 1]), make_float2(cdq, cdq));
-          const float2 a23 = __fmul2_rn(make_float2(v[4 * e + 2], v[4 * e + 3]), make_float2(cdq, cdq));
-          *reinterpret_cast<float4*>(sm + (box ^ (16u * e))) = make_float4(a01.x, a01.y, a23.x, a23.y);
+        for (int c = 0; c < SH; c += 32) {
+          float v[32];
+          tmem_load32(tl + bm * 128 + ps * C::kStageCols + wg * SH + c, v);
+          const uint32_t box = L::kDQ + ((wg * SH + c) / 32) * (kTile * 128) + rsw;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float2 a01 = __fmul2_rn(make_float2(v[4 * e], v[4 * e + 1]), make_float2(cdq, cdq));
+            const float2 a23 = __fmul2_rn(make_float2(v[4 * e + 2], v[4 * e + 3]), make_float2(cdq, cdq));
+            *reinterpret_cast<float4*>(sm + (box ^ (16u * e))) = make_float4(a01.x, a01.y, a23.x, a23.y);
+          }
         }
-      }
-      tc_fence_before();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars.bfree[bm]);
-        mbar_arrive(&bars.dq_staged);
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (ps == C::kPasses - 1) mbar_arrive(&bars.bfree[bm]);
+          mbar_arrive(&bars.dq_staged);
+        }
       }
     };
 
@@ -435,8 +515,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // completion also means dV/dK(n-1) are done).  The two warpgroups take
       // the two in opposite order, so that on every SM sub-partition one
       // warp's code conversion overlaps the other's TMEM loads and staging.
+      const int cb = C::kCodeBufs == 2 ? bn : 0;  // code tiles of this iteration
+      // one code tile of each kind: dV/dK/dQ(n-1) must have read it
+      if (C::kCodeBufs == 1 && n >= 1) wait(&bars.mma2, (n - 1) & 1, wd, 320);
       auto write_p = [&]() {
-        const uint32_t dst = L::kPt + bn * kTile * kTile + rsw_wg;
+        const uint32_t dst = L::kPt + cb * kTile * kTile + rsw_wg;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t w4[4];
@@ -506,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto write_ds = [&]() {
         uint32_t dcode[16];
         {
-          const uint32_t dst = L::kDSt + bn * kTile * kTile + rsw_wg;
+          const uint32_t dst = L::kDSt + cb * kTile * kTile + rsw_wg;
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             const float2 a01 = __fmul2_rn(make_float2(ds[4 * c], ds[4 * c + 1]), make_float2(rs, rs));
@@ -576,36 +659,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (n_iter > 0) {
       drain_dq(n_iter - 1, prev_cdq);
-      wait(&bars.dq_free, (n_iter - 1) & 1, wd, 316);  // the last dQ tile has been read
+      wait(&bars.dq_free, (n_iter * C::kPasses - 1) & 1, wd, 316);  // the last dQ pass has been read
     }
     // epilogue: this head's dV and dK tiles in true units, staged like dQ
     // (after the last dQ reduce has read the staging tile) and added into
     // global dV and dK.  An accumulator that never received a contribution
     // holds garbage and is skipped.  TMEM loads are warp-collective.
     auto reduce_acc = [&](uint32_t col, float unit, const CUtensorMap* map) {
-      if (ct == 0) bulk_wait_read_all();
-      named_bar_sync(1, 256);
-      if (unit != 0.0f) {
 #pragma unroll
-        for (int c = 0; c < DH; c += 32) {
-          float v[32];
-          tmem_load32(tl + col + wg * DH + c, v);
-          const uint32_t box = L::kDQ + ((wg * DH + c) / 32) * (kTile * 128) + rsw;
+      for (int ps = 0; ps < C::kPasses; ++ps) {
+        if (ct == 0) bulk_wait_read_all();
+        named_bar_sync(1, 256);
+        if (unit != 0.0f) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float2 a01 = __fmul2_rn(make_float2(v[4 * e], v[4 * e + 1]), make_float2(unit, unit));
-            const float2 a23 = __fmul2_rn(make_float2(v[4 * e + 2], v[4 * e + 3]), make_float2(unit, unit));
-            *reinterpret_cast<float4*>(sm + (box ^ (16u * e))) =
-                make_float4(a01.x, a01.y, a23.x, a23.y);
+          for (int c = 0; c < SH; c += 32) {
+            float v[32];
+            tmem_load32(tl + col + ps * C::kStageCols + wg * SH + c, v);
+            const uint32_t box = L::kDQ + ((wg * SH + c) / 32) * (kTile * 128) + rsw;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float2 a01 = __fmul2_rn(make_float2(v[4 * e], v[4 * e + 1]), make_float2(unit, unit));
+              const float2 a23 = __fmul2_rn(make_float2(v[4 * e + 2], v[4 * e + 3]), make_float2(unit, unit));
+              *reinterpret_cast<float4*>(sm + (box ^ (16u * e))) =
+                  make_float4(a01.x, a01.y, a23.x, a23.y);
+            }
           }
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(2, 256);
-        if (ct == 0) {
+          fence_proxy_async_smem();
+          named_bar_sync(2, 256);
+          if (ct == 0) {
 #pragma unroll
-          for (int bx = 0; bx < D / 32; ++bx)
-            tma_reduce_add_3d(map, sm + L::kDQ + bx * (kTile * 128), bx * 32, kt * kTile, bg);
-          bulk_commit();
+            for (int bx = 0; bx < C::kStageCols / 32; ++bx)
+              tma_reduce_add_3d(map, sm + L::kDQ + bx * (kTile * 128), col0 + ps * C::kStageCols + bx * 32,
+                                kt * kTile, bg);
+            bulk_commit();
+          }
         }
       }
     };
@@ -629,7 +716,7 @@ cudaError_t launch_t(const BwdLaunch& f, cudaStream_t st) {
   static_assert(smem <= 232448, "backward shared memory exceeds the per-block limit");
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)(f.args.B * f.args.Hq * f.args.T);
+  const unsigned grid = (unsigned)(f.args.B * f.args.Hq * f.args.T * (BwdCfg<D>::kSplit ? 2 : 1));
   k<<<grid, kThreads, smem, st>>>(f.tmQ, f.tmK, f.tmV, f.tmDO, f.tmDQ, f.tmDK, f.tmDV, f.args, f.lse, f.delta,
                                   f.diag);
   return cudaGetLastError();
@@ -638,6 +725,7 @@ cudaError_t launch_t(const BwdLaunch& f, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_attn_bwd(const BwdLaunch& f, int d, cudaStream_t st) {
+  if (d == 256) return launch_t<256>(f, st);
   return d == 128 ? launch_t<128>(f, st) : launch_t<64>(f, st);
 }
 

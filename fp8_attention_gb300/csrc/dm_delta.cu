@@ -9,9 +9,11 @@
 // (batch, query head, 128-row query tile), recomputing S = Q K^T and
 // dP^ = dO^ V^T on tcgen05 tile by tile.
 //
-// Two CTAs share an SM (192 threads, 256 TMEM columns, ~97 KB of shared
-// memory each): one CTA's reductions overlap the other's products, and each
-// SM has two MMA issuers.
+// For d = 64 and 128 two CTAs share an SM (192 threads, 256 TMEM columns,
+// ~97 KB of shared memory each): one CTA's reductions overlap the other's
+// products, and each SM has two MMA issuers.  For d = 256 (192 KB of tiles)
+// one CTA holds the SM and double-buffers S and dP in TMEM instead, so that
+// the products of tile t+1 run while the warpgroup reduces tile t.
 //
 // Warp roles (192 threads):
 //   warps 0-3   one warpgroup, thread = query row (TMEM lane), all key
@@ -19,7 +21,8 @@
 //               sums of P*dP (scaled by s_dO * s_V,t per key tile) and of P
 //   warp 4      TMA: Q and dO tiles once, K/V tiles double-buffered
 //   warp 5      MMA issuer (+ TMEM owner): S(t) and dP(t)
-// TMEM columns: S 0-127, dP 128-255.
+// TMEM columns: S 0-127, dP 128-255 (d = 256: a second pair at 256-511 for
+// odd key tiles).
 #include <cudaTypedefs.h>
 
 #include <type_traits>
@@ -31,10 +34,16 @@ namespace dm {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kCTAsPerSM = 2;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kKV = 2;  // K/V shared-memory stages
 constexpr uint32_t kColS = 0, kColDP = 128;
+
+template <int D>
+struct DeltaCfg {
+  static constexpr int kTBuf = D > 128 ? 2 : 1;  // (S, dP) buffer pairs in TMEM
+  static constexpr uint32_t kTmemCols = 256u * kTBuf;
+  static constexpr int kCTAsPerSM = D > 128 ? 1 : 2;
+};
 
 template <int D>
 struct DeltaLayout {
@@ -49,16 +58,17 @@ struct DeltaLayout {
 };
 
 struct DeltaBars {
-  uint64_t q, kfull[kKV], kempty[kKV], vfull[kKV], vempty[kKV], tfull, tempty, mma_done;
+  uint64_t q, kfull[kKV], kempty[kKV], vfull[kKV], vempty[kKV], tfull[2], tempty[2], mma_done;
 };
 static_assert(sizeof(DeltaBars) <= 256, "delta barriers");
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, kCTAsPerSM)
+__global__ void __launch_bounds__(kThreads, DeltaCfg<D>::kCTAsPerSM)
     attn_delta_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                       const AttnArgs a, const float* __restrict__ lse, float* __restrict__ delta) {
   using L = DeltaLayout<D>;
+  using C = DeltaCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   DeltaBars& bars = *reinterpret_cast<DeltaBars*>(sm + L::kBars);
@@ -89,13 +99,15 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
       mbar_init(&bars.vfull[s], 1);
       mbar_init(&bars.vempty[s], 1);
     }
-    mbar_init(&bars.tfull, 1);
-    mbar_init(&bars.tempty, 4);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars.tfull[s], 1);
+      mbar_init(&bars.tempty[s], 4);
+    }
     mbar_init(&bars.mma_done, 1);
     fence_barrier_init();
   }
   if (warp == 5) {
-    tmem_alloc(s_tmem, 256);
+    tmem_alloc(s_tmem, C::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -110,8 +122,8 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmDO);
       mbar_arrive_expect_tx(&bars.q, 2 * L::kTileBytes);
-      tma_load_3d(sm + L::kQ, &tmQ, &bars.q, 0, q0, bh);
-      tma_load_3d(sm + L::kDO, &tmDO, &bars.q, 0, q0, bh);
+      tma_load_tile<D>(sm + L::kQ, &tmQ, &bars.q, q0, bh);
+      tma_load_tile<D>(sm + L::kDO, &tmDO, &bars.q, q0, bh);
       int issued = 0;
       for (int t = 0; t < nkv; ++t) {
         const int s = t % kKV;
@@ -119,9 +131,9 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
         if (!wait(&bars.kempty[s], ph ^ 1, wd, 201)) break;
         if (!wait(&bars.vempty[s], ph ^ 1, wd, 202)) break;
         mbar_arrive_expect_tx(&bars.kfull[s], L::kTileBytes);
-        tma_load_3d(sm + L::kK + s * L::kTileBytes, &tmK, &bars.kfull[s], 0, t * kTile, bg);
+        tma_load_tile<D>(sm + L::kK + s * L::kTileBytes, &tmK, &bars.kfull[s], t * kTile, bg);
         mbar_arrive_expect_tx(&bars.vfull[s], L::kTileBytes);
-        tma_load_3d(sm + L::kV + s * L::kTileBytes, &tmV, &bars.vfull[s], 0, t * kTile, bg);
+        tma_load_tile<D>(sm + L::kV + s * L::kTileBytes, &tmV, &bars.vfull[s], t * kTile, bg);
         issued = t + 1;
       }
       wait_drain(&bars.q, 0, wd, 209);
@@ -138,22 +150,24 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
       tc_fence_after();
       const uint32_t sQ = smem_u32(sm + L::kQ), sDO = smem_u32(sm + L::kDO);
       for (int t = 0; t < nkv && ok; ++t) {
-        const int ks = t % kKV;
+        const int ks = t % kKV, tb = t % C::kTBuf;
         const uint32_t kph = (t / kKV) & 1;
-        // S(t) and dP(t) once K(t), V(t) have landed and tile t-1 has been read
-        ok = (t == 0 || wait(&bars.tempty, (t - 1) & 1, wd, 204)) && wait(&bars.kfull[ks], kph, wd, 205) &&
-             wait(&bars.vfull[ks], kph, wd, 206);
+        // S(t) and dP(t) once K(t), V(t) have landed and the tile that last
+        // used the TMEM pair, t - kTBuf, has been read
+        ok = (t < C::kTBuf || wait(&bars.tempty[tb], ((t / C::kTBuf) & 1) ^ 1, wd, 204)) &&
+             wait(&bars.kfull[ks], kph, wd, 205) && wait(&bars.vfull[ks], kph, wd, 206);
         if (!ok) break;
         tc_fence_after();
         const uint32_t sK = smem_u32(sm + L::kK + ks * L::kTileBytes);
         const uint32_t sV = smem_u32(sm + L::kV + ks * L::kTileBytes);
+        const uint32_t tpair = tmem + 256u * tb;
 #pragma unroll
         for (int k = 0; k < D / 32; ++k)
-          mma_f8(tmem + kColS, SwTile<D>::kmajor(sQ, k), SwTile<D>::kmajor(sK, k), kIdS, k > 0);
+          mma_f8(tpair + kColS, OpTile<D>::kmajor(sQ, k), OpTile<D>::kmajor(sK, k), kIdS, k > 0);
 #pragma unroll
         for (int k = 0; k < D / 32; ++k)
-          mma_f8(tmem + kColDP, SwTile<D>::kmajor(sDO, k), SwTile<D>::kmajor(sV, k), kIdDP, k > 0);
-        mma_commit(&bars.tfull);
+          mma_f8(tpair + kColDP, OpTile<D>::kmajor(sDO, k), OpTile<D>::kmajor(sV, k), kIdDP, k > 0);
+        mma_commit(&bars.tfull[tb]);
         mma_commit(&bars.kempty[ks]);
         mma_commit(&bars.vempty[ks]);
       }
@@ -184,7 +198,9 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
       if (a.causal) jlim = min(jlim, qi - j0 + 1);
       // warp-uniform: the TMEM loads below are warp-collective
       const bool full = __all_sync(0xffffffffu, jlim >= kTile);
-      wait(&bars.tfull, t & 1, wd, 207);
+      const int tb = t % C::kTBuf;
+      const uint32_t tp = tl + 256u * tb;  // this tile's S, dP pair
+      wait(&bars.tfull[tb], (t / C::kTBuf) & 1, wd, 207);
       tc_fence_after();
       // P = exp2(S c1 - LSE log2e) on packed pairs, 32 columns at a time;
       // masks only on the diagonal or ragged tile
@@ -195,13 +211,13 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         float x[128];  // S of 64 columns, then dP of the same columns
-        tmem_load128(tl + kColS + 64 * hh, tl + kColS + 64 * hh + 32, tl + kColDP + 64 * hh,
-                     tl + kColDP + 64 * hh + 32, x);
+        tmem_load128(tp + kColS + 64 * hh, tp + kColS + 64 * hh + 32, tp + kColDP + 64 * hh,
+                     tp + kColDP + 64 * hh + 32, x);
         if (hh == 1) {
-          // S and dP of tile t have been read: the tensor core may write tile t+1
+          // S and dP of tile t have been read: the tensor core may write the pair again
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars.tempty);
+          if (lane == 0) mbar_arrive(&bars.tempty[tb]);
         }
         auto accumulate = [&](auto full_tile) {
 #pragma unroll
@@ -237,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
   __syncthreads();
   if (warp == 5) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
@@ -245,7 +261,7 @@ template <int D>
 cudaError_t launch_t(const DeltaLaunch& f, cudaStream_t st) {
   auto k = attn_delta_kernel<D>;
   constexpr int smem = DeltaLayout<D>::kBytes;
-  static_assert(kCTAsPerSM * (smem + 1024) <= 233472, "two delta CTAs must fit in one SM's shared memory");
+  static_assert(DeltaCfg<D>::kCTAsPerSM * (smem + 1024) <= 233472, "the delta CTAs must fit in one SM's shared memory");
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(f.args.B * f.args.Hq * f.args.T);
@@ -256,6 +272,7 @@ cudaError_t launch_t(const DeltaLaunch& f, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_delta_matched(const DeltaLaunch& f, int d, cudaStream_t st) {
+  if (d == 256) return launch_t<256>(f, st);
   return d == 128 ? launch_t<128>(f, st) : launch_t<64>(f, st);
 }
 

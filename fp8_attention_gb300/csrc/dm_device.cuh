@@ -250,6 +250,41 @@ struct SwTile {
   }
 };
 
+// An FP8 [128][D] operand tile for D = 64, 128 or 256.  The 128-byte swizzle
+// spans at most 128 bytes of a row, so D = 256 is held as two [128][128]
+// sub-tiles, d columns 0-127 then 128-255, kSubBytes apart (each loaded by its
+// own TMA box).
+//  * K-major (K = d): K step k lies in sub-tile k / 4.
+//  * MN-major (N = d): the sub-tiles are the swizzle atoms along N, and the
+//    descriptor's leading byte offset (16 KB in SwTile<128>) steps between
+//    them.
+template <int D>
+struct OpTile {
+  static_assert(D == 64 || D == 128 || D == 256, "head dimension");
+  static constexpr int kRowBytes = D > 128 ? 128 : D;
+  static constexpr int kSubTiles = D / kRowBytes;
+  static constexpr uint32_t kSubBytes = (uint32_t)kTile * kRowBytes;
+  static constexpr int kStepsPerSub = kRowBytes / 32;
+  __device__ static uint64_t kmajor(uint32_t base, int kstep) {
+    return SwTile<kRowBytes>::kmajor(base + (uint32_t)(kstep / kStepsPerSub) * kSubBytes, kstep % kStepsPerSub);
+  }
+  __device__ static uint64_t mnmajor(uint32_t base, int kstep) {
+    static_assert(kSubTiles == 1 || kSubBytes == 16u * 1024u, "sub-tile stride = leading byte offset");
+    return SwTile<kRowBytes>::mnmajor(base, kstep);
+  }
+};
+
+// Loads rows [row, row + 128) of plane `plane` of a [planes][N][D] FP8 tensor
+// (map box: 128 rows x min(D, 128) bytes) as OpTile<D>; completes on `bar`
+// (kTile * D bytes in all).
+template <int D>
+__device__ __forceinline__ void tma_load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int row,
+                                              int plane) {
+#pragma unroll
+  for (int s = 0; s < OpTile<D>::kSubTiles; ++s)
+    tma_load_3d(dst + s * OpTile<D>::kSubBytes, map, bar, s * OpTile<D>::kRowBytes, row, plane);
+}
+
 // 32 lanes x 32 consecutive 32-bit columns.  Lane quarter of the warp is
 // (warp_id % 4); taddr must carry that lane base in bits 16+.
 // Each load below issues tcgen05.ld and tcgen05.wait::ld in one statement:

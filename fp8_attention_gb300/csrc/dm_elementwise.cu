@@ -128,7 +128,9 @@ cudaError_t quantize_t(const QuantBatch& b, int d, cudaStream_t st) {
   for (int j = 0; j < b.count; ++j) any_t = any_t || b.job[j].codes_t;
   const int smem = any_t ? kTile * d : 0;
   const unsigned grid = (unsigned)b.first_tile[b.count];
-  if (d == 128)
+  if (d == 256)
+    quantize_kernel<T, 256><<<grid, kQThreads, smem, st>>>(b);
+  else if (d == 128)
     quantize_kernel<T, 128><<<grid, kQThreads, smem, st>>>(b);
   else
     quantize_kernel<T, 64><<<grid, kQThreads, smem, st>>>(b);
@@ -240,6 +242,7 @@ cudaError_t launch_quantize(const QuantBatch& b, dm_dtype xt, int d, cudaStream_
 cudaError_t launch_delta_stale(const AttnArgs& a, int d, dm_delta_mode mode, const void* dO, dm_dtype do_t,
                                const uint8_t* do_codes, const void* O, dm_dtype o_t, float* delta,
                                cudaStream_t st) {
+  if (d == 256) return stale_d<256>(a, mode, dO, do_t, do_codes, O, o_t, delta, st);
   return d == 128 ? stale_d<128>(a, mode, dO, do_t, do_codes, O, o_t, delta, st)
                   : stale_d<64>(a, mode, dO, do_t, do_codes, O, o_t, delta, st);
 }

@@ -2,9 +2,11 @@
 // tile), with both matmuls on tcgen05 FP8 MMAs ("Delta-Matching for reliable
 // FP8 attention training", section 01: "What changes in FP8?").
 //
-// Two CTAs share an SM (192 threads, 256 TMEM columns and ~97 KB of shared
-// memory each), so that one CTA's softmax overlaps the other's products and
-// each SM has two independent MMA issuers.
+// For d = 64 and 128 two CTAs share an SM (192 threads, 256 TMEM columns and
+// ~97 KB of shared memory each), so that one CTA's softmax overlaps the
+// other's products and each SM has two independent MMA issuers.  For d = 256
+// (160 KB of tiles) one CTA holds the SM, and S is double-buffered in TMEM
+// instead: the tensor core computes S(t+1) while the warpgroup works on S(t).
 //
 // Warp roles (192 threads):
 //   warps 0-3   one warpgroup; thread = query row (TMEM lane), all key
@@ -23,7 +25,8 @@
 // softmax rescale).  A tile whose product is zero (flushed P or V tile) or
 // below 2^-64 of the current unit adds nothing.
 //
-// TMEM columns (256 allocated): S 0-127, O 128..128+d-1.
+// TMEM columns: d <= 128: S 0-127, O 128..128+d-1 (256 allocated);
+// d = 256: S(t even) 0-127, S(t odd) 128-255, O 256-511 (512 allocated).
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
@@ -36,21 +39,27 @@ namespace dm {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kCTAsPerSM = 2;
 constexpr int kKV = 2;  // K shared-memory stages (V has one: it is needed a whole tile later than K)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr uint32_t kColS = 0, kColO = 128;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kSBuf = D > 128 ? 2 : 1;  // S buffers in TMEM
+  static constexpr uint32_t kColO = 128u * kSBuf;
+  static constexpr uint32_t kTmemCols = D > 128 ? 512 : 256;
+  static constexpr int kCTAsPerSM = D > 128 ? 1 : 2;
+};
 
 struct FwdBars {
-  uint64_t q, kfull[kKV], kempty[kKV], vfull, vempty, sfull, sempty, pready, ofull, stall, mma_done;
+  uint64_t q, kfull[kKV], kempty[kKV], vfull, vempty, sfull[2], sempty[2], pready, ofull, stall, mma_done;
 };
 
 // Everything lives in dynamic shared memory (no static shared variables), so
 // the 1024-byte aligned tile region starts at the window's base.
 template <int D>
 struct FwdLayout {
-  static constexpr int kTileBytes = kTile * D;  // one FP8 Q/K/V tile
+  static constexpr int kTileBytes = kTile * D;  // one FP8 Q/K/V tile (OpTile<D>)
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTileBytes;          // kKV stages
   static constexpr int kV = kK + kKV * kTileBytes;    // one stage
@@ -82,11 +91,12 @@ __device__ __forceinline__ void rescale_o(uint32_t taddr, float f) {
 }
 
 template <int D, bool OUT_BF16>
-__global__ void __launch_bounds__(kThreads, kCTAsPerSM)
+__global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const AttnArgs a, void* __restrict__ O,
                     float* __restrict__ lse) {
   using L = FwdLayout<D>;
+  using C = FwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   FwdBars& bars = *reinterpret_cast<FwdBars*>(sm + L::kBars);
@@ -119,8 +129,10 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
     }
     mbar_init(&bars.vfull, 1);
     mbar_init(&bars.vempty, 1);
-    mbar_init(&bars.sfull, 1);
-    mbar_init(&bars.sempty, 4);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars.sfull[s], 1);
+      mbar_init(&bars.sempty[s], 4);
+    }
     mbar_init(&bars.pready, 4);
     mbar_init(&bars.ofull, 1);
     mbar_init(&bars.stall, 1);
@@ -128,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
     fence_barrier_init();
   }
   if (warp == 5) {
-    tmem_alloc(s_tmem, 256);
+    tmem_alloc(s_tmem, C::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -143,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       mbar_arrive_expect_tx(&bars.q, L::kTileBytes);
-      tma_load_3d(sm + L::kQ, &tmQ, &bars.q, 0, q0, bh);
+      tma_load_tile<D>(sm + L::kQ, &tmQ, &bars.q, q0, bh);
       // K runs one tile ahead of V: K(t) needs only S(t-2) to have finished
       // with its stage, V(t) needs P V(t-1), which completes a tile later.
       int k_issued = 0, v_issued = 0;  // loads issued (both stop early on abort)
@@ -152,14 +164,14 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
           const int s = t % kKV;
           if (!wait(&bars.kempty[s], ((t / kKV) & 1) ^ 1, wd, 101)) break;
           mbar_arrive_expect_tx(&bars.kfull[s], L::kTileBytes);
-          tma_load_3d(sm + L::kK + s * L::kTileBytes, &tmK, &bars.kfull[s], 0, t * kTile, bg);
+          tma_load_tile<D>(sm + L::kK + s * L::kTileBytes, &tmK, &bars.kfull[s], t * kTile, bg);
           k_issued = t + 1;
         }
         if (t >= 1) {
           const int u = t - 1;
           if (!wait(&bars.vempty, (u & 1) ^ 1, wd, 102)) break;
           mbar_arrive_expect_tx(&bars.vfull, L::kTileBytes);
-          tma_load_3d(sm + L::kV, &tmV, &bars.vfull, 0, u * kTile, bg);
+          tma_load_tile<D>(sm + L::kV, &tmV, &bars.vfull, u * kTile, bg);
           v_issued = u + 1;
         }
       }
@@ -186,17 +198,18 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
       const uint32_t sQ = smem_u32(sm + L::kQ);
       for (int t = 0; t <= nkv && ok; ++t) {
         if (t < nkv) {
-          // S(t) once K(t) has landed and the warpgroup has read S(t-1)
-          const int ks = t % kKV;
+          // S(t) once K(t) has landed and the warpgroup has read the S that
+          // last used its buffer, S(t - kSBuf)
+          const int ks = t % kKV, sb = t % C::kSBuf;
           ok = wait(&bars.kfull[ks], (t / kKV) & 1, wd, 105) &&
-               (t == 0 || wait(&bars.sempty, (t - 1) & 1, wd, 106));
+               (t < C::kSBuf || wait(&bars.sempty[sb], ((t / C::kSBuf) & 1) ^ 1, wd, 106));
           if (!ok) break;
           tc_fence_after();
           const uint32_t sK = smem_u32(sm + L::kK + ks * L::kTileBytes);
 #pragma unroll
           for (int k = 0; k < D / 32; ++k)
-            mma_f8(tmem + kColS, SwTile<D>::kmajor(sQ, k), SwTile<D>::kmajor(sK, k), kIdS, k > 0);
-          mma_commit(&bars.sfull);
+            mma_f8(tmem + 128u * sb, OpTile<D>::kmajor(sQ, k), OpTile<D>::kmajor(sK, k), kIdS, k > 0);
+          mma_commit(&bars.sfull[sb]);
           mma_commit(&bars.kempty[ks]);
         }
         if (t >= 1) {
@@ -211,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
             const uint32_t sP = smem_u32(sm + L::kP + (u & 1) * kTile * kTile);
 #pragma unroll
             for (int k = 0; k < kTile / 32; ++k)
-              mma_f8(tmem + kColO, SwTile<128>::kmajor(sP, k), SwTile<D>::mnmajor(sV, k), kIdO,
+              mma_f8(tmem + C::kColO, SwTile<128>::kmajor(sP, k), OpTile<D>::mnmajor(sV, k), kIdO,
                      (k > 0 || mode == 2) ? 1u : 0u);
           }
           mma_commit(&bars.ofull);
@@ -249,7 +262,9 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
       // warp-collective TMEM loads
       const bool full = __all_sync(0xffffffffu, jlim >= kTile);
 
-      wait(&bars.sfull, t & 1, wd, 110);
+      const int sb = t % C::kSBuf;
+      const uint32_t tS = tl + 128u * sb;  // this tile's S
+      wait(&bars.sfull[sb], (t / C::kSBuf) & 1, wd, 110);
       tc_fence_after();
 
       // row max (raw units; c1 > 0 preserves the order), S read in halves;
@@ -261,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
       for (int hh = 0; hh < 2; ++hh) {
         float v0[64];
         float(&v)[64] = hh == 0 ? v0 : v1;
-        tmem_load64(tl + kColS + 64 * hh, tl + kColS + 64 * hh + 32, v);
+        tmem_load64(tS + 64 * hh, tS + 64 * hh + 32, v);
         if (full) {
           float m4[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
@@ -309,11 +324,11 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
           float v0[64];
           float(&v)[64] = hh == 1 ? v1 : v0;
           if (hh == 0) {
-            tmem_load64(tl + kColS, tl + kColS + 32, v);
-            // S has been read: the tensor core may write S(t+1)
+            tmem_load64(tS, tS + 32, v);
+            // S has been read: the tensor core may write the buffer again
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars.sempty);
+            if (lane == 0) mbar_arrive(&bars.sempty[sb]);
           }
 #pragma unroll
           for (int c = 0; c < 64; c += 16) {
@@ -358,10 +373,10 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
         unit = c;
       } else if (c == 0.0f || !(unit / c <= 0x1p64f)) {
         mode = 0;  // nothing to add at this unit: only the softmax rescale
-        rescale_o<D>(tl + kColO, alpha);
+        rescale_o<D>(tl + C::kColO, alpha);
       } else {
         mode = 2;
-        rescale_o<D>(tl + kColO, alpha * (unit / c));
+        rescale_o<D>(tl + C::kColO, alpha * (unit / c));
         unit = c;
       }
       if (tid == 0) s_mode[t & 1] = mode;
@@ -379,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
 #pragma unroll
     for (int c0 = 0; c0 < D; c0 += 64) {
       float o[64];
-      tmem_load64(tl + kColO + c0, tl + kColO + c0 + 32, o);  // warp-collective: before the row guard
+      tmem_load64(tl + C::kColO + c0, tl + C::kColO + c0 + 32, o);  // warp-collective: before the row guard
       if (row_valid) {
         if (OUT_BF16) {
           __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(O) + ((size_t)bh * a.N + qi) * D + c0;
@@ -409,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, kCTAsPerSM)
   __syncthreads();
   if (warp == 5) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
@@ -417,7 +432,7 @@ template <int D, bool BF16>
 cudaError_t launch_fwd_t(const FwdLaunch& f, cudaStream_t st) {
   auto k = attn_fwd_kernel<D, BF16>;
   constexpr int smem = FwdLayout<D>::kBytes;
-  static_assert(kCTAsPerSM * (smem + 1024) <= 233472, "two forward CTAs must fit in one SM's shared memory");
+  static_assert(FwdCfg<D>::kCTAsPerSM * (smem + 1024) <= 233472, "the forward CTAs must fit in one SM's shared memory");
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(f.args.B * f.args.Hq * f.args.T);
@@ -428,6 +443,7 @@ cudaError_t launch_fwd_t(const FwdLaunch& f, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_attn_fwd(const FwdLaunch& f, int d, bool o_bf16, cudaStream_t st) {
+  if (d == 256) return o_bf16 ? launch_fwd_t<256, true>(f, st) : launch_fwd_t<256, false>(f, st);
   if (d == 128) return o_bf16 ? launch_fwd_t<128, true>(f, st) : launch_fwd_t<128, false>(f, st);
   return o_bf16 ? launch_fwd_t<64, true>(f, st) : launch_fwd_t<64, false>(f, st);
 }

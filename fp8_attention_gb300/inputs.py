@@ -54,6 +54,9 @@ WORKLOADS = {
     "saturation_b2_n4096_d128": Workload("saturation_b2_n4096_d128", 2, 16, 4, 4096, 128,
                                          gains={7: 5.4, 0: 3.0, 1: 3.0, 2: 3.0}),
     "long_b1_n65536_d128": Workload("long_b1_n65536_d128", 1, 16, 4, 65536, 128),
+    # head dimension 256 (the width of the gqa_b1_n8192_d128 heads, Hq * d =
+    # 2048, in half as many heads; the same U)
+    "gqa_b1_n8192_d256": Workload("gqa_b1_n8192_d256", 1, 8, 2, 8192, 256),
 }
 
 

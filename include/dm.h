@@ -28,7 +28,8 @@
  *  - FP8 tensors (dm_fp8_tensor) hold codes uint8 [B][H][N][d] and one FP32
  *    scale per 128-row x d tile, scales float [B][H][ceil(N/128)]; the decoded
  *    value of a code is scale * value(code).
- *  - Supported shapes: d in {64, 128}; any N >= 0 (ragged tails are masked);
+ *  - Supported shapes: d in {64, 128, 256} (the Q/K prologue: 64 or 128);
+ *    any N >= 0 (ragged tails are masked);
  *    Hq % Hkv == 0; B*Hq*N*d < 2^31.  B == 0 or N == 0 is a valid no-op.
  *  - Device pointers must be 16-byte aligned.
  *  - The device must be compute capability 10.3 (sm_103a build).

@@ -60,7 +60,8 @@ def _exact_all(Q, K, V, dO, causal, mode=oracle.DELTA_MATCHED, sigma=0.0):
 
 
 @pytest.mark.parametrize("causal", [True, False])
-@pytest.mark.parametrize("shape", [(1, 2, 1, 40, 8), (2, 4, 2, 150, 16), (1, 1, 1, 1, 4), (1, 2, 2, 257, 32)])
+@pytest.mark.parametrize("shape", [(1, 2, 1, 40, 8), (2, 4, 2, 150, 16), (1, 1, 1, 1, 4), (1, 2, 2, 257, 32),
+                                   (1, 2, 1, 24, 256)])
 def test_exact_matches_torch(causal, shape):
     B, Hq, Hkv, N, d = shape
     Q, K, V, dO = _case(B, Hq, Hkv, N, d, seed=N)
