@@ -43,7 +43,8 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # summarised in profiles/ (valid only for the kernel source it was taken on;
 # reported as null once dm_bwd.cu or dm_device.cuh changes).
 BWD_TRAFFIC = {
-    "gqa_b1_n8192_d128": {"sha1": "faa32ffecdab728c23d83ed0649b38cae0928fec", "bytes": 268227072},
+    "gqa_b1_n8192_d128": {"sha1": "6faa1ea50aa040f5a83a5ae0c972338076f2a70e", "bytes": 266367488},
+    "gqa_b1_n8192_d256": {"sha1": "6faa1ea50aa040f5a83a5ae0c972338076f2a70e", "bytes": 263139840},
 }
 # head dimensions the Q/K prologue is built for
 PROLOGUE_DIMS = (64, 128)

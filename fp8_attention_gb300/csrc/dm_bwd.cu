@@ -428,12 +428,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The reducer warp adds each staged pass into global dQ; a pass waits
     // until it has read the one before.  Pass ps stages columns
     // [ps * kStageCols, (ps + 1) * kStageCols) of this CTA's, each warpgroup
-    // half of them.
-    auto drain_dq = [&](int m, float cdq) {
+    // half of them.  Passes [p0, p1) run here; the TMEM buffer is released
+    // after the last.
+    auto drain_dq = [&](int m, float cdq, int p0, int p1) {
       const int bm = m & 1;
-      wait(&bars.mma2, m & 1, wd, 311);
+      if (p0 == 0) wait(&bars.mma2, m & 1, wd, 311);
 #pragma unroll
       for (int ps = 0; ps < C::kPasses; ++ps) {
+        if (ps < p0 || ps >= p1) continue;
         const int g = m * C::kPasses + ps;
         if (g >= 1) wait(&bars.dq_free, (g - 1) & 1, wd, 315);
         tc_fence_after();
@@ -537,11 +539,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (n + 2 < n_iter) row_next = row_value(bh, qt + 2);
         }
       };
+      // split: the first dQ pass here, the second after dS (the reducer
+      // reads the first meanwhile)
+      constexpr int kEarlyPasses = C::kSplit ? 1 : C::kPasses;
       if (wg == 0) {
         write_p();
-        if (n >= 1) drain_dq(n - 1, prev_cdq);
+        if (n >= 1) drain_dq(n - 1, prev_cdq, 0, kEarlyPasses);
       } else {
-        if (n >= 1) drain_dq(n - 1, prev_cdq);
+        if (n >= 1) drain_dq(n - 1, prev_cdq, 0, kEarlyPasses);
         write_p();
       }
 
@@ -574,6 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           dm1 = fmaxf(dm1, fmaxf(fabsf(d23.x), fabsf(d23.y)));
         }
       }
+      if (kEarlyPasses < C::kPasses && n >= 1) drain_dq(n - 1, prev_cdq, kEarlyPasses, C::kPasses);
       float dmax = fmaxf(dm0, dm1);
       dmax = warp_max(dmax);
       if (lane == 0) s_red[bn][1][warp - 4] = dmax;
@@ -658,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     }
     if (n_iter > 0) {
-      drain_dq(n_iter - 1, prev_cdq);
+      drain_dq(n_iter - 1, prev_cdq, 0, C::kPasses);
       wait(&bars.dq_free, (n_iter * C::kPasses - 1) & 1, wd, 316);  // the last dQ pass has been read
     }
     // epilogue: this head's dV and dK tiles in true units, staged like dQ

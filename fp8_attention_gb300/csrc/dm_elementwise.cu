@@ -16,7 +16,11 @@
 namespace dm {
 namespace {
 
-constexpr int kQThreads = 256;
+// Threads per quantiser CTA: d = 256 tiles (64 KB of bf16) are spread over
+// 1024 threads, so that each holds as many values as at d = 128 (the tile sits
+// in registers between the amax reduction and the encode).
+template <int D>
+__host__ __device__ constexpr int quant_threads() { return D > 128 ? 1024 : 256; }
 
 template <typename T>
 struct Vec;
@@ -46,7 +50,8 @@ struct Vec<__nv_bfloat16> {
 // quantises Q, K, V and dO together); the CTA finds its tensor from the
 // running tile counts.  fmt is per tensor (0 E4M3, 1 E5M2).
 template <typename T, int D>
-__global__ void __launch_bounds__(kQThreads) quantize_kernel(const QuantBatch batch) {
+__global__ void __launch_bounds__(quant_threads<D>()) quantize_kernel(const QuantBatch batch) {
+  constexpr int kQThreads = quant_threads<D>();
   constexpr int V = Vec<T>::kElems;
   constexpr int kVecs = kTile * D / V;     // vectors in a full tile
   constexpr int kPer = kVecs / kQThreads;  // per thread
@@ -129,11 +134,11 @@ cudaError_t quantize_t(const QuantBatch& b, int d, cudaStream_t st) {
   const int smem = any_t ? kTile * d : 0;
   const unsigned grid = (unsigned)b.first_tile[b.count];
   if (d == 256)
-    quantize_kernel<T, 256><<<grid, kQThreads, smem, st>>>(b);
+    quantize_kernel<T, 256><<<grid, quant_threads<256>(), smem, st>>>(b);
   else if (d == 128)
-    quantize_kernel<T, 128><<<grid, kQThreads, smem, st>>>(b);
+    quantize_kernel<T, 128><<<grid, quant_threads<128>(), smem, st>>>(b);
   else
-    quantize_kernel<T, 64><<<grid, kQThreads, smem, st>>>(b);
+    quantize_kernel<T, 64><<<grid, quant_threads<64>(), smem, st>>>(b);
   return cudaGetLastError();
 }
 
