@@ -47,7 +47,7 @@ BWD_TRAFFIC = {
     "gqa_b1_n8192_d256": {"sha1": "6faa1ea50aa040f5a83a5ae0c972338076f2a70e", "bytes": 263139840},
 }
 # head dimensions the Q/K prologue is built for
-PROLOGUE_DIMS = (64, 128)
+PROLOGUE_DIMS = (64, 128, 256)
 
 
 def bwd_source_hash():

@@ -310,7 +310,7 @@ dm_status dm_qk_prologue_batch(const dm_prologue_job* jobs, int njobs, dm_dtype 
   if (njobs == 0) return DM_OK;
   if (!jobs) return DM_ERR_INVALID_ARG;
   const int d = jobs[0].d;
-  if (d != 64 && d != 128) return DM_ERR_SHAPE;
+  if (d != 64 && d != 128 && d != 256) return DM_ERR_SHAPE;
   dm::PrologueBatch b{};
   long long tiles = 0;
   for (int i = 0; i < njobs; ++i) {

@@ -10,7 +10,8 @@
 // paired with i + d/2, angle n * base^(-2i/d) at sequence position n.
 //
 // HBM-bound: one persistent CTA per SM streams 128-row x d tiles through a
-// shared-memory ring filled by bulk copies; d/32 threads per row.  Thread p
+// shared-memory ring filled by bulk copies; d/32 threads per row (at d = 256
+// each thread takes two rows of a tile).  Thread p
 // of a row holds channels [16p, 16p + 16) and the same range shifted by d/2,
 // so each rotary pair sits in one thread and the row's sum of squares needs a
 // shuffle or two.
@@ -29,8 +30,6 @@ namespace {
 // elements per thread.
 template <int D>
 __host__ __device__ constexpr int row_threads() { return D / 32; }
-template <int D>
-__host__ __device__ constexpr int tile_threads() { return kTile * row_threads<D>(); }
 
 template <typename T>
 struct RowLoad;
@@ -103,10 +102,18 @@ __device__ __forceinline__ void tile_advance(const PrologueBatch& batch, int g, 
 
 template <typename T, int D>
 struct PrologueCfg {
-  static constexpr int kRowThreads = row_threads<D>(), kThreads = tile_threads<D>();
+  static constexpr int kRowThreads = row_threads<D>();
+  // d = 256: a 128-row tile is taken as two groups of 64 rows (each thread
+  // one row of each), so that 512 threads hold the whole tile in registers
+  // under the 128-register cap until its scale is known
+  static constexpr int kRowGroups = D > 128 ? 2 : 1;
+  static constexpr int kRowsPerGroup = kTile / kRowGroups;
+  static constexpr int kThreads = kRowsPerGroup * kRowThreads;
   static constexpr int Q = D / (2 * kRowThreads);  // channels per thread and half-row
+  // one row group: the gains stay in registers; two: read through L1 where used
+  static constexpr bool kHoldGains = kRowGroups == 1;
   static constexpr int kTileBytes = kTile * D * (int)sizeof(T);
-  static constexpr int kStages = 4 * kTileBytes <= 160 * 1024 ? 4 : 2;
+  static constexpr int kStages = 4 * kTileBytes <= 160 * 1024 ? 4 : (2 * kTileBytes <= 200 * 1024 ? 2 : 1);
   static constexpr int kSmem = kStages * kTileBytes;
 };
 
@@ -115,9 +122,10 @@ struct PrologueCfg {
 // of one head is one contiguous block of rows), so the SM always has loads
 // outstanding while it normalises, rotates and encodes the current tile.
 template <typename T, int D>
-__global__ void __launch_bounds__(tile_threads<D>(), 1) prologue_kernel(const PrologueBatch batch, float eps) {
+__global__ void __launch_bounds__(PrologueCfg<T, D>::kThreads, 1)
+    prologue_kernel(const PrologueBatch batch, float eps) {
   using C = PrologueCfg<T, D>;
-  constexpr int Q = C::Q, kRowThreads = C::kRowThreads;
+  constexpr int Q = C::Q, kRowThreads = C::kRowThreads, G = C::kRowGroups;
   static_assert(Q == 16, "sixteen channels per thread and half-row");
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ float s_red[2][C::kThreads / 32];
@@ -147,7 +155,7 @@ __global__ void __launch_bounds__(tile_threads<D>(), 1) prologue_kernel(const Pr
   const int row = threadIdx.x / kRowThreads, part = threadIdx.x % kRowThreads;
   const int ca = part * Q, cb = D / 2 + part * Q;  // first channel of each half-row
   // this thread's channel gains (ones without gains), reloaded when the job changes
-  float ga[Q], gb[Q];
+  float ga[C::kHoldGains ? Q : 1], gb[C::kHoldGains ? Q : 1];
   int gain_job = -1;
   int it = 0;
   TileRef r;
@@ -159,71 +167,97 @@ __global__ void __launch_bounds__(tile_threads<D>(), 1) prologue_kernel(const Pr
     const float* rope_cos = batch.job[r.j].rope_cos;
     const float* rope_sin = batch.job[r.j].rope_sin;
     const int N = batch.job[r.j].N;
-    if (r.j != gain_job) {
-      gain_job = r.j;
-      if (gain) {
-        RowLoad<float>::template load<Q>(gain + ca, ga);
-        RowLoad<float>::template load<Q>(gain + cb, gb);
-      } else {
+    if constexpr (C::kHoldGains) {
+      if (r.j != gain_job) {
+        gain_job = r.j;
+        if (gain) {
+          RowLoad<float>::template load<Q>(gain + ca, ga);
+          RowLoad<float>::template load<Q>(gain + cb, gb);
+        } else {
 #pragma unroll
-        for (int k = 0; k < Q; ++k) ga[k] = gb[k] = 1.0f;
+          for (int k = 0; k < Q; ++k) ga[k] = gb[k] = 1.0f;
+        }
       }
     }
-    const int n = r.t * kTile + row;  // sequence position
-    const bool valid = row < r.rows;
     const bool rope = rope_cos != nullptr;
-    // the row's angles (L2) while the rows arrive
-    float c[Q], sn[Q];
-    if (rope && valid) {
-      RowLoad<float>::template load<Q>(rope_cos + (size_t)n * (D / 2) + ca, c);
-      RowLoad<float>::template load<Q>(rope_sin + (size_t)n * (D / 2) + ca, sn);
-    }
-    wait(&full[stage], (uint32_t)(it / C::kStages) & 1, wd, 401);
-    float a[Q], b[Q];
-    if (valid) {
-      const T* xr = reinterpret_cast<const T*>(ring + stage * C::kTileBytes) + row * D;
-      RowLoad<T>::template load_shared<Q>(xr + ca, a);
-      RowLoad<T>::template load_shared<Q>(xr + cb, b);
-    } else {
-#pragma unroll
-      for (int k = 0; k < Q; ++k) a[k] = b[k] = 0.0f;
-    }
-    // RMSNorm: the row's sum of squares over its kRowThreads threads (pairs of
-    // adjacent channels in packed FP32x2 arithmetic throughout)
-    float2 ss2 = make_float2(0.0f, 0.0f);
-#pragma unroll
-    for (int k = 0; k < Q; k += 2) {
-      ss2 = __ffma2_rn(make_float2(a[k], a[k + 1]), make_float2(a[k], a[k + 1]), ss2);
-      ss2 = __ffma2_rn(make_float2(b[k], b[k + 1]), make_float2(b[k], b[k + 1]), ss2);
-    }
-    float ss = ss2.x + ss2.y;
-#pragma unroll
-    for (int o = 1; o < kRowThreads; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    // eps > 0 (checked by the API), so an all-zero row normalises to zeros
-    const float inv = valid ? __frsqrt_rn(__fadd_rn(ss * (1.0f / D), eps)) : 0.0f;
-    const float2 inv2 = make_float2(inv, inv);
-#pragma unroll
-    for (int k = 0; k < Q; k += 2) {
-      const float2 ya = __fmul2_rn(__fmul2_rn(make_float2(a[k], a[k + 1]), inv2), make_float2(ga[k], ga[k + 1]));
-      const float2 yb = __fmul2_rn(__fmul2_rn(make_float2(b[k], b[k + 1]), inv2), make_float2(gb[k], gb[k + 1]));
-      a[k] = ya.x, a[k + 1] = ya.y, b[k] = yb.x, b[k + 1] = yb.y;
-    }
-    // rotary embedding: channel ca + k pairs with cb + k, angle index ca + k
-    if (rope && valid) {
-#pragma unroll
-      for (int k = 0; k < Q; k += 2) {
-        const float2 x0 = make_float2(a[k], a[k + 1]), x1 = make_float2(b[k], b[k + 1]);
-        const float2 c2 = make_float2(c[k], c[k + 1]), s2 = make_float2(sn[k], sn[k + 1]);
-        const float2 t1 = __fmul2_rn(x1, s2), t0 = __fmul2_rn(x0, s2);
-        const float2 ra = __ffma2_rn(x0, c2, make_float2(-t1.x, -t1.y));
-        const float2 rb = __ffma2_rn(x1, c2, t0);
-        a[k] = ra.x, a[k + 1] = ra.y, b[k] = rb.x, b[k + 1] = rb.y;
-      }
-    }
-    // tile amax, scale and E4M3 codes (the rule of dm_quantize)
+    float a[G][Q], b[G][Q];  // this thread's channels of its row in each group
     float amax = 0.0f;
 #pragma unroll
-    for (int k = 0; k < Q; ++k) amax = fmaxf(amax, fmaxf(fabsf(a[k]), fabsf(b[k])));  // |x| folds into the max
+    for (int rg = 0; rg < G; ++rg) {
+      const int rr = rg * C::kRowsPerGroup + row;  // row within the tile
+      const int n = r.t * kTile + rr;              // sequence position
+      const bool valid = rr < r.rows;
+      // the row's angles (L2) while the rows arrive (two row groups: read
+      // where used, which keeps the other group's row in registers)
+      float c[C::kHoldGains ? Q : 1], sn[C::kHoldGains ? Q : 1];
+      if (C::kHoldGains && rope && valid) {
+        RowLoad<float>::template load<Q>(rope_cos + (size_t)n * (D / 2) + ca, c);
+        RowLoad<float>::template load<Q>(rope_sin + (size_t)n * (D / 2) + ca, sn);
+      }
+      if (rg == 0) wait(&full[stage], (uint32_t)(it / C::kStages) & 1, wd, 401);
+      float(&x)[Q] = a[rg];
+      float(&y)[Q] = b[rg];
+      if (valid) {
+        const T* xr = reinterpret_cast<const T*>(ring + stage * C::kTileBytes) + rr * D;
+        RowLoad<T>::template load_shared<Q>(xr + ca, x);
+        RowLoad<T>::template load_shared<Q>(xr + cb, y);
+      } else {
+#pragma unroll
+        for (int k = 0; k < Q; ++k) x[k] = y[k] = 0.0f;
+      }
+      // RMSNorm: the row's sum of squares over its kRowThreads threads (pairs of
+      // adjacent channels in packed FP32x2 arithmetic throughout)
+      float2 ss2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int k = 0; k < Q; k += 2) {
+        ss2 = __ffma2_rn(make_float2(x[k], x[k + 1]), make_float2(x[k], x[k + 1]), ss2);
+        ss2 = __ffma2_rn(make_float2(y[k], y[k + 1]), make_float2(y[k], y[k + 1]), ss2);
+      }
+      float ss = ss2.x + ss2.y;
+#pragma unroll
+      for (int o = 1; o < kRowThreads; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      // eps > 0 (checked by the API), so an all-zero row normalises to zeros
+      const float inv = valid ? __frsqrt_rn(__fadd_rn(ss * (1.0f / D), eps)) : 0.0f;
+      const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+      for (int k = 0; k < Q; k += 2) {
+        float2 g0, g1;
+        if constexpr (C::kHoldGains) {
+          g0 = make_float2(ga[k], ga[k + 1]);
+          g1 = make_float2(gb[k], gb[k + 1]);
+        } else if (gain) {
+          g0 = __ldg(reinterpret_cast<const float2*>(gain + ca + k));
+          g1 = __ldg(reinterpret_cast<const float2*>(gain + cb + k));
+        } else {
+          g0 = g1 = make_float2(1.0f, 1.0f);
+        }
+        const float2 ya = __fmul2_rn(__fmul2_rn(make_float2(x[k], x[k + 1]), inv2), g0);
+        const float2 yb = __fmul2_rn(__fmul2_rn(make_float2(y[k], y[k + 1]), inv2), g1);
+        x[k] = ya.x, x[k + 1] = ya.y, y[k] = yb.x, y[k + 1] = yb.y;
+      }
+      // rotary embedding: channel ca + k pairs with cb + k, angle index ca + k
+      if (rope && valid) {
+#pragma unroll
+        for (int k = 0; k < Q; k += 2) {
+          const float2 x0 = make_float2(x[k], x[k + 1]), x1 = make_float2(y[k], y[k + 1]);
+          float2 c2, s2;
+          if constexpr (C::kHoldGains) {
+            c2 = make_float2(c[k], c[k + 1]);
+            s2 = make_float2(sn[k], sn[k + 1]);
+          } else {
+            c2 = __ldg(reinterpret_cast<const float2*>(rope_cos + (size_t)n * (D / 2) + ca + k));
+            s2 = __ldg(reinterpret_cast<const float2*>(rope_sin + (size_t)n * (D / 2) + ca + k));
+          }
+          const float2 t1 = __fmul2_rn(x1, s2), t0 = __fmul2_rn(x0, s2);
+          const float2 ra = __ffma2_rn(x0, c2, make_float2(-t1.x, -t1.y));
+          const float2 rb = __ffma2_rn(x1, c2, t0);
+          x[k] = ra.x, x[k + 1] = ra.y, y[k] = rb.x, y[k + 1] = rb.y;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < Q; ++k) amax = fmaxf(amax, fmaxf(fabsf(x[k]), fabsf(y[k])));  // |x| folds into the max
+    }
+    // tile amax, scale and E4M3 codes (the rule of dm_quantize)
     amax = warp_max(amax);
     if ((threadIdx.x & 31) == 0) s_red[it & 1][threadIdx.x >> 5] = amax;
     __syncthreads();
@@ -233,19 +267,23 @@ __global__ void __launch_bounds__(tile_threads<D>(), 1) prologue_kernel(const Pr
       const int lane = threadIdx.x & 31;
       amax = warp_max(lane < C::kThreads / 32 ? s_red[it & 1][lane] : 0.0f);
     }
-    float rr;
-    const float sc = tile_scale<0>(amax, rr);
+    float rcp;
+    const float sc = tile_scale<0>(amax, rcp);
     if (threadIdx.x == 0) batch.job[r.j].scales[r.tile] = sc;
-    if (valid) {
-      const bool flushed = sc == 0.0f;  // all codes +0
-      const float2 r2 = make_float2(rr, rr);
+    const bool flushed = sc == 0.0f;  // all codes +0
+    const float2 r2 = make_float2(rcp, rcp);
+#pragma unroll
+    for (int rg = 0; rg < G; ++rg) {
+      const int rr = rg * C::kRowsPerGroup + row;
+      if (rr >= r.rows) continue;
+      const int n = r.t * kTile + rr;
       uint32_t wa[Q / 4], wb[Q / 4];
 #pragma unroll
       for (int k = 0; k < Q / 4; ++k) {
-        const float2 a01 = __fmul2_rn(make_float2(a[4 * k], a[4 * k + 1]), r2);
-        const float2 a23 = __fmul2_rn(make_float2(a[4 * k + 2], a[4 * k + 3]), r2);
-        const float2 b01 = __fmul2_rn(make_float2(b[4 * k], b[4 * k + 1]), r2);
-        const float2 b23 = __fmul2_rn(make_float2(b[4 * k + 2], b[4 * k + 3]), r2);
+        const float2 a01 = __fmul2_rn(make_float2(a[rg][4 * k], a[rg][4 * k + 1]), r2);
+        const float2 a23 = __fmul2_rn(make_float2(a[rg][4 * k + 2], a[rg][4 * k + 3]), r2);
+        const float2 b01 = __fmul2_rn(make_float2(b[rg][4 * k], b[rg][4 * k + 1]), r2);
+        const float2 b23 = __fmul2_rn(make_float2(b[rg][4 * k + 2], b[rg][4 * k + 3]), r2);
         wa[k] = flushed ? 0u : pack4<0>(a01.x, a01.y, a23.x, a23.y);
         wb[k] = flushed ? 0u : pack4<0>(b01.x, b01.y, b23.x, b23.y);
       }
@@ -292,6 +330,7 @@ cudaError_t prologue_d(const PrologueBatch& b, float eps, cudaStream_t st) {
 
 template <typename T>
 cudaError_t prologue_t(const PrologueBatch& b, int d, float eps, cudaStream_t st) {
+  if (d == 256) return prologue_d<T, 256>(b, eps, st);
   return d == 128 ? prologue_d<T, 128>(b, eps, st) : prologue_d<T, 64>(b, eps, st);
 }
 

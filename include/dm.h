@@ -28,8 +28,7 @@
  *  - FP8 tensors (dm_fp8_tensor) hold codes uint8 [B][H][N][d] and one FP32
  *    scale per 128-row x d tile, scales float [B][H][ceil(N/128)]; the decoded
  *    value of a code is scale * value(code).
- *  - Supported shapes: d in {64, 128, 256} (the Q/K prologue: 64 or 128);
- *    any N >= 0 (ragged tails are masked);
+ *  - Supported shapes: d in {64, 128, 256}; any N >= 0 (ragged tails are masked);
  *    Hq % Hkv == 0; B*Hq*N*d < 2^31.  B == 0 or N == 0 is a valid no-op.
  *  - Device pointers must be 16-byte aligned.
  *  - The device must be compute capability 10.3 (sm_103a build).
@@ -154,8 +153,8 @@ dm_status dm_rope_table(int N, int d, double base, float* cos_table, float* sin_
  * 128-row x d tile): codes [B][H][N][d], scales [B][H][ceil(N/128)], ready
  * for dm_attn_fwd.  All arithmetic is FP32 (correctly rounded 1/sqrt), so
  * codes can differ from an exact evaluation only where y * (448 / amax) lies
- * within FP32 rounding of a code boundary.  All jobs share x_dtype, d (64 or
- * 128) and eps (finite, > 0); x, codes, scales, gain and the tables are
+ * within FP32 rounding of a code boundary.  All jobs share x_dtype, d (64,
+ * 128 or 256) and eps (finite, > 0); x, codes, scales, gain and the tables are
  * 16-byte aligned.  Every job is validated before the launch;
  * empty tensors are skipped.  Errors: DM_ERR_DTYPE, DM_ERR_SHAPE,
  * DM_ERR_INVALID_ARG (njobs out of range, bad eps, one table without the

@@ -27,7 +27,7 @@ def _ulp_diff32(a, b):
     return np.abs(ia - ib)
 
 
-@pytest.mark.parametrize("N,d", [(8192, 128), (1000, 64), (1, 128)])
+@pytest.mark.parametrize("N,d", [(8192, 128), (1000, 64), (1, 128), (8192, 256)])
 def test_rope_table_matches_oracle(N, d):
     """Within one FP32 ulp of the FP64 value, plus 2^-36 absolute: both sides
     form the angle n * base^(-2i/d) in FP64, whose last-bit differences move
@@ -69,7 +69,8 @@ def check_codes(got, x, gain, rope):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("shape", [(1, 2, 256, 64), (2, 3, 300, 128), (1, 1, 1, 128), (1, 4, 1000, 64)])
+@pytest.mark.parametrize("shape", [(1, 2, 256, 64), (2, 3, 300, 128), (1, 1, 1, 128), (1, 4, 1000, 64),
+                                   (1, 2, 300, 256), (1, 1, 1, 256)])
 @pytest.mark.parametrize("rope,gains", [(True, {7: 5.4, 0: 3.0, 1: 3.0, 2: 3.0}), (False, {}), (True, None)])
 def test_prologue_matches_oracle(dtype, shape, rope, gains):
     B, H, N, d = shape
@@ -92,15 +93,16 @@ def test_prologue_matches_oracle(dtype, shape, rope, gains):
         assert not got.codes.cpu().numpy()[0, 0, :128].any()
 
 
-def test_prologue_batch_q_and_k_of_the_bench_workload():
-    """Q and K of the 8K workload (pre-normalisation draws, bf16) in one launch
+@pytest.mark.parametrize("name", ["gqa_b1_n8192_d128", "gqa_b1_n8192_d256"])
+def test_prologue_batch_q_and_k_of_the_bench_workload(name):
+    """Q and K of an 8K workload (pre-normalisation draws, bf16) in one launch
     at the bench's configuration; whole heads checked against the oracle."""
-    w = WORKLOADS["gqa_b1_n8192_d128"]
+    w = WORKLOADS[name]
     xq, xk, gain = make_prologue_inputs(w)
     table = dm.dm_rope_table(w.N, w.d, device=DEV)
     gq, gk = dm.dm_qk_prologue_batch([(xq.to(DEV), gain.to(DEV)), (xk.to(DEV), gain.to(DEV))], rope=table)
     assert dm.dm_get_status() == 0
-    for got, x, heads in ((gq, xq, [0, 9, 15]), (gk, xk, [0, 3])):
+    for got, x, heads in ((gq, xq, [0, w.Hq // 2 + 1, w.Hq - 1]), (gk, xk, [0, w.Hkv - 1])):
         for h in heads:
             sub = dm.Fp8(got.codes[:, h:h + 1].contiguous(), got.scales[:, h:h + 1].contiguous())
             check_codes(sub, x[:, h:h + 1], gain, True)
