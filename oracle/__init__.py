@@ -75,11 +75,11 @@ def _load():
             lib.or_quantize.argtypes = [P, I, I, I, I, I, P, P]
             lib.or_dequantize.argtypes = [P, P, I, I, I, I, I, P]
             lib.or_attn_fwd.restype = I
-            lib.or_attn_fwd.argtypes = [I, I, I, I, I, I, D, I, P, P, P, P, I, P, I, P, P, P]
+            lib.or_attn_fwd.argtypes = [I, I, I, I, I, I, I, D, I, P, P, P, P, I, P, I, P, P, P]
             lib.or_attn_delta.restype = I
-            lib.or_attn_delta.argtypes = [I, I, I, I, I, I, D, I, I, P, P, P, P, P, P, P, P, I, P, I, P]
+            lib.or_attn_delta.argtypes = [I, I, I, I, I, I, I, D, I, I, P, P, P, P, P, P, P, P, I, P, I, P]
             lib.or_attn_bwd.restype = I
-            lib.or_attn_bwd.argtypes = [I, I, I, I, I, I, D, I, P, P, P, P, P, P,
+            lib.or_attn_bwd.argtypes = [I, I, I, I, I, I, I, D, I, P, P, P, P, P, P,
                                         P, I, P, I, P, I, P, P, P, P, P, P, P]
             lib.or_rope_table.argtypes = [I, I, D, P, P]
             lib.or_qk_prologue.restype = I
@@ -97,16 +97,17 @@ def _f64(a):
     return None if a is None else np.ascontiguousarray(a, dtype=np.float64)
 
 
-def _check(Q, K, V, *rows_q):
-    """Shape checks: Q [B][Hq][N][d], K and V [B][Hkv][N][d], Hkv | Hq; rows_q arrays like Q."""
-    if Q.ndim != 4 or K.shape != V.shape or K.ndim != 4:
-        raise ValueError("Q, K, V must be [B][H][N][d] with K.shape == V.shape")
+def _check(Q, K, V, *rows_v):
+    """Shape checks: Q [B][Hq][N][d], K [B][Hkv][N][d], V [B][Hkv][N][dv] (dv may
+    differ from d), Hkv | Hq; rows_v arrays (dO, O) [B][Hq][N][dv]."""
+    if Q.ndim != 4 or K.ndim != 4 or V.ndim != 4 or K.shape[:3] != V.shape[:3]:
+        raise ValueError("Q, K, V must be [B][H][N][d] with K and V of the same B, H, N")
     B, Hq, N, d = Q.shape
     if K.shape[0] != B or K.shape[2:] != (N, d) or Hq % K.shape[1]:
         raise ValueError(f"shape mismatch: Q {Q.shape} K {K.shape}")
-    for a in rows_q:
-        if a is not None and a.shape != Q.shape:
-            raise ValueError(f"shape mismatch: {a.shape} vs Q {Q.shape}")
+    for a in rows_v:
+        if a is not None and a.shape != (B, Hq, N, V.shape[3]):
+            raise ValueError(f"shape mismatch: {a.shape} vs (B, Hq, N, dv) {(B, Hq, N, V.shape[3])}")
 
 
 def _sel(tiles):
@@ -177,13 +178,13 @@ def attn_fwd(Q, K, V, causal=True, sigma=0.0, flags=GPU_CONTRACT, q_tiles=None, 
     Q, K, V = _f64(Q), _f64(K), _f64(V)
     _check(Q, K, V)
     B, Hq, N, d = Q.shape
-    Hkv = K.shape[1]
-    O = np.full(Q.shape, np.nan)
+    Hkv, dv = K.shape[1], V.shape[3]
+    O = np.full((B, Hq, N, dv), np.nan)
     LSE = np.full((B, Hq, N), np.nan)
     P = np.zeros((B, Hq, N, N)) if want_pfwd else None
     qs, nq = _sel(q_tiles)
     gs, ng = _groups(groups)
-    rc = lib.or_attn_fwd(B, Hq, Hkv, N, d, int(causal), float(sigma), int(flags), _p(Q), _p(K), _p(V),
+    rc = lib.or_attn_fwd(B, Hq, Hkv, N, d, dv, int(causal), float(sigma), int(flags), _p(Q), _p(K), _p(V),
                          _p(qs), nq, _p(gs), ng, _p(O), _p(LSE), _p(P))
     if rc != 0:
         raise ValueError("or_attn_fwd: bad arguments")
@@ -204,11 +205,11 @@ def attn_delta(Q, K, V, dOhat, LSE, mode=DELTA_MATCHED, dO=None, O=None, causal=
     if mode == DELTA_STALE_DOHAT and O is None:
         raise ValueError("stale_dOhat needs O")
     B, Hq, N, d = Q.shape
-    Hkv = K.shape[1]
+    Hkv, dv = K.shape[1], V.shape[3]
     delta = np.full((B, Hq, N), np.nan)
     qs, nq = _sel(q_tiles)
     gs, ng = _groups(groups)
-    rc = lib.or_attn_delta(B, Hq, Hkv, N, d, int(causal), float(sigma), int(flags), int(mode),
+    rc = lib.or_attn_delta(B, Hq, Hkv, N, d, dv, int(causal), float(sigma), int(flags), int(mode),
                            _p(Q), _p(K), _p(V), _p(dOhat), _p(dO), _p(O), _p(LSE),
                            _p(qs), nq, _p(gs), ng, _p(delta))
     if rc != 0:
@@ -225,7 +226,7 @@ def attn_bwd(Q, K, V, dOhat, LSE, delta, causal=True, sigma=0.0, flags=GPU_CONTR
     if LSE.shape != Q.shape[:3] or delta.shape != Q.shape[:3]:
         raise ValueError("LSE and delta must be [B][Hq][N]")
     B, Hq, N, d = Q.shape
-    Hkv = K.shape[1]
+    Hkv, dv = K.shape[1], V.shape[3]
     out = {
         "dQ": np.full(Q.shape, np.nan),
         "dK": np.full(K.shape, np.nan),
@@ -236,7 +237,7 @@ def attn_bwd(Q, K, V, dOhat, LSE, delta, causal=True, sigma=0.0, flags=GPU_CONTR
     qs, nq = _sel(q_tiles)
     ks, nk = _sel(kv_tiles)
     gs, ng = _groups(groups)
-    rc = lib.or_attn_bwd(B, Hq, Hkv, N, d, int(causal), float(sigma), int(flags),
+    rc = lib.or_attn_bwd(B, Hq, Hkv, N, d, dv, int(causal), float(sigma), int(flags),
                          _p(Q), _p(K), _p(V), _p(dOhat), _p(LSE), _p(delta),
                          _p(qs), nq, _p(ks), nk, _p(gs), ng,
                          _p(out["dQ"]), _p(out["dK"]), _p(out["dV"]), _p(diag),

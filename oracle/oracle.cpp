@@ -143,13 +143,17 @@ float qz_tile(int rows, int cols, int f, Get get, Valid valid, uint8_t* codes /*
 
 inline float fl32(double x) { return (float)x; }
 
+// d is the query/key head dimension, dv the value head dimension (V, dO, O
+// and dV rows); they differ for heads shaped like multi-head latent attention.
 struct Dims {
-  int B, Hq, Hkv, N, d, causal;
+  int B, Hq, Hkv, N, d, dv, causal;
   double sigma;
   int G() const { return Hq / Hkv; }
   int T() const { return (N + kTile - 1) / kTile; }
   size_t qoff(int b, int h) const { return ((size_t)b * Hq + h) * N * d; }
   size_t kvoff(int b, int g) const { return ((size_t)b * Hkv + g) * N * d; }
+  size_t qvoff(int b, int h) const { return ((size_t)b * Hq + h) * N * dv; }
+  size_t kvvoff(int b, int g) const { return ((size_t)b * Hkv + g) * N * dv; }
   size_t rowoff(int b, int h) const { return ((size_t)b * Hq + h) * N; }
 };
 
@@ -273,12 +277,12 @@ void or_dequantize(const uint8_t* codes, const float* scales, int B, int H, int 
 //
 // Pfwd (nullable, [B][Hq][N][N]) receives the effective forward
 // probabilities, i.e. the matrix with O = Pfwd V exactly.
-int or_attn_fwd(int B, int Hq, int Hkv, int N, int d, int causal, double sigma, int flags,
+int or_attn_fwd(int B, int Hq, int Hkv, int N, int d, int dv, int causal, double sigma, int flags,
                 const double* Q, const double* K, const double* V,
                 const int* q_tiles, int n_q_tiles, const int* groups, int n_groups,
                 double* O, double* LSE, double* Pfwd) {
-  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || N < 0 || d <= 0) return 1;
-  Dims D{B, Hq, Hkv, N, d, causal, sigma > 0 ? sigma : 1.0 / std::sqrt((double)d)};
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || N < 0 || d <= 0 || dv <= 0) return 1;
+  Dims D{B, Hq, Hkv, N, d, dv, causal, sigma > 0 ? sigma : 1.0 / std::sqrt((double)d)};
   const int T = D.T();
   const std::vector<int> qts = tiles_or_all(q_tiles, n_q_tiles, T);
   const std::vector<Group> gs = groups_or_all(groups, n_groups, D);
@@ -291,8 +295,8 @@ int or_attn_fwd(int B, int Hq, int Hkv, int N, int d, int causal, double sigma, 
     const int qt = qts[u % qts.size()];
     const double* Qh = Q + D.qoff(gr.b, h);
     const double* Kg = K + D.kvoff(gr.b, gr.g);
-    const double* Vg = V + D.kvoff(gr.b, gr.g);
-    double* Oh = O + D.qoff(gr.b, h);
+    const double* Vg = V + D.kvvoff(gr.b, gr.g);
+    double* Oh = O + D.qvoff(gr.b, h);
     double* Lh = LSE + D.rowoff(gr.b, h);
     double* Ph = Pfwd ? Pfwd + ((size_t)gr.b * Hq + h) * N * N : nullptr;
     const int i0 = qt * kTile;
@@ -312,12 +316,12 @@ int or_attn_fwd(int B, int Hq, int Hkv, int N, int d, int causal, double sigma, 
         double l = 0.0;
         for (int j = 0; j < N; ++j)
           if (visible(D, i, j)) l += std::exp(s[j] - m);
-        for (int k = 0; k < d; ++k) Oh[(size_t)i * d + k] = 0.0;
+        for (int k = 0; k < dv; ++k) Oh[(size_t)i * dv + k] = 0.0;
         for (int j = 0; j < N; ++j) {
           const double p = visible(D, i, j) ? std::exp(s[j] - m) / l : 0.0;
           if (Ph) Ph[(size_t)i * N + j] = p;
           if (p != 0.0)
-            for (int k = 0; k < d; ++k) Oh[(size_t)i * d + k] += p * Vg[(size_t)j * d + k];
+            for (int k = 0; k < dv; ++k) Oh[(size_t)i * dv + k] += p * Vg[(size_t)j * dv + k];
         }
         Lh[i] = m + std::log(l);
       }
@@ -325,7 +329,7 @@ int or_attn_fwd(int B, int Hq, int Hkv, int N, int d, int causal, double sigma, 
     }
 
     // One-pass online forward with per-tile quantisation of P~.
-    std::vector<double> m(rows, -INFINITY), l(rows, 0.0), acc((size_t)rows * d, 0.0);
+    std::vector<double> m(rows, -INFINITY), l(rows, 0.0), acc((size_t)rows * dv, 0.0);
     std::vector<double> mt((size_t)(ktmax + 1) * rows);  // m^(t) per tile, for Pfwd
     std::vector<double> S;
     std::vector<float> pt;
@@ -359,13 +363,13 @@ int or_attn_fwd(int B, int Hq, int Hkv, int N, int d, int causal, double sigma, 
         double rowsum = 0.0;
         for (int c = 0; c < cols; ++c) rowsum += pd[(size_t)r * cols + c];
         l[r] = alpha * l[r] + rowsum;
-        double* a = &acc[(size_t)r * d];
-        for (int k = 0; k < d; ++k) a[k] *= alpha;
+        double* a = &acc[(size_t)r * dv];
+        for (int k = 0; k < dv; ++k) a[k] *= alpha;
         for (int c = 0; c < cols; ++c) {
           const double ph = (double)sP * fp8_decode(codes[(size_t)r * cols + c], 0);
           if (Ph) Ph[(size_t)(i0 + r) * N + j0 + c] = ph;  // finalised below
           if (ph != 0.0)
-            for (int k = 0; k < d; ++k) a[k] += ph * Vg[(size_t)(j0 + c) * d + k];
+            for (int k = 0; k < dv; ++k) a[k] += ph * Vg[(size_t)(j0 + c) * dv + k];
         }
         m[r] = mnew[r];
         mt[(size_t)kt * rows + r] = mnew[r];
@@ -373,7 +377,7 @@ int or_attn_fwd(int B, int Hq, int Hkv, int N, int d, int causal, double sigma, 
     }
     for (int r = 0; r < rows; ++r) {
       const int i = i0 + r;
-      for (int k = 0; k < d; ++k) Oh[(size_t)i * d + k] = acc[(size_t)r * d + k] / l[r];
+      for (int k = 0; k < dv; ++k) Oh[(size_t)i * dv + k] = acc[(size_t)r * dv + k] / l[r];
       Lh[i] = m[r] + std::log(l[r]);
       if (Ph) {
         for (int kt = 0; kt <= ktmax; ++kt) {
@@ -402,12 +406,12 @@ int or_attn_fwd(int B, int Hq, int Hkv, int N, int d, int causal, double sigma, 
 //                its FP8 cast, O as stored by the forward;
 //   stale_dOhat  (section 03, last paragraph): delta_i = <dO^_i, O_i>.
 // LSE is the stored forward value (the caller rounds it to FP32).
-int or_attn_delta(int B, int Hq, int Hkv, int N, int d, int causal, double sigma, int flags, int mode,
+int or_attn_delta(int B, int Hq, int Hkv, int N, int d, int dv, int causal, double sigma, int flags, int mode,
                   const double* Q, const double* K, const double* V, const double* dOhat,
                   const double* dO, const double* O, const double* LSE,
                   const int* q_tiles, int n_q_tiles, const int* groups, int n_groups, double* delta) {
-  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || N < 0 || d <= 0 || mode < 0 || mode > 2) return 1;
-  Dims D{B, Hq, Hkv, N, d, causal, sigma > 0 ? sigma : 1.0 / std::sqrt((double)d)};
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || N < 0 || d <= 0 || dv <= 0 || mode < 0 || mode > 2) return 1;
+  Dims D{B, Hq, Hkv, N, d, dv, causal, sigma > 0 ? sigma : 1.0 / std::sqrt((double)d)};
   const std::vector<int> qts = tiles_or_all(q_tiles, n_q_tiles, D.T());
   const std::vector<Group> gs = groups_or_all(groups, n_groups, D);
   const int G = D.G();
@@ -418,14 +422,15 @@ int or_attn_delta(int B, int Hq, int Hkv, int N, int d, int causal, double sigma
     const int h = gr.g * G + (int)((u / qts.size()) % G);
     const int qt = qts[u % qts.size()];
     const size_t qo = D.qoff(gr.b, h), ko = D.kvoff(gr.b, gr.g), ro = D.rowoff(gr.b, h);
+    const size_t qvo = D.qvoff(gr.b, h), kvo = D.kvvoff(gr.b, gr.g);
     const int i0 = qt * kTile, rows = std::min(kTile, N - i0);
     for (int r = 0; r < rows; ++r) {
       const int i = i0 + r;
       double dl = 0.0;
       if (mode == OR_DELTA_STALE_DO) {
-        dl = dot(dO + qo + (size_t)i * d, O + qo + (size_t)i * d, d);
+        dl = dot(dO + qvo + (size_t)i * dv, O + qvo + (size_t)i * dv, dv);
       } else if (mode == OR_DELTA_STALE_DOHAT) {
-        dl = dot(dOhat + qo + (size_t)i * d, O + qo + (size_t)i * d, d);
+        dl = dot(dOhat + qvo + (size_t)i * dv, O + qvo + (size_t)i * dv, dv);
       } else {
         double psum = 0.0;
         for (int j = 0; j < N; ++j) {
@@ -433,7 +438,7 @@ int or_attn_delta(int B, int Hq, int Hkv, int N, int d, int causal, double sigma
           const double s = D.sigma * dot(Q + qo + (size_t)i * d, K + ko + (size_t)j * d, d);
           double p = std::exp(s - LSE[ro + i]);
           if (flags & OR_ROUND32) p = fl32(p);
-          const double dp = dot(dOhat + qo + (size_t)i * d, V + ko + (size_t)j * d, d);
+          const double dp = dot(dOhat + qvo + (size_t)i * dv, V + kvo + (size_t)j * dv, dv);
           dl += p * dp;
           psum += p;
         }
@@ -461,15 +466,15 @@ int or_attn_delta(int B, int Hq, int Hkv, int N, int d, int causal, double sigma
 // diag (nullable) is [4][B][Hq][N]: sum_j dS, sum_j |dS|, sum_j dS^, sum_j |dS^|.
 // dS, dShat, Phat (nullable, [B][Hq][N][N]) receive the tiles computed for
 // the selected query tiles (small test cases only).
-int or_attn_bwd(int B, int Hq, int Hkv, int N, int d, int causal, double sigma, int flags,
+int or_attn_bwd(int B, int Hq, int Hkv, int N, int d, int dv, int causal, double sigma, int flags,
                 const double* Q, const double* K, const double* V, const double* dOhat,
                 const double* LSE, const double* delta,
                 const int* q_tiles, int n_q_tiles, const int* kv_tiles, int n_kv_tiles,
                 const int* groups, int n_groups,
                 double* dQ, double* dK, double* dV, double* diag,
                 double* dS_out, double* dShat_out, double* Phat_out) {
-  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || N < 0 || d <= 0) return 1;
-  Dims D{B, Hq, Hkv, N, d, causal, sigma > 0 ? sigma : 1.0 / std::sqrt((double)d)};
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || N < 0 || d <= 0 || dv <= 0) return 1;
+  Dims D{B, Hq, Hkv, N, d, dv, causal, sigma > 0 ? sigma : 1.0 / std::sqrt((double)d)};
   const int T = D.T(), G = D.G();
   const std::vector<int> qts = tiles_or_all(q_tiles, n_q_tiles, T);
   const std::vector<int> kts = tiles_or_all(kv_tiles, n_kv_tiles, T);
@@ -484,8 +489,8 @@ int or_attn_bwd(int B, int Hq, int Hkv, int N, int d, int causal, double sigma, 
     const int g = h / G;
     const double* Qh = Q + D.qoff(b, h);
     const double* Kg = K + D.kvoff(b, g);
-    const double* Vg = V + D.kvoff(b, g);
-    const double* dOh = dOhat + D.qoff(b, h);
+    const double* Vg = V + D.kvvoff(b, g);
+    const double* dOh = dOhat + D.qvoff(b, h);
     const double* Lh = LSE + D.rowoff(b, h);
     const double* dl = delta + D.rowoff(b, h);
     std::vector<double> S;
@@ -499,7 +504,7 @@ int or_attn_bwd(int B, int Hq, int Hkv, int N, int d, int causal, double sigma, 
         if (!valid(r, c)) continue;
         double p = std::exp(S[(size_t)r * cols + c] - Lh[i0 + r]);
         if (flags & OR_ROUND32) p = fl32(p);
-        const double dp = dot(dOh + (size_t)(i0 + r) * d, Vg + (size_t)(j0 + c) * d, d);
+        const double dp = dot(dOh + (size_t)(i0 + r) * dv, Vg + (size_t)(j0 + c) * dv, dv);
         double ds = p * (dp - dl[i0 + r]);
         if (flags & OR_ROUND32) ds = fl32(ds);
         pt.P[(size_t)r * cols + c] = p;
@@ -579,14 +584,16 @@ int or_attn_bwd(int B, int Hq, int Hkv, int N, int d, int causal, double sigma, 
       const int kt = kts[u % kts.size()];
       const int j0 = kt * kTile, cols = std::min(kTile, N - j0);
       double* dKg = dK + D.kvoff(gr.b, gr.g);
-      double* dVg = dV + D.kvoff(gr.b, gr.g);
-      for (int c = 0; c < cols; ++c)
-        for (int k = 0; k < d; ++k) dKg[(size_t)(j0 + c) * d + k] = dVg[(size_t)(j0 + c) * d + k] = 0.0;
+      double* dVg = dV + D.kvvoff(gr.b, gr.g);
+      for (int c = 0; c < cols; ++c) {
+        for (int k = 0; k < d; ++k) dKg[(size_t)(j0 + c) * d + k] = 0.0;
+        for (int k = 0; k < dv; ++k) dVg[(size_t)(j0 + c) * dv + k] = 0.0;
+      }
       PairTile pt;
       for (int hh = 0; hh < G; ++hh) {
         const int h = gr.g * G + hh;
         const double* Qh = Q + D.qoff(gr.b, h);
-        const double* dOh = dOhat + D.qoff(gr.b, h);
+        const double* dOh = dOhat + D.qvoff(gr.b, h);
         for (int qt = D.causal ? kt : 0; qt < T; ++qt) {
           compute_pair(gr.b, h, qt, kt, pt);
           const int i0 = qt * kTile;
@@ -594,12 +601,12 @@ int or_attn_bwd(int B, int Hq, int Hkv, int N, int d, int causal, double sigma, 
             for (int c = 0; c < pt.cols; ++c) {
               const double ph = pt.Ph[(size_t)r * pt.cols + c];
               const double ds = pt.dSh[(size_t)r * pt.cols + c];
-              double* dv = dVg + (size_t)(j0 + c) * d;
+              double* dvr = dVg + (size_t)(j0 + c) * dv;
               double* dk = dKg + (size_t)(j0 + c) * d;
-              const double* dor = dOh + (size_t)(i0 + r) * d;
+              const double* dor = dOh + (size_t)(i0 + r) * dv;
               const double* qr = Qh + (size_t)(i0 + r) * d;
               if (ph != 0.0)
-                for (int k = 0; k < d; ++k) dv[k] += ph * dor[k];
+                for (int k = 0; k < dv; ++k) dvr[k] += ph * dor[k];
               if (ds != 0.0)
                 for (int k = 0; k < d; ++k) dk[k] += D.sigma * ds * qr[k];
             }

@@ -34,11 +34,12 @@ def _rand(shape, seed, scale=1.0):
     return np.random.default_rng(seed).standard_normal(shape) * scale
 
 
-def _case(B=1, Hq=2, Hkv=1, N=40, d=8, seed=0, qscale=1.0):
+def _case(B=1, Hq=2, Hkv=1, N=40, d=8, seed=0, qscale=1.0, dv=None):
+    dv = d if dv is None else dv
     Q = _rand((B, Hq, N, d), seed, qscale)
     K = _rand((B, Hkv, N, d), seed + 1, qscale)
-    V = _rand((B, Hkv, N, d), seed + 2)
-    dO = _rand((B, Hq, N, d), seed + 3)
+    V = _rand((B, Hkv, N, dv), seed + 2)
+    dO = _rand((B, Hq, N, dv), seed + 3)
     return Q, K, V, dO
 
 
@@ -77,6 +78,25 @@ def test_exact_matches_torch(causal, shape):
     if causal:
         s = s.masked_fill(torch.ones(N, N, dtype=torch.bool).triu(1), float("-inf"))
     np.testing.assert_allclose(LSE, torch.logsumexp(s, -1).numpy(), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("shape", [(1, 2, 1, 40, 24, 16), (2, 4, 2, 150, 16, 40), (1, 2, 1, 20, 192, 128)])
+def test_value_width_differs_matches_torch(causal, shape):
+    """Heads whose value dimension differs from the query/key one (multi-head
+    latent attention shapes): exact mode against torch's attention and
+    autograd, and the saved-output shortcut sum_j P dP = <dO, O> over dv."""
+    B, Hq, Hkv, N, d, dv = shape
+    Q, K, V, dO = _case(B, Hq, Hkv, N, d, seed=N + d, dv=dv)
+    O, LSE, delta, g = _exact_all(Q, K, V, dO, causal)
+    assert O.shape == (B, Hq, N, dv) and g["dV"].shape == V.shape and g["dK"].shape == K.shape
+    q, k, v, o = _torch_attn(Q, K, V, causal)
+    o.backward(torch.tensor(dO))
+    np.testing.assert_allclose(O, o.detach().numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(g["dQ"], q.grad.numpy(), rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(g["dK"], k.grad.numpy(), rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(g["dV"], v.grad.numpy(), rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(delta, np.sum(dO * O, axis=-1), rtol=1e-10, atol=1e-12)
 
 
 def test_explicit_sigma_matches_torch():
