@@ -96,6 +96,12 @@ def flops_of(w):
     return w.flops()
 
 
+def kernel_width(w):
+    """Head dimension of the kernels the library runs for the workload: d when
+    Q/K and V share a built width, else 256 (missing channels read as zeros)."""
+    return w.d if (w.d == w.d_v and w.d != 192) else 256
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     """nvidia-smi sampled every 200 ms while the timed region runs."""
@@ -167,7 +173,7 @@ def run_native(args, rank, world, local_rank):
         dist.init_process_group("nccl", device_id=dev)
 
     q, k, v, do = make_inputs(w)
-    p = dm.AttnParams(w.B, w.Hq, w.Hkv, w.N, w.d, causal=w.causal)
+    p = dm.AttnParams(w.B, w.Hq, w.Hkv, w.N, w.d, causal=w.causal, d_v=w.d_v)
     st = torch.cuda.Stream(dev)
     # inputs resident in HBM
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
@@ -176,12 +182,20 @@ def run_native(args, rank, world, local_rank):
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
+    def quantize(qx, kx, vx, dox, stream):
+        # one launch per head dimension (Q/K and V/dO differ for value-width heads)
+        if w.d == w.d_v:
+            return dm.dm_quantize_batch(
+                [(qx, dm.DM_E4M3), (kx, dm.DM_E4M3), (vx, dm.DM_E4M3), (dox, dm.DM_E5M2)], stream=stream)
+        qq, kk = dm.dm_quantize_batch([(qx, dm.DM_E4M3), (kx, dm.DM_E4M3)], stream=stream)
+        vv, dd = dm.dm_quantize_batch([(vx, dm.DM_E4M3), (dox, dm.DM_E5M2)], stream=stream)
+        return qq, kk, vv, dd
+
     def step(inputs, stream, times=None):
         qx, kx, vx, dox = inputs
         marks = [ev() for _ in range(5)]
         marks[0].record(stream)
-        qq, kk, vv, dd = dm.dm_quantize_batch(
-            [(qx, dm.DM_E4M3), (kx, dm.DM_E4M3), (vx, dm.DM_E4M3), (dox, dm.DM_E5M2)], stream=stream)
+        qq, kk, vv, dd = quantize(qx, kx, vx, dox, stream)
         marks[1].record(stream)
         O, lse = dm.dm_attn_fwd(p, qq, kk, vv, stream=stream)
         marks[2].record(stream)
@@ -193,7 +207,8 @@ def run_native(args, rank, world, local_rank):
             times.append(marks)
         return g
 
-    launches_per_step = 1 + 1 + 1 + 2  # quantise (Q, K, V, dO in one launch), forward, delta, zero fill + backward
+    # quantise (Q, K, V, dO in one launch; two when the widths differ), forward, delta, zero fill + backward
+    launches_per_step = (1 if w.d == w.d_v else 2) + 1 + 1 + 2
     inputs = (qd, kd, vd, dod)
     with torch.cuda.stream(st):
         for _ in range(args.warmup):
@@ -214,8 +229,7 @@ def run_native(args, rank, world, local_rank):
             pool = None
             cap = {}
             stages = [
-                lambda: cap.update(zip(("qq", "kk", "vv", "dd"), dm.dm_quantize_batch(
-                    [(qd, dm.DM_E4M3), (kd, dm.DM_E4M3), (vd, dm.DM_E4M3), (dod, dm.DM_E5M2)], stream=st))),
+                lambda: cap.update(zip(("qq", "kk", "vv", "dd"), quantize(qd, kd, vd, dod, st))),
                 lambda: cap.update(zip(("O", "lse"), dm.dm_attn_fwd(p, cap["qq"], cap["kk"], cap["vv"], stream=st))),
                 lambda: cap.update(delta=dm.dm_attn_delta(p, dm.DM_DELTA_MATCHED, cap["qq"], cap["kk"], cap["vv"],
                                                           cap["dd"], cap["lse"], stream=st)),
@@ -292,7 +306,7 @@ def run_native(args, rank, world, local_rank):
     # steps' compute (two device input slots); the L2 flush stays in front of
     # every step's compute, inside the timed region.
     h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh, doh))
-    out_shapes = {"dQ": (w.B, w.Hq, w.N, w.d), "dK": (w.B, w.Hkv, w.N, w.d), "dV": (w.B, w.Hkv, w.N, w.d)}
+    out_shapes = {"dQ": (w.B, w.Hq, w.N, w.d), "dK": (w.B, w.Hkv, w.N, w.d), "dV": (w.B, w.Hkv, w.N, w.d_v)}
     outs = [{k2: torch.empty(sh, dtype=torch.float32).pin_memory() for k2, sh in out_shapes.items()}
             for _ in range(2)]
     d2h = sum(t.numel() * t.element_size() for t in outs[0].values())
@@ -361,8 +375,10 @@ def run_native(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "fp8 (e4m3/e5m2 operands, fp32 accumulate)",
         "data": "synthetic (seeded randn, RMS-normalised Q/K, bf16 storage)",
-        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d, "causal": w.causal,
-                   "delta_mode": "matched", "flop_accounting": "issued, causal-halved, 9U per step",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d, "d_v": w.d_v,
+                   "causal": w.causal, "delta_mode": "matched",
+                   "flop_accounting": "issued, causal-halved: fwd S+O, delta S+dP, bwd S+dP+dV+dQ+dK "
+                                      "(9U per step when d_v = d)",
                    "l2": "flushed between timed steps (256 MiB write)", "parallelism": f"independent x{world}",
                    "launch": "CUDA graph of the step, replayed (per-kernel split: one graph per stage)"
                    if graphs is not None else "eager launches"},
@@ -378,7 +394,8 @@ def run_native(args, rank, world, local_rank):
                            / 1e12, 1),
         # quantisation of Q, K, V, dO: 2 B read + 1 B code written per element, plus the tile scales
         "quantize_gbs": round(quant_bytes(w) / (kernel_ms["quantize"] * 1e-3) / 1e9, 1),
-        "roofline": {"kernel": f"attn_bwd_kernel<{w.d}>", "bound": "tensor", "achieved": round(bwd_tflops, 1),
+        "roofline": {"kernel": f"attn_bwd_kernel<{kernel_width(w)}>", "bound": "tensor",
+                     "achieved": round(bwd_tflops, 1),
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(bwd_tflops / fp8_peak, 4),
                      "peak_source": f"{src} bf16 burst x {FP8_PER_BF16} (fp8/bf16 nominal ratio)",
                      "traffic": traffic},
@@ -457,11 +474,11 @@ def timed_prologue(args, w, dm, dev, st, flush, use_graph):
 
 def quant_bytes(w):
     """Algorithmic HBM bytes of quantising Q, K, V and dO (bf16 in, FP8 codes and FP32 tile scales out)."""
-    el_q = w.B * w.Hq * w.N * w.d
-    el_kv = w.B * w.Hkv * w.N * w.d
+    el_q = w.B * w.Hq * w.N * (w.d + w.d_v)     # Q and dO
+    el_kv = w.B * w.Hkv * w.N * (w.d + w.d_v)   # K and V
     tiles = (w.N + 127) // 128
     in_bytes = 2 if w.storage == "bf16" else 4
-    elements = 2 * el_q + 2 * el_kv
+    elements = el_q + el_kv
     scales = 4 * tiles * (2 * w.B * w.Hq + 2 * w.B * w.Hkv)
     return elements * (in_bytes + 1) + scales
 
@@ -490,10 +507,12 @@ def oracle_sample(w, rounds=1):
     groups = [(0, g) for g in range(w.Hkv)]
     G = w.Hq // w.Hkv
     # issued FLOPs of the sample, counted like the GPU path: per visible
-    # 128x128 tile pair one matmul is 2*128*128*d FLOPs
-    mm = 2.0 * 128 * 128 * w.d
+    # 128x128 tile pair one matmul is 2*128*128*width FLOPs, width d for S,
+    # dQ, dK and d_v for O, dP, dV
+    mm, mmv = 2.0 * 128 * 128 * w.d, 2.0 * 128 * 128 * w.d_v
     pairs_q = sum((t + 1) if w.causal else T for t in q_tiles)
-    per_head = pairs_q * (2 + 2 + 3) * mm + len(kv_tiles) * 4 * mm
+    # query tiles: forward S + O, delta S + dP, dQ pass S + dP + dQ; key tile: S + dP + dV + dK
+    per_head = pairs_q * (4 * mm + 3 * mmv) + len(kv_tiles) * (2 * mm + 2 * mmv)
     sample_flops = per_head * G * len(groups) * rounds
     t0 = time.perf_counter()
     for _ in range(rounds):
@@ -532,7 +551,7 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000 * total / args.steps, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded randn, RMS-normalised Q/K, bf16 storage)",
-        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d, "d_v": w.d_v,
                    "causal": w.causal, "delta_mode": "matched", "flop_accounting": "issued, causal-halved"},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
                          "kind": "oracle", "sample": desc},

@@ -49,7 +49,8 @@ class DMError(RuntimeError):
 
 class _Params(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("N", ctypes.c_int),
-                ("d", ctypes.c_int), ("causal", ctypes.c_int), ("softmax_scale", ctypes.c_float)]
+                ("d", ctypes.c_int), ("causal", ctypes.c_int), ("softmax_scale", ctypes.c_float),
+                ("d_v", ctypes.c_int)]
 
 
 class _Fp8(ctypes.Structure):
@@ -70,10 +71,15 @@ class AttnParams:
     d: int
     causal: bool = True
     softmax_scale: float = 0.0   # <= 0 selects 1/sqrt(d)
+    d_v: int = 0                 # head dimension of V, dO, O, dV; 0 selects d
 
     def c(self) -> _Params:
         return _Params(self.B, self.Hq, self.Hkv, self.N, self.d, int(bool(self.causal)),
-                       float(self.softmax_scale))
+                       float(self.softmax_scale), int(self.d_v))
+
+    @property
+    def dv(self) -> int:
+        return self.d_v if self.d_v else self.d
 
     @property
     def T(self) -> int:
@@ -279,10 +285,10 @@ def dm_qk_prologue_batch(tensors, rope=None, eps: float = RMS_EPS, stream=None):
 
 
 def dm_attn_fwd(p: AttnParams, q: Fp8, k: Fp8, v: Fp8, O=None, o_dtype=torch.float32, lse=None, stream=None):
-    """Forward: returns (O [B][Hq][N][d], LSE [B][Hq][N])."""
+    """Forward: returns (O [B][Hq][N][d_v], LSE [B][Hq][N])."""
     dev = q.codes.device
     if O is None:
-        O = torch.empty((p.B, p.Hq, p.N, p.d), dtype=o_dtype, device=dev)
+        O = torch.empty((p.B, p.Hq, p.N, p.dv), dtype=o_dtype, device=dev)
     if lse is None:
         lse = torch.empty((p.B, p.Hq, p.N), dtype=torch.float32, device=dev)
     cp = p.c()
@@ -319,7 +325,7 @@ def dm_attn_bwd(p: AttnParams, mode: int, q: Fp8, k: Fp8, v: Fp8, do_hat: Fp8, l
     if dK is None:
         dK = torch.empty((p.B, p.Hkv, p.N, p.d), dtype=torch.float32, device=dev)
     if dV is None:
-        dV = torch.empty((p.B, p.Hkv, p.N, p.d), dtype=torch.float32, device=dev)
+        dV = torch.empty((p.B, p.Hkv, p.N, p.dv), dtype=torch.float32, device=dev)
     out = {"dQ": dQ, "dK": dK, "dV": dV}
     cdiag = None
     if diag:
@@ -356,7 +362,7 @@ def dm_attn_bwd_noalloc(p: AttnParams, mode: int, q: Fp8, k: Fp8, v: Fp8, do_hat
     if dK is None:
         dK = torch.empty((p.B, p.Hkv, p.N, p.d), dtype=torch.float32, device=dev)
     if dV is None:
-        dV = torch.empty((p.B, p.Hkv, p.N, p.d), dtype=torch.float32, device=dev)
+        dV = torch.empty((p.B, p.Hkv, p.N, p.dv), dtype=torch.float32, device=dev)
     cp = p.c()
     rc = lib().dm_attn_bwd_noalloc(ctypes.byref(cp), int(mode), _fp8(q), _fp8(k), _fp8(v), _fp8(do_hat),
                                    _ptr(lse), _ptr(dO), _dtype(dO), _ptr(O), _dtype(O), _ptr(dQ), _ptr(dK),

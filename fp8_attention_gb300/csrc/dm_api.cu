@@ -62,10 +62,12 @@ dm_status device_state(unsigned int** status) {
   return DM_OK;
 }
 
-// FP8 codes viewed as [BH][N][d]; box = 128 rows x min(d, 128) bytes with the
-// hardware swizzle of that width (d = 256 rows are loaded as two boxes).
-dm_status encode_codes_map(CUtensorMap* m, const uint8_t* codes, int BH, int N, int d) {
-  const int box_x = d < 128 ? d : 128;
+// FP8 codes viewed as [BH][N][d]; box = 128 rows x min(kw, 128) bytes with
+// the hardware swizzle of that width, kw the kernel's head dimension (a
+// kw = 256 row is loaded as two boxes; channels from d to kw lie outside the
+// tensor and are read as zeros).
+dm_status encode_codes_map(CUtensorMap* m, const uint8_t* codes, int BH, int N, int d, int kw) {
+  const int box_x = kw < 128 ? kw : 128;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d, (cuuint64_t)d * (cuuint64_t)N};
   cuuint32_t box[3] = {(cuuint32_t)box_x, (cuuint32_t)kTileRows, 1};
@@ -89,12 +91,28 @@ dm_status encode_f32_rows_map(CUtensorMap* m, const float* x, int BH, int N, int
   return r == CUDA_SUCCESS ? DM_OK : DM_ERR_CUDA;
 }
 
+// Head dimension of V, dO, O and dV (0 selects d).
+inline int value_dim(const dm_attn_params* p) { return p->d_v ? p->d_v : p->d; }
+
+// The kernels' head dimension: d itself when Q/K and V share one of the
+// widths the kernels are built for, else 256 (missing channels read as zeros).
+inline int kernel_dim(const dm_attn_params* p) {
+  const int dv = value_dim(p);
+  return (p->d == dv && p->d != 192) ? p->d : 256;
+}
+
 dm_status check_params(const dm_attn_params* p) {
   if (!p) return DM_ERR_INVALID_ARG;
   if (p->B < 0 || p->Hq <= 0 || p->Hkv <= 0 || p->N < 0) return DM_ERR_SHAPE;
-  if (p->d != 64 && p->d != 128 && p->d != 256) return DM_ERR_SHAPE;
+  const int dv = value_dim(p);
+  auto wide = [](int x) { return x == 128 || x == 192 || x == 256; };
+  if (p->d == dv) {
+    if (p->d != 64 && !wide(p->d)) return DM_ERR_SHAPE;
+  } else if (!wide(p->d) || !wide(dv)) {
+    return DM_ERR_SHAPE;
+  }
   if (p->Hq % p->Hkv != 0) return DM_ERR_SHAPE;
-  if ((long long)p->B * p->Hq * p->N * p->d >= (1ll << 31)) return DM_ERR_SHAPE;
+  if ((long long)p->B * p->Hq * p->N * (p->d > dv ? p->d : dv) >= (1ll << 31)) return DM_ERR_SHAPE;
   if (!std::isfinite(p->softmax_scale)) return DM_ERR_INVALID_ARG;
   return DM_OK;
 }
@@ -122,6 +140,8 @@ dm::AttnArgs make_args(const dm_attn_params* p, unsigned int* status) {
   a.B = p->B, a.Hq = p->Hq, a.Hkv = p->Hkv, a.N = p->N;
   a.T = (p->N + kTileRows - 1) / kTileRows;
   a.causal = p->causal ? 1 : 0;
+  a.dqk = p->d;
+  a.dv = value_dim(p);
   a.sigma = p->softmax_scale > 0.f ? p->softmax_scale : (float)(1.0 / std::sqrt((double)p->d));
   a.status = status;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -168,18 +188,20 @@ dm_status delta_impl(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor 
   dm::AttnArgs a = make_args(p, status);
   if (mode == DM_DELTA_MATCHED) {
     dm::DeltaLaunch f{};
-    DM_TRY(encode_codes_map(&f.tmQ, q.codes, p->B * p->Hq, p->N, p->d));
-    DM_TRY(encode_codes_map(&f.tmK, k.codes, p->B * p->Hkv, p->N, p->d));
-    DM_TRY(encode_codes_map(&f.tmV, v.codes, p->B * p->Hkv, p->N, p->d));
-    DM_TRY(encode_codes_map(&f.tmDO, do_hat.codes, p->B * p->Hq, p->N, p->d));
+    const int kw = kernel_dim(p), dv = value_dim(p);
+    DM_TRY(encode_codes_map(&f.tmQ, q.codes, p->B * p->Hq, p->N, p->d, kw));
+    DM_TRY(encode_codes_map(&f.tmK, k.codes, p->B * p->Hkv, p->N, p->d, kw));
+    DM_TRY(encode_codes_map(&f.tmV, v.codes, p->B * p->Hkv, p->N, dv, kw));
+    DM_TRY(encode_codes_map(&f.tmDO, do_hat.codes, p->B * p->Hq, p->N, dv, kw));
     a.q_scales = q.scales, a.k_scales = k.scales, a.v_scales = v.scales, a.do_scales = do_hat.scales;
     f.args = a;
     f.lse = lse;
     f.delta = delta;
-    return cuda_status(dm::launch_delta_matched(f, p->d, st));
+    return cuda_status(dm::launch_delta_matched(f, kw, st));
   }
   a.do_scales = do_hat.scales;
-  return cuda_status(dm::launch_delta_stale(a, p->d, mode, dO, do_dtype, do_hat.codes, O, o_dtype, delta, st));
+  return cuda_status(
+      dm::launch_delta_stale(a, value_dim(p), mode, dO, do_dtype, do_hat.codes, O, o_dtype, delta, st));
 }
 
 }  // namespace
@@ -255,7 +277,7 @@ dm_status dm_quantize_batch(const dm_quantize_job* jobs, int njobs, dm_dtype x_d
   if (njobs == 0) return DM_OK;
   if (!jobs) return DM_ERR_INVALID_ARG;
   const int d = jobs[0].d;
-  if (d != 64 && d != 128 && d != 256) return DM_ERR_SHAPE;
+  if (d != 64 && d != 128 && d != 192 && d != 256) return DM_ERR_SHAPE;
   dm::QuantBatch b{};
   long long tiles = 0;
   for (int i = 0; i < njobs; ++i) {
@@ -284,7 +306,7 @@ dm_status dm_quantize_batch(const dm_quantize_job* jobs, int njobs, dm_dtype x_d
 dm_status dm_quantize(const void* x, dm_dtype x_dtype, int B, int H, int N, int d, dm_fp8 fmt, uint8_t* codes,
                       float* scales, uint8_t* codes_t, void* stream) {
   const dm_quantize_job job{x, B, H, N, d, fmt, codes, scales, codes_t};
-  if (d != 64 && d != 128 && d != 256) return valid_dtype(x_dtype) ? DM_ERR_SHAPE : DM_ERR_DTYPE;
+  if (d != 64 && d != 128 && d != 192 && d != 256) return valid_dtype(x_dtype) ? DM_ERR_SHAPE : DM_ERR_DTYPE;
   return dm_quantize_batch(&job, 1, x_dtype, stream);
 }
 
@@ -364,9 +386,10 @@ dm_status dm_attn_fwd(const dm_attn_params* p, dm_fp8_tensor q, dm_fp8_tensor k,
   unsigned int* status = nullptr;
   DM_TRY(device_state(&status));
   dm::FwdLaunch f{};
-  DM_TRY(encode_codes_map(&f.tmQ, q.codes, p->B * p->Hq, p->N, p->d));
-  DM_TRY(encode_codes_map(&f.tmK, k.codes, p->B * p->Hkv, p->N, p->d));
-  DM_TRY(encode_codes_map(&f.tmV, v.codes, p->B * p->Hkv, p->N, p->d));
+  const int kw = kernel_dim(p);
+  DM_TRY(encode_codes_map(&f.tmQ, q.codes, p->B * p->Hq, p->N, p->d, kw));
+  DM_TRY(encode_codes_map(&f.tmK, k.codes, p->B * p->Hkv, p->N, p->d, kw));
+  DM_TRY(encode_codes_map(&f.tmV, v.codes, p->B * p->Hkv, p->N, value_dim(p), kw));
   f.args = make_args(p, status);
   f.args.q_scales = q.scales, f.args.k_scales = k.scales, f.args.v_scales = v.scales;
   {
@@ -376,7 +399,7 @@ dm_status dm_attn_fwd(const dm_attn_params* p, dm_fp8_tensor q, dm_fp8_tensor k,
   }
   f.O = O;
   f.lse = lse;
-  return cuda_status(dm::launch_attn_fwd(f, p->d, o_dtype == DM_BF16, as_stream(stream)));
+  return cuda_status(dm::launch_attn_fwd(f, kw, o_dtype == DM_BF16, as_stream(stream)));
 }
 
 dm_status dm_attn_delta(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor q, dm_fp8_tensor k,
@@ -437,20 +460,21 @@ dm_status dm_attn_bwd(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor
   }
   // dQ, dK and dV are sums of bulk reduce-adds; the diagnostics sums of atomics
   dm::ZeroList z{};
+  const int kw = kernel_dim(p), dv = value_dim(p);
   z.add(dQ, (size_t)p->B * p->Hq * p->N * p->d);
   z.add(dK, (size_t)p->B * p->Hkv * p->N * p->d);
-  z.add(dV, (size_t)p->B * p->Hkv * p->N * p->d);
+  z.add(dV, (size_t)p->B * p->Hkv * p->N * dv);
   const size_t nrow = (size_t)p->B * p->Hq * p->N;
   for (float* ptr : {dg.rowsum_pre, dg.abssum_pre, dg.rowsum_post, dg.abssum_post}) z.add(ptr, nrow);
   DM_TRY(cuda_status(dm::launch_zero(z, st)));
   dm::BwdLaunch f{};
-  DM_TRY(encode_codes_map(&f.tmQ, q.codes, p->B * p->Hq, p->N, p->d));
-  DM_TRY(encode_codes_map(&f.tmK, k.codes, p->B * p->Hkv, p->N, p->d));
-  DM_TRY(encode_codes_map(&f.tmV, v.codes, p->B * p->Hkv, p->N, p->d));
-  DM_TRY(encode_codes_map(&f.tmDO, do_hat.codes, p->B * p->Hq, p->N, p->d));
+  DM_TRY(encode_codes_map(&f.tmQ, q.codes, p->B * p->Hq, p->N, p->d, kw));
+  DM_TRY(encode_codes_map(&f.tmK, k.codes, p->B * p->Hkv, p->N, p->d, kw));
+  DM_TRY(encode_codes_map(&f.tmV, v.codes, p->B * p->Hkv, p->N, dv, kw));
+  DM_TRY(encode_codes_map(&f.tmDO, do_hat.codes, p->B * p->Hq, p->N, dv, kw));
   DM_TRY(encode_f32_rows_map(&f.tmDQ, dQ, p->B * p->Hq, p->N, p->d));
   DM_TRY(encode_f32_rows_map(&f.tmDK, dK, p->B * p->Hkv, p->N, p->d));
-  DM_TRY(encode_f32_rows_map(&f.tmDV, dV, p->B * p->Hkv, p->N, p->d));
+  DM_TRY(encode_f32_rows_map(&f.tmDV, dV, p->B * p->Hkv, p->N, dv));
   f.args = make_args(p, status);
   f.args.q_scales = q.scales, f.args.k_scales = k.scales, f.args.v_scales = v.scales;
   f.args.do_scales = do_hat.scales;
@@ -458,7 +482,7 @@ dm_status dm_attn_bwd(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor
   f.delta = dl;
   f.dQ = dQ, f.dK = dK, f.dV = dV;
   f.diag = dg;
-  return cuda_status(dm::launch_attn_bwd(f, p->d, st));
+  return cuda_status(dm::launch_attn_bwd(f, kw, st));
 }
 
 }  // extern "C"

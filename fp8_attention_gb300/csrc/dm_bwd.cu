@@ -153,6 +153,26 @@ __device__ __forceinline__ void rescale_pair(uint32_t tdv, float fv, uint32_t td
   }
 }
 
+// dK *= fk over this warp's lanes and this warpgroup's DH columns (a CTA
+// that holds no dV columns).
+template <int DH>
+__device__ __forceinline__ void rescale_single(uint32_t tdk, float fk) {
+  static_assert(DH == 32 || DH == 64, "unsupported column split");
+  float v[64];
+  if constexpr (DH == 64)
+    tmem_load64(tdk, tdk + 32, v);
+  else
+    tmem_load32(tdk, *reinterpret_cast<float(*)[32]>(&v[0]));
+#pragma unroll
+  for (int k = 0; k < DH; k += 2) {
+    const float2 x = __fmul2_rn(make_float2(v[k], v[k + 1]), make_float2(fk, fk));
+    v[k] = x.x;
+    v[k + 1] = x.y;
+  }
+  tmem_store32(tdk, *reinterpret_cast<const float(*)[32]>(&v[0]));
+  if constexpr (DH == 64) tmem_store32(tdk + 32, *reinterpret_cast<const float(*)[32]>(&v[32]));
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -182,6 +202,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kt = (int)(blk / BH);  // key tile 0 sees the most query tiles: first
   const int bh0 = (int)(blk % BH);
   const int col0 = hf * C::kDC;  // this CTA's first d column
+  // dV columns exist only below the value head dimension (narrower than the
+  // kernel's d for heads shaped like multi-head latent attention)
+  const bool own_dv = col0 < a.dv;
   const int bg = (bh0 / a.Hq) * a.Hkv + (bh0 % a.Hq) / (a.Hq / a.Hkv);
   const int qt0 = a.causal ? kt : 0;
   const int n_iter = a.T - qt0;
@@ -368,9 +391,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait(&bars.dq_staged, g & 1, wd, 314)) break;
         const int m = g / C::kPasses, ps = g % C::kPasses;
 #pragma unroll
-        for (int bx = 0; bx < C::kStageCols / 32; ++bx)
-          tma_reduce_add_3d(&tmDQ, sm + L::kDQ + bx * (kTile * 128), col0 + ps * C::kStageCols + bx * 32,
-                            (qt0 + m) * kTile, bh0);
+        for (int bx = 0; bx < C::kStageCols / 32; ++bx) {
+          const int x = col0 + ps * C::kStageCols + bx * 32;
+          if (x < a.dqk)  // boxes beyond the head dimension hold zeros
+            tma_reduce_add_3d(&tmDQ, sm + L::kDQ + bx * (kTile * 128), x, (qt0 + m) * kTile, bh0);
+        }
         bulk_commit();
         bulk_wait_read_all();
         mbar_arrive(&bars.dq_free);
@@ -589,8 +614,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float sds = tile_scale_fast<1>(amax, rs);
       // both accumulators into the units of this iteration's products (dV/dK
       // of n - 1 completed before the drain above), after the dS codes
-      float fv, fk;
-      const int mode_dv = unit_step(unit_dv, sp * sdo, fv);
+      float fv = 1.0f, fk;
+      const int mode_dv = own_dv ? unit_step(unit_dv, sp * sdo, fv) : 0;
       const int mode_dk = unit_step(unit_dk, a.sigma * sds * sq, fk);
       auto write_ds = [&]() {
         uint32_t dcode[16];
@@ -651,7 +676,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       write_ds();
-      if (fv != 1.0f || fk != 1.0f) rescale_pair<DH>(tl + 256 + wg * DH, fv, tl + 384 + wg * DH, fk);
+      if (!own_dv) {
+        if (fk != 1.0f) rescale_single<DH>(tl + 384 + wg * DH, fk);
+      } else if (fv != 1.0f || fk != 1.0f) {
+        rescale_pair<DH>(tl + 256 + wg * DH, fv, tl + 384 + wg * DH, fk);
+      }
       if (ct == 0) {
         s_mode[bn][0] = mode_dv;
         s_mode[bn][1] = mode_dk;
@@ -671,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (after the last dQ reduce has read the staging tile) and added into
     // global dV and dK.  An accumulator that never received a contribution
     // holds garbage and is skipped.  TMEM loads are warp-collective.
-    auto reduce_acc = [&](uint32_t col, float unit, const CUtensorMap* map) {
+    auto reduce_acc = [&](uint32_t col, float unit, const CUtensorMap* map, int width) {
 #pragma unroll
       for (int ps = 0; ps < C::kPasses; ++ps) {
         if (ct == 0) bulk_wait_read_all();
@@ -694,16 +723,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           named_bar_sync(2, 256);
           if (ct == 0) {
 #pragma unroll
-            for (int bx = 0; bx < C::kStageCols / 32; ++bx)
-              tma_reduce_add_3d(map, sm + L::kDQ + bx * (kTile * 128), col0 + ps * C::kStageCols + bx * 32,
-                                kt * kTile, bg);
+            for (int bx = 0; bx < C::kStageCols / 32; ++bx) {
+              const int x = col0 + ps * C::kStageCols + bx * 32;
+              if (x < width) tma_reduce_add_3d(map, sm + L::kDQ + bx * (kTile * 128), x, kt * kTile, bg);
+            }
             bulk_commit();
           }
         }
       }
     };
-    reduce_acc(256, unit_dv, &tmDV);
-    reduce_acc(384, unit_dk, &tmDK);
+    reduce_acc(256, unit_dv, &tmDV, a.dv);
+    reduce_acc(384, unit_dk, &tmDK, a.dqk);
     if (ct == 0) bulk_wait_all();
   }
 

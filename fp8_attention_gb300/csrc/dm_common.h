@@ -13,6 +13,8 @@ constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 // Arguments common to the attention kernels (all device pointers).
 struct AttnArgs {
   int B, Hq, Hkv, N, T;      // T = ceil(N / 128)
+  int dqk, dv;               // head dimensions of Q/K and of V/dO/O; the kernel's
+                             // width may be larger (missing channels read as zeros)
   int causal;
   float sigma;               // softmax scale
   const float* q_scales;     // [B][Hq][T]

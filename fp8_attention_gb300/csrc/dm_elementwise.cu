@@ -135,6 +135,8 @@ cudaError_t quantize_t(const QuantBatch& b, int d, cudaStream_t st) {
   const unsigned grid = (unsigned)b.first_tile[b.count];
   if (d == 256)
     quantize_kernel<T, 256><<<grid, quant_threads<256>(), smem, st>>>(b);
+  else if (d == 192)
+    quantize_kernel<T, 192><<<grid, quant_threads<192>(), smem, st>>>(b);
   else if (d == 128)
     quantize_kernel<T, 128><<<grid, quant_threads<128>(), smem, st>>>(b);
   else
@@ -248,6 +250,7 @@ cudaError_t launch_delta_stale(const AttnArgs& a, int d, dm_delta_mode mode, con
                                const uint8_t* do_codes, const void* O, dm_dtype o_t, float* delta,
                                cudaStream_t st) {
   if (d == 256) return stale_d<256>(a, mode, dO, do_t, do_codes, O, o_t, delta, st);
+  if (d == 192) return stale_d<192>(a, mode, dO, do_t, do_codes, O, o_t, delta, st);
   return d == 128 ? stale_d<128>(a, mode, dO, do_t, do_codes, O, o_t, delta, st)
                   : stale_d<64>(a, mode, dO, do_t, do_codes, O, o_t, delta, st);
 }

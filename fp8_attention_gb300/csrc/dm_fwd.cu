@@ -386,18 +386,21 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
       if (lane == 0) mbar_arrive(&bars.pready);
     }
 
-    // LSE and O / l
+    // LSE and O / l; O rows are a.dv wide (the kernel's d columns of O hold
+    // zeros beyond the value head dimension)
     if (row_valid) lse[(size_t)bh * a.N + qi] = m * kLn2 + logf(l);
     wait(&bars.ofull, (nkv - 1) & 1, wd, 115);
     tc_fence_after();
     const float linv = unit / l;
+    const int dv = a.dv;
 #pragma unroll
     for (int c0 = 0; c0 < D; c0 += 64) {
+      if (c0 >= dv) break;  // uniform over the CTA
       float o[64];
       tmem_load64(tl + C::kColO + c0, tl + C::kColO + c0 + 32, o);  // warp-collective: before the row guard
       if (row_valid) {
         if (OUT_BF16) {
-          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(O) + ((size_t)bh * a.N + qi) * D + c0;
+          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(O) + ((size_t)bh * a.N + qi) * dv + c0;
 #pragma unroll
           for (int k = 0; k < 64; k += 8) {
             uint4 w;
@@ -410,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
             *reinterpret_cast<uint4*>(dst + k) = w;
           }
         } else {
-          float* dst = reinterpret_cast<float*>(O) + ((size_t)bh * a.N + qi) * D + c0;
+          float* dst = reinterpret_cast<float*>(O) + ((size_t)bh * a.N + qi) * dv + c0;
 #pragma unroll
           for (int k = 0; k < 64; k += 4)
             *reinterpret_cast<float4*>(dst + k) =

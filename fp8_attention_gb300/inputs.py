@@ -5,7 +5,8 @@ arithmetic, so both the CUDA path and the CPU oracle are fed from it.
 
 Recipe (the same for every workload): a fresh ``torch.Generator`` on the CPU
 seeded with ``seed``; draws in the order Q, K, V, dO, each ``randn`` in fp32
-of shape [B][H][N][d]; Q, K, V ~ N(0, 1) and dO = 1e-3 * N(0, 1).  Where the
+of shape [B][H][N][d] (V and dO [B][H][N][dv] where the value head dimension
+differs); Q, K, V ~ N(0, 1) and dO = 1e-3 * N(0, 1).  Where the
 workload asks for it, Q and K are RMS-normalised per (b, h, n) row,
 ``x / sqrt(mean_k x_k^2 + 1e-6) * g`` with per-channel gains g.  Storage is
 bf16 (round to nearest even) except for the tiny workload, which stays fp32.
@@ -35,6 +36,11 @@ class Workload:
     rms_norm: bool = True
     gains: dict = field(default_factory=dict)   # channel -> gain (others 1.0)
     seed: int = 0
+    dv: int = 0                    # value head dimension (V, dO, O, dV); 0 = d
+
+    @property
+    def d_v(self) -> int:
+        return self.dv if self.dv else self.d
 
     @property
     def units(self) -> int:
@@ -42,9 +48,13 @@ class Workload:
         return self.B * self.Hq * self.N * self.N * self.d
 
     def flops(self, causal_halved: bool = True) -> dict:
-        U = float(self.units)
+        """Issued FLOPs per pass.  Each matmul contracts or produces over d (S,
+        dQ, dK) or over d_v (O, dP, dV): fwd S + O, delta S + dP, bwd S + dP +
+        dV + dQ + dK, 2 B Hq N^2 x width each (halved when causal)."""
         f = 0.5 if (self.causal and causal_halved) else 1.0
-        return {"fwd": 4 * U * f, "delta": 4 * U * f, "bwd": 10 * U * f}
+        base = 2.0 * self.B * self.Hq * self.N * self.N * f
+        d, dv = self.d, self.d_v
+        return {"fwd": base * (d + dv), "delta": base * (d + dv), "bwd": base * (3 * d + 2 * dv)}
 
 
 WORKLOADS = {
@@ -57,12 +67,15 @@ WORKLOADS = {
     # head dimension 256 (the width of the gqa_b1_n8192_d128 heads, Hq * d =
     # 2048, in half as many heads; the same U)
     "gqa_b1_n8192_d256": Workload("gqa_b1_n8192_d256", 1, 8, 2, 8192, 256),
+    # heads shaped like multi-head latent attention: query/key dimension 192
+    # (128 + 64 rotary channels), value dimension 128, one kv head per query head
+    "mla_b1_n8192_d192_dv128": Workload("mla_b1_n8192_d192_dv128", 1, 16, 16, 8192, 192, dv=128),
 }
 
 
 def custom(B, Hq, Hkv, N, d, causal=True, storage="bf16", rms_norm=True, gains=None, seed=0,
-           name="custom") -> Workload:
-    return Workload(name, B, Hq, Hkv, N, d, causal, storage, rms_norm, dict(gains or {}), seed)
+           name="custom", dv=0) -> Workload:
+    return Workload(name, B, Hq, Hkv, N, d, causal, storage, rms_norm, dict(gains or {}), seed, dv)
 
 
 def _rms_norm(x: torch.Tensor, gains: dict) -> torch.Tensor:
@@ -79,8 +92,8 @@ def make_inputs(w: Workload):
     gen.manual_seed(w.seed)
     q = torch.randn(w.B, w.Hq, w.N, w.d, generator=gen, dtype=torch.float32)
     k = torch.randn(w.B, w.Hkv, w.N, w.d, generator=gen, dtype=torch.float32)
-    v = torch.randn(w.B, w.Hkv, w.N, w.d, generator=gen, dtype=torch.float32)
-    do = 1e-3 * torch.randn(w.B, w.Hq, w.N, w.d, generator=gen, dtype=torch.float32)
+    v = torch.randn(w.B, w.Hkv, w.N, w.d_v, generator=gen, dtype=torch.float32)
+    do = 1e-3 * torch.randn(w.B, w.Hq, w.N, w.d_v, generator=gen, dtype=torch.float32)
     if w.rms_norm:
         q = _rms_norm(q, w.gains)
         k = _rms_norm(k, w.gains)

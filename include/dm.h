@@ -28,7 +28,8 @@
  *  - FP8 tensors (dm_fp8_tensor) hold codes uint8 [B][H][N][d] and one FP32
  *    scale per 128-row x d tile, scales float [B][H][ceil(N/128)]; the decoded
  *    value of a code is scale * value(code).
- *  - Supported shapes: d in {64, 128, 256}; any N >= 0 (ragged tails are masked);
+ *  - Supported shapes: d = d_v in {64, 128, 192, 256}, or d != d_v with both in
+ *    {128, 192, 256} (see dm_attn_params); any N >= 0 (ragged tails are masked);
  *    Hq % Hkv == 0; B*Hq*N*d < 2^31.  B == 0 or N == 0 is a valid no-op.
  *  - Device pointers must be 16-byte aligned.
  *  - The device must be compute capability 10.3 (sm_103a build).
@@ -75,11 +76,17 @@ typedef enum {
 } dm_delta_mode;
 
 /* Problem description.  causal: key j visible to query i iff j <= i.
- * softmax_scale: sigma in S = sigma*Q*K^T; <= 0 selects 1/sqrt(d). */
+ * softmax_scale: sigma in S = sigma*Q*K^T; <= 0 selects 1/sqrt(d).
+ * d is the head dimension of Q, K, dQ and dK; d_v that of V, dO, O and dV
+ * (0 selects d).  They may differ (heads shaped like multi-head latent
+ * attention, e.g. d = 192, d_v = 128) when both are 128, 192 or 256; such
+ * heads run on the d = 256 kernels, which read the missing channels as
+ * zeros and write only the real ones. */
 typedef struct {
   int B, Hq, Hkv, N, d;
   int causal;
   float softmax_scale;
+  int d_v;
 } dm_attn_params;
 
 /* A block-scaled FP8 tensor: codes [B][H][N][d], scales [B][H][ceil(N/128)]. */

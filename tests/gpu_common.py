@@ -25,7 +25,7 @@ def gpu_pipeline(q, k, v, do, causal=True, mode=dm.DM_DELTA_MATCHED, o_dtype=tor
                  diag=False, delta_in_bwd=False):
     """Quantise, forward, delta and backward on the GPU; returns torch tensors on the GPU."""
     B, Hq, N, d = q.shape
-    p = dm.AttnParams(B, Hq, k.shape[1], N, d, causal=causal, softmax_scale=sigma)
+    p = dm.AttnParams(B, Hq, k.shape[1], N, d, causal=causal, softmax_scale=sigma, d_v=v.shape[-1])
     res = {"p": p}
     qh = dm.dm_quantize(q.to(DEV), dm.DM_E4M3)
     kh = dm.dm_quantize(k.to(DEV), dm.DM_E4M3)

@@ -51,8 +51,8 @@ def test_knobs(lib):
     assert lib.dm_set_knob(dm.DM_KNOB_WAIT_LIMIT_NS, 0) == 0
 
 
-def _p(B=1, Hq=2, Hkv=1, N=256, d=64, causal=1, scale=0.0):
-    return dm._Params(B, Hq, Hkv, N, d, causal, scale)
+def _p(B=1, Hq=2, Hkv=1, N=256, d=64, causal=1, scale=0.0, d_v=0):
+    return dm._Params(B, Hq, Hkv, N, d, causal, scale, d_v)
 
 
 def test_validation_without_gpu(lib):
@@ -62,6 +62,12 @@ def test_validation_without_gpu(lib):
     fwd = lib.dm_attn_fwd
     assert fwd(None, f, f, f, A, 0, A, None) == dm.DM_ERR_INVALID_ARG
     assert fwd(ctypes.byref(_p(d=96)), f, f, f, A, 0, A, None) == dm.DM_ERR_SHAPE
+    # value head dimension: d != d_v only with both in {128, 192, 256}
+    for d, d_v in ((192, 64), (64, 128), (128, 96), (320, 128), (192, 320)):
+        assert fwd(ctypes.byref(_p(d=d, d_v=d_v)), f, f, f, A, 0, A, None) == dm.DM_ERR_SHAPE, (d, d_v)
+    for d, d_v in ((192, 128), (256, 128), (128, 256), (192, 0), (192, 192)):
+        # passes the shape checks; stopped here by the bad dtype that follows them
+        assert fwd(ctypes.byref(_p(d=d, d_v=d_v)), f, f, f, A, 5, A, None) == dm.DM_ERR_DTYPE, (d, d_v)
     assert fwd(ctypes.byref(_p(Hq=3, Hkv=2)), f, f, f, A, 0, A, None) == dm.DM_ERR_SHAPE
     assert fwd(ctypes.byref(_p(N=-1)), f, f, f, A, 0, A, None) == dm.DM_ERR_SHAPE
     assert fwd(ctypes.byref(_p(B=1 << 20, Hq=64, Hkv=1, N=1 << 10, d=128)), f, f, f, A, 0, A, None) \
