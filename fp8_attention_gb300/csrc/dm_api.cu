@@ -101,6 +101,13 @@ inline int kernel_dim(const dm_attn_params* p) {
   return (p->d == dv && p->d != 192) ? p->d : 256;
 }
 
+// The forward's and delta pass's V/O head dimension: 128 for a 128-wide V
+// beside wider Q/K, else the kernel's head dimension.
+inline int kernel_value_dim(const dm_attn_params* p) {
+  const int kw = kernel_dim(p);
+  return (kw == 256 && value_dim(p) == 128) ? 128 : kw;
+}
+
 dm_status check_params(const dm_attn_params* p) {
   if (!p) return DM_ERR_INVALID_ARG;
   if (p->B < 0 || p->Hq <= 0 || p->Hkv <= 0 || p->N < 0) return DM_ERR_SHAPE;
@@ -197,7 +204,7 @@ dm_status delta_impl(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor 
     f.args = a;
     f.lse = lse;
     f.delta = delta;
-    return cuda_status(dm::launch_delta_matched(f, kw, st));
+    return cuda_status(dm::launch_delta_matched(f, kw, kernel_value_dim(p), st));
   }
   a.do_scales = do_hat.scales;
   return cuda_status(
@@ -399,7 +406,7 @@ dm_status dm_attn_fwd(const dm_attn_params* p, dm_fp8_tensor q, dm_fp8_tensor k,
   }
   f.O = O;
   f.lse = lse;
-  return cuda_status(dm::launch_attn_fwd(f, kw, o_dtype == DM_BF16, as_stream(stream)));
+  return cuda_status(dm::launch_attn_fwd(f, kw, kernel_value_dim(p), o_dtype == DM_BF16, as_stream(stream)));
 }
 
 dm_status dm_attn_delta(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor q, dm_fp8_tensor k,

@@ -45,14 +45,15 @@ struct DeltaCfg {
   static constexpr int kCTAsPerSM = D > 128 ? 1 : 2;
 };
 
-template <int D>
+template <int D, int DV>
 struct DeltaLayout {
-  static constexpr int kTileBytes = kTile * D;
+  static constexpr int kTileBytes = kTile * D;   // Q, K (OpTile<D>)
+  static constexpr int kVBytes = kTile * DV;     // dO, V (OpTile<DV>)
   static constexpr int kQ = 0;
   static constexpr int kDO = kQ + kTileBytes;
-  static constexpr int kK = kDO + kTileBytes;       // kKV stages
+  static constexpr int kK = kDO + kVBytes;          // kKV stages
   static constexpr int kV = kK + kKV * kTileBytes;  // kKV stages
-  static constexpr int kBars = kV + kKV * kTileBytes;
+  static constexpr int kBars = kV + kKV * kVBytes;
   static constexpr int kMisc = kBars + 256;  // tmem address, abort flag
   static constexpr int kBytes = kMisc + 16;
 };
@@ -62,12 +63,13 @@ struct DeltaBars {
 };
 static_assert(sizeof(DeltaBars) <= 256, "delta barriers");
 
-template <int D>
+// D: head dimension of Q and K; DV: of dO and V (DV <= D).
+template <int D, int DV>
 __global__ void __launch_bounds__(kThreads, DeltaCfg<D>::kCTAsPerSM)
     attn_delta_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                       const AttnArgs a, const float* __restrict__ lse, float* __restrict__ delta) {
-  using L = DeltaLayout<D>;
+  using L = DeltaLayout<D, DV>;
   using C = DeltaCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
@@ -121,9 +123,9 @@ __global__ void __launch_bounds__(kThreads, DeltaCfg<D>::kCTAsPerSM)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmDO);
-      mbar_arrive_expect_tx(&bars.q, 2 * L::kTileBytes);
+      mbar_arrive_expect_tx(&bars.q, L::kTileBytes + L::kVBytes);
       tma_load_tile<D>(sm + L::kQ, &tmQ, &bars.q, q0, bh);
-      tma_load_tile<D>(sm + L::kDO, &tmDO, &bars.q, q0, bh);
+      tma_load_tile<DV>(sm + L::kDO, &tmDO, &bars.q, q0, bh);
       int issued = 0;
       for (int t = 0; t < nkv; ++t) {
         const int s = t % kKV;
@@ -132,8 +134,8 @@ __global__ void __launch_bounds__(kThreads, DeltaCfg<D>::kCTAsPerSM)
         if (!wait(&bars.vempty[s], ph ^ 1, wd, 202)) break;
         mbar_arrive_expect_tx(&bars.kfull[s], L::kTileBytes);
         tma_load_tile<D>(sm + L::kK + s * L::kTileBytes, &tmK, &bars.kfull[s], t * kTile, bg);
-        mbar_arrive_expect_tx(&bars.vfull[s], L::kTileBytes);
-        tma_load_tile<D>(sm + L::kV + s * L::kTileBytes, &tmV, &bars.vfull[s], t * kTile, bg);
+        mbar_arrive_expect_tx(&bars.vfull[s], L::kVBytes);
+        tma_load_tile<DV>(sm + L::kV + s * L::kVBytes, &tmV, &bars.vfull[s], t * kTile, bg);
         issued = t + 1;
       }
       wait_drain(&bars.q, 0, wd, 209);
@@ -159,14 +161,14 @@ __global__ void __launch_bounds__(kThreads, DeltaCfg<D>::kCTAsPerSM)
         if (!ok) break;
         tc_fence_after();
         const uint32_t sK = smem_u32(sm + L::kK + ks * L::kTileBytes);
-        const uint32_t sV = smem_u32(sm + L::kV + ks * L::kTileBytes);
+        const uint32_t sV = smem_u32(sm + L::kV + ks * L::kVBytes);
         const uint32_t tpair = tmem + 256u * tb;
 #pragma unroll
         for (int k = 0; k < D / 32; ++k)
           mma_f8(tpair + kColS, OpTile<D>::kmajor(sQ, k), OpTile<D>::kmajor(sK, k), kIdS, k > 0);
 #pragma unroll
-        for (int k = 0; k < D / 32; ++k)
-          mma_f8(tpair + kColDP, OpTile<D>::kmajor(sDO, k), OpTile<D>::kmajor(sV, k), kIdDP, k > 0);
+        for (int k = 0; k < DV / 32; ++k)
+          mma_f8(tpair + kColDP, OpTile<DV>::kmajor(sDO, k), OpTile<DV>::kmajor(sV, k), kIdDP, k > 0);
         mma_commit(&bars.tfull[tb]);
         mma_commit(&bars.kempty[ks]);
         mma_commit(&bars.vempty[ks]);
@@ -257,10 +259,10 @@ __global__ void __launch_bounds__(kThreads, DeltaCfg<D>::kCTAsPerSM)
   }
 }
 
-template <int D>
+template <int D, int DV>
 cudaError_t launch_t(const DeltaLaunch& f, cudaStream_t st) {
-  auto k = attn_delta_kernel<D>;
-  constexpr int smem = DeltaLayout<D>::kBytes;
+  auto k = attn_delta_kernel<D, DV>;
+  constexpr int smem = DeltaLayout<D, DV>::kBytes;
   static_assert(DeltaCfg<D>::kCTAsPerSM * (smem + 1024) <= 233472, "the delta CTAs must fit in one SM's shared memory");
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -271,9 +273,9 @@ cudaError_t launch_t(const DeltaLaunch& f, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_delta_matched(const DeltaLaunch& f, int d, cudaStream_t st) {
-  if (d == 256) return launch_t<256>(f, st);
-  return d == 128 ? launch_t<128>(f, st) : launch_t<64>(f, st);
+cudaError_t launch_delta_matched(const DeltaLaunch& f, int d, int dv, cudaStream_t st) {
+  if (d == 256) return dv == 128 ? launch_t<256, 128>(f, st) : launch_t<256, 256>(f, st);
+  return d == 128 ? launch_t<128, 128>(f, st) : launch_t<64, 64>(f, st);
 }
 
 }  // namespace dm

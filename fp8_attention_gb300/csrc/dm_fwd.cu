@@ -26,7 +26,8 @@
 // below 2^-64 of the current unit adds nothing.
 //
 // TMEM columns: d <= 128: S 0-127, O 128..128+d-1 (256 allocated);
-// d = 256: S(t even) 0-127, S(t odd) 128-255, O 256-511 (512 allocated).
+// d = 256: S(t even) 0-127, S(t odd) 128-255, O from 256 (512 allocated; O
+// takes 128 columns when V is 128 wide).
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
@@ -57,13 +58,14 @@ struct FwdBars {
 
 // Everything lives in dynamic shared memory (no static shared variables), so
 // the 1024-byte aligned tile region starts at the window's base.
-template <int D>
+template <int D, int DV>
 struct FwdLayout {
-  static constexpr int kTileBytes = kTile * D;  // one FP8 Q/K/V tile (OpTile<D>)
+  static constexpr int kTileBytes = kTile * D;   // one FP8 Q or K tile (OpTile<D>)
+  static constexpr int kVBytes = kTile * DV;     // one FP8 V tile (OpTile<DV>)
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTileBytes;          // kKV stages
   static constexpr int kV = kK + kKV * kTileBytes;    // one stage
-  static constexpr int kP = kV + kTileBytes;          // 2 x (128 x 128) P^ codes
+  static constexpr int kP = kV + kVBytes;             // 2 x (128 x 128) P^ codes
   static constexpr int kRed = kP + 2 * kTile * kTile;  // float [2][4] per-warp amax exponents
   static constexpr int kMode = kRed + 2 * 4 * 4;      // int [2] per-tile P V mode
   static constexpr int kBars = kMode + 16;
@@ -90,12 +92,13 @@ __device__ __forceinline__ void rescale_o(uint32_t taddr, float f) {
   }
 }
 
-template <int D, bool OUT_BF16>
+// D: head dimension of Q and K; DV: of V and O (DV <= D).
+template <int D, int DV, bool OUT_BF16>
 __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const AttnArgs a, void* __restrict__ O,
                     float* __restrict__ lse) {
-  using L = FwdLayout<D>;
+  using L = FwdLayout<D, DV>;
   using C = FwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
@@ -170,8 +173,8 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
         if (t >= 1) {
           const int u = t - 1;
           if (!wait(&bars.vempty, (u & 1) ^ 1, wd, 102)) break;
-          mbar_arrive_expect_tx(&bars.vfull, L::kTileBytes);
-          tma_load_tile<D>(sm + L::kV, &tmV, &bars.vfull, u * kTile, bg);
+          mbar_arrive_expect_tx(&bars.vfull, L::kVBytes);
+          tma_load_tile<DV>(sm + L::kV, &tmV, &bars.vfull, u * kTile, bg);
           v_issued = u + 1;
         }
       }
@@ -185,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f8(0, 0, 0, 0, kTile, kTile);  // Q K^T, both K-major
-      constexpr uint32_t kIdO = idesc_f8(0, 0, 0, 1, kTile, D);      // P^ (K-major) V (MN-major)
+      constexpr uint32_t kIdO = idesc_f8(0, 0, 0, 1, kTile, DV);     // P^ (K-major) V (MN-major)
       bool ok = true;
       if (a.stall_test) {
         // watchdog test: a barrier nothing signals, with half the limit so
@@ -224,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
             const uint32_t sP = smem_u32(sm + L::kP + (u & 1) * kTile * kTile);
 #pragma unroll
             for (int k = 0; k < kTile / 32; ++k)
-              mma_f8(tmem + C::kColO, SwTile<128>::kmajor(sP, k), OpTile<D>::mnmajor(sV, k), kIdO,
+              mma_f8(tmem + C::kColO, SwTile<128>::kmajor(sP, k), OpTile<DV>::mnmajor(sV, k), kIdO,
                      (k > 0 || mode == 2) ? 1u : 0u);
           }
           mma_commit(&bars.ofull);
@@ -373,10 +376,10 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
         unit = c;
       } else if (c == 0.0f || !(unit / c <= 0x1p64f)) {
         mode = 0;  // nothing to add at this unit: only the softmax rescale
-        rescale_o<D>(tl + C::kColO, alpha);
+        rescale_o<DV>(tl + C::kColO, alpha);
       } else {
         mode = 2;
-        rescale_o<D>(tl + C::kColO, alpha * (unit / c));
+        rescale_o<DV>(tl + C::kColO, alpha * (unit / c));
         unit = c;
       }
       if (tid == 0) s_mode[t & 1] = mode;
@@ -394,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
     const float linv = unit / l;
     const int dv = a.dv;
 #pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 64) {
+    for (int c0 = 0; c0 < DV; c0 += 64) {
       if (c0 >= dv) break;  // uniform over the CTA
       float o[64];
       tmem_load64(tl + C::kColO + c0, tl + C::kColO + c0 + 32, o);  // warp-collective: before the row guard
@@ -431,10 +434,10 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
   }
 }
 
-template <int D, bool BF16>
+template <int D, int DV, bool BF16>
 cudaError_t launch_fwd_t(const FwdLaunch& f, cudaStream_t st) {
-  auto k = attn_fwd_kernel<D, BF16>;
-  constexpr int smem = FwdLayout<D>::kBytes;
+  auto k = attn_fwd_kernel<D, DV, BF16>;
+  constexpr int smem = FwdLayout<D, DV>::kBytes;
   static_assert(FwdCfg<D>::kCTAsPerSM * (smem + 1024) <= 233472, "the forward CTAs must fit in one SM's shared memory");
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -445,10 +448,11 @@ cudaError_t launch_fwd_t(const FwdLaunch& f, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_attn_fwd(const FwdLaunch& f, int d, bool o_bf16, cudaStream_t st) {
-  if (d == 256) return o_bf16 ? launch_fwd_t<256, true>(f, st) : launch_fwd_t<256, false>(f, st);
-  if (d == 128) return o_bf16 ? launch_fwd_t<128, true>(f, st) : launch_fwd_t<128, false>(f, st);
-  return o_bf16 ? launch_fwd_t<64, true>(f, st) : launch_fwd_t<64, false>(f, st);
+cudaError_t launch_attn_fwd(const FwdLaunch& f, int d, int dv, bool o_bf16, cudaStream_t st) {
+  if (d == 256 && dv == 128) return o_bf16 ? launch_fwd_t<256, 128, true>(f, st) : launch_fwd_t<256, 128, false>(f, st);
+  if (d == 256) return o_bf16 ? launch_fwd_t<256, 256, true>(f, st) : launch_fwd_t<256, 256, false>(f, st);
+  if (d == 128) return o_bf16 ? launch_fwd_t<128, 128, true>(f, st) : launch_fwd_t<128, 128, false>(f, st);
+  return o_bf16 ? launch_fwd_t<64, 64, true>(f, st) : launch_fwd_t<64, 64, false>(f, st);
 }
 
 }  // namespace dm

@@ -71,8 +71,10 @@ struct PrologueBatch {
 };
 cudaError_t launch_prologue(const PrologueBatch& b, dm_dtype xt, int d, float eps, cudaStream_t st);
 cudaError_t launch_rope_table(int N, int d, double base, float* cos_t, float* sin_t, cudaStream_t st);
-cudaError_t launch_attn_fwd(const FwdLaunch& f, int d, bool o_bf16, cudaStream_t st);
-cudaError_t launch_delta_matched(const DeltaLaunch& f, int d, cudaStream_t st);
+// d: the kernel's Q/K head dimension; dv: its V/O head dimension (d, or 128
+// with d = 256).
+cudaError_t launch_attn_fwd(const FwdLaunch& f, int d, int dv, bool o_bf16, cudaStream_t st);
+cudaError_t launch_delta_matched(const DeltaLaunch& f, int d, int dv, cudaStream_t st);
 cudaError_t launch_delta_stale(const AttnArgs& a, int d, dm_delta_mode mode, const void* dO, dm_dtype do_t,
                                const uint8_t* do_codes, const void* O, dm_dtype o_t, float* delta,
                                cudaStream_t st);
