@@ -205,6 +205,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // dV columns exist only below the value head dimension (narrower than the
   // kernel's d for heads shaped like multi-head latent attention)
   const bool own_dv = col0 < a.dv;
+  // dQ/dK columns this CTA holds below the query/key head dimension (split:
+  // 0, 64 or 128 of its 128; the rest hold zeros) and the dQ staging passes
+  // they need
+  const int own_qk = C::kSplit ? max(0, min(C::kDC, a.dqk - col0)) : C::kDC;
+  const int n_passes = C::kSplit ? (own_qk + C::kStageCols - 1) / C::kStageCols : C::kPasses;
   const int bg = (bh0 / a.Hq) * a.Hkv + (bh0 % a.Hq) / (a.Hq / a.Hkv);
   const int qt0 = a.causal ? kt : 0;
   const int n_iter = a.T - qt0;
@@ -387,9 +392,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // box) and frees the staging tile once the copies have read it, so that
     // no compute thread waits on the bulk copies.
     if (lane == 0) {
-      for (int g = 0; g < n_iter * C::kPasses; ++g) {
+      for (int g = 0; g < n_iter * n_passes; ++g) {
         if (!wait(&bars.dq_staged, g & 1, wd, 314)) break;
-        const int m = g / C::kPasses, ps = g % C::kPasses;
+        const int m = g / n_passes, ps = g % n_passes;
 #pragma unroll
         for (int bx = 0; bx < C::kStageCols / 32; ++bx) {
           const int x = col0 + ps * C::kStageCols + bx * 32;
@@ -453,15 +458,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The reducer warp adds each staged pass into global dQ; a pass waits
     // until it has read the one before.  Pass ps stages columns
     // [ps * kStageCols, (ps + 1) * kStageCols) of this CTA's, each warpgroup
-    // half of them.  Passes [p0, p1) run here; the TMEM buffer is released
-    // after the last.
+    // half of them.  Passes [p0, p1) of the n_passes run here; the TMEM
+    // buffer is released after the last (at once when there is none).
     auto drain_dq = [&](int m, float cdq, int p0, int p1) {
       const int bm = m & 1;
       if (p0 == 0) wait(&bars.mma2, m & 1, wd, 311);
+      if (p0 == 0 && n_passes == 0) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.bfree[bm]);
+      }
 #pragma unroll
       for (int ps = 0; ps < C::kPasses; ++ps) {
-        if (ps < p0 || ps >= p1) continue;
-        const int g = m * C::kPasses + ps;
+        if (ps < p0 || ps >= p1 || ps >= n_passes) continue;
+        const int g = m * n_passes + ps;
         if (g >= 1) wait(&bars.dq_free, (g - 1) & 1, wd, 315);
         tc_fence_after();
         // 32 columns at a time (the P registers of the current iteration are live)
@@ -481,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          if (ps == C::kPasses - 1) mbar_arrive(&bars.bfree[bm]);
+          if (ps == n_passes - 1) mbar_arrive(&bars.bfree[bm]);
           mbar_arrive(&bars.dq_staged);
         }
       }
@@ -616,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // of n - 1 completed before the drain above), after the dS codes
       float fv = 1.0f, fk;
       const int mode_dv = own_dv ? unit_step(unit_dv, sp * sdo, fv) : 0;
-      const int mode_dk = unit_step(unit_dk, a.sigma * sds * sq, fk);
+      const int mode_dk = own_qk > 0 ? unit_step(unit_dk, a.sigma * sds * sq, fk) : (fk = 1.0f, 0);
       auto write_ds = [&]() {
         uint32_t dcode[16];
         {
@@ -676,10 +686,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       write_ds();
-      if (!own_dv) {
-        if (fk != 1.0f) rescale_single<DH>(tl + 384 + wg * DH, fk);
-      } else if (fv != 1.0f || fk != 1.0f) {
-        rescale_pair<DH>(tl + 256 + wg * DH, fv, tl + 384 + wg * DH, fk);
+      if (own_dv && own_qk == C::kDC) {
+        if (fv != 1.0f || fk != 1.0f) rescale_pair<DH>(tl + 256 + wg * DH, fv, tl + 384 + wg * DH, fk);
+      } else if constexpr (C::kSplit) {
+        // a split CTA with part of the accumulators: dV whole or absent, dK
+        // whole, half (its first 64 columns, 32 per warpgroup) or absent
+        if (own_dv && fv != 1.0f) rescale_single<DH>(tl + 256 + wg * DH, fv);
+        if (fk != 1.0f) {
+          if (own_qk == C::kDC)
+            rescale_single<DH>(tl + 384 + wg * DH, fk);
+          else if (own_qk == C::kDC / 2)
+            rescale_single<DH / 2>(tl + 384 + wg * (DH / 2), fk);
+        }
       }
       if (ct == 0) {
         s_mode[bn][0] = mode_dv;
@@ -694,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (n_iter > 0) {
       drain_dq(n_iter - 1, prev_cdq, 0, C::kPasses);
-      wait(&bars.dq_free, (n_iter * C::kPasses - 1) & 1, wd, 316);  // the last dQ pass has been read
+      if (n_passes > 0) wait(&bars.dq_free, (n_iter * n_passes - 1) & 1, wd, 316);  // the last dQ pass has been read
     }
     // epilogue: this head's dV and dK tiles in true units, staged like dQ
     // (after the last dQ reduce has read the staging tile) and added into
@@ -705,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ps = 0; ps < C::kPasses; ++ps) {
         if (ct == 0) bulk_wait_read_all();
         named_bar_sync(1, 256);
-        if (unit != 0.0f) {
+        if (unit != 0.0f && (int)col0 + ps * C::kStageCols < width) {  // uniform; passes past the width hold zeros
 #pragma unroll
           for (int c = 0; c < SH; c += 32) {
             float v[32];
