@@ -43,9 +43,9 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # summarised in profiles/ (valid only for the kernel source it was taken on;
 # reported as null once dm_bwd.cu or dm_device.cuh changes).
 BWD_TRAFFIC = {
-    "gqa_b1_n8192_d128": {"sha1": "50c1a45791d9d93e772f427c56de858710cd13da", "bytes": 268120320},
-    "gqa_b1_n8192_d256": {"sha1": "50c1a45791d9d93e772f427c56de858710cd13da", "bytes": 264026624},
-    "mla_b1_n8192_d192_dv128": {"sha1": "50c1a45791d9d93e772f427c56de858710cd13da", "bytes": 1539751168},
+    "gqa_b1_n8192_d128": {"sha1": "f3e6a8887209ab35b43541ffc3ab318997007424", "bytes": 268475136},
+    "gqa_b1_n8192_d256": {"sha1": "f3e6a8887209ab35b43541ffc3ab318997007424", "bytes": 263747584},
+    "mla_b1_n8192_d192_dv128": {"sha1": "f3e6a8887209ab35b43541ffc3ab318997007424", "bytes": 1953857536},
 }
 # head dimensions the Q/K prologue is built for
 PROLOGUE_DIMS = (64, 128, 256)

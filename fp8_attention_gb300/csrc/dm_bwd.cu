@@ -203,8 +203,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bh0 = (int)(blk % BH);
   const int col0 = hf * C::kDC;  // this CTA's first d column
   // dV columns exist only below the value head dimension (narrower than the
-  // kernel's d for heads shaped like multi-head latent attention)
-  const bool own_dv = col0 < a.dv;
+  // kernel's d for heads shaped like multi-head latent attention; the
+  // unsplit kernels run only with the value dimension equal to d)
+  const bool own_dv = !C::kSplit || col0 < a.dv;
   // dQ/dK columns this CTA holds below the query/key head dimension (split:
   // 0, 64 or 128 of its 128; the rest hold zeros) and the dQ staging passes
   // they need
@@ -398,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int bx = 0; bx < C::kStageCols / 32; ++bx) {
           const int x = col0 + ps * C::kStageCols + bx * 32;
-          if (x < a.dqk)  // boxes beyond the head dimension hold zeros
+          if (!C::kSplit || x < a.dqk)  // boxes beyond the head dimension hold zeros
             tma_reduce_add_3d(&tmDQ, sm + L::kDQ + bx * (kTile * 128), x, (qt0 + m) * kTile, bh0);
         }
         bulk_commit();
@@ -723,7 +724,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ps = 0; ps < C::kPasses; ++ps) {
         if (ct == 0) bulk_wait_read_all();
         named_bar_sync(1, 256);
-        if (unit != 0.0f && (int)col0 + ps * C::kStageCols < width) {  // uniform; passes past the width hold zeros
+        // uniform; passes past the width hold zeros (split kernels only)
+        if (unit != 0.0f && (!C::kSplit || (int)col0 + ps * C::kStageCols < width)) {
 #pragma unroll
           for (int c = 0; c < SH; c += 32) {
             float v[32];
@@ -743,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int bx = 0; bx < C::kStageCols / 32; ++bx) {
               const int x = col0 + ps * C::kStageCols + bx * 32;
-              if (x < width) tma_reduce_add_3d(map, sm + L::kDQ + bx * (kTile * 128), x, kt * kTile, bg);
+              if (!C::kSplit || x < width) tma_reduce_add_3d(map, sm + L::kDQ + bx * (kTile * 128), x, kt * kTile, bg);
             }
             bulk_commit();
           }
