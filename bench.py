@@ -43,9 +43,9 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # summarised in profiles/ (valid only for the kernel source it was taken on;
 # reported as null once dm_bwd.cu or dm_device.cuh changes).
 BWD_TRAFFIC = {
-    "gqa_b1_n8192_d128": {"sha1": "f3e6a8887209ab35b43541ffc3ab318997007424", "bytes": 268475136},
-    "gqa_b1_n8192_d256": {"sha1": "f3e6a8887209ab35b43541ffc3ab318997007424", "bytes": 263747584},
-    "mla_b1_n8192_d192_dv128": {"sha1": "f3e6a8887209ab35b43541ffc3ab318997007424", "bytes": 1953857536},
+    "gqa_b1_n8192_d128": {"sha1": "f3166a04ac2435833d507e693c46adbae3f30673", "bytes": 266310400},
+    "gqa_b1_n8192_d256": {"sha1": "f3166a04ac2435833d507e693c46adbae3f30673", "bytes": 262452224},
+    "mla_b1_n8192_d192_dv128": {"sha1": "f3166a04ac2435833d507e693c46adbae3f30673", "bytes": 1962547200},
 }
 # head dimensions the Q/K prologue is built for
 PROLOGUE_DIMS = (64, 128, 256)

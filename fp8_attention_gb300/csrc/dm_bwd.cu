@@ -88,6 +88,8 @@ struct BwdLayout {
   static constexpr int kMisc = kBars + ((int)(sizeof(BwdBars) + 15) / 16) * 16;  // tmem address, abort flag
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kDynSmem = kBytes;
+  // the unsplit epilogue stages dK over the Q/dO stages
+  static_assert(C::kSplit || kPt - kQ >= kTile * C::kStageCols * 4, "Q/dO stages hold a staging tile");
 };
 
 // Column sums over the 32 lanes of a warp: on return lane l holds the sum over
@@ -719,10 +721,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (after the last dQ reduce has read the staging tile) and added into
     // global dV and dK.  An accumulator that never received a contribution
     // holds garbage and is skipped.  TMEM loads are warp-collective.
-    auto reduce_acc = [&](uint32_t col, float unit, const CUtensorMap* map, int width) {
+    // base: the staging tile; reuse: it held an earlier reduction's source
+    auto reduce_acc = [&](uint32_t col, float unit, const CUtensorMap* map, int width, uint32_t base, bool reuse) {
 #pragma unroll
       for (int ps = 0; ps < C::kPasses; ++ps) {
-        if (ct == 0) bulk_wait_read_all();
+        if (ct == 0 && (reuse || ps > 0)) bulk_wait_read_all();
         named_bar_sync(1, 256);
         // uniform; passes past the width hold zeros (split kernels only)
         if (unit != 0.0f && (!C::kSplit || (int)col0 + ps * C::kStageCols < width)) {
@@ -730,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < SH; c += 32) {
             float v[32];
             tmem_load32(tl + col + ps * C::kStageCols + wg * SH + c, v);
-            const uint32_t box = L::kDQ + ((wg * SH + c) / 32) * (kTile * 128) + rsw;
+            const uint32_t box = base + ((wg * SH + c) / 32) * (kTile * 128) + rsw;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const float2 a01 = __fmul2_rn(make_float2(v[4 * e], v[4 * e + 1]), make_float2(unit, unit));
@@ -745,15 +748,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int bx = 0; bx < C::kStageCols / 32; ++bx) {
               const int x = col0 + ps * C::kStageCols + bx * 32;
-              if (!C::kSplit || x < width) tma_reduce_add_3d(map, sm + L::kDQ + bx * (kTile * 128), x, kt * kTile, bg);
+              if (!C::kSplit || x < width) tma_reduce_add_3d(map, sm + base + bx * (kTile * 128), x, kt * kTile, bg);
             }
             bulk_commit();
           }
         }
       }
     };
-    reduce_acc(256, unit_dv, &tmDV, a.dv);
-    reduce_acc(384, unit_dk, &tmDK, a.dqk);
+    // unsplit: dK is staged in the Q/dO stages (free once the last products
+    // have completed), so both tiles' reductions are in flight together
+    reduce_acc(256, unit_dv, &tmDV, a.dv, L::kDQ, true);
+    if constexpr (C::kSplit)
+      reduce_acc(384, unit_dk, &tmDK, a.dqk, L::kDQ, true);
+    else
+      reduce_acc(384, unit_dk, &tmDK, a.dqk, L::kQ, false);
     if (ct == 0) bulk_wait_all();
   }
 
