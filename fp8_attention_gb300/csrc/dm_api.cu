@@ -142,10 +142,21 @@ bool valid_mode(dm_delta_mode m) {
   return m == DM_DELTA_MATCHED || m == DM_DELTA_STALE_DO || m == DM_DELTA_STALE_DOHAT;
 }
 
+// The backward's first key tile taken by CTAs that walk two query heads:
+// with a causal mask and an even group size, the key tiles that see at most
+// half of the query tiles (all of them up to 32 query tiles, where the
+// per-CTA fill and drain weigh more); none otherwise (equal-length CTAs
+// would only fill fewer, longer waves).
+int bwd_pair_kt(const dm_attn_params* p, int T) {
+  if (!p->causal || (p->Hq / p->Hkv) % 2 != 0) return T;
+  return T <= 32 ? 0 : T - T / 2;
+}
+
 dm::AttnArgs make_args(const dm_attn_params* p, unsigned int* status) {
   dm::AttnArgs a{};
   a.B = p->B, a.Hq = p->Hq, a.Hkv = p->Hkv, a.N = p->N;
   a.T = (p->N + kTileRows - 1) / kTileRows;
+  a.bwd_pair_kt = bwd_pair_kt(p, a.T);
   a.causal = p->causal ? 1 : 0;
   a.dqk = p->d;
   a.dv = value_dim(p);

@@ -2,7 +2,12 @@
 // ("Delta-Matching for reliable FP8 attention training", section 01, "Write
 // down softmax backward", and section 03 for delta).  One CTA per (batch,
 // query head, 128-row key tile), launched longest first; it loops over the
-// query tiles that see the key tile (iterations n).  Its dK and dV tiles (the
+// query tiles that see the key tile (iterations n).  The key tiles from
+// a.bwd_pair_kt on (the short ones under a causal mask) are taken by CTAs
+// that walk two query heads of a GQA group, head by head, so that each CTA's
+// fill and drain serve twice the work and its dV and dK sum over both heads
+// before one reduction; pairing the long ones as well would leave a longer
+// tail of CTAs at the end of the launch.  Its dK and dV tiles (the
 // head's share of the kv head's gradients) are added into global dK and dV
 // with TMA bulk reduce-adds, like dQ.  Products are computed transposed (key
 // rows on TMEM lanes) so that dV and dK accumulate in TMEM:
@@ -200,9 +205,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int BH = a.B * a.Hq;
   // split: the two halves of a key tile are neighbouring CTAs
   const int hf = C::kSplit ? (int)(blockIdx.x & 1u) : 0;
-  const unsigned blk = C::kSplit ? blockIdx.x >> 1 : blockIdx.x;
-  const int kt = (int)(blk / BH);  // key tile 0 sees the most query tiles: first
-  const int bh0 = (int)(blk % BH);
+  const int blk = (int)(C::kSplit ? blockIdx.x >> 1 : blockIdx.x);
+  // key tile 0 sees the most query tiles: first.  Key tiles below
+  // a.bwd_pair_kt have one CTA per query head, the rest one per head pair.
+  const int n_single = a.bwd_pair_kt * BH;
+  const int hpc = blk < n_single ? 1 : 2;  // query heads of this CTA
+  const int kt = blk < n_single ? blk / BH : a.bwd_pair_kt + (blk - n_single) / (BH / 2);
+  const int bh0 = blk < n_single ? blk % BH : ((blk - n_single) % (BH / 2)) * 2;  // first b * Hq + h
   const int col0 = hf * C::kDC;  // this CTA's first d column
   // dV columns exist only below the value head dimension (narrower than the
   // kernel's d for heads shaped like multi-head latent attention; the
@@ -215,7 +224,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_passes = C::kSplit ? (own_qk + C::kStageCols - 1) / C::kStageCols : C::kPasses;
   const int bg = (bh0 / a.Hq) * a.Hkv + (bh0 % a.Hq) / (a.Hq / a.Hkv);
   const int qt0 = a.causal ? kt : 0;
-  const int n_iter = a.T - qt0;
+  const int n_head = a.T - qt0;  // iterations per query head (>= 1)
+  const int n_iter = hpc * n_head;
+  // query head (b * Hq + h) and query tile of iteration n
+  auto head_of = [&](int n) { return bh0 + (hpc == 2 && n >= n_head ? 1 : 0); };
+  auto qtile_of = [&](int n) { return qt0 + (n >= n_head ? n - n_head : n); };
   // the halves of a split key tile compute the same dS: one adds the diagnostics
   const bool want_diag =
       hf == 0 && (diag.rowsum_pre || diag.abssum_pre || diag.rowsum_post || diag.abssum_post);
@@ -271,12 +284,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_tile<D>(sm + L::kK, &tmK, &bars.kv, kt * kTile, bg);
       tma_load_tile<D>(sm + L::kV, &tmV, &bars.kv, kt * kTile, bg);
       int issued = 0, o_issued = 0;
-      const int bh = bh0;
-      int qt = qt0;  // query tile of iteration n
       for (int n = 0; n < n_iter; ++n) {
         const int s = n & 1;
         const uint32_t ph = (n >> 1) & 1;
-        if (n > 0) ++qt;
+        const int bh = head_of(n), qt = qtile_of(n);
         // this CTA's columns: stage s, free once dV/dK(n-2) have read it
         if (!wait(&bars.qempty[s], ph ^ 1, wd, 301)) break;
         mbar_arrive_expect_tx(&bars.qfull[s], 2 * L::kOwnBytes);
@@ -402,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int bx = 0; bx < C::kStageCols / 32; ++bx) {
           const int x = col0 + ps * C::kStageCols + bx * 32;
           if (!C::kSplit || x < a.dqk)  // boxes beyond the head dimension hold zeros
-            tma_reduce_add_3d(&tmDQ, sm + L::kDQ + bx * (kTile * 128), x, (qt0 + m) * kTile, bh0);
+            tma_reduce_add_3d(&tmDQ, sm + L::kDQ + bx * (kTile * 128), x, qtile_of(m) * kTile, head_of(m));
         }
         bulk_commit();
         bulk_wait_read_all();
@@ -445,12 +456,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       else
         s_dl[m & 1][ct - 128] = -value;
     };
-    const int bh = bh0;
-    int qt = qt0;  // query tile of the current iteration (one query head)
-    if (n_iter > 0) stage_row(0, row_value(bh, qt0));
-    float row_next = n_iter > 1 ? row_value(bh, qt0 + 1) : 0.0f;  // staged during iteration 0
-    float pre_sq = n_iter > 0 ? a.q_scales[bh * a.T + qt] : 0.0f;
-    float pre_sdo = n_iter > 0 ? a.do_scales[bh * a.T + qt] : 0.0f;
+    if (n_iter > 0) stage_row(0, row_value(head_of(0), qtile_of(0)));
+    float row_next = n_iter > 1 ? row_value(head_of(1), qtile_of(1)) : 0.0f;  // staged during iteration 0
+    float pre_sq = n_iter > 0 ? a.q_scales[head_of(0) * a.T + qtile_of(0)] : 0.0f;
+    float pre_sdo = n_iter > 0 ? a.do_scales[head_of(0) * a.T + qtile_of(0)] : 0.0f;
     float prev_cdq = 0.0f;  // dQ scale of the previous iteration, drained one iteration late
     named_bar_sync(1, 256);
 
@@ -500,14 +509,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
 
-    for (int n = 0; n < n_iter; ++n, ++qt) {
+    for (int n = 0; n < n_iter; ++n) {
+      const int bh = head_of(n), qt = qtile_of(n);  // this iteration's query head and tile
       const int qi0 = qt * kTile;
       const int bn = n & 1;
       const uint32_t ph = (n >> 1) & 1;
       const float sq = pre_sq, sdo = pre_sdo;
       if (n + 1 < n_iter) {
-        pre_sq = a.q_scales[bh * a.T + qt + 1];
-        pre_sdo = a.do_scales[bh * a.T + qt + 1];
+        pre_sq = a.q_scales[head_of(n + 1) * a.T + qtile_of(n + 1)];
+        pre_sdo = a.do_scales[head_of(n + 1) * a.T + qtile_of(n + 1)];
       }
       const float c1 = a.sigma * sq * sk * kLog2e;
       const float cdp = sdo * svv;
@@ -574,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (n + 1 < n_iter) {
           stage_row(n + 1, row_next);
-          if (n + 2 < n_iter) row_next = row_value(bh, qt + 2);
+          if (n + 2 < n_iter) row_next = row_value(head_of(n + 2), qtile_of(n + 2));
         }
       };
       // split: the first dQ pass here, the second after dS (the reducer
@@ -780,7 +790,8 @@ cudaError_t launch_t(const BwdLaunch& f, cudaStream_t st) {
   static_assert(smem <= 232448, "backward shared memory exceeds the per-block limit");
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)(f.args.B * f.args.Hq * f.args.T * (BwdCfg<D>::kSplit ? 2 : 1));
+  const int BH = f.args.B * f.args.Hq, pk = f.args.bwd_pair_kt;
+  const unsigned grid = (unsigned)((pk * BH + (f.args.T - pk) * (BH / 2)) * (BwdCfg<D>::kSplit ? 2 : 1));
   k<<<grid, kThreads, smem, st>>>(f.tmQ, f.tmK, f.tmV, f.tmDO, f.tmDQ, f.tmDK, f.tmDV, f.args, f.lse, f.delta,
                                   f.diag);
   return cudaGetLastError();

@@ -10,6 +10,7 @@ namespace dm {
 
 constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 
+
 // Arguments common to the attention kernels (all device pointers).
 struct AttnArgs {
   int B, Hq, Hkv, N, T;      // T = ceil(N / 128)
@@ -24,6 +25,8 @@ struct AttnArgs {
   unsigned int* status;      // device status word
   unsigned long long wait_limit_ns;
   int stall_test;            // 1: the MMA warp waits on a barrier nothing signals
+  int bwd_pair_kt;           // backward: key tiles from this one on are taken by CTAs
+                             // that walk two query heads of a group (T: none)
 };
 
 }  // namespace dm
