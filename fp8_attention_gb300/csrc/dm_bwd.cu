@@ -180,7 +180,10 @@ __device__ __forceinline__ void rescale_single(uint32_t tdk, float fk) {
   if constexpr (DH == 64) tmem_store32(tdk + 32, *reinterpret_cast<const float(*)[32]>(&v[32]));
 }
 
-template <int D>
+// PARTIAL (d = 256 kernels only): the value or query/key head dimension is
+// narrower than D, so a half may own fewer dV, dK or dQ columns than its 128
+// (checked at run time); without it every half owns all of its columns.
+template <int D, bool PARTIAL>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -216,12 +219,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // dV columns exist only below the value head dimension (narrower than the
   // kernel's d for heads shaped like multi-head latent attention; the
   // unsplit kernels run only with the value dimension equal to d)
-  const bool own_dv = !C::kSplit || col0 < a.dv;
+  constexpr bool kPart = C::kSplit && PARTIAL;
+  const bool own_dv = !kPart || col0 < a.dv;
   // dQ/dK columns this CTA holds below the query/key head dimension (split:
   // 0, 64 or 128 of its 128; the rest hold zeros) and the dQ staging passes
   // they need
-  const int own_qk = C::kSplit ? max(0, min(C::kDC, a.dqk - col0)) : C::kDC;
-  const int n_passes = C::kSplit ? (own_qk + C::kStageCols - 1) / C::kStageCols : C::kPasses;
+  const int own_qk = kPart ? max(0, min(C::kDC, a.dqk - col0)) : C::kDC;
+  const int n_passes = kPart ? (own_qk + C::kStageCols - 1) / C::kStageCols : C::kPasses;
   const int bg = (bh0 / a.Hq) * a.Hkv + (bh0 % a.Hq) / (a.Hq / a.Hkv);
   const int qt0 = a.causal ? kt : 0;
   const int n_head = a.T - qt0;  // iterations per query head (>= 1)
@@ -412,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int bx = 0; bx < C::kStageCols / 32; ++bx) {
           const int x = col0 + ps * C::kStageCols + bx * 32;
-          if (!C::kSplit || x < a.dqk)  // boxes beyond the head dimension hold zeros
+          if (!kPart || x < a.dqk)  // boxes beyond the head dimension hold zeros
             tma_reduce_add_3d(&tmDQ, sm + L::kDQ + bx * (kTile * 128), x, qtile_of(m) * kTile, head_of(m));
         }
         bulk_commit();
@@ -701,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       write_ds();
       if (own_dv && own_qk == C::kDC) {
         if (fv != 1.0f || fk != 1.0f) rescale_pair<DH>(tl + 256 + wg * DH, fv, tl + 384 + wg * DH, fk);
-      } else if constexpr (C::kSplit) {
+      } else if constexpr (kPart) {
         // a split CTA with part of the accumulators: dV whole or absent, dK
         // whole, half (its first 64 columns, 32 per warpgroup) or absent
         if (own_dv && fv != 1.0f) rescale_single<DH>(tl + 256 + wg * DH, fv);
@@ -738,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ct == 0 && (reuse || ps > 0)) bulk_wait_read_all();
         named_bar_sync(1, 256);
         // uniform; passes past the width hold zeros (split kernels only)
-        if (unit != 0.0f && (!C::kSplit || (int)col0 + ps * C::kStageCols < width)) {
+        if (unit != 0.0f && (!kPart || (int)col0 + ps * C::kStageCols < width)) {
 #pragma unroll
           for (int c = 0; c < SH; c += 32) {
             float v[32];
@@ -758,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int bx = 0; bx < C::kStageCols / 32; ++bx) {
               const int x = col0 + ps * C::kStageCols + bx * 32;
-              if (!C::kSplit || x < width) tma_reduce_add_3d(map, sm + base + bx * (kTile * 128), x, kt * kTile, bg);
+              if (!kPart || x < width) tma_reduce_add_3d(map, sm + base + bx * (kTile * 128), x, kt * kTile, bg);
             }
             bulk_commit();
           }
@@ -783,9 +787,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool PARTIAL>
 cudaError_t launch_t(const BwdLaunch& f, cudaStream_t st) {
-  auto k = attn_bwd_kernel<D>;
+  auto k = attn_bwd_kernel<D, PARTIAL>;
   constexpr int smem = BwdLayout<D>::kDynSmem;
   static_assert(smem <= 232448, "backward shared memory exceeds the per-block limit");
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -800,8 +804,9 @@ cudaError_t launch_t(const BwdLaunch& f, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_attn_bwd(const BwdLaunch& f, int d, cudaStream_t st) {
-  if (d == 256) return launch_t<256>(f, st);
-  return d == 128 ? launch_t<128>(f, st) : launch_t<64>(f, st);
+  if (d == 256)
+    return (f.args.dqk == 256 && f.args.dv == 256) ? launch_t<256, false>(f, st) : launch_t<256, true>(f, st);
+  return d == 128 ? launch_t<128, false>(f, st) : launch_t<64, false>(f, st);
 }
 
 }  // namespace dm
