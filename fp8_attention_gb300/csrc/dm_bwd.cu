@@ -7,8 +7,8 @@
 // that walk two query heads of a GQA group, head by head, so that each CTA's
 // fill and drain serve twice the work and its dV and dK sum over both heads
 // before one reduction; pairing the long ones as well would leave a longer
-// tail of CTAs at the end of the launch.  Its dK and dV tiles (the
-// head's share of the kv head's gradients) are added into global dK and dV
+// tail of CTAs at the end of the launch.  A CTA's dK and dV tiles (its
+// heads' share of the kv head's gradients) are added into global dK and dV
 // with TMA bulk reduce-adds, like dQ.  Products are computed transposed (key
 // rows on TMEM lanes) so that dV and dK accumulate in TMEM:
 //   S^T  = K Q^T                 P  = exp(S - LSE) in FP32,   P^  = E4M3 per 128x128 tile
@@ -35,8 +35,8 @@
 // dV, dK and dQ of 128 key/query rows x 256 columns, plus the work buffers,
 // do not fit one SM's 512 TMEM columns.  Each half owns 128 of the d columns
 // of dV, dK and dQ (its accumulators take the same TMEM columns as d = 128)
-// and computes S and dP itself over the full d (two K steps per sub-tile, the
-// products dV, dK, dQ only over its columns).  Shared memory (227 KB) holds K
+// and computes S and dP itself over the full d (four K steps on each
+// 128-column sub-tile; the products dV, dK, dQ only over its columns).  Shared memory (227 KB) holds K
 // and V whole, this half's columns of Q and dO in two stages, the other
 // columns in one stage (needed only by S and dP, which finish early in an
 // iteration), one P^ and one dS^ code tile, and a 64-column dQ staging tile
@@ -49,7 +49,7 @@
 namespace dm {
 namespace {
 
-constexpr int kThreads = 384;  // warps 0-3: TMA, MMA, two idle; warps 4-11: compute
+constexpr int kThreads = 384;  // warps 0-3: TMA, MMA, dQ reducer, idle; warps 4-11: compute
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMinUnit = 0x1p-100f;
 
