@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("fmt", [dm.DM_E4M3, dm.DM_E5M2])
 @pytest.mark.parametrize("shape", [(1, 2, 256, 64), (2, 3, 200, 128), (1, 1, 77, 64), (1, 2, 1, 128),
-                                   (3, 4, 1000, 128)])
+                                   (3, 4, 1000, 128), (1, 2, 300, 192), (2, 1, 129, 256), (1, 1, 5, 256)])
 def test_quantize_bit_exact(dtype, fmt, shape):
     g = torch.Generator().manual_seed(sum(shape) + fmt)
     x = torch.randn(shape, generator=g) * torch.exp(torch.randn(shape[:3] + (1,), generator=g) * 4)
