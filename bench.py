@@ -43,9 +43,9 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # summarised in profiles/ (valid only for the kernel source it was taken on;
 # reported as null once dm_bwd.cu or dm_device.cuh changes).
 BWD_TRAFFIC = {
-    "gqa_b1_n8192_d128": {"sha1": "1b28567e4845b6fe3046a3b84fa389b5730a5787", "bytes": 264656640},
-    "gqa_b1_n8192_d256": {"sha1": "1b28567e4845b6fe3046a3b84fa389b5730a5787", "bytes": 261586944},
-    "mla_b1_n8192_d192_dv128": {"sha1": "1b28567e4845b6fe3046a3b84fa389b5730a5787", "bytes": 1999222784},
+    "gqa_b1_n8192_d128": {"sha1": "9326d58103d94ee75d90212ca108624860506c9c", "bytes": 263727104},
+    "gqa_b1_n8192_d256": {"sha1": "9326d58103d94ee75d90212ca108624860506c9c", "bytes": 261324032},
+    "mla_b1_n8192_d192_dv128": {"sha1": "9326d58103d94ee75d90212ca108624860506c9c", "bytes": 1987614464},
 }
 # head dimensions the Q/K prologue is built for
 PROLOGUE_DIMS = (64, 128, 256)

@@ -93,8 +93,9 @@ struct BwdLayout {
   static constexpr int kMisc = kBars + ((int)(sizeof(BwdBars) + 15) / 16) * 16;  // tmem address, abort flag
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kDynSmem = kBytes;
-  // the unsplit epilogue stages dK over the Q/dO stages
+  // the unsplit epilogue stages dK over the Q/dO stages and dV over the code tiles
   static_assert(C::kSplit || kPt - kQ >= kTile * C::kStageCols * 4, "Q/dO stages hold a staging tile");
+  static_assert(C::kSplit || kDQ - kPt >= kTile * C::kStageCols * 4, "code tiles hold a staging tile");
 };
 
 // Column sums over the 32 lanes of a warp: on return lane l holds the sum over
@@ -729,7 +730,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (n_iter > 0) {
       drain_dq(n_iter - 1, prev_cdq, 0, C::kPasses);
-      if (n_passes > 0) wait(&bars.dq_free, (n_iter * n_passes - 1) & 1, wd, 316);  // the last dQ pass has been read
+      // split: the epilogue stages over the dQ staging tile, which the
+      // reducer must have read (unsplit: dV and dK go elsewhere; the reducer
+      // waits for its own copies before the CTA exits)
+      if (C::kSplit && n_passes > 0) wait(&bars.dq_free, (n_iter * n_passes - 1) & 1, wd, 316);
     }
     // epilogue: this head's dV and dK tiles in true units, staged like dQ
     // (after the last dQ reduce has read the staging tile) and added into
@@ -769,13 +773,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     };
-    // unsplit: dK is staged in the Q/dO stages (free once the last products
-    // have completed), so both tiles' reductions are in flight together
-    reduce_acc(256, unit_dv, &tmDV, a.dv, L::kDQ, true);
-    if constexpr (C::kSplit)
+    // unsplit: dV is staged over the P/dS code tiles and dK over the Q/dO
+    // stages (both free once the last products have completed), so the two
+    // reductions are in flight together and neither waits for the reducer
+    // to have read the last dQ tile
+    if constexpr (C::kSplit) {
+      reduce_acc(256, unit_dv, &tmDV, a.dv, L::kDQ, true);
       reduce_acc(384, unit_dk, &tmDK, a.dqk, L::kDQ, true);
-    else
+    } else {
+      reduce_acc(256, unit_dv, &tmDV, a.dv, L::kPt, false);
       reduce_acc(384, unit_dk, &tmDK, a.dqk, L::kQ, false);
+    }
     if (ct == 0) bulk_wait_all();
   }
 
