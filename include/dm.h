@@ -179,14 +179,15 @@ typedef struct {
 dm_status dm_qk_prologue_batch(const dm_prologue_job* jobs, int njobs, dm_dtype x_dtype, float eps, void* stream);
 
 /* dm_attn_fwd -- O = P^ V^ and LSE (section 01).  q, k, v: E4M3 tensors of
- * shapes [B][Hq][N][d], [B][Hkv][N][d], [B][Hkv][N][d].  O: [B][Hq][N][d] of
- * o_dtype (DM_F32 or DM_BF16).  lse: float [B][Hq][N], natural log of the
+ * shapes [B][Hq][N][d], [B][Hkv][N][d], [B][Hkv][N][d_v].  O: [B][Hq][N][d_v]
+ * of o_dtype (DM_F32 or DM_BF16).  lse: float [B][Hq][N], natural log of the
  * softmax denominator including the scale sigma, i.e. LSE_i = ln sum_j
  * exp(S_ij).  O and LSE are the only saved forward outputs. */
 dm_status dm_attn_fwd(const dm_attn_params* p, dm_fp8_tensor q, dm_fp8_tensor k, dm_fp8_tensor v,
                       void* O, dm_dtype o_dtype, float* lse, void* stream);
 
 /* dm_attn_delta -- the softmax row correction, float delta [B][Hq][N].
+ * dO, do_hat and O are [B][Hq][N][d_v].
  *  DM_DELTA_MATCHED:     needs q, k, v, do_hat (E5M2), lse; recomputes S and
  *                        dP^ = dO^ V^T tile by tile in FP32 (the separate
  *                        correction pass).  dO and O may be NULL.
@@ -201,8 +202,8 @@ dm_status dm_attn_delta(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tens
  * FP8.  delta: float [B][Hq][N] from dm_attn_delta, or NULL, in which case it
  * is computed first for `mode` into `workspace` (which then needs
  * dm_attn_bwd_workspace_size(p) bytes, 16-byte aligned).  dQ float
- * [B][Hq][N][d] (overwritten, not accumulated), dK and dV float
- * [B][Hkv][N][d] (summed over each kv head's query heads).  diag: optional
+ * [B][Hq][N][d] (overwritten, not accumulated), dK float [B][Hkv][N][d] and
+ * dV float [B][Hkv][N][d_v] (summed over each kv head's query heads).  diag: optional
  * row-sum diagnostics (NULL = off).  dO/O are needed only when delta is NULL
  * and the mode is stale.  */
 dm_status dm_attn_bwd(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor q, dm_fp8_tensor k,
