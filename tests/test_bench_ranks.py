@@ -62,5 +62,11 @@ def test_reference_arm_under_two_ranks(rank):
         assert len(lines) == 1
         line = json.loads(lines[0])
         assert line["impl"] == "reference" and line["n_gpus"] == 2
+        assert line["unit"] == "TFLOP/s" and line["higher_is_better"] is True and line["value"] > 0
+        assert line["config"]["workload"] == "tiny_gqa_n256_d64" and line["warmup"] == 0 and line["steps"] == 1
+        cb = line["cpu_baseline"]
+        assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1 and cb["sample"]
+        assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                               "d2h_bytes_per_step": 0}
     else:
         assert lines == []
