@@ -389,6 +389,9 @@ def run_native(args, rank, world, local_rank):
             "fwd": round(fl["fwd"] / (kernel_ms["fwd"] * 1e-3) / 1e12, 1),
             "delta": round(fl["delta"] / (kernel_ms["delta"] * 1e-3) / 1e12, 1),
             "bwd": round(bwd_tflops, 1)},
+        # each attention kernel's issued TFLOP/s as a fraction of the FP8 peak
+        "per_kernel_frac": {k2: round(fl[k2] / (kernel_ms[k2] * 1e-3) / 1e12 / fp8_peak, 4)
+                            for k2 in ("fwd", "delta", "bwd")},
         # the flash-attention convention: fwd + bwd = 7U over the attention
         # kernels' time (the delta pass counted as part of the backward)
         "tflops_7U": round((fl["fwd"] + fl["bwd"]) / ((kernel_ms["fwd"] + kernel_ms["delta"] + kernel_ms["bwd"]) * 1e-3)
