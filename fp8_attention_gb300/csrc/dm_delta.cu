@@ -28,6 +28,7 @@
 #include <type_traits>
 
 #include "dm_device.cuh"
+#include "dm_pdl.cuh"
 #include "dm_internal.h"
 
 namespace dm {
@@ -115,6 +116,7 @@ __global__ void __launch_bounds__(kThreads, DeltaCfg<D>::kCTAsPerSM)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  grid_dependency_sync();  // barriers and TMEM are set up; inputs of earlier kernels from here on
   const uint32_t tmem = *s_tmem;
 
   if (warp == 4) {
@@ -267,8 +269,7 @@ cudaError_t launch_t(const DeltaLaunch& f, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(f.args.B * f.args.Hq * f.args.T);
-  k<<<grid, kThreads, smem, st>>>(f.tmQ, f.tmK, f.tmV, f.tmDO, f.args, f.lse, f.delta);
-  return cudaGetLastError();
+  return launch_overlapped(k, grid, kThreads, smem, st, f.tmQ, f.tmK, f.tmV, f.tmDO, f.args, f.lse, f.delta);
 }
 
 }  // namespace

@@ -11,6 +11,7 @@
 #include <cuda_bf16.h>
 
 #include "dm_device.cuh"
+#include "dm_pdl.cuh"
 #include "dm_internal.h"
 
 namespace dm {
@@ -58,6 +59,7 @@ __global__ void __launch_bounds__(quant_threads<D>()) quantize_kernel(const Quan
   __shared__ float s_red[kQThreads / 32];
   extern __shared__ __align__(16) uint8_t s_codes[];  // [kTile * D] when a transposed copy is wanted
 
+  grid_dependency_sync();
   int j = 0;
   while (j + 1 < batch.count && (int)blockIdx.x >= batch.first_tile[j + 1]) ++j;
   const QuantJob& job = batch.job[j];

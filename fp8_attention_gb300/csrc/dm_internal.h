@@ -5,9 +5,30 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "dm_common.h"
 
 namespace dm {
+
+// Launches kernel `k` with programmatic stream serialisation: it may start
+// while the kernel before it in the stream finishes, and waits for that
+// kernel's completion in grid_dependency_sync() before touching global memory.
+template <typename... P, typename... A>
+inline cudaError_t launch_overlapped(void (*k)(P...), unsigned grid, unsigned threads, size_t smem,
+                                     cudaStream_t st, A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, std::forward<A>(args)...);
+}
 
 struct FwdLaunch {
   CUtensorMap tmQ, tmK, tmV;  // [B*H][N][d] FP8 codes, box 128 x d, hardware swizzle of width d
