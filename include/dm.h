@@ -23,6 +23,13 @@
  *    entry point it looks up once and a device status word.
  *  - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *    stream) and is asynchronous; the call returns after the launches.
+ *    Stream order holds as usual.  The forward and delta kernels are launched
+ *    with programmatic stream serialisation: their blocks may be scheduled
+ *    while the previous kernel of the stream finishes, but they touch no
+ *    memory until it has completed.  The quantiser, forward and delta kernels
+ *    allow a following kernel that was itself launched that way to be
+ *    scheduled early; such a kernel must wait (griddepcontrol.wait) before it
+ *    reads their outputs.
  *  - Arguments are validated before any launch.  On an error nothing is
  *    launched and no output is touched.
  *  - FP8 tensors (dm_fp8_tensor) hold codes uint8 [B][H][N][d] and one FP32
