@@ -17,9 +17,11 @@ Every array here is numpy, laid out [B][H][N][d] (d fastest).  FP8 formats:
 * ``EXACT``        none: plain attention in FP64
 
 Parity status: every function below is pinned by ``tests/test_oracle_*.py``
-(see the module docstrings there); nothing here is "parity unpinned" except
-the full-size dK/dV of the 65536-token workload, which tests only check
-through invariants.
+(see the module docstrings there): the backward's per-tile P^ and dS^
+quantisation and the one-pass forward over several key tiles by
+``tests/test_oracle_tile_pins.py`` (torch-cast emulations on exact grid
+inputs).  Nothing here is "parity unpinned" except the full-size dK/dV of the
+65536-token workload, which tests only check through invariants.
 """
 from __future__ import annotations
 

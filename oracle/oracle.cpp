@@ -22,7 +22,9 @@
 // central finite differences and torch autograd in FP64; the identities of
 // sections 01-03 (saved-output shortcut, zero row sum, shift invariance, the
 // two-term split of the stale residual, dS_stale = dS_centered + eps*P); the
-// attention-input prologue against textbook rotary values, the rotation as
+// backward's P^ / dS^ tile quantisation and the multi-tile one-pass forward
+// against independent torch-cast emulations on exact grid inputs
+// (tests/test_oracle_tile_pins.py); the attention-input prologue against textbook rotary values, the rotation as
 // complex multiplication, the relative-position property and the RMSNorm
 // invariants (tests/test_oracle_prologue.py).
 
