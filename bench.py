@@ -80,6 +80,7 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of the captured step")
+    ap.add_argument("--no-fp8-peak", action="store_true", help="skip the dense FP8 GEMM peak measurement")
     return ap.parse_args()
 
 
@@ -351,12 +352,28 @@ def run_native(args, rank, world, local_rank):
     prologue_line = timed_prologue(args, w, dm, dev, st, flush, graphs is not None) \
         if w.d in PROLOGUE_DIMS else {"skipped": f"the prologue is built for d in {PROLOGUE_DIMS}"}
 
+    # ---- outside the step: the stale-delta passes (HBM-bound row dots), the
+    # per-row dS diagnostics in the three delta modes, and the dense FP8 peak
+    with torch.cuda.stream(st):
+        qq, kk, vv, dd = quantize(qd, kd, vd, dod, st)
+        O_fwd, lse_fwd = dm.dm_attn_fwd(p, qq, kk, vv, stream=st)
+    torch.cuda.synchronize(dev)
+    stale_line = timed_stale_delta(args, w, dm, p, dev, st, flush, qq, kk, vv, dd, lse_fwd, dod, O_fwd)
+    diag_line = row_sum_diagnostics(w, dm, p, st, qq, kk, vv, dd, lse_fwd, dod, O_fwd)
+    del qq, kk, vv, dd, O_fwd, lse_fwd
+    fp8_line = measure_fp8_peak(dev) if not args.no_fp8_peak else {"skipped": "--no-fp8-peak"}
+
     fl = flops_of(w)
     step_flops = fl["fwd"] + fl["delta"] + fl["bwd"]
     ms_per_step = total_ms / args.steps
     value = world * step_flops / (ms_per_step * 1e-3) / 1e12
     mp, src = peaks()
-    fp8_peak = FP8_PER_BF16 * float(mp.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    # the FP8 peak the fractions use: the larger of the dense FP8 GEMM rate
+    # measured here and the bf16 peak x 2 (so that no fraction is flattered)
+    stand_in = FP8_PER_BF16 * float(mp.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    measured = fp8_line.get("burst_tflops")
+    fp8_peak = max(stand_in, measured or 0.0)
+    peak_name = "measured fp8 burst" if measured and measured >= stand_in else f"{src} bf16 burst x {FP8_PER_BF16}"
     kernel_ms = {name: statistics.mean(x[i] for x in per)
                  for i, name in enumerate(("quantize", "fwd", "delta", "bwd"))}
     bwd_tflops = fl["bwd"] / (kernel_ms["bwd"] * 1e-3) / 1e12
@@ -384,14 +401,23 @@ def run_native(args, rank, world, local_rank):
                    "launch": "CUDA graph of the step, replayed (per-kernel split: one graph per stage)"
                    if graphs is not None else "eager launches"},
         "pct_of_fp8_peak": round(100.0 * value / (world * fp8_peak), 2),
+        "fp8_peak": {"used_tflops": round(fp8_peak, 1), "used": peak_name, "stand_in_tflops": round(stand_in, 1),
+                     "stand_in": f"{src} bf16 burst x {FP8_PER_BF16} (nominal fp8/bf16 ratio)", "measured": fp8_line,
+                     "pct_stand_in": round(100.0 * value / (world * stand_in), 2),
+                     "pct_measured": round(100.0 * value / (world * measured), 2) if measured else None},
         "per_kernel_ms": {k2: round(v2, 4) for k2, v2 in kernel_ms.items()},
         "per_kernel_tflops": {
             "fwd": round(fl["fwd"] / (kernel_ms["fwd"] * 1e-3) / 1e12, 1),
             "delta": round(fl["delta"] / (kernel_ms["delta"] * 1e-3) / 1e12, 1),
             "bwd": round(bwd_tflops, 1)},
         # each attention kernel's issued TFLOP/s as a fraction of the FP8 peak
+        # used, and of each of the two candidates
         "per_kernel_frac": {k2: round(fl[k2] / (kernel_ms[k2] * 1e-3) / 1e12 / fp8_peak, 4)
                             for k2 in ("fwd", "delta", "bwd")},
+        "per_kernel_frac_by_peak": {
+            name: ({k2: round(fl[k2] / (kernel_ms[k2] * 1e-3) / 1e12 / pk, 4) for k2 in ("fwd", "delta", "bwd")}
+                   if pk else None)
+            for name, pk in (("stand_in", stand_in), ("measured", measured))},
         # the flash-attention convention: fwd + bwd = 7U over the attention
         # kernels' time (the delta pass counted as part of the backward)
         "tflops_7U": round((fl["fwd"] + fl["bwd"]) / ((kernel_ms["fwd"] + kernel_ms["delta"] + kernel_ms["bwd"]) * 1e-3)
@@ -401,8 +427,12 @@ def run_native(args, rank, world, local_rank):
         "roofline": {"kernel": f"attn_bwd_kernel<{kernel_width(w)}>", "bound": "tensor",
                      "achieved": round(bwd_tflops, 1),
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s", "frac": round(bwd_tflops / fp8_peak, 4),
-                     "peak_source": f"{src} bf16 burst x {FP8_PER_BF16} (fp8/bf16 nominal ratio)",
-                     "traffic": traffic},
+                     "peak_source": peak_name + " (the larger of the two; see fp8_peak)",
+                     "traffic": traffic,
+                     "traffic_source": "DRAM bytes of one launch from a recorded ncu capture of this kernel source "
+                                       "(null once the source differs)"},
+        "stale_delta": stale_line,
+        "diagnostics": diag_line,
         "e2e": {"value": round(world * step_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                 "steps": e2e_steps,
@@ -474,6 +504,133 @@ def timed_prologue(args, w, dm, dev, st, flush, use_graph):
             "gbs_clean_l2": round(prologue_bytes(w) / (pro_clean_ms * 1e-3) / 1e9, 1),
             "timed": "alone (one launch, replayed as a CUDA graph), after the step's timed region; "
                      "ms after the 256 MiB write flush, ms_clean_l2 after a 256 MiB read sweep"}
+
+
+def measure_fp8_peak(dev, n=8192, burst_reps=10, sustained_s=1.0):
+    """Dense FP8 (E4M3 x E4M3, fp32 accumulate) GEMM rate of this GPU, n^3, through
+    torch._scaled_mm (cuBLASLt): the best of `burst_reps` single calls, and the mean
+    over about `sustained_s` of back-to-back calls with the clocks sampled."""
+    import torch
+    try:
+        g = torch.Generator(device=dev).manual_seed(0)
+        a = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn)
+        one = torch.ones((), device=dev)
+        mm = lambda: torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        for _ in range(5):
+            mm()
+        torch.cuda.synchronize(dev)
+        best = float("inf")
+        for _ in range(burst_reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            mm()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            best = min(best, e0.elapsed_time(e1))
+        flops = 2.0 * n ** 3
+        reps = max(10, int(sustained_s / (best * 1e-3)))
+        with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                mm()
+            e1.record()
+            torch.cuda.synchronize(dev)
+        sustained = flops * reps / (e0.elapsed_time(e1) * 1e-3) / 1e12
+        del a, b
+        return {"burst_tflops": round(flops / (best * 1e-3) / 1e12, 1), "sustained_tflops": round(sustained, 1),
+                "how": f"torch._scaled_mm e4m3 x e4m3 -> bf16, {n}^3, best of {burst_reps} (burst); "
+                       f"{reps} back to back (sustained)", "clocks": clk.summary()}
+    except (RuntimeError, TypeError) as exc:   # FP8 GEMM not available in this torch build
+        return {"burst_tflops": None, "error": str(exc).splitlines()[0][:200]}
+
+
+def stale_delta_bytes(w, mode_name):
+    """Algorithmic HBM bytes of one stale-delta pass: per query element dO (bf16, 2 B) or its
+    E5M2 code (1 B), and O (fp32, 4 B); 4 B of delta per row (+ the dO tile scales)."""
+    el = w.B * w.Hq * w.N * w.d_v
+    rows = w.B * w.Hq * w.N
+    if mode_name == "stale_dO":
+        return el * (2 + 4) + 4 * rows
+    return el * (1 + 4) + 4 * rows + 4 * w.B * w.Hq * ((w.N + 127) // 128)
+
+
+def timed_stale_delta(args, w, dm, p, dev, st, flush, qq, kk, vv, dd, lse, do_dev, O):
+    """Times each stale-delta pass alone (one launch, replayed as a CUDA graph, after
+    the L2 write flush) and reports its HBM throughput against the copy peak."""
+    import torch
+    mp, _ = peaks()
+    hbm = float(mp.get("hbm_gbs", 6800.0))
+    out = {}
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    for name, mode in (("stale_dO", dm.DM_DELTA_STALE_DO), ("stale_dOhat", dm.DM_DELTA_STALE_DOHAT)):
+        delta = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=dev)
+        call = lambda: dm.dm_attn_delta(p, mode, qq, kk, vv, dd, lse, dO=do_dev, O=O, delta=delta, stream=st)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=st):
+            call()
+        marks = []
+        with torch.cuda.stream(st):
+            for i in range(3 + max(3, min(args.steps, 50))):
+                flush.zero_()
+                a, b = ev(), ev()
+                a.record(st)
+                graph.replay()
+                b.record(st)
+                if i >= 3:
+                    marks.append((a, b))
+        torch.cuda.synchronize(dev)
+        ms = statistics.mean(a.elapsed_time(b) for a, b in marks)
+        nbytes = stale_delta_bytes(w, name)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"ms": round(ms, 4), "bytes": nbytes, "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 3)}
+    if dm.dm_get_status(st) != 0:
+        raise RuntimeError("device status error in the stale-delta passes")
+    out["timed"] = "alone, one launch replayed as a CUDA graph after the 256 MiB L2 write flush; O fp32 from the forward"
+    return out
+
+
+def row_sum_diagnostics(w, dm, p, st, qq, kk, vv, dd, lse, do_dev, O):
+    """Per-row sums of dS before and after its E5M2 cast in the three delta
+    modes (project page section 03: the matched correction brings the pre-cast
+    row sums back to zero within FP32 rounding; the authors' probes put the
+    post-cast residual of stale delta 5.3-6.3x above Delta-Matching's)."""
+    import torch
+    res = {}
+    for name, mode in (("matched", dm.DM_DELTA_MATCHED), ("stale_dO", dm.DM_DELTA_STALE_DO),
+                       ("stale_dOhat", dm.DM_DELTA_STALE_DOHAT)):
+        delta = dm.dm_attn_delta(p, mode, qq, kk, vv, dd, lse, dO=do_dev, O=O, stream=st)
+        g = dm.dm_attn_bwd(p, mode, qq, kk, vv, dd, lse, delta, diag=True, stream=st)
+        torch.cuda.synchronize()
+        rs_pre, ab_pre = g["rowsum_pre"].double(), g["abssum_pre"].double()
+        rs_post, ab_post = g["rowsum_post"].double(), g["abssum_post"].double()
+        live_pre, live_post = ab_pre > 0, ab_post > 0
+        rel_pre = rs_pre.abs()[live_pre] / ab_pre[live_pre]
+        rel_post = rs_post.abs()[live_post] / ab_post[live_post]
+        entry = {"mean_rel_rowsum_pre": float(rel_pre.mean()), "max_rel_rowsum_pre": float(rel_pre.max()),
+                 "mean_rel_rowsum_post": float(rel_post.mean()), "rows": int(rs_pre.numel())}
+        if name == "matched":
+            d64 = delta.double()
+            within = rs_pre.abs() <= 1e-4 * ab_pre
+            fp32_term = rs_pre.abs() <= 1e-4 * ab_pre + 2.0 ** -20 * d64.abs()
+            entry.update({"rows_within_1e-4": int(within.sum()),
+                          "rows_within_1e-4_plus_fp32_term": int(fp32_term.sum()),
+                          "max_abs_rowsum_over_abs_delta_outside_1e-4":
+                              float((rs_pre.abs()[~within] / d64.abs()[~within]).max()) if (~within).any() else None})
+        res[name] = entry
+        del g, delta
+    if dm.dm_get_status(st) != 0:
+        raise RuntimeError("device status error in the diagnostics")
+    m = res["matched"]
+    res["ratio_stale_over_matched"] = {
+        "post_cast": {k: round(res[k]["mean_rel_rowsum_post"] / m["mean_rel_rowsum_post"], 3)
+                      for k in ("stale_dO", "stale_dOhat")},
+        "pre_cast": {k: round(res[k]["mean_rel_rowsum_pre"] / m["mean_rel_rowsum_pre"], 1)
+                     for k in ("stale_dO", "stale_dOhat")},
+        "pages": "5.3-6.3x post-cast (the authors' kernel probes; workload not stated)",
+        "measure": "mean over rows of |sum_j dS_ij| / sum_j |dS_ij|, stale / matched"}
+    return res
 
 
 def quant_bytes(w):

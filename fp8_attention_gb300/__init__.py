@@ -12,6 +12,7 @@ scales float32 [B][H][ceil(N/128)], both contiguous CUDA tensors.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -165,6 +166,19 @@ def _stream(stream) -> Optional[int]:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def _on(dev):
+    """Makes `dev` the current CUDA device around a library call: the library
+    keeps per-device state (the status word, the no-allocation array) and looks
+    it up on the current device, so tensors on another GPU must switch to it."""
+    dev = torch.device(dev)
+    if dev.type != "cuda":
+        return contextlib.nullcontext()
+    idx = dev.index if dev.index is not None else torch.cuda.current_device()
+    if idx == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(idx)
+
+
 def _check(rc: int, where: str):
     if rc != DM_OK:
         raise DMError(rc, where)
@@ -203,8 +217,9 @@ def dm_quantize(x: torch.Tensor, fmt: int, codes=None, scales=None, codes_t=None
         scales = torch.empty((B, H, T), dtype=torch.float32, device=x.device)
     if want_transposed and codes_t is None:
         codes_t = torch.empty((B, H, d, N), dtype=torch.uint8, device=x.device)
-    rc = lib().dm_quantize(_ptr(x), _dtype(x), B, H, N, d, int(fmt), _ptr(codes), _ptr(scales), _ptr(codes_t),
-                           _stream(stream))
+    with _on(x.device):
+        rc = lib().dm_quantize(_ptr(x), _dtype(x), B, H, N, d, int(fmt), _ptr(codes), _ptr(scales),
+                               _ptr(codes_t), _stream(stream))
     _check(rc, "dm_quantize")
     out = Fp8(codes, scales)
     return (out, codes_t) if codes_t is not None else out
@@ -233,7 +248,8 @@ def dm_quantize_batch(tensors, stream=None):
     if any(_dtype(x) != dtype for x, _ in tensors):
         raise DMError(DM_ERR_DTYPE, "dm_quantize_batch: tensors of different dtypes")
     arr = (_QuantJob * len(jobs))(*jobs)
-    rc = lib().dm_quantize_batch(arr, len(jobs), dtype, _stream(stream))
+    with _on(tensors[0][0].device):
+        rc = lib().dm_quantize_batch(arr, len(jobs), dtype, _stream(stream))
     _check(rc, "dm_quantize_batch")
     return outs
 
@@ -247,7 +263,8 @@ def dm_rope_table(N: int, d: int, base: float = ROPE_BASE, device="cuda", stream
     """cos and sin of the rotary angles n * base^(-2i/d): two float32 tensors [N][d/2] on the device."""
     cos = torch.empty((N, d // 2), dtype=torch.float32, device=device)
     sin = torch.empty((N, d // 2), dtype=torch.float32, device=device)
-    rc = lib().dm_rope_table(int(N), int(d), float(base), _ptr(cos), _ptr(sin), _stream(stream))
+    with _on(cos.device):
+        rc = lib().dm_rope_table(int(N), int(d), float(base), _ptr(cos), _ptr(sin), _stream(stream))
     _check(rc, "dm_rope_table")
     return cos, sin
 
@@ -279,7 +296,8 @@ def dm_qk_prologue_batch(tensors, rope=None, eps: float = RMS_EPS, stream=None):
     if any(_dtype(x) != dtype for x, _ in tensors):
         raise DMError(DM_ERR_DTYPE, "dm_qk_prologue_batch: tensors of different dtypes")
     arr = (_PrologueJob * len(jobs))(*jobs)
-    rc = lib().dm_qk_prologue_batch(arr, len(jobs), dtype, float(eps), _stream(stream))
+    with _on(tensors[0][0].device):
+        rc = lib().dm_qk_prologue_batch(arr, len(jobs), dtype, float(eps), _stream(stream))
     _check(rc, "dm_qk_prologue_batch")
     return outs
 
@@ -292,8 +310,9 @@ def dm_attn_fwd(p: AttnParams, q: Fp8, k: Fp8, v: Fp8, O=None, o_dtype=torch.flo
     if lse is None:
         lse = torch.empty((p.B, p.Hq, p.N), dtype=torch.float32, device=dev)
     cp = p.c()
-    rc = lib().dm_attn_fwd(ctypes.byref(cp), _fp8(q), _fp8(k), _fp8(v), _ptr(O), _dtype(O), _ptr(lse),
-                           _stream(stream))
+    with _on(dev):
+        rc = lib().dm_attn_fwd(ctypes.byref(cp), _fp8(q), _fp8(k), _fp8(v), _ptr(O), _dtype(O), _ptr(lse),
+                               _stream(stream))
     _check(rc, "dm_attn_fwd")
     return O, lse
 
@@ -305,8 +324,10 @@ def dm_attn_delta(p: AttnParams, mode: int, q: Fp8, k: Fp8, v: Fp8, do_hat: Fp8,
     if delta is None:
         delta = torch.empty((p.B, p.Hq, p.N), dtype=torch.float32, device=ref.device)
     cp = p.c()
-    rc = lib().dm_attn_delta(ctypes.byref(cp), int(mode), _fp8(q), _fp8(k), _fp8(v), _fp8(do_hat), _ptr(lse),
-                             _ptr(dO), _dtype(dO), _ptr(O), _dtype(O), _ptr(delta), _stream(stream))
+    with _on(delta.device):
+        rc = lib().dm_attn_delta(ctypes.byref(cp), int(mode), _fp8(q), _fp8(k), _fp8(v), _fp8(do_hat),
+                                 _ptr(lse), _ptr(dO), _dtype(dO), _ptr(O), _dtype(O), _ptr(delta),
+                                 _stream(stream))
     _check(rc, "dm_attn_delta")
     return delta
 
@@ -314,6 +335,20 @@ def dm_attn_delta(p: AttnParams, mode: int, q: Fp8, k: Fp8, v: Fp8, do_hat: Fp8,
 def dm_attn_bwd_workspace_size(p: AttnParams) -> int:
     cp = p.c()
     return int(lib().dm_attn_bwd_workspace_size(ctypes.byref(cp)))
+
+
+def _diag(p: AttnParams, diag, dev, out: dict):
+    """The dm_diag struct for `diag` (False: none; True: four new row-sum
+    buffers; a dict: the caller's buffers by name), recording them in `out`."""
+    if not diag:
+        return None
+    names = ("rowsum_pre", "abssum_pre", "rowsum_post", "abssum_post")
+    if isinstance(diag, dict):
+        bufs = {n: diag.get(n) for n in names}
+    else:
+        bufs = {n: torch.empty((p.B, p.Hq, p.N), dtype=torch.float32, device=dev) for n in names}
+    out.update({n: t for n, t in bufs.items() if t is not None})
+    return _Diag(*[_ptr(bufs[n]) for n in names])
 
 
 def dm_attn_bwd(p: AttnParams, mode: int, q: Fp8, k: Fp8, v: Fp8, do_hat: Fp8, lse, delta=None, dO=None,
@@ -327,15 +362,7 @@ def dm_attn_bwd(p: AttnParams, mode: int, q: Fp8, k: Fp8, v: Fp8, do_hat: Fp8, l
     if dV is None:
         dV = torch.empty((p.B, p.Hkv, p.N, p.dv), dtype=torch.float32, device=dev)
     out = {"dQ": dQ, "dK": dK, "dV": dV}
-    cdiag = None
-    if diag:
-        names = ("rowsum_pre", "abssum_pre", "rowsum_post", "abssum_post")
-        if isinstance(diag, dict):
-            bufs = {n: diag.get(n) for n in names}
-        else:
-            bufs = {n: torch.empty((p.B, p.Hq, p.N), dtype=torch.float32, device=dev) for n in names}
-        cdiag = _Diag(*[_ptr(bufs[n]) for n in names])
-        out.update({n: t for n, t in bufs.items() if t is not None})
+    cdiag = _diag(p, diag, dev, out)
     ws_bytes = 0
     if delta is None:
         ws_bytes = dm_attn_bwd_workspace_size(p)
@@ -343,19 +370,20 @@ def dm_attn_bwd(p: AttnParams, mode: int, q: Fp8, k: Fp8, v: Fp8, do_hat: Fp8, l
             workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
         ws_bytes = workspace.numel() * workspace.element_size()
     cp = p.c()
-    rc = lib().dm_attn_bwd(ctypes.byref(cp), int(mode), _fp8(q), _fp8(k), _fp8(v), _fp8(do_hat), _ptr(lse),
-                           _ptr(delta), _ptr(dO), _dtype(dO), _ptr(O), _dtype(O), _ptr(dQ), _ptr(dK), _ptr(dV),
-                           ctypes.byref(cdiag) if cdiag is not None else None, _ptr(workspace), ws_bytes,
-                           _stream(stream))
+    with _on(dev):
+        rc = lib().dm_attn_bwd(ctypes.byref(cp), int(mode), _fp8(q), _fp8(k), _fp8(v), _fp8(do_hat), _ptr(lse),
+                               _ptr(delta), _ptr(dO), _dtype(dO), _ptr(O), _dtype(O), _ptr(dQ), _ptr(dK),
+                               _ptr(dV), ctypes.byref(cdiag) if cdiag is not None else None, _ptr(workspace),
+                               ws_bytes, _stream(stream))
     _check(rc, "dm_attn_bwd")
     return out
 
 
 def dm_attn_bwd_noalloc(p: AttnParams, mode: int, q: Fp8, k: Fp8, v: Fp8, do_hat: Fp8, lse, dO=None, O=None,
-                        dQ=None, dK=None, dV=None, stream=None):
+                        dQ=None, dK=None, dV=None, diag=False, stream=None):
     """Backward with delta computed for `mode` in the library's fixed device array (no
-    workspace, no allocation inside the call; the outputs here are allocated by torch only
-    when the caller passes none)."""
+    workspace, no allocation inside the call; the outputs and diagnostic buffers here are
+    allocated by torch only when the caller passes none)."""
     dev = lse.device
     if dQ is None:
         dQ = torch.empty((p.B, p.Hq, p.N, p.d), dtype=torch.float32, device=dev)
@@ -363,9 +391,13 @@ def dm_attn_bwd_noalloc(p: AttnParams, mode: int, q: Fp8, k: Fp8, v: Fp8, do_hat
         dK = torch.empty((p.B, p.Hkv, p.N, p.d), dtype=torch.float32, device=dev)
     if dV is None:
         dV = torch.empty((p.B, p.Hkv, p.N, p.dv), dtype=torch.float32, device=dev)
+    out = {"dQ": dQ, "dK": dK, "dV": dV}
+    cdiag = _diag(p, diag, dev, out)
     cp = p.c()
-    rc = lib().dm_attn_bwd_noalloc(ctypes.byref(cp), int(mode), _fp8(q), _fp8(k), _fp8(v), _fp8(do_hat),
-                                   _ptr(lse), _ptr(dO), _dtype(dO), _ptr(O), _dtype(O), _ptr(dQ), _ptr(dK),
-                                   _ptr(dV), None, _stream(stream))
+    with _on(dev):
+        rc = lib().dm_attn_bwd_noalloc(ctypes.byref(cp), int(mode), _fp8(q), _fp8(k), _fp8(v), _fp8(do_hat),
+                                       _ptr(lse), _ptr(dO), _dtype(dO), _ptr(O), _dtype(O), _ptr(dQ), _ptr(dK),
+                                       _ptr(dV), ctypes.byref(cdiag) if cdiag is not None else None,
+                                       _stream(stream))
     _check(rc, "dm_attn_bwd_noalloc")
-    return {"dQ": dQ, "dK": dK, "dV": dV}
+    return out

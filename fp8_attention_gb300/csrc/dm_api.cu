@@ -224,6 +224,11 @@ dm_status delta_impl(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor 
 
 }  // namespace
 
+dm_status dm::check_attn_problem(const dm_attn_params* p, dm_delta_mode mode) {
+  DM_TRY(check_params(p));
+  return valid_mode(mode) ? DM_OK : DM_ERR_INVALID_ARG;
+}
+
 extern "C" {
 
 int dm_version(void) { return 100; }

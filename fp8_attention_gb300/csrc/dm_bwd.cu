@@ -22,9 +22,12 @@
 // S(n+1), [dV dK dQ](n) and dP(n+1) while the compute warps work on n:
 //   cols 0-127 work buffer 0, 128-255 work buffer 1, 256.. dV, 384.. dK.
 // dV and dK accumulate in units of the current iteration's scale product
-// (s_P * s_dO, resp. sigma * s_dS * s_Q): before each accumulation the compute
-// warps rescale the accumulator by old/new unit.  Iterations whose product is
-// below 2^-100 (a flushed or negligible tile) add nothing.
+// (s_P * s_dO, resp. s_dS * sigma * s_Q): before each accumulation the compute
+// warps rescale the accumulator by old/new unit.  Each unit is held as its two
+// factors, so that neither a unit nor a ratio of two units leaves the FP32
+// range for any tile scales the quantiser produces (down to its 2^-96 flush).
+// An iteration adds nothing when one of its scales is zero (a flushed tile)
+// or its product is below 2^-64 of the accumulator's unit.
 //
 // Warp roles (384 threads): warp 0 TMA, warp 1 MMA, warp 2 the dQ reducer,
 // warp 3 idle (each warpgroup starts at a multiple of four warps), warps 4-11
@@ -51,7 +54,6 @@ namespace {
 
 constexpr int kThreads = 384;  // warps 0-3: TMA, MMA, dQ reducer, idle; warps 4-11: compute
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kMinUnit = 0x1p-100f;
 
 struct BwdBars {
   uint64_t kv, qfull[2], qempty[2], sfull[2], sread[2], dpfull[2], bfree[2], pds, mma2, mma_done, dq_staged,
@@ -121,18 +123,32 @@ __device__ __forceinline__ float max8(const float (&v)[8]) {
 }
 
 // Unit bookkeeping for one TMEM accumulator; every compute thread holds an
-// identical copy.  Sets f to the factor the accumulator must be multiplied by
-// (1 when it stays) and returns the MMA mode: 0 skip, 1 overwrite,
-// 2 accumulate.
-__device__ __forceinline__ int unit_step(float& unit, float c, float& f) {
+// identical copy.  The accumulator's true value is ua * ub * D_tmem; the
+// iteration's product comes in units ca * cb (ra = 1 / ca, known from the
+// tile's quantisation).  Sets f to the factor the accumulator must be
+// multiplied by (1 when it stays) and returns the MMA mode: 0 skip,
+// 1 overwrite, 2 accumulate.
+__device__ __forceinline__ int unit_step(float& ua, float& ub, float ca, float ra, float cb, float& f) {
   f = 1.0f;
-  if (!(c >= kMinUnit)) return 0;
-  if (unit == 0.0f) {
-    unit = c;
+  if (ca == 0.0f || cb == 0.0f) return 0;  // a flushed tile adds exactly nothing
+  if (ua == 0.0f) {
+    ua = ca;
+    ub = cb;
     return 1;
   }
-  f = unit / c;
-  unit = c;
+  f = (ua * ra) * __fdividef(ub, cb);  // unit / c
+  if (!(f >= 0x1p-100f && f <= 0x1p64f)) {
+    // out of the common range (or a ratio of the factors out of FP32 range):
+    // decide on the logarithm
+    const float lg = (__log2f(ua) - __log2f(ca)) + (__log2f(ub) - __log2f(cb));
+    if (lg > 64.0f) {  // below 2^-64 of the accumulator's unit
+      f = 1.0f;
+      return 0;
+    }
+    f = ex2(lg);  // a tiny factor only shrinks what the new product outweighs
+  }
+  ua = ca;
+  ub = cb;
   return 2;
 }
 
@@ -440,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ct = tid - 128;  // 0..255
     const float sk = a.k_scales[bg * a.T + kt];
     const float svv = a.v_scales[bg * a.T + kt];
-    float unit_dv = 0.0f, unit_dk = 0.0f;
+    float udv_a = 0.0f, udv_b = 0.0f, udk_a = 0.0f, udk_b = 0.0f;  // accumulator units (two factors each)
     // Per-iteration global values are loaded one iteration ahead: this
     // thread's element of the query tile's LSE (threads 0-127; +inf for absent
     // rows) or delta (threads 128-255; 0 for absent rows), and the tile's Q and
@@ -643,8 +659,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // both accumulators into the units of this iteration's products (dV/dK
       // of n - 1 completed before the drain above), after the dS codes
       float fv = 1.0f, fk;
-      const int mode_dv = own_dv ? unit_step(unit_dv, sp * sdo, fv) : 0;
-      const int mode_dk = own_qk > 0 ? unit_step(unit_dk, a.sigma * sds * sq, fk) : (fk = 1.0f, 0);
+      const int mode_dv = own_dv ? unit_step(udv_a, udv_b, sp, rp, sdo, fv) : 0;
+      // 1 / s = FMAX / amax = the tile's code reciprocal r
+      const int mode_dk = own_qk > 0 ? unit_step(udk_a, udk_b, sds, rs, a.sigma * sq, fk) : (fk = 1.0f, 0);
       auto write_ds = [&]() {
         uint32_t dcode[16];
         {
@@ -740,13 +757,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // global dV and dK.  An accumulator that never received a contribution
     // holds garbage and is skipped.  TMEM loads are warp-collective.
     // base: the staging tile; reuse: it held an earlier reduction's source
-    auto reduce_acc = [&](uint32_t col, float unit, const CUtensorMap* map, int width, uint32_t base, bool reuse) {
+    auto reduce_acc = [&](uint32_t col, float ua, float ub, const CUtensorMap* map, int width, uint32_t base,
+                          bool reuse) {
 #pragma unroll
       for (int ps = 0; ps < C::kPasses; ++ps) {
         if (ct == 0 && (reuse || ps > 0)) bulk_wait_read_all();
         named_bar_sync(1, 256);
         // uniform; passes past the width hold zeros (split kernels only)
-        if (unit != 0.0f && (!kPart || (int)col0 + ps * C::kStageCols < width)) {
+        if (ua != 0.0f && (!kPart || (int)col0 + ps * C::kStageCols < width)) {
 #pragma unroll
           for (int c = 0; c < SH; c += 32) {
             float v[32];
@@ -754,8 +772,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t box = base + ((wg * SH + c) / 32) * (kTile * 128) + rsw;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              const float2 a01 = __fmul2_rn(make_float2(v[4 * e], v[4 * e + 1]), make_float2(unit, unit));
-              const float2 a23 = __fmul2_rn(make_float2(v[4 * e + 2], v[4 * e + 3]), make_float2(unit, unit));
+              // two products, so that the unit's factors never underflow together
+              const float2 a01 = __fmul2_rn(__fmul2_rn(make_float2(v[4 * e], v[4 * e + 1]), make_float2(ua, ua)),
+                                            make_float2(ub, ub));
+              const float2 a23 = __fmul2_rn(__fmul2_rn(make_float2(v[4 * e + 2], v[4 * e + 3]), make_float2(ua, ua)),
+                                            make_float2(ub, ub));
               *reinterpret_cast<float4*>(sm + (box ^ (16u * e))) =
                   make_float4(a01.x, a01.y, a23.x, a23.y);
             }
@@ -778,11 +799,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // reductions are in flight together and neither waits for the reducer
     // to have read the last dQ tile
     if constexpr (C::kSplit) {
-      reduce_acc(256, unit_dv, &tmDV, a.dv, L::kDQ, true);
-      reduce_acc(384, unit_dk, &tmDK, a.dqk, L::kDQ, true);
+      reduce_acc(256, udv_a, udv_b, &tmDV, a.dv, L::kDQ, true);
+      reduce_acc(384, udk_a, udk_b, &tmDK, a.dqk, L::kDQ, true);
     } else {
-      reduce_acc(256, unit_dv, &tmDV, a.dv, L::kPt, false);
-      reduce_acc(384, unit_dk, &tmDK, a.dqk, L::kQ, false);
+      reduce_acc(256, udv_a, udv_b, &tmDV, a.dv, L::kPt, false);
+      reduce_acc(384, udk_a, udk_b, &tmDK, a.dqk, L::kQ, false);
     }
     if (ct == 0) bulk_wait_all();
   }

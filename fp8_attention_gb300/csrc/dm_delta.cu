@@ -87,8 +87,11 @@ __global__ void __launch_bounds__(kThreads, DeltaCfg<D>::kCTAsPerSM)
   const int q0 = qt * kTile;
   const int nkv = a.causal ? qt + 1 : a.T;
 
-  // the swizzled tiles need a 1024-byte aligned window (no static shared variables)
+  // the swizzled tiles need a 1024-byte aligned window (no static shared
+  // variables); the status word is written only after the wait for the
+  // previous kernel, like every other global access of this kernel
   if (smem_u32(smem_raw) & 1023u) {
+    grid_dependency_sync();
     if (tid == 0) atomicCAS(a.status, 0u, (unsigned)DM_ERR_UNSUPPORTED);
     return;
   }

@@ -22,8 +22,13 @@
 // Each key tile brings its own FP32 scale product c_t = s_P,t * s_V,t.  O is
 // kept in TMEM in units of the latest c: before tile t's product is added,
 // every row is multiplied by alpha_t * c_{t-1} / c_t (alpha_t the online
-// softmax rescale).  A tile whose product is zero (flushed P or V tile) or
-// below 2^-64 of the current unit adds nothing.
+// softmax rescale).  The unit is held as its two factors (s_P and s_V of the
+// tile it came from), so that neither the unit nor a ratio of two units
+// leaves the FP32 range for any pair of tile scales the quantiser produces.
+// A tile adds nothing when its product is zero (a flushed P or V tile), or
+// when alpha_t * c_{t-1} / c_t exceeds 2^64 in every row (its contribution is
+// below 2^-64 of every row's accumulator unit); a row whose maximum jumped in
+// tile t (alpha_t tiny) keeps the tile however small c_t is.
 //
 // TMEM columns: d <= 128: S 0-127, O 128..128+d-1 (256 allocated);
 // d = 256: S(t even) 0-127, S(t odd) 128-255, O from 256 (512 allocated; O
@@ -118,8 +123,11 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
   const int q0 = qt * kTile;
   const int nkv = a.causal ? qt + 1 : a.T;
 
-  // the swizzled tiles need a 1024-byte aligned window (no static shared variables)
+  // the swizzled tiles need a 1024-byte aligned window (no static shared
+  // variables); the status word is written only after the wait for the
+  // previous kernel, like every other global access of this kernel
   if (smem_u32(smem_raw) & 1023u) {
+    grid_dependency_sync();
     if (tid == 0) atomicCAS(a.status, 0u, (unsigned)DM_ERR_UNSUPPORTED);
     return;
   }
@@ -250,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
     const float* vsc = a.v_scales + (size_t)bg * a.T;
     float sk_next = ksc[0], sv_next = vsc[0];  // per-tile scales, loaded one tile ahead
     float m = -INFINITY, l = 0.0f;             // running max (log2 units), row sum
-    float unit = 0.0f;                         // O in true units = unit * O_tmem
+    float u_p = 0.0f, u_v = 0.0f;              // O in true units = u_p * u_v * O_tmem
 
     for (int t = 0; t < nkv; ++t) {
       const float c1 = a.sigma * sq * sk_next * kLog2e;
@@ -312,6 +320,43 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
       float r;
       const float sp = tile_scale_fast<0>(amax, r);
       const float alpha = ex2(m - m_new);
+      // How O enters the units of this tile's product (uniform over the CTA:
+      // the scales are the same for every row, only alpha differs; the
+      // largest rise of a row maximum in this tile is max(xmax, 0)), decided
+      // here so that fewer values stay live across the code conversion.
+      // mode 0: the tile adds nothing (O *= alpha); 1: O holds nothing yet
+      // (or only zeros), overwrite; 2: O *= g, then accumulate.
+      int mode;
+      float g = alpha;
+      if (u_p == 0.0f) {
+        mode = 1;
+      } else if (sp == 0.0f || sv == 0.0f) {
+        mode = 0;  // a flushed P or V tile adds exactly nothing
+      } else {
+        // unit / c, with 1 / s_P = r (the tile's code reciprocal); up to 2^64
+        // every row accumulates (its factor is at most unit / c)
+        const float ratio = (u_p * r) * (u_v / sv);
+        if (ratio <= 0x1p64f) {
+          mode = 2;
+          g = alpha * ratio;
+        } else {
+          // the smallest per-row factor is 2^(lg - max rise), lg = log2(unit / c)
+          const float lg = (__log2f(u_p) - __log2f(sp)) + (__log2f(u_v) - __log2f(sv));
+          if (lg - fmaxf(xmax, 0.0f) > 64.0f) {
+            mode = 0;  // below 2^-64 of every row's accumulator unit
+          } else {
+            mode = 2;
+            g = alpha * ratio;
+            // a ratio of the factors out of range (inf, or 0 * inf): the same
+            // factor from its logarithm, capped where FP32 ends
+            if (!(g <= 0x1p100f)) g = ex2(fminf((m - m_new) + lg, 126.0f));
+          }
+        }
+      }
+      if (mode != 0) {
+        u_p = sp;
+        u_v = sv;
+      }
 
       // P~ r = exp2(S c1 - m + log2 r) straight into E4M3 codes (P buffer
       // t%2, last read by P V(t-2), whose completion this thread saw before
@@ -365,25 +410,12 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
       l = alpha * l + (rs2.x + rs2.y) * sp;
       m = m_new;
 
-      // O into the units of this tile's product (uniform decisions over the
-      // CTA: c and unit are the same for every row, only alpha differs)
-      const float c = sp * sv;
+      // O into the units of this tile's product
       if (t >= 1) {
         wait(&bars.ofull, (t - 1) & 1, wd, 114);  // P V(t-1) has been added into O
         tc_fence_after();
       }
-      int mode;
-      if (t == 0 || unit == 0.0f) {
-        mode = 1;  // O holds nothing yet (or only zeros): overwrite
-        unit = c;
-      } else if (c == 0.0f || !(unit / c <= 0x1p64f)) {
-        mode = 0;  // nothing to add at this unit: only the softmax rescale
-        rescale_o<DV>(tl + C::kColO, alpha);
-      } else {
-        mode = 2;
-        rescale_o<DV>(tl + C::kColO, alpha * (unit / c));
-        unit = c;
-      }
+      if (mode != 1) rescale_o<DV>(tl + C::kColO, g);
       if (tid == 0) s_mode[t & 1] = mode;
       fence_proxy_async_smem();
       tc_fence_before();
@@ -396,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
     if (row_valid) lse[(size_t)bh * a.N + qi] = m * kLn2 + logf(l);
     wait(&bars.ofull, (nkv - 1) & 1, wd, 115);
     tc_fence_after();
-    const float linv = unit / l;
+    const float linv = u_p / l;  // O = O_tmem * (u_p / l) * u_v, two products so that no factor underflows
     const int dv = a.dv;
 #pragma unroll
     for (int c0 = 0; c0 < DV; c0 += 64) {
@@ -412,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
             uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(o[k + 2 * e] * linv, o[k + 2 * e + 1] * linv);
+              __nv_bfloat162 h2 = __floats2bfloat162_rn((o[k + 2 * e] * linv) * u_v, (o[k + 2 * e + 1] * linv) * u_v);
               wp[e] = *reinterpret_cast<uint32_t*>(&h2);
             }
             *reinterpret_cast<uint4*>(dst + k) = w;
@@ -421,8 +453,8 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
           float* dst = reinterpret_cast<float*>(O) + ((size_t)bh * a.N + qi) * dv + c0;
 #pragma unroll
           for (int k = 0; k < 64; k += 4)
-            *reinterpret_cast<float4*>(dst + k) =
-                make_float4(o[k] * linv, o[k + 1] * linv, o[k + 2] * linv, o[k + 3] * linv);
+            *reinterpret_cast<float4*>(dst + k) = make_float4((o[k] * linv) * u_v, (o[k + 1] * linv) * u_v,
+                                                              (o[k + 2] * linv) * u_v, (o[k + 3] * linv) * u_v);
         }
       }
     }

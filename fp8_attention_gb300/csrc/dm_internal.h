@@ -117,4 +117,9 @@ struct ZeroList {
 cudaError_t launch_zero(const ZeroList& z, cudaStream_t st);
 cudaError_t launch_attn_bwd(const BwdLaunch& f, int d, cudaStream_t st);
 
+// The checks dm_attn_bwd makes on its problem description and delta mode
+// before anything else (DM_OK, DM_ERR_INVALID_ARG or DM_ERR_SHAPE), for entry
+// points that wrap it.
+dm_status check_attn_problem(const dm_attn_params* p, dm_delta_mode mode);
+
 }  // namespace dm

@@ -19,7 +19,7 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/dm.h"
+#include "dm_internal.h"
 
 namespace {
 
@@ -71,8 +71,10 @@ extern "C" dm_status dm_attn_bwd_noalloc(const dm_attn_params* p, dm_delta_mode 
                                          const float* lse, const void* dO, dm_dtype do_dtype, const void* O,
                                          dm_dtype o_dtype, float* dQ, float* dK, float* dV, const dm_diag* diag,
                                          void* stream) {
-  if (!p) return DM_ERR_INVALID_ARG;
-  if (p->B < 0 || p->Hq <= 0 || p->N < 0) return DM_ERR_SHAPE;
+  // the same problem checks as dm_attn_bwd first, so that a bad empty call
+  // gets the same status from both entry points
+  const dm_status pv = dm::check_attn_problem(p, mode);
+  if (pv != DM_OK) return pv;
   if ((long long)p->B * p->Hq * p->N > (long long)DM_NOALLOC_MAX_DELTA_ROWS) return DM_ERR_SHAPE;
   if (p->B == 0 || p->N == 0) return DM_OK;
   const dm_fp8_tensor t4[4] = {q, k, v, do_hat};

@@ -20,7 +20,9 @@
  *  - Every pointer is DEVICE memory owned by the caller, except `p`/`diag`
  *    struct pointers, which are host memory read during the call.  The library
  *    allocates no memory and keeps no state between calls other than the TMA
- *    entry point it looks up once and a device status word.
+ *    entry point it looks up once, a device status word, and the fixed 8 MiB
+ *    device array that dm_attn_bwd_noalloc keeps delta in (on every GPU that
+ *    loads the library, until the process exits).
  *  - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *    stream) and is asynchronous; the call returns after the launches.
  *    Stream order holds as usual.  The forward and delta kernels are launched
@@ -51,7 +53,20 @@
  *    P~ = exp(S - running row max) in FP32, one E4M3 scale per 128x128 tile
  *    of P~, the row sum l taken from the unquantised P~;
  *  - backward P = exp(S - LSE) in FP32, quantised E4M3 per 128x128 tile;
- *    dS = P*(dP^ - delta) in FP32, quantised E5M2 per 128x128 tile.
+ *    dS = P*(dP^ - delta) in FP32, quantised E5M2 per 128x128 tile;
+ *  - the P~, P and dS tiles never leave the chip, and their scales are formed
+ *    with a hardware reciprocal (r = FMAX/amax to within 2 ulp, s = amax *
+ *    (1/FMAX)) instead of IEEE divisions, and the forward forms P~ * r as one
+ *    base-2 exponential exp2(S*c - m + log2 r): a code of these tiles can
+ *    differ from the oracle's where P~ * r lies within FP32 rounding of a code
+ *    boundary (the Q, K, V and dO codes of dm_quantize are bit-exact);
+ *  - accumulator units: each key tile (forward) or query tile (backward)
+ *    contributes in units of its own scale product; a tile adds nothing when
+ *    one of its scales is zero (a flushed tile) or when its contribution is
+ *    below 2^-64 of the accumulator's current unit in every row.  dQ is exact
+ *    down to sigma * s_dS * s_K >= 2^-126 (the FP32 normal range of one
+ *    iteration's dQ unit); the forward's O stays finite while the V tiles one
+ *    query row sees have scales within about 2^90 of each other.
  */
 #ifndef DM_H_
 #define DM_H_

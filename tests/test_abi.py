@@ -103,6 +103,31 @@ def test_validation_without_gpu(lib):
         == dm.DM_ERR_INVALID_ARG  # workspace too small for the internally computed delta
 
 
+def test_noalloc_validates_like_the_workspace_backward(lib):
+    """dm_attn_bwd_noalloc answers a bad call with the status dm_attn_bwd gives
+    it, also when the problem is empty (B = 0 or N = 0), before any CUDA call."""
+    A = 0x10000
+    f = dm._Fp8(A, A)
+    z = dm._Fp8(None, None)
+
+    def both(params, mode, ff):
+        na = lib.dm_attn_bwd_noalloc(ctypes.byref(params), mode, ff, ff, ff, ff, A, None, 0, None, 0, A, A, A,
+                                     None, None)
+        ws = lib.dm_attn_bwd(ctypes.byref(params), mode, ff, ff, ff, ff, A, None, None, 0, None, 0, A, A, A,
+                             None, A, 1 << 30, None)
+        return na, ws
+
+    for params, mode, ff, want in ((_p(B=0, d=100), 0, z, dm.DM_ERR_SHAPE),
+                                   (_p(N=0, Hq=3, Hkv=2), 0, z, dm.DM_ERR_SHAPE),
+                                   (_p(B=0), 7, z, dm.DM_ERR_INVALID_ARG),
+                                   (_p(B=0, scale=float("inf")), 0, z, dm.DM_ERR_INVALID_ARG),
+                                   (_p(B=0), 0, z, dm.DM_OK),
+                                   (_p(d=96), 0, f, dm.DM_ERR_SHAPE)):
+        assert both(params, mode, ff) == (want, want), (params.B, params.N, params.d, mode)
+    assert lib.dm_attn_bwd_noalloc(None, 0, f, f, f, f, A, None, 0, None, 0, A, A, A, None, None) \
+        == dm.DM_ERR_INVALID_ARG
+
+
 def test_workspace_size(lib):
     assert dm.dm_attn_bwd_workspace_size(dm.AttnParams(2, 4, 2, 1000, 64)) == ((2 * 4 * 1000 * 4 + 255) // 256) * 256
     assert dm.dm_attn_bwd_workspace_size(dm.AttnParams(2, 4, 3, 1000, 64)) == 0

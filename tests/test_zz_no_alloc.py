@@ -35,10 +35,10 @@ def test_noalloc_matches_workspace_backward_twice(mode):
     cases = [(1, 4, 2, 384, 128, 11), (2, 2, 1, 200, 64, 12)]   # second call: a different, ragged problem
     for B, Hq, Hkv, N, d, seed in cases:
         p, qh, kh, vh, doh, lse, do, O = _inputs(B, Hq, Hkv, N, d, seed)
-        ref = dm.dm_attn_bwd(p, mode, qh, kh, vh, doh, lse, None, dO=do, O=O)   # workspace path
-        got = dm.dm_attn_bwd_noalloc(p, mode, qh, kh, vh, doh, lse, dO=do, O=O)
+        ref = dm.dm_attn_bwd(p, mode, qh, kh, vh, doh, lse, None, dO=do, O=O, diag=True)   # workspace path
+        got = dm.dm_attn_bwd_noalloc(p, mode, qh, kh, vh, doh, lse, dO=do, O=O, diag=True)
         assert dm.dm_get_status() == dm.DM_OK
-        for key in ("dQ", "dK", "dV"):
+        for key in ("dQ", "dK", "dV", "abssum_pre", "abssum_post"):
             err = rel_err(got[key].double().cpu().numpy(), ref[key].double().cpu().numpy())
             assert err <= TOL, (key, err)
 
