@@ -77,12 +77,15 @@ def _load():
             lib.or_quantize.argtypes = [P, I, I, I, I, I, P, P]
             lib.or_dequantize.argtypes = [P, P, I, I, I, I, I, P]
             lib.or_attn_fwd.restype = I
-            lib.or_attn_fwd.argtypes = [I, I, I, I, I, I, I, D, I, P, P, P, P, I, P, I, P, P, P]
+            lib.or_attn_fwd.argtypes = [I, I, I, I, I, I, I, D, I, P, P, P, P, I, P, I, P, P, P, I, I]
             lib.or_attn_delta.restype = I
-            lib.or_attn_delta.argtypes = [I, I, I, I, I, I, I, D, I, I, P, P, P, P, P, P, P, P, I, P, I, P]
+            lib.or_attn_delta.argtypes = [I, I, I, I, I, I, I, D, I, I, P, P, P, P, P, P, P, P, I, P, I, P,
+                                          I, I, P]
             lib.or_attn_bwd.restype = I
             lib.or_attn_bwd.argtypes = [I, I, I, I, I, I, I, D, I, P, P, P, P, P, P,
-                                        P, I, P, I, P, I, P, P, P, P, P, P, P]
+                                        P, I, P, I, P, I, P, P, P, P, P, P, P, I, I]
+            lib.or_attn_merge.restype = I
+            lib.or_attn_merge.argtypes = [I, ctypes.c_int64, I, P, P, P, P]
             lib.or_rope_table.argtypes = [I, I, D, P, P]
             lib.or_qk_prologue.restype = I
             lib.or_qk_prologue.argtypes = [P, I, I, I, I, P, D, I, D, P]
@@ -171,11 +174,21 @@ def dequantize(codes, scales, fmt: int) -> np.ndarray:
 
 
 # ----------------------------------------------------------------- attention
+def _kv_range(kv_range):
+    """(begin, end) of a key range for the C calls; None selects every key."""
+    if kv_range is None:
+        return 0, 0
+    b, e = kv_range
+    return int(b), int(e)
+
+
 def attn_fwd(Q, K, V, causal=True, sigma=0.0, flags=GPU_CONTRACT, q_tiles=None, groups=None,
-             want_pfwd=False):
+             want_pfwd=False, kv_range=None):
     """Forward on decoded operands.  Returns (O, LSE[, Pfwd]) in FP64.
 
-    Rows outside the selected query tiles / groups are left at NaN."""
+    Rows outside the selected query tiles / groups are left at NaN.  kv_range
+    = (begin, end) restricts attention to those keys (a key block of
+    context-parallel attention; rows seeing none get O = 0, LSE = -inf)."""
     lib = _load()
     Q, K, V = _f64(Q), _f64(K), _f64(V)
     _check(Q, K, V)
@@ -186,16 +199,19 @@ def attn_fwd(Q, K, V, causal=True, sigma=0.0, flags=GPU_CONTRACT, q_tiles=None, 
     P = np.zeros((B, Hq, N, N)) if want_pfwd else None
     qs, nq = _sel(q_tiles)
     gs, ng = _groups(groups)
+    kb, ke = _kv_range(kv_range)
     rc = lib.or_attn_fwd(B, Hq, Hkv, N, d, dv, int(causal), float(sigma), int(flags), _p(Q), _p(K), _p(V),
-                         _p(qs), nq, _p(gs), ng, _p(O), _p(LSE), _p(P))
+                         _p(qs), nq, _p(gs), ng, _p(O), _p(LSE), _p(P), kb, ke)
     if rc != 0:
         raise ValueError("or_attn_fwd: bad arguments")
     return (O, LSE, P) if want_pfwd else (O, LSE)
 
 
 def attn_delta(Q, K, V, dOhat, LSE, mode=DELTA_MATCHED, dO=None, O=None, causal=True, sigma=0.0,
-               flags=GPU_CONTRACT, q_tiles=None, groups=None):
-    """Softmax row correction delta [B][Hq][N] for the given mode."""
+               flags=GPU_CONTRACT, q_tiles=None, groups=None, kv_range=None, partial=False):
+    """Softmax row correction delta [B][Hq][N] for the given mode.  Matched mode
+    with kv_range sums over those keys only; partial=True returns the two sums
+    (sum_j P dP^, sum_j P) apart instead of their quotient."""
     lib = _load()
     Q, K, V, dOhat, LSE = _f64(Q), _f64(K), _f64(V), _f64(dOhat), _f64(LSE)
     dO, O = _f64(dO), _f64(O)
@@ -209,19 +225,22 @@ def attn_delta(Q, K, V, dOhat, LSE, mode=DELTA_MATCHED, dO=None, O=None, causal=
     B, Hq, N, d = Q.shape
     Hkv, dv = K.shape[1], V.shape[3]
     delta = np.full((B, Hq, N), np.nan)
+    den = np.full((B, Hq, N), np.nan) if partial else None
     qs, nq = _sel(q_tiles)
     gs, ng = _groups(groups)
+    kb, ke = _kv_range(kv_range)
     rc = lib.or_attn_delta(B, Hq, Hkv, N, d, dv, int(causal), float(sigma), int(flags), int(mode),
                            _p(Q), _p(K), _p(V), _p(dOhat), _p(dO), _p(O), _p(LSE),
-                           _p(qs), nq, _p(gs), ng, _p(delta))
+                           _p(qs), nq, _p(gs), ng, _p(delta), kb, ke, _p(den))
     if rc != 0:
         raise ValueError("or_attn_delta: bad arguments")
-    return delta
+    return (delta, den) if partial else delta
 
 
 def attn_bwd(Q, K, V, dOhat, LSE, delta, causal=True, sigma=0.0, flags=GPU_CONTRACT, q_tiles=None,
-             kv_tiles=None, groups=None, want_diag=False, want_tiles=False):
-    """Backward on decoded operands.  Returns dict with dQ, dK, dV (+ diag, dS, dShat, Phat)."""
+             kv_tiles=None, groups=None, want_diag=False, want_tiles=False, kv_range=None):
+    """Backward on decoded operands.  Returns dict with dQ, dK, dV (+ diag, dS, dShat, Phat).
+    With kv_range only those keys take part: dQ is the key block's partial sum."""
     lib = _load()
     Q, K, V, dOhat, LSE, delta = _f64(Q), _f64(K), _f64(V), _f64(dOhat), _f64(LSE), _f64(delta)
     _check(Q, K, V, dOhat)
@@ -243,7 +262,7 @@ def attn_bwd(Q, K, V, dOhat, LSE, delta, causal=True, sigma=0.0, flags=GPU_CONTR
                          _p(Q), _p(K), _p(V), _p(dOhat), _p(LSE), _p(delta),
                          _p(qs), nq, _p(ks), nk, _p(gs), ng,
                          _p(out["dQ"]), _p(out["dK"]), _p(out["dV"]), _p(diag),
-                         _p(tiles[0]), _p(tiles[1]), _p(tiles[2]))
+                         _p(tiles[0]), _p(tiles[1]), _p(tiles[2]), *_kv_range(kv_range))
     if rc != 0:
         raise ValueError("or_attn_bwd: bad arguments")
     if want_diag:
@@ -251,6 +270,24 @@ def attn_bwd(Q, K, V, dOhat, LSE, delta, causal=True, sigma=0.0, flags=GPU_CONTR
     if want_tiles:
         out["dS"], out["dShat"], out["Phat"] = tiles
     return out
+
+
+def attn_merge(O_parts, LSE_parts):
+    """Merge of per-key-block attention results: O_parts [S][B][H][N][dv],
+    LSE_parts [S][B][H][N] -> (O, LSE) of the union of the blocks."""
+    lib = _load()
+    Op = np.ascontiguousarray(O_parts, dtype=np.float64)
+    Lp = np.ascontiguousarray(LSE_parts, dtype=np.float64)
+    S = Op.shape[0]
+    rows = int(np.prod(Lp.shape[1:]))
+    dv = Op.shape[-1]
+    if Op.shape[:-1] != Lp.shape:
+        raise ValueError("O_parts must be LSE_parts' shape plus a value dimension")
+    O = np.empty(Op.shape[1:])
+    LSE = np.empty(Lp.shape[1:])
+    if lib.or_attn_merge(S, rows, dv, _p(Op), _p(Lp), _p(O), _p(LSE)) != 0:
+        raise ValueError("or_attn_merge: bad arguments")
+    return O, LSE
 
 
 # ------------------------------------------------------------ whole pipeline
@@ -293,6 +330,49 @@ def pipeline(q, k, v, do, causal=True, sigma=0.0, mode=DELTA_MATCHED, o_bf16=Fal
     res["delta"] = delta
     res.update(attn_bwd(dec["q"], dec["k"], dec["v"], dec["do"], LSE_st, delta, causal, sigma, flags,
                         q_tiles, kv_tiles, groups, want_diag=want_diag))
+    return res
+
+
+def pipeline_key_blocks(q, k, v, do, bounds, causal=True, sigma=0.0, flags=GPU_CONTRACT, o_bf16=False):
+    """The pipeline with the keys split into blocks [bounds[r], bounds[r+1])
+    (context parallelism): quantise, forward per block, merge of O and LSE,
+    matched delta from the blocks' partial sums (added before the division),
+    backward per block with the merged LSE and delta, dQ summed over blocks.
+    Returns the same keys as pipeline() plus the per-block partials."""
+    q = np.asarray(q, np.float32)
+    k = np.asarray(k, np.float32)
+    v = np.asarray(v, np.float32)
+    do = np.asarray(do, np.float32)
+    res, dec = {}, {}
+    for name, x, fmt in (("q", q, E4M3), ("k", k, E4M3), ("v", v, E4M3), ("do", do, E5M2)):
+        c, s = quantize(x, fmt)
+        res[name + "_codes"], res[name + "_scales"] = c, s
+        dec[name] = dequantize(c, s, fmt)
+    blocks = list(zip(bounds[:-1], bounds[1:]))
+    parts = [attn_fwd(dec["q"], dec["k"], dec["v"], causal, sigma, flags, kv_range=b) for b in blocks]
+    # each block's O as the GPU stores it (fp32), its LSE in fp32
+    O_parts = np.stack([p[0].astype(np.float32).astype(np.float64) for p in parts])
+    L_parts = np.stack([p[1].astype(np.float32).astype(np.float64) for p in parts])
+    O, LSE = attn_merge(O_parts, L_parts)
+    O_st = round_bf16(O) if o_bf16 else O.astype(np.float32).astype(np.float64)
+    LSE_st = LSE.astype(np.float32).astype(np.float64)
+    num = np.zeros(LSE.shape)
+    den = np.zeros(LSE.shape)
+    for b in blocks:
+        n_r, d_r = attn_delta(dec["q"], dec["k"], dec["v"], dec["do"], LSE_st, DELTA_MATCHED, causal=causal,
+                              sigma=sigma, flags=flags, kv_range=b, partial=True)
+        num += n_r.astype(np.float32)
+        den += d_r.astype(np.float32)
+    delta = num / den
+    dQ = np.zeros(q.shape)
+    dK = np.zeros(k.shape)
+    dV = np.zeros(v.shape)
+    for b in blocks:
+        g = attn_bwd(dec["q"], dec["k"], dec["v"], dec["do"], LSE_st, delta, causal, sigma, flags, kv_range=b)
+        dQ += g["dQ"]
+        dK[:, :, b[0]:b[1]] = g["dK"][:, :, b[0]:b[1]]
+        dV[:, :, b[0]:b[1]] = g["dV"][:, :, b[0]:b[1]]
+    res.update(O_parts=O_parts, LSE_parts=L_parts, O=O_st, LSE=LSE_st, delta=delta, dQ=dQ, dK=dK, dV=dV)
     return res
 
 

@@ -150,6 +150,7 @@ inline float fl32(double x) { return (float)x; }
 struct Dims {
   int B, Hq, Hkv, N, d, dv, causal;
   double sigma;
+  int kb = 0, ke = 0;  // key range [kb, ke): the keys this call sees (ke = N: all)
   int G() const { return Hq / Hkv; }
   int T() const { return (N + kTile - 1) / kTile; }
   size_t qoff(int b, int h) const { return ((size_t)b * Hq + h) * N * d; }
@@ -159,7 +160,7 @@ struct Dims {
   size_t rowoff(int b, int h) const { return ((size_t)b * Hq + h) * N; }
 };
 
-bool visible(const Dims& D, int i, int j) { return j < D.N && (!D.causal || j <= i); }
+bool visible(const Dims& D, int i, int j) { return j >= D.kb && j < D.ke && (!D.causal || j <= i); }
 
 double dot(const double* a, const double* b, int n) {
   double s = 0.0;
@@ -204,8 +205,19 @@ void score_tile(const Dims& D, const double* Qh, const double* Kg, int qt, int k
         S[(size_t)r * cols + c] = D.sigma * dot(Qh + (size_t)(i0 + r) * D.d, Kg + (size_t)(j0 + c) * D.d, D.d);
 }
 
+// Key tiles a query tile sees: [first_key_tile, last_key_tile] (empty when
+// first > last).
+int first_key_tile(const Dims& D) { return D.kb / kTile; }
 int last_key_tile(const Dims& D, int qt) {
-  return D.causal ? std::min(qt, D.T() - 1) : D.T() - 1;
+  const int last = (D.ke - 1) / kTile;
+  return D.causal ? std::min(qt, last) : last;
+}
+
+// Key range [kb, ke) of a call: kv_end <= 0 selects every key from kv_begin on.
+bool set_key_range(Dims& D, int kv_begin, int kv_end) {
+  D.kb = kv_begin;
+  D.ke = kv_end > 0 ? kv_end : D.N;
+  return kv_begin >= 0 && D.ke <= D.N && (D.N == 0 || kv_begin < D.ke);
 }
 
 }  // namespace
@@ -279,12 +291,20 @@ void or_dequantize(const uint8_t* codes, const float* scales, int B, int H, int 
 //
 // Pfwd (nullable, [B][Hq][N][N]) receives the effective forward
 // probabilities, i.e. the matrix with O = Pfwd V exactly.
+//
+// Key range [kv_begin, kv_end) (kv_end <= 0: to N): the attention of every
+// query row over those keys only, a key block of context-parallel attention
+// (project page section 06 extends the context from 8K to 64K tokens; the
+// pages do not say how the sequence is split).  A row that sees none of them
+// gets O = 0 and LSE = -inf.  The one-pass quantised forward walks the range's
+// key tiles only, so its running maximum starts at the block's first tile.
 int or_attn_fwd(int B, int Hq, int Hkv, int N, int d, int dv, int causal, double sigma, int flags,
                 const double* Q, const double* K, const double* V,
                 const int* q_tiles, int n_q_tiles, const int* groups, int n_groups,
-                double* O, double* LSE, double* Pfwd) {
+                double* O, double* LSE, double* Pfwd, int kv_begin, int kv_end) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || N < 0 || d <= 0 || dv <= 0) return 1;
   Dims D{B, Hq, Hkv, N, d, dv, causal, sigma > 0 ? sigma : 1.0 / std::sqrt((double)d)};
+  if (!set_key_range(D, kv_begin, kv_end)) return 1;
   const int T = D.T();
   const std::vector<int> qts = tiles_or_all(q_tiles, n_q_tiles, T);
   const std::vector<Group> gs = groups_or_all(groups, n_groups, D);
@@ -319,6 +339,12 @@ int or_attn_fwd(int B, int Hq, int Hkv, int N, int d, int dv, int causal, double
         for (int j = 0; j < N; ++j)
           if (visible(D, i, j)) l += std::exp(s[j] - m);
         for (int k = 0; k < dv; ++k) Oh[(size_t)i * dv + k] = 0.0;
+        if (l == 0.0) {  // no visible key
+          Lh[i] = -INFINITY;
+          if (Ph)
+            for (int j = 0; j < N; ++j) Ph[(size_t)i * N + j] = 0.0;
+          continue;
+        }
         for (int j = 0; j < N; ++j) {
           const double p = visible(D, i, j) ? std::exp(s[j] - m) / l : 0.0;
           if (Ph) Ph[(size_t)i * N + j] = p;
@@ -332,11 +358,12 @@ int or_attn_fwd(int B, int Hq, int Hkv, int N, int d, int dv, int causal, double
 
     // One-pass online forward with per-tile quantisation of P~.
     std::vector<double> m(rows, -INFINITY), l(rows, 0.0), acc((size_t)rows * dv, 0.0);
-    std::vector<double> mt((size_t)(ktmax + 1) * rows);  // m^(t) per tile, for Pfwd
+    const int ktmin = first_key_tile(D);
+    std::vector<double> mt((size_t)std::max(ktmax + 1, 1) * rows);  // m^(t) per tile, for Pfwd
     std::vector<double> S;
     std::vector<float> pt;
     std::vector<uint8_t> codes;
-    for (int kt = 0; kt <= ktmax; ++kt) {
+    for (int kt = ktmin; kt <= ktmax; ++kt) {
       int rr, cols;
       score_tile(D, Qh, Kg, qt, kt, S, rr, cols);
       const int j0 = kt * kTile;
@@ -379,10 +406,18 @@ int or_attn_fwd(int B, int Hq, int Hkv, int N, int d, int dv, int causal, double
     }
     for (int r = 0; r < rows; ++r) {
       const int i = i0 + r;
+      if (l[r] == 0.0) {  // no visible key
+        for (int k = 0; k < dv; ++k) Oh[(size_t)i * dv + k] = 0.0;
+        Lh[i] = -INFINITY;
+        if (Ph)
+          for (int j = 0; j < N; ++j) Ph[(size_t)i * N + j] = 0.0;
+        continue;
+      }
       for (int k = 0; k < dv; ++k) Oh[(size_t)i * dv + k] = acc[(size_t)r * dv + k] / l[r];
       Lh[i] = m[r] + std::log(l[r]);
       if (Ph) {
-        for (int kt = 0; kt <= ktmax; ++kt) {
+        for (int j = 0; j < std::min(N, ktmin * kTile); ++j) Ph[(size_t)i * N + j] = 0.0;
+        for (int kt = ktmin; kt <= ktmax; ++kt) {
           const double w = std::exp(mt[(size_t)kt * rows + r] - m[r]) / l[r];
           for (int c = 0; c < std::min(kTile, N - kt * kTile); ++c)
             Ph[(size_t)i * N + kt * kTile + c] *= w;
@@ -408,12 +443,20 @@ int or_attn_fwd(int B, int Hq, int Hkv, int N, int d, int dv, int causal, double
 //                its FP8 cast, O as stored by the forward;
 //   stale_dOhat  (section 03, last paragraph): delta_i = <dO^_i, O_i>.
 // LSE is the stored forward value (the caller rounds it to FP32).
+//
+// Key range [kv_begin, kv_end) (matched mode): the sums run over those keys
+// only.  With den != NULL the two sums are returned apart, delta_i = sum_j
+// P_ij dP^_ij and den_i = sum_j P_ij (0 for a row that sees none of the keys),
+// so that the blocks of a split key range add up before the one division.
 int or_attn_delta(int B, int Hq, int Hkv, int N, int d, int dv, int causal, double sigma, int flags, int mode,
                   const double* Q, const double* K, const double* V, const double* dOhat,
                   const double* dO, const double* O, const double* LSE,
-                  const int* q_tiles, int n_q_tiles, const int* groups, int n_groups, double* delta) {
+                  const int* q_tiles, int n_q_tiles, const int* groups, int n_groups, double* delta,
+                  int kv_begin, int kv_end, double* den) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || N < 0 || d <= 0 || dv <= 0 || mode < 0 || mode > 2) return 1;
   Dims D{B, Hq, Hkv, N, d, dv, causal, sigma > 0 ? sigma : 1.0 / std::sqrt((double)d)};
+  if (!set_key_range(D, kv_begin, kv_end)) return 1;
+  if (den && mode != OR_DELTA_MATCHED) return 1;
   const std::vector<int> qts = tiles_or_all(q_tiles, n_q_tiles, D.T());
   const std::vector<Group> gs = groups_or_all(groups, n_groups, D);
   const int G = D.G();
@@ -444,7 +487,10 @@ int or_attn_delta(int B, int Hq, int Hkv, int N, int d, int dv, int causal, doub
           dl += p * dp;
           psum += p;
         }
-        dl /= psum;
+        if (den)
+          den[ro + i] = psum;
+        else
+          dl /= psum;
       }
       delta[ro + i] = dl;
     }
@@ -468,15 +514,20 @@ int or_attn_delta(int B, int Hq, int Hkv, int N, int d, int dv, int causal, doub
 // diag (nullable) is [4][B][Hq][N]: sum_j dS, sum_j |dS|, sum_j dS^, sum_j |dS^|.
 // dS, dShat, Phat (nullable, [B][Hq][N][N]) receive the tiles computed for
 // the selected query tiles (small test cases only).
+//
+// Key range [kv_begin, kv_end): only those keys take part; dQ (and the
+// diagnostics) are then the block's partial sums, and dK, dV of keys outside
+// the range are zero.
 int or_attn_bwd(int B, int Hq, int Hkv, int N, int d, int dv, int causal, double sigma, int flags,
                 const double* Q, const double* K, const double* V, const double* dOhat,
                 const double* LSE, const double* delta,
                 const int* q_tiles, int n_q_tiles, const int* kv_tiles, int n_kv_tiles,
                 const int* groups, int n_groups,
                 double* dQ, double* dK, double* dV, double* diag,
-                double* dS_out, double* dShat_out, double* Phat_out) {
+                double* dS_out, double* dShat_out, double* Phat_out, int kv_begin, int kv_end) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || N < 0 || d <= 0 || dv <= 0) return 1;
   Dims D{B, Hq, Hkv, N, d, dv, causal, sigma > 0 ? sigma : 1.0 / std::sqrt((double)d)};
+  if (!set_key_range(D, kv_begin, kv_end)) return 1;
   const int T = D.T(), G = D.G();
   const std::vector<int> qts = tiles_or_all(q_tiles, n_q_tiles, T);
   const std::vector<int> kts = tiles_or_all(kv_tiles, n_kv_tiles, T);
@@ -544,7 +595,7 @@ int or_attn_bwd(int B, int Hq, int Hkv, int N, int d, int dv, int causal, double
           for (int q = 0; q < 4; ++q) diag[(size_t)q * B * Hq * N + D.rowoff(gr.b, h) + i0 + r] = 0.0;
       }
       PairTile pt;
-      for (int kt = 0; kt <= last_key_tile(D, qt); ++kt) {
+      for (int kt = first_key_tile(D); kt <= last_key_tile(D, qt); ++kt) {
         compute_pair(gr.b, h, qt, kt, pt);
         const int j0 = kt * kTile;
         for (int r = 0; r < pt.rows; ++r) {
@@ -614,6 +665,39 @@ int or_attn_bwd(int B, int Hq, int Hkv, int N, int d, int dv, int causal, double
             }
         }
       }
+    }
+  }
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
+// Merge of the attention of one query row over disjoint key blocks (context
+// parallelism): with block r's LSE_r = ln sum_{j in r} exp(S_ij) and
+// O_r = sum_{j in r} exp(S_ij - LSE_r) V_j, the whole row has
+//   LSE = ln sum_r exp(LSE_r),   O = sum_r exp(LSE_r - LSE) O_r,
+// which is the softmax over the union of the blocks written out.  Blocks with
+// LSE_r = -inf (no visible key) weigh zero; a row with none at all gets O = 0
+// and LSE = -inf.  O_parts [nparts][rows][dv], LSE_parts [nparts][rows].
+int or_attn_merge(int nparts, int64_t rows, int dv, const double* O_parts, const double* LSE_parts, double* O,
+                  double* LSE) {
+  if (nparts <= 0 || rows < 0 || dv <= 0) return 1;
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < rows; ++i) {
+    double m = -INFINITY;
+    for (int r = 0; r < nparts; ++r) m = std::max(m, LSE_parts[(size_t)r * rows + i]);
+    double* o = O + (size_t)i * dv;
+    for (int k = 0; k < dv; ++k) o[k] = 0.0;
+    if (m == -INFINITY) {
+      LSE[i] = -INFINITY;
+      continue;
+    }
+    double wsum = 0.0;
+    for (int r = 0; r < nparts; ++r) wsum += std::exp(LSE_parts[(size_t)r * rows + i] - m);
+    LSE[i] = m + std::log(wsum);
+    for (int r = 0; r < nparts; ++r) {
+      const double w = std::exp(LSE_parts[(size_t)r * rows + i] - LSE[i]);
+      const double* orow = O_parts + ((size_t)r * rows + i) * dv;
+      for (int k = 0; k < dv; ++k) o[k] += w * orow[k];
     }
   }
   return 0;
