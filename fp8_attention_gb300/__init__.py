@@ -26,6 +26,7 @@ __all__ = [
     "dm_get_status", "dm_last_timeout_site", "dm_quantize", "dm_quantize_batch", "dm_rope_table",
     "dm_qk_prologue_batch", "ROPE_BASE", "RMS_EPS", "DM_PROLOGUE_MAX_JOBS", "dm_attn_fwd", "dm_attn_delta", "dm_attn_bwd",
     "dm_attn_bwd_workspace_size", "dm_attn_bwd_noalloc", "DM_NOALLOC_MAX_DELTA_ROWS",
+    "dm_attn_delta_partial", "dm_attn_merge", "dm_attn_delta_combine",
     "DM_F32", "DM_BF16", "DM_E4M3", "DM_E5M2", "DM_DELTA_MATCHED", "DM_DELTA_STALE_DO",
     "DM_DELTA_STALE_DOHAT", "DM_KNOB_WAIT_LIMIT_NS", "DM_KNOB_STALL_TEST",
 ]
@@ -51,7 +52,7 @@ class DMError(RuntimeError):
 class _Params(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("N", ctypes.c_int),
                 ("d", ctypes.c_int), ("causal", ctypes.c_int), ("softmax_scale", ctypes.c_float),
-                ("d_v", ctypes.c_int)]
+                ("d_v", ctypes.c_int), ("kv_offset", ctypes.c_int), ("kv_len", ctypes.c_int)]
 
 
 class _Fp8(ctypes.Structure):
@@ -73,14 +74,21 @@ class AttnParams:
     causal: bool = True
     softmax_scale: float = 0.0   # <= 0 selects 1/sqrt(d)
     d_v: int = 0                 # head dimension of V, dO, O, dV; 0 selects d
+    kv_offset: int = 0           # key block: keys at [kv_offset, kv_offset + kv_len) only
+    kv_len: int = 0              # (both 0: the whole sequence; kv_len 0: up to N)
 
     def c(self) -> _Params:
         return _Params(self.B, self.Hq, self.Hkv, self.N, self.d, int(bool(self.causal)),
-                       float(self.softmax_scale), int(self.d_v))
+                       float(self.softmax_scale), int(self.d_v), int(self.kv_offset), int(self.kv_len))
 
     @property
     def dv(self) -> int:
         return self.d_v if self.d_v else self.d
+
+    @property
+    def Nk(self) -> int:
+        """Rows of K, V, dK and dV (the key block's, else N)."""
+        return self.kv_len if self.kv_len > 0 else self.N - self.kv_offset
 
     @property
     def T(self) -> int:
@@ -135,6 +143,12 @@ def lib():
                                               ctypes.POINTER(_Diag), P]
             L.dm_attn_bwd_workspace_size.restype = S
             L.dm_attn_bwd_workspace_size.argtypes = [PP]
+            L.dm_attn_delta_partial.restype = I
+            L.dm_attn_delta_partial.argtypes = [PP, _Fp8, _Fp8, _Fp8, _Fp8, P, P, P, P]
+            L.dm_attn_merge.restype = I
+            L.dm_attn_merge.argtypes = [PP, I, P, P, P, I, P, P]
+            L.dm_attn_delta_combine.restype = I
+            L.dm_attn_delta_combine.argtypes = [PP, I, P, P, P, P]
             _lib = L
     return _lib
 
@@ -358,9 +372,9 @@ def dm_attn_bwd(p: AttnParams, mode: int, q: Fp8, k: Fp8, v: Fp8, do_hat: Fp8, l
     if dQ is None:
         dQ = torch.empty((p.B, p.Hq, p.N, p.d), dtype=torch.float32, device=dev)
     if dK is None:
-        dK = torch.empty((p.B, p.Hkv, p.N, p.d), dtype=torch.float32, device=dev)
+        dK = torch.empty((p.B, p.Hkv, p.Nk, p.d), dtype=torch.float32, device=dev)
     if dV is None:
-        dV = torch.empty((p.B, p.Hkv, p.N, p.dv), dtype=torch.float32, device=dev)
+        dV = torch.empty((p.B, p.Hkv, p.Nk, p.dv), dtype=torch.float32, device=dev)
     out = {"dQ": dQ, "dK": dK, "dV": dV}
     cdiag = _diag(p, diag, dev, out)
     ws_bytes = 0
@@ -401,3 +415,49 @@ def dm_attn_bwd_noalloc(p: AttnParams, mode: int, q: Fp8, k: Fp8, v: Fp8, do_hat
                                        _stream(stream))
     _check(rc, "dm_attn_bwd_noalloc")
     return out
+
+
+def dm_attn_delta_partial(p: AttnParams, q: Fp8, k: Fp8, v: Fp8, do_hat: Fp8, lse, num=None, den=None,
+                          stream=None):
+    """The matched correction's two sums over the key block of p: returns
+    (num, den), each float32 [B][Hq][N] (sum_j P dP^ and sum_j P over the block)."""
+    dev = lse.device
+    if num is None:
+        num = torch.empty((p.B, p.Hq, p.N), dtype=torch.float32, device=dev)
+    if den is None:
+        den = torch.empty((p.B, p.Hq, p.N), dtype=torch.float32, device=dev)
+    cp = p.c()
+    with _on(dev):
+        rc = lib().dm_attn_delta_partial(ctypes.byref(cp), _fp8(q), _fp8(k), _fp8(v), _fp8(do_hat), _ptr(lse),
+                                         _ptr(num), _ptr(den), _stream(stream))
+    _check(rc, "dm_attn_delta_partial")
+    return num, den
+
+
+def dm_attn_merge(p: AttnParams, O_parts, lse_parts, O=None, o_dtype=torch.float32, lse=None, stream=None):
+    """(O, LSE) of the union of key blocks from their stacked results:
+    O_parts float32 [S][B][Hq][N][d_v], lse_parts float32 [S][B][Hq][N]."""
+    dev = lse_parts.device
+    if O is None:
+        O = torch.empty((p.B, p.Hq, p.N, p.dv), dtype=o_dtype, device=dev)
+    if lse is None:
+        lse = torch.empty((p.B, p.Hq, p.N), dtype=torch.float32, device=dev)
+    cp = p.c()
+    with _on(dev):
+        rc = lib().dm_attn_merge(ctypes.byref(cp), int(lse_parts.shape[0]), _ptr(O_parts), _ptr(lse_parts),
+                                 _ptr(O), _dtype(O), _ptr(lse), _stream(stream))
+    _check(rc, "dm_attn_merge")
+    return O, lse
+
+
+def dm_attn_delta_combine(p: AttnParams, num_parts, den_parts, delta=None, stream=None):
+    """delta = sum of the stacked num parts / sum of the den parts ([S][B][Hq][N] each)."""
+    dev = num_parts.device
+    if delta is None:
+        delta = torch.empty((p.B, p.Hq, p.N), dtype=torch.float32, device=dev)
+    cp = p.c()
+    with _on(dev):
+        rc = lib().dm_attn_delta_combine(ctypes.byref(cp), int(num_parts.shape[0]), _ptr(num_parts),
+                                         _ptr(den_parts), _ptr(delta), _stream(stream))
+    _check(rc, "dm_attn_delta_combine")
+    return delta

@@ -94,6 +94,11 @@ dm_status encode_f32_rows_map(CUtensorMap* m, const float* x, int BH, int N, int
 // Head dimension of V, dO, O and dV (0 selects d).
 inline int value_dim(const dm_attn_params* p) { return p->d_v ? p->d_v : p->d; }
 
+// Rows of K, V, dK and dV: the key block's length (kv_len <= 0: every key
+// from kv_offset on; the whole sequence by default).
+inline int key_rows(const dm_attn_params* p) { return p->kv_len > 0 ? p->kv_len : p->N - p->kv_offset; }
+inline bool key_block(const dm_attn_params* p) { return p->kv_offset != 0 || p->kv_len != 0; }
+
 // The kernels' head dimension: d itself when Q/K and V share one of the
 // widths the kernels are built for, else 256 (missing channels read as zeros).
 inline int kernel_dim(const dm_attn_params* p) {
@@ -121,6 +126,9 @@ dm_status check_params(const dm_attn_params* p) {
   if (p->Hq % p->Hkv != 0) return DM_ERR_SHAPE;
   if ((long long)p->B * p->Hq * p->N * (p->d > dv ? p->d : dv) >= (1ll << 31)) return DM_ERR_SHAPE;
   if (!std::isfinite(p->softmax_scale)) return DM_ERR_INVALID_ARG;
+  // key block: 128-aligned start inside the sequence, at least one key
+  if (p->kv_offset < 0 || p->kv_offset % kTileRows != 0 || p->kv_len < 0) return DM_ERR_SHAPE;
+  if (p->N > 0 && (p->kv_offset >= p->N || (long long)p->kv_offset + key_rows(p) > p->N)) return DM_ERR_SHAPE;
   return DM_OK;
 }
 
@@ -147,16 +155,22 @@ bool valid_mode(dm_delta_mode m) {
 // half of the query tiles (all of them up to 32 query tiles, where the
 // per-CTA fill and drain weigh more); none otherwise (equal-length CTAs
 // would only fill fewer, longer waves).
-int bwd_pair_kt(const dm_attn_params* p, int T) {
-  if (!p->causal || (p->Hq / p->Hkv) % 2 != 0) return T;
-  return T <= 32 ? 0 : T - T / 2;
+// The key tiles are counted in the sequence's numbering and the result is
+// given in the key block's (Tk tiles from kt_off on).
+int bwd_pair_kt(const dm_attn_params* p, int T, int Tk, int kt_off) {
+  if (!p->causal || (p->Hq / p->Hkv) % 2 != 0) return Tk;
+  const int global = T <= 32 ? 0 : T - T / 2;
+  return std::min(Tk, std::max(0, global - kt_off));
 }
 
 dm::AttnArgs make_args(const dm_attn_params* p, unsigned int* status) {
   dm::AttnArgs a{};
   a.B = p->B, a.Hq = p->Hq, a.Hkv = p->Hkv, a.N = p->N;
   a.T = (p->N + kTileRows - 1) / kTileRows;
-  a.bwd_pair_kt = bwd_pair_kt(p, a.T);
+  a.Nk = key_rows(p);
+  a.Tk = (a.Nk + kTileRows - 1) / kTileRows;
+  a.kt_off = p->kv_offset / kTileRows;
+  a.bwd_pair_kt = bwd_pair_kt(p, a.T, a.Tk, a.kt_off);
   a.causal = p->causal ? 1 : 0;
   a.dqk = p->d;
   a.dv = value_dim(p);
@@ -202,19 +216,21 @@ dm_status check_delta_inputs(dm_delta_mode mode, dm_fp8_tensor q, dm_fp8_tensor 
 
 dm_status delta_impl(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor q, dm_fp8_tensor k,
                      dm_fp8_tensor v, dm_fp8_tensor do_hat, const float* lse, const void* dO, dm_dtype do_dtype,
-                     const void* O, dm_dtype o_dtype, float* delta, unsigned int* status, cudaStream_t st) {
+                     const void* O, dm_dtype o_dtype, float* delta, unsigned int* status, cudaStream_t st,
+                     float* den = nullptr) {
   dm::AttnArgs a = make_args(p, status);
   if (mode == DM_DELTA_MATCHED) {
     dm::DeltaLaunch f{};
     const int kw = kernel_dim(p), dv = value_dim(p);
     DM_TRY(encode_codes_map(&f.tmQ, q.codes, p->B * p->Hq, p->N, p->d, kw));
-    DM_TRY(encode_codes_map(&f.tmK, k.codes, p->B * p->Hkv, p->N, p->d, kw));
-    DM_TRY(encode_codes_map(&f.tmV, v.codes, p->B * p->Hkv, p->N, dv, kw));
+    DM_TRY(encode_codes_map(&f.tmK, k.codes, p->B * p->Hkv, key_rows(p), p->d, kw));
+    DM_TRY(encode_codes_map(&f.tmV, v.codes, p->B * p->Hkv, key_rows(p), dv, kw));
     DM_TRY(encode_codes_map(&f.tmDO, do_hat.codes, p->B * p->Hq, p->N, dv, kw));
     a.q_scales = q.scales, a.k_scales = k.scales, a.v_scales = v.scales, a.do_scales = do_hat.scales;
     f.args = a;
     f.lse = lse;
     f.delta = delta;
+    f.den = den;
     return cuda_status(dm::launch_delta_matched(f, kw, kernel_value_dim(p), st));
   }
   a.do_scales = do_hat.scales;
@@ -228,6 +244,8 @@ dm_status dm::check_attn_problem(const dm_attn_params* p, dm_delta_mode mode) {
   DM_TRY(check_params(p));
   return valid_mode(mode) ? DM_OK : DM_ERR_INVALID_ARG;
 }
+
+bool dm::is_key_block(const dm_attn_params* p) { return key_block(p); }
 
 extern "C" {
 
@@ -411,8 +429,8 @@ dm_status dm_attn_fwd(const dm_attn_params* p, dm_fp8_tensor q, dm_fp8_tensor k,
   dm::FwdLaunch f{};
   const int kw = kernel_dim(p);
   DM_TRY(encode_codes_map(&f.tmQ, q.codes, p->B * p->Hq, p->N, p->d, kw));
-  DM_TRY(encode_codes_map(&f.tmK, k.codes, p->B * p->Hkv, p->N, p->d, kw));
-  DM_TRY(encode_codes_map(&f.tmV, v.codes, p->B * p->Hkv, p->N, value_dim(p), kw));
+  DM_TRY(encode_codes_map(&f.tmK, k.codes, p->B * p->Hkv, key_rows(p), p->d, kw));
+  DM_TRY(encode_codes_map(&f.tmV, v.codes, p->B * p->Hkv, key_rows(p), value_dim(p), kw));
   f.args = make_args(p, status);
   f.args.q_scales = q.scales, f.args.k_scales = k.scales, f.args.v_scales = v.scales;
   {
@@ -468,6 +486,8 @@ dm_status dm_attn_bwd(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor
   const float* dl = delta;
   if (delta) {
     DM_TRY(check_ptr(delta));
+  } else if (key_block(p)) {
+    return DM_ERR_INVALID_ARG;  // a key block's backward needs the merged delta of the whole sequence
   } else {
     DM_TRY(check_delta_inputs(mode, q, k, v, do_hat, lse, dO, do_dtype, O, o_dtype));
     DM_TRY(check_ptr(workspace));
@@ -485,19 +505,20 @@ dm_status dm_attn_bwd(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor
   dm::ZeroList z{};
   const int kw = kernel_dim(p), dv = value_dim(p);
   z.add(dQ, (size_t)p->B * p->Hq * p->N * p->d);
-  z.add(dK, (size_t)p->B * p->Hkv * p->N * p->d);
-  z.add(dV, (size_t)p->B * p->Hkv * p->N * dv);
+  const int nk = key_rows(p);
+  z.add(dK, (size_t)p->B * p->Hkv * nk * p->d);
+  z.add(dV, (size_t)p->B * p->Hkv * nk * dv);
   const size_t nrow = (size_t)p->B * p->Hq * p->N;
   for (float* ptr : {dg.rowsum_pre, dg.abssum_pre, dg.rowsum_post, dg.abssum_post}) z.add(ptr, nrow);
   DM_TRY(cuda_status(dm::launch_zero(z, st)));
   dm::BwdLaunch f{};
   DM_TRY(encode_codes_map(&f.tmQ, q.codes, p->B * p->Hq, p->N, p->d, kw));
-  DM_TRY(encode_codes_map(&f.tmK, k.codes, p->B * p->Hkv, p->N, p->d, kw));
-  DM_TRY(encode_codes_map(&f.tmV, v.codes, p->B * p->Hkv, p->N, dv, kw));
+  DM_TRY(encode_codes_map(&f.tmK, k.codes, p->B * p->Hkv, nk, p->d, kw));
+  DM_TRY(encode_codes_map(&f.tmV, v.codes, p->B * p->Hkv, nk, dv, kw));
   DM_TRY(encode_codes_map(&f.tmDO, do_hat.codes, p->B * p->Hq, p->N, dv, kw));
   DM_TRY(encode_f32_rows_map(&f.tmDQ, dQ, p->B * p->Hq, p->N, p->d));
-  DM_TRY(encode_f32_rows_map(&f.tmDK, dK, p->B * p->Hkv, p->N, p->d));
-  DM_TRY(encode_f32_rows_map(&f.tmDV, dV, p->B * p->Hkv, p->N, dv));
+  DM_TRY(encode_f32_rows_map(&f.tmDK, dK, p->B * p->Hkv, nk, p->d));
+  DM_TRY(encode_f32_rows_map(&f.tmDV, dV, p->B * p->Hkv, nk, dv));
   f.args = make_args(p, status);
   f.args.q_scales = q.scales, f.args.k_scales = k.scales, f.args.v_scales = v.scales;
   f.args.do_scales = do_hat.scales;
@@ -506,6 +527,51 @@ dm_status dm_attn_bwd(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor
   f.dQ = dQ, f.dK = dK, f.dV = dV;
   f.diag = dg;
   return cuda_status(dm::launch_attn_bwd(f, kw, st));
+}
+
+dm_status dm_attn_delta_partial(const dm_attn_params* p, dm_fp8_tensor q, dm_fp8_tensor k, dm_fp8_tensor v,
+                                dm_fp8_tensor do_hat, const float* lse, float* num, float* den, void* stream) {
+  DM_TRY(check_params(p));
+  if (is_empty(p)) return DM_OK;
+  DM_TRY(check_delta_inputs(DM_DELTA_MATCHED, q, k, v, do_hat, lse, nullptr, DM_F32, nullptr, DM_F32));
+  DM_TRY(check_ptr(num));
+  DM_TRY(check_ptr(den));
+  unsigned int* status = nullptr;
+  DM_TRY(device_state(&status));
+  return delta_impl(p, DM_DELTA_MATCHED, q, k, v, do_hat, lse, nullptr, DM_F32, nullptr, DM_F32, num, status,
+                    as_stream(stream), den);
+}
+
+dm_status dm_attn_merge(const dm_attn_params* p, int nparts, const float* O_parts, const float* lse_parts, void* O,
+                        dm_dtype o_dtype, float* lse, void* stream) {
+  DM_TRY(check_params(p));
+  if (nparts < 1) return DM_ERR_INVALID_ARG;
+  if (!valid_dtype(o_dtype)) return DM_ERR_DTYPE;
+  if (is_empty(p)) return DM_OK;
+  DM_TRY(check_ptr(O_parts));
+  DM_TRY(check_ptr(lse_parts));
+  DM_TRY(check_ptr(O));
+  DM_TRY(check_ptr(lse));
+  const long long rows = (long long)p->B * p->Hq * p->N;
+  if (rows * nparts * value_dim(p) >= (1ll << 40)) return DM_ERR_SHAPE;
+  unsigned int* status = nullptr;
+  DM_TRY(device_state(&status));
+  return cuda_status(dm::launch_attn_merge(nparts, O_parts, lse_parts, rows, value_dim(p), O, o_dtype == DM_BF16,
+                                           lse, as_stream(stream)));
+}
+
+dm_status dm_attn_delta_combine(const dm_attn_params* p, int nparts, const float* num_parts, const float* den_parts,
+                                float* delta, void* stream) {
+  DM_TRY(check_params(p));
+  if (nparts < 1) return DM_ERR_INVALID_ARG;
+  if (is_empty(p)) return DM_OK;
+  DM_TRY(check_ptr(num_parts));
+  DM_TRY(check_ptr(den_parts));
+  DM_TRY(check_ptr(delta));
+  unsigned int* status = nullptr;
+  DM_TRY(device_state(&status));
+  return cuda_status(dm::launch_delta_combine(nparts, num_parts, den_parts, (long long)p->B * p->Hq * p->N, delta,
+                                              as_stream(stream)));
 }
 
 }  // extern "C"

@@ -9,7 +9,10 @@
 // before one reduction; pairing the long ones as well would leave a longer
 // tail of CTAs at the end of the launch.  A CTA's dK and dV tiles (its
 // heads' share of the kv head's gradients) are added into global dK and dV
-// with TMA bulk reduce-adds, like dQ.  Products are computed transposed (key
+// with TMA bulk reduce-adds, like dQ.  Over a key block (context
+// parallelism) the CTAs take the block's key tiles only (kt is the block's
+// own tile index, kt + kt_off the global one), and dQ holds the block's
+// partial sums.  Products are computed transposed (key
 // rows on TMEM lanes) so that dV and dK accumulate in TMEM:
 //   S^T  = K Q^T                 P  = exp(S - LSE) in FP32,   P^  = E4M3 per 128x128 tile
 //   dP^T = V dO^T                dS = P (dP - delta) in FP32, dS^ = E5M2 per 128x128 tile
@@ -244,7 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int own_qk = kPart ? max(0, min(C::kDC, a.dqk - col0)) : C::kDC;
   const int n_passes = kPart ? (own_qk + C::kStageCols - 1) / C::kStageCols : C::kPasses;
   const int bg = (bh0 / a.Hq) * a.Hkv + (bh0 % a.Hq) / (a.Hq / a.Hkv);
-  const int qt0 = a.causal ? kt : 0;
+  const int ktg = kt + a.kt_off;  // the key tile's index in the whole sequence
+  const int qt0 = a.causal ? ktg : 0;
   const int n_head = a.T - qt0;  // iterations per query head (>= 1)
   const int n_iter = hpc * n_head;
   // query head (b * Hq + h) and query tile of iteration n
@@ -451,11 +455,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (tile + rsw) ^ 16 c; rsw_wg starts at this warpgroup's 64-byte half
     const uint32_t rsw = SwTile<128>::row_base(r);
     const uint32_t rsw_wg = rsw ^ (64u * wg);
-    const bool kv_valid = kt * kTile + r < a.N;
+    const bool kv_valid = kt * kTile + r < a.Nk;
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
     const int ct = tid - 128;  // 0..255
-    const float sk = a.k_scales[bg * a.T + kt];
-    const float svv = a.v_scales[bg * a.T + kt];
+    const float sk = a.k_scales[bg * a.Tk + kt];
+    const float svv = a.v_scales[bg * a.Tk + kt];
     float udv_a = 0.0f, udv_b = 0.0f, udk_a = 0.0f, udk_b = 0.0f;  // accumulator units (two factors each)
     // Per-iteration global values are loaded one iteration ahead: this
     // thread's element of the query tile's LSE (threads 0-127; +inf for absent
@@ -542,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float c1 = a.sigma * sq * sk * kLog2e;
       const float cdp = sdo * svv;
-      const int cmin = !kv_valid ? (1 << 30) : (a.causal && qt == kt) ? r - wg * 64 : 0;
+      const int cmin = !kv_valid ? (1 << 30) : (a.causal && qt == ktg) ? r - wg * 64 : 0;
 
       // P = exp(S - LSE), its tile amax and E4M3 codes
       float p[64];
@@ -824,7 +828,7 @@ cudaError_t launch_t(const BwdLaunch& f, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int BH = f.args.B * f.args.Hq, pk = f.args.bwd_pair_kt;
-  const unsigned grid = (unsigned)((pk * BH + (f.args.T - pk) * (BH / 2)) * (BwdCfg<D>::kSplit ? 2 : 1));
+  const unsigned grid = (unsigned)((pk * BH + (f.args.Tk - pk) * (BH / 2)) * (BwdCfg<D>::kSplit ? 2 : 1));
   k<<<grid, kThreads, smem, st>>>(f.tmQ, f.tmK, f.tmV, f.tmDO, f.tmDQ, f.tmDK, f.tmDV, f.args, f.lse, f.delta,
                                   f.diag);
   return cudaGetLastError();

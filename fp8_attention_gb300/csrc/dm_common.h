@@ -26,7 +26,11 @@ struct AttnArgs {
   unsigned long long wait_limit_ns;
   int stall_test;            // 1: the MMA warp waits on a barrier nothing signals
   int bwd_pair_kt;           // backward: key tiles from this one on are taken by CTAs
-                             // that walk two query heads of a group (T: none)
+                             // that walk two query heads of a group (Tk: none)
+  // Key block: K, V (and dK, dV) hold Nk rows, the keys at sequence positions
+  // [128 * kt_off, 128 * kt_off + Nk); key tile t of the block is global key
+  // tile t + kt_off.  The whole sequence: Nk = N, Tk = T, kt_off = 0.
+  int Nk, Tk, kt_off;
 };
 
 }  // namespace dm

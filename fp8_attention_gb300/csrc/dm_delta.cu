@@ -7,7 +7,9 @@
 // hold for the P the backward actually uses (identical to the undivided form
 // when P sums to 1).  This is the separate correction pass: one CTA per
 // (batch, query head, 128-row query tile), recomputing S = Q K^T and
-// dP^ = dO^ V^T on tcgen05 tile by tile.
+// dP^ = dO^ V^T on tcgen05 tile by tile.  Over a key block (context
+// parallelism) the two sums can be written apart (den != NULL), so that the
+// blocks' sums add up before the one division.
 //
 // For d = 64 and 128 two CTAs share an SM (192 threads, 256 TMEM columns,
 // ~97 KB of shared memory each): one CTA's reductions overlap the other's
@@ -69,7 +71,8 @@ template <int D, int DV>
 __global__ void __launch_bounds__(kThreads, DeltaCfg<D>::kCTAsPerSM)
     attn_delta_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                      const AttnArgs a, const float* __restrict__ lse, float* __restrict__ delta) {
+                      const AttnArgs a, const float* __restrict__ lse, float* __restrict__ delta,
+                      float* __restrict__ den) {
   using L = DeltaLayout<D, DV>;
   using C = DeltaCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -85,7 +88,8 @@ __global__ void __launch_bounds__(kThreads, DeltaCfg<D>::kCTAsPerSM)
   const int b = bh / a.Hq, h = bh % a.Hq;
   const int bg = b * a.Hkv + h / (a.Hq / a.Hkv);
   const int q0 = qt * kTile;
-  const int nkv = a.causal ? qt + 1 : a.T;
+  // key tiles of the block this query tile sees (0: none)
+  const int nkv = a.causal ? max(0, min(qt + 1 - a.kt_off, a.Tk)) : a.Tk;
 
   // the swizzled tiles need a 1024-byte aligned window (no static shared
   // variables); the status word is written only after the wait for the
@@ -189,8 +193,8 @@ __global__ void __launch_bounds__(kThreads, DeltaCfg<D>::kCTAsPerSM)
     const float sq = a.q_scales[bh * a.T + qt];
     const float sdo = a.do_scales[bh * a.T + qt];
     const float lse2 = row_valid ? lse[(size_t)bh * a.N + qi] * kLog2e : 0.0f;
-    const float* ksc = a.k_scales + (size_t)bg * a.T;
-    const float* vsc = a.v_scales + (size_t)bg * a.T;
+    const float* ksc = a.k_scales + (size_t)bg * a.Tk;
+    const float* vsc = a.v_scales + (size_t)bg * a.Tk;
     float sk_next = ksc[0], sv_next = vsc[0];  // per-tile scales, loaded one tile ahead
     float dl = 0.0f, psum = 0.0f;
     for (int t = 0; t < nkv; ++t) {
@@ -201,8 +205,8 @@ __global__ void __launch_bounds__(kThreads, DeltaCfg<D>::kCTAsPerSM)
         sv_next = vsc[t + 1];
       }
       const int j0 = t * kTile;
-      int jlim = min(kTile, a.N - j0);
-      if (a.causal) jlim = min(jlim, qi - j0 + 1);
+      int jlim = min(kTile, a.Nk - j0);
+      if (a.causal) jlim = min(jlim, qi - (j0 + a.kt_off * kTile) + 1);
       // warp-uniform: the TMEM loads below are warp-collective
       const bool full = __all_sync(0xffffffffu, jlim >= kTile);
       const int tb = t % C::kTBuf;
@@ -253,7 +257,15 @@ __global__ void __launch_bounds__(kThreads, DeltaCfg<D>::kCTAsPerSM)
       dl = fmaf((acc0.x + acc0.y) + (acc1.x + acc1.y), c2, dl);
       psum += (ps0.x + ps0.y) + (ps1.x + ps1.y);
     }
-    if (row_valid) delta[(size_t)bh * a.N + qi] = dl / psum;
+    if (row_valid) {
+      const size_t o = (size_t)bh * a.N + qi;
+      if (den) {  // the block's two sums, apart
+        delta[o] = dl;
+        den[o] = psum;
+      } else {
+        delta[o] = psum > 0.0f ? dl / psum : 0.0f;  // 0 for a row that sees no key of the block
+      }
+    }
   }
 
   tc_fence_before();
@@ -272,7 +284,8 @@ cudaError_t launch_t(const DeltaLaunch& f, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(f.args.B * f.args.Hq * f.args.T);
-  return launch_overlapped(k, grid, kThreads, smem, st, f.tmQ, f.tmK, f.tmV, f.tmDO, f.args, f.lse, f.delta);
+  return launch_overlapped(k, grid, kThreads, smem, st, f.tmQ, f.tmK, f.tmV, f.tmDO, f.args, f.lse, f.delta,
+                           f.den);
 }
 
 }  // namespace

@@ -8,6 +8,12 @@
 //
 // Stale corrections: delta_i = <dO_i, O_i> (section 01, "Why can we reuse the
 // forward output?") and delta_i = <dO^_i, O_i> (section 03), one warp per row.
+//
+// Key-block merges (context parallelism over the sequence; the project page's
+// section 06 extends the context to 64K tokens): the attention of every query
+// row over disjoint key blocks r merges as LSE = ln sum_r exp(LSE_r),
+// O = sum_r exp(LSE_r - LSE) O_r, and the matched delta as
+// sum_r (sum_j P dP^)_r / sum_r (sum_j P)_r.
 #include <cuda_bf16.h>
 
 #include "dm_device.cuh"
@@ -160,6 +166,14 @@ __device__ __forceinline__ void load_row(const __nv_bfloat16* p, int k0, int n, 
   }
 }
 
+__device__ __forceinline__ void store_row(float* p, int k0, int n, const float* v) {
+  for (int k = 0; k < n; k += 2) *reinterpret_cast<float2*>(p + k0 + k) = make_float2(v[k], v[k + 1]);
+}
+__device__ __forceinline__ void store_row(__nv_bfloat16* p, int k0, int n, const float* v) {
+  for (int k = 0; k < n; k += 2)
+    *reinterpret_cast<__nv_bfloat162*>(p + k0 + k) = __floats2bfloat162_rn(v[k], v[k + 1]);
+}
+
 // MODE 1: delta = <dO, O>; MODE 2: delta = s_dO * <codes(dO^), O>.  One warp
 // per row, each lane holds d/32 consecutive channels.
 template <int MODE, int D, typename TD, typename TO>
@@ -222,6 +236,71 @@ cudaError_t stale_d(const AttnArgs& a, dm_delta_mode mode, const void* dO, dm_dt
                               delta, st);
 }
 
+// Merge of nparts stacked key-block results, one warp per row, each lane
+// holding D/32 consecutive channels: O_parts [nparts][rows][D] fp32,
+// lse_parts [nparts][rows].  Blocks that see none of a row's keys carry
+// LSE = -inf and weigh zero; a row no block sees gets O = 0, LSE = -inf.
+template <int D, typename TO>
+__global__ void __launch_bounds__(256) merge_kernel(int nparts, const float* __restrict__ O_parts,
+                                                    const float* __restrict__ lse_parts, long long rows,
+                                                    TO* __restrict__ O, float* __restrict__ lse) {
+  constexpr int PER = D / 32;
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  float m = -INFINITY;
+  for (int r = 0; r < nparts; ++r) m = fmaxf(m, __ldg(lse_parts + r * rows + row));
+  float o[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) o[k] = 0.0f;
+  float lse_row = -INFINITY;
+  if (m != -INFINITY) {
+    float wsum = 0.0f;
+    for (int r = 0; r < nparts; ++r) {
+      const float w = expf(__ldg(lse_parts + r * rows + row) - m);
+      wsum += w;
+      if (w == 0.0f) continue;  // uniform over the warp (one row)
+      float x[PER];
+      load_row(O_parts + ((size_t)r * rows + row) * D, lane * PER, PER, x);
+#pragma unroll
+      for (int k = 0; k < PER; ++k) o[k] = fmaf(w, x[k], o[k]);
+    }
+    const float inv = 1.0f / wsum;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) o[k] *= inv;
+    lse_row = m + logf(wsum);
+  }
+  store_row(O + (size_t)row * D, lane * PER, PER, o);
+  if (lane == 0) lse[row] = lse_row;
+}
+
+// delta = sum_r num_r / sum_r den_r per row (0 where no block sees the row).
+__global__ void __launch_bounds__(256) delta_combine_kernel(int nparts, const float* __restrict__ num,
+                                                            const float* __restrict__ den, long long rows,
+                                                            float* __restrict__ delta) {
+  for (long long row = (long long)blockIdx.x * blockDim.x + threadIdx.x; row < rows;
+       row += (long long)gridDim.x * blockDim.x) {
+    float a = 0.0f, b = 0.0f;
+    for (int r = 0; r < nparts; ++r) {
+      a += __ldg(num + r * rows + row);
+      b += __ldg(den + r * rows + row);
+    }
+    delta[row] = b > 0.0f ? a / b : 0.0f;
+  }
+}
+
+template <int D>
+cudaError_t merge_d(int nparts, const float* O_parts, const float* lse_parts, long long rows, void* O, bool o_bf16,
+                    float* lse, cudaStream_t st) {
+  const unsigned grid = (unsigned)((rows + 7) / 8);
+  if (o_bf16)
+    merge_kernel<D, __nv_bfloat16><<<grid, 256, 0, st>>>(nparts, O_parts, lse_parts, rows,
+                                                          reinterpret_cast<__nv_bfloat16*>(O), lse);
+  else
+    merge_kernel<D, float><<<grid, 256, 0, st>>>(nparts, O_parts, lse_parts, rows, reinterpret_cast<float*>(O), lse);
+  return cudaGetLastError();
+}
+
 // Zero fill of several FP32 buffers in one launch.  Each buffer is written
 // with 16-byte stores between its first and last 16-byte boundary and with
 // scalar stores at its ragged ends, so any 4-byte aligned pointer works.
@@ -255,6 +334,24 @@ cudaError_t launch_delta_stale(const AttnArgs& a, int d, dm_delta_mode mode, con
   if (d == 192) return stale_d<192>(a, mode, dO, do_t, do_codes, O, o_t, delta, st);
   return d == 128 ? stale_d<128>(a, mode, dO, do_t, do_codes, O, o_t, delta, st)
                   : stale_d<64>(a, mode, dO, do_t, do_codes, O, o_t, delta, st);
+}
+
+cudaError_t launch_attn_merge(int nparts, const float* O_parts, const float* lse_parts, long long rows, int dv,
+                              void* O, bool o_bf16, float* lse, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  if (dv == 256) return merge_d<256>(nparts, O_parts, lse_parts, rows, O, o_bf16, lse, st);
+  if (dv == 192) return merge_d<192>(nparts, O_parts, lse_parts, rows, O, o_bf16, lse, st);
+  return dv == 128 ? merge_d<128>(nparts, O_parts, lse_parts, rows, O, o_bf16, lse, st)
+                   : merge_d<64>(nparts, O_parts, lse_parts, rows, O, o_bf16, lse, st);
+}
+
+cudaError_t launch_delta_combine(int nparts, const float* num_parts, const float* den_parts, long long rows,
+                                 float* delta, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  long long blocks = (rows + 255) / 256;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  delta_combine_kernel<<<(unsigned)blocks, 256, 0, st>>>(nparts, num_parts, den_parts, rows, delta);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_zero(const ZeroList& z, cudaStream_t st) {

@@ -121,7 +121,9 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
   const int b = bh / a.Hq, h = bh % a.Hq;
   const int bg = b * a.Hkv + h / (a.Hq / a.Hkv);
   const int q0 = qt * kTile;
-  const int nkv = a.causal ? qt + 1 : a.T;
+  // key tiles of the block this query tile sees (0: none, for a causal query
+  // tile before the block)
+  const int nkv = a.causal ? max(0, min(qt + 1 - a.kt_off, a.Tk)) : a.Tk;
 
   // the swizzled tiles need a 1024-byte aligned window (no static shared
   // variables); the status word is written only after the wait for the
@@ -254,8 +256,8 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
     const bool row_valid = qi < a.N;
     const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
     const float sq = a.q_scales[bh * a.T + qt];
-    const float* ksc = a.k_scales + (size_t)bg * a.T;
-    const float* vsc = a.v_scales + (size_t)bg * a.T;
+    const float* ksc = a.k_scales + (size_t)bg * a.Tk;
+    const float* vsc = a.v_scales + (size_t)bg * a.Tk;
     float sk_next = ksc[0], sv_next = vsc[0];  // per-tile scales, loaded one tile ahead
     float m = -INFINITY, l = 0.0f;             // running max (log2 units), row sum
     float u_p = 0.0f, u_v = 0.0f;              // O in true units = u_p * u_v * O_tmem
@@ -267,9 +269,9 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
         sk_next = ksc[t + 1];
         sv_next = vsc[t + 1];
       }
-      const int j0 = t * kTile;
-      int jlim = min(kTile, a.N - j0);
-      if (a.causal) jlim = min(jlim, qi - j0 + 1);
+      const int j0 = t * kTile;  // first key of the tile within the block
+      int jlim = min(kTile, a.Nk - j0);
+      if (a.causal) jlim = min(jlim, qi - (j0 + a.kt_off * kTile) + 1);
       // no masked column in this warp's rows (all but the diagonal/ragged
       // tile); warp-uniform, because the masked and unmasked paths both issue
       // warp-collective TMEM loads
@@ -424,17 +426,25 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
     }
 
     // LSE and O / l; O rows are a.dv wide (the kernel's d columns of O hold
-    // zeros beyond the value head dimension)
-    if (row_valid) lse[(size_t)bh * a.N + qi] = m * kLn2 + logf(l);
-    wait(&bars.ofull, (nkv - 1) & 1, wd, 115);
-    tc_fence_after();
-    const float linv = u_p / l;  // O = O_tmem * (u_p / l) * u_v, two products so that no factor underflows
+    // zeros beyond the value head dimension).  A query tile that sees no key
+    // of the block writes LSE = -inf and O = 0.
+    if (row_valid) lse[(size_t)bh * a.N + qi] = nkv > 0 ? m * kLn2 + logf(l) : -INFINITY;
+    if (nkv > 0) {
+      wait(&bars.ofull, (nkv - 1) & 1, wd, 115);
+      tc_fence_after();
+    }
+    const float linv = nkv > 0 ? u_p / l : 0.0f;  // O = O_tmem * (u_p / l) * u_v, two products so that no factor underflows
     const int dv = a.dv;
 #pragma unroll
     for (int c0 = 0; c0 < DV; c0 += 64) {
       if (c0 >= dv) break;  // uniform over the CTA
       float o[64];
-      tmem_load64(tl + C::kColO + c0, tl + C::kColO + c0 + 32, o);  // warp-collective: before the row guard
+      if (nkv > 0) {  // uniform: TMEM loads are warp-collective, before the row guard
+        tmem_load64(tl + C::kColO + c0, tl + C::kColO + c0 + 32, o);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 64; ++k) o[k] = 0.0f;
+      }
       if (row_valid) {
         if (OUT_BF16) {
           __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(O) + ((size_t)bh * a.N + qi) * dv + c0;

@@ -41,7 +41,8 @@ struct DeltaLaunch {
   CUtensorMap tmQ, tmK, tmV, tmDO;
   AttnArgs args;
   const float* lse;
-  float* delta;
+  float* delta;  // delta, or (with den) sum_j P dP^ over the key block
+  float* den;    // nullable: sum_j P over the key block
 };
 
 struct BwdLaunch {
@@ -115,11 +116,20 @@ struct ZeroList {
 };
 
 cudaError_t launch_zero(const ZeroList& z, cudaStream_t st);
+// Key-block merges (context parallelism), rows = B * Hq * N: O [rows][dv]
+// (fp32 or bf16) and LSE from nparts stacked block results; delta from
+// nparts stacked (sum P dP^, sum P) pairs.
+cudaError_t launch_attn_merge(int nparts, const float* O_parts, const float* lse_parts, long long rows, int dv,
+                              void* O, bool o_bf16, float* lse, cudaStream_t st);
+cudaError_t launch_delta_combine(int nparts, const float* num_parts, const float* den_parts, long long rows,
+                                 float* delta, cudaStream_t st);
 cudaError_t launch_attn_bwd(const BwdLaunch& f, int d, cudaStream_t st);
 
 // The checks dm_attn_bwd makes on its problem description and delta mode
 // before anything else (DM_OK, DM_ERR_INVALID_ARG or DM_ERR_SHAPE), for entry
 // points that wrap it.
 dm_status check_attn_problem(const dm_attn_params* p, dm_delta_mode mode);
+// Whether the call covers a key block rather than the whole sequence.
+bool is_key_block(const dm_attn_params* p);
 
 }  // namespace dm

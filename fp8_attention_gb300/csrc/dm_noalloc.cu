@@ -75,6 +75,7 @@ extern "C" dm_status dm_attn_bwd_noalloc(const dm_attn_params* p, dm_delta_mode 
   // gets the same status from both entry points
   const dm_status pv = dm::check_attn_problem(p, mode);
   if (pv != DM_OK) return pv;
+  if (dm::is_key_block(p)) return DM_ERR_INVALID_ARG;  // a key block needs the merged delta: dm_attn_bwd
   if ((long long)p->B * p->Hq * p->N > (long long)DM_NOALLOC_MAX_DELTA_ROWS) return DM_ERR_SHAPE;
   if (p->B == 0 || p->N == 0) return DM_OK;
   const dm_fp8_tensor t4[4] = {q, k, v, do_hat};

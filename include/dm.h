@@ -103,12 +103,24 @@ typedef enum {
  * (0 selects d).  They may differ (heads shaped like multi-head latent
  * attention, e.g. d = 192, d_v = 128) when both are 128, 192 or 256; such
  * heads run on the d = 256 kernels, which read the missing channels as
- * zeros and write only the real ones. */
+ * zeros and write only the real ones.
+ *
+ * Key block (context parallelism over the sequence; the project page's
+ * section 06 extends the context from 8K to 64K tokens and does not say how
+ * the sequence is split): with kv_offset or kv_len set, a call sees only the
+ * keys at sequence positions [kv_offset, kv_offset + kv_len) (kv_len <= 0:
+ * up to N), and K, V, dK, dV hold just those kv_len rows ([B][Hkv][kv_len][.],
+ * scales [B][Hkv][ceil(kv_len/128)]); queries, dO, O, LSE, delta and dQ keep
+ * all N rows.  kv_offset is a multiple of 128 (the key tiles then are the
+ * sequence's own, so K and V quantised by block match the whole tensor's
+ * codes and scales), 0 <= kv_offset < N and kv_offset + kv_len <= N.  Both 0
+ * (a zero-initialised struct) is the whole sequence. */
 typedef struct {
   int B, Hq, Hkv, N, d;
   int causal;
   float softmax_scale;
   int d_v;
+  int kv_offset, kv_len;
 } dm_attn_params;
 
 /* A block-scaled FP8 tensor: codes [B][H][N][d], scales [B][H][ceil(N/128)]. */
@@ -204,7 +216,10 @@ dm_status dm_qk_prologue_batch(const dm_prologue_job* jobs, int njobs, dm_dtype 
  * shapes [B][Hq][N][d], [B][Hkv][N][d], [B][Hkv][N][d_v].  O: [B][Hq][N][d_v]
  * of o_dtype (DM_F32 or DM_BF16).  lse: float [B][Hq][N], natural log of the
  * softmax denominator including the scale sigma, i.e. LSE_i = ln sum_j
- * exp(S_ij).  O and LSE are the only saved forward outputs. */
+ * exp(S_ij).  O and LSE are the only saved forward outputs.  Over a key block
+ * (see dm_attn_params) O and LSE are the block's own attention (its one-pass
+ * quantisation starting at the block's first key tile); a row that sees no
+ * key of the block gets O = 0 and LSE = -inf.  dm_attn_merge combines blocks. */
 dm_status dm_attn_fwd(const dm_attn_params* p, dm_fp8_tensor q, dm_fp8_tensor k, dm_fp8_tensor v,
                       void* O, dm_dtype o_dtype, float* lse, void* stream);
 
@@ -212,7 +227,9 @@ dm_status dm_attn_fwd(const dm_attn_params* p, dm_fp8_tensor q, dm_fp8_tensor k,
  * dO, do_hat and O are [B][Hq][N][d_v].
  *  DM_DELTA_MATCHED:     needs q, k, v, do_hat (E5M2), lse; recomputes S and
  *                        dP^ = dO^ V^T tile by tile in FP32 (the separate
- *                        correction pass).  dO and O may be NULL.
+ *                        correction pass).  dO and O may be NULL.  Over a key
+ *                        block: the block's own correction (for the blocks of
+ *                        one sequence use dm_attn_delta_partial).
  *  DM_DELTA_STALE_DO:    needs dO (do_dtype) and O (o_dtype).
  *  DM_DELTA_STALE_DOHAT: needs do_hat and O (o_dtype).  */
 dm_status dm_attn_delta(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor q, dm_fp8_tensor k,
@@ -227,7 +244,10 @@ dm_status dm_attn_delta(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tens
  * [B][Hq][N][d] (overwritten, not accumulated), dK float [B][Hkv][N][d] and
  * dV float [B][Hkv][N][d_v] (summed over each kv head's query heads).  diag: optional
  * row-sum diagnostics (NULL = off).  dO/O are needed only when delta is NULL
- * and the mode is stale.  */
+ * and the mode is stale.  Over a key block: lse and delta must be the whole
+ * sequence's (merged; delta NULL gives DM_ERR_INVALID_ARG), dK and dV are the
+ * block's rows ([B][Hkv][kv_len][.]) and dQ and diag hold the block's partial
+ * sums (the blocks' dQ add up to the sequence's). */
 dm_status dm_attn_bwd(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor q, dm_fp8_tensor k,
                       dm_fp8_tensor v, dm_fp8_tensor do_hat, const float* lse, const float* delta,
                       const void* dO, dm_dtype do_dtype, const void* O, dm_dtype o_dtype, float* dQ,
@@ -243,7 +263,8 @@ size_t dm_attn_bwd_workspace_size(const dm_attn_params* p);
  * ahead of the step and forbids allocations inside it, or a host program that
  * reaches this library only through this C ABI with no device allocator of its
  * own.  The method's pages have no counterpart to this call; it exists only
- * for such callers.
+ * for such callers.  A key block (dm_attn_params) is rejected with
+ * DM_ERR_INVALID_ARG: its delta must be the merged one of the whole sequence.
  *
  * Arguments are those of dm_attn_bwd without delta and workspace.  delta is
  * kept in a fixed device array of DM_NOALLOC_MAX_DELTA_ROWS floats (8 MiB),
@@ -261,6 +282,36 @@ dm_status dm_attn_bwd_noalloc(const dm_attn_params* p, dm_delta_mode mode, dm_fp
                               dm_fp8_tensor v, dm_fp8_tensor do_hat, const float* lse, const void* dO,
                               dm_dtype do_dtype, const void* O, dm_dtype o_dtype, float* dQ, float* dK,
                               float* dV, const dm_diag* diag, void* stream);
+
+/* dm_attn_delta_partial -- the two sums of the matched correction over a key
+ * block (section 03's delta_i = sum_j P_ij dP^_ij / sum_j P_ij, split by key
+ * blocks so that the blocks of one sequence add up before the division):
+ * num_i = sum_{j in block} P_ij dP^_ij and den_i = sum_{j in block} P_ij, each
+ * float [B][Hq][N] (0 for a row that sees no key of the block), with P =
+ * exp(S - LSE) from the whole sequence's (merged) lse.  Arguments as
+ * dm_attn_delta in DM_DELTA_MATCHED mode.  dm_attn_delta_combine divides. */
+dm_status dm_attn_delta_partial(const dm_attn_params* p, dm_fp8_tensor q, dm_fp8_tensor k, dm_fp8_tensor v,
+                                dm_fp8_tensor do_hat, const float* lse, float* num, float* den, void* stream);
+
+/* dm_attn_merge -- the attention of every query row over the union of nparts
+ * disjoint key blocks from the blocks' own results (dm_attn_fwd over each):
+ * LSE_i = ln sum_r exp(LSE_r,i) and O_i = sum_r exp(LSE_r,i - LSE_i) O_r,i.
+ * O_parts: float [nparts][B][Hq][N][d_v] (the blocks' fp32 O, stacked, e.g. by
+ * an all-gather), lse_parts: float [nparts][B][Hq][N]; O: [B][Hq][N][d_v] of
+ * o_dtype (DM_F32 or DM_BF16), lse: float [B][Hq][N].  Blocks with LSE = -inf
+ * weigh zero; a row that no block sees gets O = 0 and LSE = -inf.  p gives B,
+ * Hq, N and d_v (its key block is ignored).  Errors: DM_ERR_INVALID_ARG
+ * (nparts < 1, NULL pointer), DM_ERR_DTYPE, DM_ERR_ALIGNMENT, DM_ERR_SHAPE. */
+dm_status dm_attn_merge(const dm_attn_params* p, int nparts, const float* O_parts, const float* lse_parts, void* O,
+                        dm_dtype o_dtype, float* lse, void* stream);
+
+/* dm_attn_delta_combine -- delta_i = sum_r num_r,i / sum_r den_r,i from
+ * nparts stacked dm_attn_delta_partial results (num_parts and den_parts each
+ * float [nparts][B][Hq][N]; nparts = 1 after the sums were reduced across
+ * devices), 0 where every den is 0.  delta: float [B][Hq][N].  p gives B, Hq
+ * and N.  Errors as dm_attn_merge. */
+dm_status dm_attn_delta_combine(const dm_attn_params* p, int nparts, const float* num_parts, const float* den_parts,
+                                float* delta, void* stream);
 
 /* Synchronises `stream`, then returns and clears the device status word of
  * the current device: DM_ERR_TIMEOUT if a kernel's bounded wait expired since

@@ -333,12 +333,14 @@ def pipeline(q, k, v, do, causal=True, sigma=0.0, mode=DELTA_MATCHED, o_bf16=Fal
     return res
 
 
-def pipeline_key_blocks(q, k, v, do, bounds, causal=True, sigma=0.0, flags=GPU_CONTRACT, o_bf16=False):
+def pipeline_key_blocks(q, k, v, do, bounds, causal=True, sigma=0.0, flags=GPU_CONTRACT, o_bf16=False,
+                        q_tiles=None, kv_tiles=None, groups=None):
     """The pipeline with the keys split into blocks [bounds[r], bounds[r+1])
     (context parallelism): quantise, forward per block, merge of O and LSE,
     matched delta from the blocks' partial sums (added before the division),
     backward per block with the merged LSE and delta, dQ summed over blocks.
-    Returns the same keys as pipeline() plus the per-block partials."""
+    Returns the same keys as pipeline() plus the per-block O_parts, LSE_parts.
+    q_tiles / kv_tiles / groups select outputs as in pipeline() (other rows NaN)."""
     q = np.asarray(q, np.float32)
     k = np.asarray(k, np.float32)
     v = np.asarray(v, np.float32)
@@ -348,31 +350,45 @@ def pipeline_key_blocks(q, k, v, do, bounds, causal=True, sigma=0.0, flags=GPU_C
         c, s = quantize(x, fmt)
         res[name + "_codes"], res[name + "_scales"] = c, s
         dec[name] = dequantize(c, s, fmt)
+    rows = _delta_tiles(q_tiles, kv_tiles, q.shape[2], causal)
     blocks = list(zip(bounds[:-1], bounds[1:]))
-    parts = [attn_fwd(dec["q"], dec["k"], dec["v"], causal, sigma, flags, kv_range=b) for b in blocks]
+    parts = [attn_fwd(dec["q"], dec["k"], dec["v"], causal, sigma, flags, rows, groups, kv_range=b) for b in blocks]
     # each block's O as the GPU stores it (fp32), its LSE in fp32
     O_parts = np.stack([p[0].astype(np.float32).astype(np.float64) for p in parts])
     L_parts = np.stack([p[1].astype(np.float32).astype(np.float64) for p in parts])
-    O, LSE = attn_merge(O_parts, L_parts)
+    with np.errstate(invalid="ignore"):
+        O, LSE = attn_merge(O_parts, L_parts)
+    unsel = np.isnan(L_parts).any(0)      # rows the selection left out stay NaN
+    O[unsel] = np.nan
+    LSE[unsel] = np.nan
     O_st = round_bf16(O) if o_bf16 else O.astype(np.float32).astype(np.float64)
     LSE_st = LSE.astype(np.float32).astype(np.float64)
     num = np.zeros(LSE.shape)
     den = np.zeros(LSE.shape)
     for b in blocks:
         n_r, d_r = attn_delta(dec["q"], dec["k"], dec["v"], dec["do"], LSE_st, DELTA_MATCHED, causal=causal,
-                              sigma=sigma, flags=flags, kv_range=b, partial=True)
+                              sigma=sigma, flags=flags, q_tiles=rows, groups=groups, kv_range=b, partial=True)
         num += n_r.astype(np.float32)
         den += d_r.astype(np.float32)
-    delta = num / den
-    dQ = np.zeros(q.shape)
-    dK = np.zeros(k.shape)
-    dV = np.zeros(v.shape)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        delta = np.where(den > 0, num / den, 0.0)
+    delta[np.isnan(num)] = np.nan
+    dQ = np.full(q.shape, np.nan) if q_tiles is not None or groups is not None else np.zeros(q.shape)
+    dK = np.full(k.shape, np.nan)
+    dV = np.full(v.shape, np.nan)
+    T = (q.shape[2] + TILE - 1) // TILE
     for b in blocks:
-        g = attn_bwd(dec["q"], dec["k"], dec["v"], dec["do"], LSE_st, delta, causal, sigma, flags, kv_range=b)
-        dQ += g["dQ"]
-        dK[:, :, b[0]:b[1]] = g["dK"][:, :, b[0]:b[1]]
-        dV[:, :, b[0]:b[1]] = g["dV"][:, :, b[0]:b[1]]
-    res.update(O_parts=O_parts, LSE_parts=L_parts, O=O_st, LSE=LSE_st, delta=delta, dQ=dQ, dK=dK, dV=dV)
+        block_tiles = range(b[0] // TILE, (b[1] + TILE - 1) // TILE)
+        kts = [t for t in block_tiles if kv_tiles is None or t in set(kv_tiles)]
+        g = attn_bwd(dec["q"], dec["k"], dec["v"], dec["do"], LSE_st, delta, causal, sigma, flags, q_tiles, kts,
+                     groups, kv_range=b)
+        dQ = np.where(np.isnan(g["dQ"]), dQ, np.nan_to_num(dQ) + g["dQ"])
+        for t in kts:
+            rs = slice(t * TILE, min(b[1], t * TILE + TILE))
+            dK[:, :, rs] = g["dK"][:, :, rs]
+            dV[:, :, rs] = g["dV"][:, :, rs]
+    res.update(O_parts=O_parts, LSE_parts=L_parts, O=O_st, LSE=LSE_st, delta=delta, dQ=dQ, dK=dK, dV=dV,
+               O_exact=O)
     return res
 
 

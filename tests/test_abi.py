@@ -51,8 +51,8 @@ def test_knobs(lib):
     assert lib.dm_set_knob(dm.DM_KNOB_WAIT_LIMIT_NS, 0) == 0
 
 
-def _p(B=1, Hq=2, Hkv=1, N=256, d=64, causal=1, scale=0.0, d_v=0):
-    return dm._Params(B, Hq, Hkv, N, d, causal, scale, d_v)
+def _p(B=1, Hq=2, Hkv=1, N=256, d=64, causal=1, scale=0.0, d_v=0, kv_offset=0, kv_len=0):
+    return dm._Params(B, Hq, Hkv, N, d, causal, scale, d_v, kv_offset, kv_len)
 
 
 def test_validation_without_gpu(lib):
@@ -126,6 +126,32 @@ def test_noalloc_validates_like_the_workspace_backward(lib):
         assert both(params, mode, ff) == (want, want), (params.B, params.N, params.d, mode)
     assert lib.dm_attn_bwd_noalloc(None, 0, f, f, f, f, A, None, 0, None, 0, A, A, A, None, None) \
         == dm.DM_ERR_INVALID_ARG
+
+
+def test_key_block_validation_without_gpu(lib):
+    """Key blocks: a 128-aligned start inside the sequence; the backward of a
+    block needs the merged delta; the merges reject bad part counts and dtypes."""
+    A = 0x10000
+    f = dm._Fp8(A, A)
+    fwd = lib.dm_attn_fwd
+    for off, ln in ((64, 0), (-128, 0), (256, 0), (128, 129), (0, -1)):
+        p = _p(N=256, kv_offset=off, kv_len=ln)
+        assert fwd(ctypes.byref(p), f, f, f, A, 5, A, None) == dm.DM_ERR_SHAPE, (off, ln)
+    for off, ln in ((128, 0), (128, 128), (0, 128), (0, 256)):
+        p = _p(N=256, kv_offset=off, kv_len=ln)   # valid: stopped by the bad dtype after the shape checks
+        assert fwd(ctypes.byref(p), f, f, f, A, 5, A, None) == dm.DM_ERR_DTYPE, (off, ln)
+    blk = _p(N=256, kv_offset=128)
+    assert lib.dm_attn_bwd(ctypes.byref(blk), 0, f, f, f, f, A, None, None, 0, None, 0, A, A, A, None, A, 1 << 20,
+                           None) == dm.DM_ERR_INVALID_ARG
+    assert lib.dm_attn_bwd_noalloc(ctypes.byref(blk), 0, f, f, f, f, A, None, 0, None, 0, A, A, A, None,
+                                   None) == dm.DM_ERR_INVALID_ARG
+    assert lib.dm_attn_merge(ctypes.byref(_p()), 0, A, A, A, 0, A, None) == dm.DM_ERR_INVALID_ARG
+    assert lib.dm_attn_merge(ctypes.byref(_p()), 2, A, A, A, 4, A, None) == dm.DM_ERR_DTYPE
+    assert lib.dm_attn_merge(ctypes.byref(_p()), 2, A + 4, A, A, 0, A, None) == dm.DM_ERR_ALIGNMENT
+    assert lib.dm_attn_merge(ctypes.byref(_p(B=0)), 2, None, None, None, 0, None, None) == 0
+    assert lib.dm_attn_delta_combine(ctypes.byref(_p()), 0, A, A, A, None) == dm.DM_ERR_INVALID_ARG
+    assert lib.dm_attn_delta_combine(ctypes.byref(_p()), 1, A, None, A, None) == dm.DM_ERR_INVALID_ARG
+    assert lib.dm_attn_delta_partial(ctypes.byref(_p()), f, f, f, f, A, A, None, None) == dm.DM_ERR_INVALID_ARG
 
 
 def test_workspace_size(lib):
