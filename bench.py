@@ -81,6 +81,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of the captured step")
     ap.add_argument("--no-fp8-peak", action="store_true", help="skip the dense FP8 GEMM peak measurement")
+    ap.add_argument("--key-blocks", type=int, default=2,
+                    help="also time the step with the keys split into this many blocks (1: skip)")
     return ap.parse_args()
 
 
@@ -360,7 +362,10 @@ def run_native(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     stale_line = timed_stale_delta(args, w, dm, p, dev, st, flush, qq, kk, vv, dd, lse_fwd, dod, O_fwd)
     diag_line = row_sum_diagnostics(w, dm, p, st, qq, kk, vv, dd, lse_fwd, dod, O_fwd)
-    del qq, kk, vv, dd, O_fwd, lse_fwd
+    del O_fwd, lse_fwd
+    kb_line = timed_key_blocks(args, w, dm, dev, st, flush, qd, kd, vd, dod, qq, dd) if args.key_blocks > 1 \
+        else {"skipped": "--key-blocks 1"}
+    del qq, kk, vv, dd
     fp8_line = measure_fp8_peak(dev) if not args.no_fp8_peak else {"skipped": "--no-fp8-peak"}
 
     fl = flops_of(w)
@@ -433,6 +438,7 @@ def run_native(args, rank, world, local_rank):
                                        "(null once the source differs)"},
         "stale_delta": stale_line,
         "diagnostics": diag_line,
+        "key_blocks": kb_line,
         "e2e": {"value": round(world * step_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                 "steps": e2e_steps,
@@ -544,6 +550,100 @@ def measure_fp8_peak(dev, n=8192, burst_reps=10, sustained_s=1.0):
                        f"{reps} back to back (sustained)", "clocks": clk.summary()}
     except (RuntimeError, TypeError) as exc:   # FP8 GEMM not available in this torch build
         return {"burst_tflops": None, "error": str(exc).splitlines()[0][:200]}
+
+
+def timed_key_blocks(args, w, dm, dev, st, flush, qd, kd, vd, dod, qq, dd):
+    """The step with the keys split into S blocks (the per-rank work of an
+    S-way context-parallel group, run one block after the other on this GPU):
+    forward per block, merge, partial delta sums per block, combine, backward
+    per block.  The collectives (all-gather of O/LSE, all-reduce of the delta
+    sums and of dQ) are not part of it.  Replayed as a CUDA graph after the L2
+    flush; the merge and combine kernels are also timed alone, in GB/s."""
+    import torch
+    S = args.key_blocks
+    T = (w.N + 127) // 128
+    if T < S:
+        return {"skipped": f"{T} key tiles for {S} blocks"}
+    cuts = [128 * (T * r // S) for r in range(S)] + [w.N]
+    full = dm.AttnParams(w.B, w.Hq, w.Hkv, w.N, w.d, causal=w.causal, d_v=w.d_v)
+    blocks = []
+    with torch.cuda.stream(st):
+        for kb, ke in zip(cuts[:-1], cuts[1:]):
+            pb = dm.AttnParams(w.B, w.Hq, w.Hkv, w.N, w.d, causal=w.causal, d_v=w.d_v, kv_offset=kb,
+                               kv_len=ke - kb)
+            kh = dm.dm_quantize(kd[:, :, kb:ke].contiguous(), dm.DM_E4M3, stream=st)
+            vh = dm.dm_quantize(vd[:, :, kb:ke].contiguous(), dm.DM_E4M3, stream=st)
+            blocks.append((pb, kh, vh))
+    O_parts = torch.empty((S, w.B, w.Hq, w.N, w.d_v), dtype=torch.float32, device=dev)
+    L_parts = torch.empty((S, w.B, w.Hq, w.N), dtype=torch.float32, device=dev)
+    nd = torch.empty((2, S, w.B, w.Hq, w.N), dtype=torch.float32, device=dev)
+    O = torch.empty((w.B, w.Hq, w.N, w.d_v), dtype=torch.float32, device=dev)
+    lse = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=dev)
+    delta = torch.empty_like(lse)
+    grads = [{"dQ": torch.empty((w.B, w.Hq, w.N, w.d), dtype=torch.float32, device=dev),
+              "dK": torch.empty((w.B, w.Hkv, pb.Nk, w.d), dtype=torch.float32, device=dev),
+              "dV": torch.empty((w.B, w.Hkv, pb.Nk, w.d_v), dtype=torch.float32, device=dev)} for pb, _, _ in blocks]
+
+    def merge():
+        dm.dm_attn_merge(full, O_parts, L_parts, O=O, lse=lse, stream=st)
+
+    def combine():
+        dm.dm_attn_delta_combine(full, nd[0], nd[1], delta=delta, stream=st)
+
+    def split_step():
+        for r, (pb, kh, vh) in enumerate(blocks):
+            dm.dm_attn_fwd(pb, qq, kh, vh, O=O_parts[r], lse=L_parts[r], stream=st)
+        merge()
+        for r, (pb, kh, vh) in enumerate(blocks):
+            dm.dm_attn_delta_partial(pb, qq, kh, vh, dd, lse, num=nd[0, r], den=nd[1, r], stream=st)
+        combine()
+        for r, (pb, kh, vh) in enumerate(blocks):
+            g = grads[r]
+            dm.dm_attn_bwd(pb, dm.DM_DELTA_MATCHED, qq, kh, vh, dd, lse, delta, dQ=g["dQ"], dK=g["dK"], dV=g["dV"],
+                           stream=st)
+
+    def timed(fn, reps):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=st):
+            fn()
+        marks = []
+        with torch.cuda.stream(st):
+            for i in range(3 + reps):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(st)
+                graph.replay()
+                b.record(st)
+                if i >= 3:
+                    marks.append((a, b))
+        torch.cuda.synchronize(dev)
+        return statistics.mean(a.elapsed_time(b) for a, b in marks)
+
+    with torch.cuda.stream(st):
+        split_step()          # warm-up, and outside any capture (first calls look up per-device state)
+    torch.cuda.synchronize(dev)
+    reps = max(3, min(args.steps, 50))
+    step_ms = timed(split_step, reps)
+    merge_ms = timed(merge, reps)
+    combine_ms = timed(combine, reps)
+    if dm.dm_get_status(st) != 0:
+        raise RuntimeError("device status error in the key-block step")
+    mp, _ = peaks()
+    hbm = float(mp.get("hbm_gbs", 6800.0))
+    rows = w.B * w.Hq * w.N
+    merge_bytes = 4 * rows * (S * (w.d_v + 1) + w.d_v + 1)
+    combine_bytes = 4 * rows * (2 * S + 1)
+    fl = w.flops()
+    flops = fl["fwd"] + fl["delta"] + fl["bwd"]
+    return {"blocks": S, "cuts": cuts, "ms_per_step": round(step_ms, 4),
+            "tflops": round(flops / (step_ms * 1e-3) / 1e12, 1),
+            "merge": {"ms": round(merge_ms, 4), "bytes": merge_bytes,
+                      "gbs": round(merge_bytes / (merge_ms * 1e-3) / 1e9, 1),
+                      "hbm_frac": round(merge_bytes / (merge_ms * 1e-3) / 1e9 / hbm, 3)},
+            "delta_combine": {"ms": round(combine_ms, 4), "bytes": combine_bytes,
+                              "gbs": round(combine_bytes / (combine_ms * 1e-3) / 1e9, 1)},
+            "timed": "one GPU, the blocks one after the other (an S-rank group's per-rank work), replayed as a "
+                     "CUDA graph after the L2 flush; collectives not included; Q/K/V/dO quantised outside"}
 
 
 def stale_delta_bytes(w, mode_name):

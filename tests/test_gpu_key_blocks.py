@@ -159,3 +159,32 @@ def test_key_block_argument_errors():
     # causal: query tile 0 sees no key of the block [128, 256)
     assert torch.all(torch.isneginf(lse[:, :, :128])) and float(O[:, :, :128].abs().max()) == 0.0
     assert dm.dm_get_status() == 0
+
+
+def test_context_parallel_module_one_rank_nccl():
+    """fp8_attention_gb300.context_parallel with the library's kernels and NCCL
+    collectives in a one-rank group (the whole sequence as the one key block):
+    the same results as the unsplit oracle."""
+    import socket
+
+    import torch.distributed as dist
+
+    from fp8_attention_gb300 import context_parallel as cp
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1,
+                            device_id=DEV)
+    try:
+        w = custom(1, 4, 2, 384, 128, seed=23)
+        q, k, v, do = make_inputs(w)
+        p = dm.AttnParams(w.B, w.Hq, w.Hkv, w.N, w.d, kv_offset=0, kv_len=w.N)
+        qh, kh, vh = (dm.dm_quantize(t.to(DEV), dm.DM_E4M3) for t in (q, k, v))
+        doh = dm.dm_quantize(do.to(DEV), dm.DM_E5M2)
+        res = cp.step(p, qh, kh, vh, doh)
+        assert dm.dm_get_status() == 0
+        r = oracle.pipeline(*[np32(t) for t in (q, k, v, do)])
+        for key in ("O", "LSE", "delta", "dQ", "dK", "dV"):
+            assert rel_err(np32(res[key]), r[key]) <= TOL, key
+    finally:
+        dist.destroy_process_group()
