@@ -66,6 +66,23 @@ def test_long_workloads_sampled(name):
     print(name, "errors", errs, "row-sum rows", rows, "needing the FP32 term", needed)
 
 
+@pytest.mark.parametrize("mode,omode", [(dm.DM_DELTA_STALE_DO, oracle.DELTA_STALE_DO),
+                                        (dm.DM_DELTA_STALE_DOHAT, oracle.DELTA_STALE_DOHAT)])
+def test_saturation_stale_modes_sampled(mode, omode):
+    """The stale corrections (diagnostic modes: section 01's saved-output
+    shortcut and section 03's dO-matched one) at full size on the saturation
+    workload, where they differ most from the matched one: sampled whole tiles
+    in the launch configuration the benchmark times."""
+    w = WORKLOADS["saturation_b2_n4096_d128"]
+    q, k, v, do = make_inputs(w)
+    g = gpu_pipeline(q, k, v, do, mode=mode)
+    q_tiles, kv_tiles = _sampled(w)
+    r = oracle_pipeline(q, k, v, do, mode=omode, groups=[(1, 3)], q_tiles=q_tiles, kv_tiles=kv_tiles)
+    _codes_match(g, r)
+    errs = _compare_sampled(g, r, w)
+    print(w.name, "mode", mode, "errors", errs)
+
+
 def test_saturation_post_cast_residual_ratio():
     """Section 03 reports post-cast row-sum residuals 5.3-6.3x larger with stale delta than
     with Delta-Matching on the authors' probes (workload unstated); here the ratio of
