@@ -174,8 +174,46 @@ __device__ __forceinline__ void store_row(__nv_bfloat16* p, int k0, int n, const
     *reinterpret_cast<__nv_bfloat162*>(p + k0 + k) = __floats2bfloat162_rn(v[k], v[k + 1]);
 }
 
-// MODE 1: delta = <dO, O>; MODE 2: delta = s_dO * <codes(dO^), O>.  One warp
-// per row, each lane holds d/32 consecutive channels.
+// MODE 1: delta = <dO, O>; MODE 2: delta = s_dO * <codes(dO^), O>.  Each
+// warp takes kStaleRows rows and issues all of their loads before the first
+// reduction (each lane d/32 consecutive channels of a row, 16-byte loads of O
+// where a lane's share allows), so that enough bytes are in flight per SM.
+constexpr int kStaleRows = 4;
+
+template <int PER>
+__device__ __forceinline__ void load_vals(const float* p, float* out) {
+  if constexpr (PER % 4 == 0) {
+#pragma unroll
+    for (int k = 0; k < PER; k += 4) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(p + k));
+      out[k] = v.x, out[k + 1] = v.y, out[k + 2] = v.z, out[k + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < PER; k += 2) {
+      const float2 v = __ldg(reinterpret_cast<const float2*>(p + k));
+      out[k] = v.x, out[k + 1] = v.y;
+    }
+  }
+}
+template <int PER>
+__device__ __forceinline__ void load_vals(const __nv_bfloat16* p, float* out) {
+  if constexpr (PER % 4 == 0) {
+#pragma unroll
+    for (int k = 0; k < PER; k += 4) {
+      const uint2 w = __ldg(reinterpret_cast<const uint2*>(p + k));
+      out[k] = __uint_as_float(w.x << 16), out[k + 1] = __uint_as_float(w.x & 0xFFFF0000u);
+      out[k + 2] = __uint_as_float(w.y << 16), out[k + 3] = __uint_as_float(w.y & 0xFFFF0000u);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < PER; k += 2) {
+      const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(p + k));
+      out[k] = __uint_as_float(w << 16), out[k + 1] = __uint_as_float(w & 0xFFFF0000u);
+    }
+  }
+}
+
 template <int MODE, int D, typename TD, typename TO>
 __global__ void __launch_bounds__(256) stale_delta_kernel(const TD* __restrict__ dO,
                                                           const uint8_t* __restrict__ do_codes,
@@ -183,36 +221,44 @@ __global__ void __launch_bounds__(256) stale_delta_kernel(const TD* __restrict__
                                                           const TO* __restrict__ O, long long rows, int N,
                                                           int T_tiles, float* __restrict__ delta) {
   constexpr int PER = D / 32;
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const long long row0 = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * kStaleRows;
   const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const size_t off = (size_t)row * D;
-  float o[PER], g[PER];
-  load_row(O + off, lane * PER, PER, o);
-  float sc = 1.0f;
-  if (MODE == 1) {
-    load_row(dO + off, lane * PER, PER, g);
-  } else {
-    const long long bh = row / N;
-    const int n = (int)(row % N);
-    sc = do_scales[bh * T_tiles + n / kTile];
+  if (row0 >= rows) return;
+  float o[kStaleRows][PER], g[kStaleRows][PER];
 #pragma unroll
-    for (int k = 0; k < PER; k += 2) {
-      const float2 f = unpack2<1>(*reinterpret_cast<const uint16_t*>(do_codes + off + lane * PER + k));
-      g[k] = f.x, g[k + 1] = f.y;
+  for (int rr = 0; rr < kStaleRows; ++rr) {
+    const long long row = row0 + rr < rows ? row0 + rr : rows - 1;  // a ragged last warp rereads its last row
+    const size_t off = (size_t)row * D + lane * PER;
+    load_vals<PER>(O + off, o[rr]);
+    if (MODE == 1) {
+      load_vals<PER>(dO + off, g[rr]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < PER; k += 2) {
+        const float2 f = unpack2<1>(__ldg(reinterpret_cast<const unsigned short*>(do_codes + off + k)));
+        g[rr][k] = f.x, g[rr][k + 1] = f.y;
+      }
     }
   }
-  float acc = 0.0f;
 #pragma unroll
-  for (int k = 0; k < PER; ++k) acc = fmaf(g[k], o[k], acc);
-  acc = warp_sum(acc);
-  if (lane == 0) delta[row] = acc * sc;
+  for (int rr = 0; rr < kStaleRows; ++rr) {
+    const long long row = row0 + rr;
+    float acc = 0.0f;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) acc = fmaf(g[rr][k], o[rr][k], acc);
+    acc = warp_sum(acc);
+    if (lane == 0 && row < rows) {
+      float sc = 1.0f;
+      if (MODE == 2) sc = do_scales[(row / N) * T_tiles + (int)(row % N) / kTile];
+      delta[row] = acc * sc;
+    }
+  }
 }
 
 template <int MODE, int D, typename TD>
 cudaError_t stale_o(const TD* dO, const uint8_t* codes, const float* scales, const void* O, dm_dtype o_t,
                     long long rows, int N, int T, float* delta, cudaStream_t st) {
-  const unsigned grid = (unsigned)((rows + 7) / 8);
+  const unsigned grid = (unsigned)((rows + 8 * kStaleRows - 1) / (8 * kStaleRows));
   if (o_t == DM_BF16)
     stale_delta_kernel<MODE, D, TD, __nv_bfloat16><<<grid, 256, 0, st>>>(
         dO, codes, scales, reinterpret_cast<const __nv_bfloat16*>(O), rows, N, T, delta);
