@@ -579,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         pm1 = max3(pm1, p[c + 2], p[c + 3]);
       }
       float pmax = fmaxf(pm0, pm1);
-      pmax = warp_max(pmax);
+      pmax = warp_max_nonneg(pmax);  // P >= 0 (+0 where masked)
       if (lane == 0) s_red[bn][0][warp - 4] = pmax;
       named_bar_sync(1, 256);
       float amax = max8(s_red[bn][0]);
@@ -654,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (kEarlyPasses < C::kPasses && n >= 1) drain_dq(n - 1, prev_cdq, kEarlyPasses, C::kPasses);
       float dmax = fmaxf(dm0, dm1);
-      dmax = warp_max(dmax);
+      dmax = warp_max_nonneg(dmax);  // |dS|
       if (lane == 0) s_red[bn][1][warp - 4] = dmax;
       named_bar_sync(1, 256);
       amax = max8(s_red[bn][1]);
