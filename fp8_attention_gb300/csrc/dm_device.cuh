@@ -437,6 +437,15 @@ __device__ __forceinline__ float warp_max(float v) {
 __device__ __forceinline__ float warp_max_nonneg(float v) {
   return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v)));
 }
+// Largest value over the warp, of any sign (-inf included, no NaN), in one
+// integer reduction: the bit patterns are first mapped to unsigned integers
+// in the same order (negative values complemented, the sign bit set on the
+// others) and mapped back after.
+__device__ __forceinline__ float warp_max_any(float v) {
+  const uint32_t u = __float_as_uint(v);
+  const uint32_t m = __reduce_max_sync(0xffffffffu, (u & 0x80000000u) ? ~u : (u | 0x80000000u));
+  return __uint_as_float((m & 0x80000000u) ? (m & 0x7fffffffu) : ~m);
+}
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

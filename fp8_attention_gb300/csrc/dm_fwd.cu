@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
       // exp2(min(0, max over rows of (tmax_i - m_i))): one exchange.
       const float tmax = mx * c1;
       float x = (row_valid && mx != -INFINITY) ? tmax - m : -INFINITY;
-      x = warp_max(x);
+      x = warp_max_any(x);
       if (lane == 0) s_red[t & 1][warp] = x;
       named_bar_sync(1, 128);
       const float m_new = fmaxf(m, tmax);
