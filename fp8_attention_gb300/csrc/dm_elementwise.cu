@@ -29,22 +29,26 @@ namespace {
 template <int D>
 __host__ __device__ constexpr int quant_threads() { return D > 128 ? 1024 : 256; }
 
+// 16-byte vectors of the input, held raw (bf16 words stay packed, so that a
+// tile takes half the registers and more tiles are in flight per SM) and
+// widened to FP32 where used.
 template <typename T>
 struct Vec;
 template <>
 struct Vec<float> {
-  static constexpr int kElems = 4;  // 16 bytes
-  __device__ static void load(const float* p, float* out) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(p));
-    out[0] = v.x, out[1] = v.y, out[2] = v.z, out[3] = v.w;
+  static constexpr int kElems = 4;
+  __device__ static uint4 load(const float* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+  __device__ static void widen(const uint4& r, float* out) {
+    out[0] = __uint_as_float(r.x), out[1] = __uint_as_float(r.y);
+    out[2] = __uint_as_float(r.z), out[3] = __uint_as_float(r.w);
   }
 };
 template <>
 struct Vec<__nv_bfloat16> {
   static constexpr int kElems = 8;
-  __device__ static void load(const __nv_bfloat16* p, float* out) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  __device__ static uint4 load(const __nv_bfloat16* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+  __device__ static void widen(const uint4& r, float* out) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       out[2 * k] = __uint_as_float(w[k] << 16);
@@ -57,7 +61,7 @@ struct Vec<__nv_bfloat16> {
 // quantises Q, K, V and dO together); the CTA finds its tensor from the
 // running tile counts.  fmt is per tensor (0 E4M3, 1 E5M2).
 template <typename T, int D>
-__global__ void __launch_bounds__(quant_threads<D>()) quantize_kernel(const QuantBatch batch) {
+__global__ void __launch_bounds__(quant_threads<D>(), 1024 / quant_threads<D>()) quantize_kernel(const QuantBatch batch) {
   constexpr int kQThreads = quant_threads<D>();
   constexpr int V = Vec<T>::kElems;
   constexpr int kVecs = kTile * D / V;     // vectors in a full tile
@@ -77,19 +81,19 @@ __global__ void __launch_bounds__(quant_threads<D>()) quantize_kernel(const Quan
   const size_t base = ((size_t)bh * N + (size_t)t * kTile) * D;
   const int nvec = rows * D / V;
 
-  float v[kPer][V];
-  float amax = 0.0f;
+  uint4 raw[kPer];
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const int idx = threadIdx.x + i * kQThreads;
-    if (idx < nvec) {
-      Vec<T>::load(x + base + (size_t)idx * V, v[i]);
+    raw[i] = idx < nvec ? Vec<T>::load(x + base + (size_t)idx * V) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float amax = 0.0f;
 #pragma unroll
-      for (int k = 0; k < V; ++k) amax = fmaxf(amax, fabsf(v[i][k]));
-    } else {
+  for (int i = 0; i < kPer; ++i) {
+    float f[V];
+    Vec<T>::widen(raw[i], f);
 #pragma unroll
-      for (int k = 0; k < V; ++k) v[i][k] = 0.0f;
-    }
+    for (int k = 0; k < V; ++k) amax = fmaxf(amax, fabsf(f[k]));
   }
   amax = warp_max(amax);
   if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = amax;
@@ -108,11 +112,13 @@ __global__ void __launch_bounds__(quant_threads<D>()) quantize_kernel(const Quan
   for (int i = 0; i < kPer; ++i) {
     const int idx = threadIdx.x + i * kQThreads;
     if (idx >= nvec) continue;
+    float f[V];
+    Vec<T>::widen(raw[i], f);
     uint32_t w[V / 4];
 #pragma unroll
     for (int k = 0; k < V / 4; ++k) {
-      const float x0 = __fmul_rn(v[i][4 * k], r), x1 = __fmul_rn(v[i][4 * k + 1], r);
-      const float x2 = __fmul_rn(v[i][4 * k + 2], r), x3 = __fmul_rn(v[i][4 * k + 3], r);
+      const float x0 = __fmul_rn(f[4 * k], r), x1 = __fmul_rn(f[4 * k + 1], r);
+      const float x2 = __fmul_rn(f[4 * k + 2], r), x3 = __fmul_rn(f[4 * k + 3], r);
       w[k] = flushed ? 0u : (e5m2 ? pack4<1>(x0, x1, x2, x3) : pack4<0>(x0, x1, x2, x3));
     }
     uint8_t* dst = job.codes + base + (size_t)idx * V;
