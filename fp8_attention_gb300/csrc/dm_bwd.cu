@@ -556,33 +556,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.sread[bn]);
+      // The exponents x = S c1 - LSE log2e first, masked ones -inf; the tile
+      // amax of P = exp2(x) is exp2 of the exponents' maximum (exp2 is
+      // monotonic), so the maximum is reduced and exchanged while the
+      // exponentials are still in flight.
       const float2 c1_2 = make_float2(c1, c1);
       const float4* nlse4 = reinterpret_cast<const float4*>(&s_lse[bn][wg * 64]);  // broadcast reads
-      float pm0 = 0.0f, pm1 = 0.0f;
 #pragma unroll
       for (int c = 0; c < 64; c += 4) {
         const float4 l4 = nlse4[c / 4];
         const float2 x01 = __ffma2_rn(make_float2(p[c], p[c + 1]), c1_2, make_float2(l4.x, l4.y));
         const float2 x23 = __ffma2_rn(make_float2(p[c + 2], p[c + 3]), c1_2, make_float2(l4.z, l4.w));
-        p[c] = ex2(x01.x);
-        p[c + 1] = ex2(x01.y);
-        p[c + 2] = ex2(x23.x);
-        p[c + 3] = ex2(x23.y);
+        p[c] = x01.x;
+        p[c + 1] = x01.y;
+        p[c + 2] = x23.x;
+        p[c + 3] = x23.y;
       }
       if (cmin > 0) {  // diagonal tile or absent key row: mask
 #pragma unroll
-        for (int c = 0; c < 64; ++c) p[c] = c >= cmin ? p[c] : 0.0f;
+        for (int c = 0; c < 64; ++c) p[c] = c >= cmin ? p[c] : -INFINITY;
       }
+      float xm0 = -INFINITY, xm1 = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 64; c += 4) {
-        pm0 = max3(pm0, p[c], p[c + 1]);
-        pm1 = max3(pm1, p[c + 2], p[c + 3]);
+        xm0 = max3(xm0, p[c], p[c + 1]);
+        xm1 = max3(xm1, p[c + 2], p[c + 3]);
       }
-      float pmax = fmaxf(pm0, pm1);
-      pmax = warp_max_nonneg(pmax);  // P >= 0 (+0 where masked)
-      if (lane == 0) s_red[bn][0][warp - 4] = pmax;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) p[c] = ex2(p[c]);  // exp2(-inf) = +0 where masked
+      const float xmax = warp_max_any(fmaxf(xm0, xm1));
+      if (lane == 0) s_red[bn][0][warp - 4] = xmax;
       named_bar_sync(1, 256);
-      float amax = max8(s_red[bn][0]);
+      float amax;
+      {
+        const float4 a4 = reinterpret_cast<const float4*>(s_red[bn][0])[0];
+        const float4 b4 = reinterpret_cast<const float4*>(s_red[bn][0])[1];
+        amax = ex2(fmaxf(max3(a4.x, a4.y, a4.z), max3(a4.w, b4.x, max3(b4.y, b4.z, b4.w))));
+      }
       float rp;
       const float sp = tile_scale_fast<0>(amax, rp);
       // P^T codes and the next iteration's LSE / delta (read after this
