@@ -43,9 +43,9 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # summarised in profiles/ (valid only for the kernel source it was taken on;
 # reported as null once dm_bwd.cu or dm_device.cuh changes).
 BWD_TRAFFIC = {
-    "gqa_b1_n8192_d128": {"sha1": "8b8082ca3c8df6ce60ef95ee2a1a43667fe66968", "bytes": 261701376},
-    "gqa_b1_n8192_d256": {"sha1": "9326d58103d94ee75d90212ca108624860506c9c", "bytes": 261324032},
-    "mla_b1_n8192_d192_dv128": {"sha1": "9326d58103d94ee75d90212ca108624860506c9c", "bytes": 1987614464},
+    "gqa_b1_n8192_d128": {"sha1": "bc47305d5d20107e027d3de4cf8aedf51b170cce", "bytes": 262611200},
+    "gqa_b1_n8192_d256": {"sha1": "bc47305d5d20107e027d3de4cf8aedf51b170cce", "bytes": 262288128},
+    "mla_b1_n8192_d192_dv128": {"sha1": "bc47305d5d20107e027d3de4cf8aedf51b170cce", "bytes": 1961824768},
 }
 # head dimensions the Q/K prologue is built for
 PROLOGUE_DIMS = (64, 128, 256)
