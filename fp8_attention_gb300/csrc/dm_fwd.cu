@@ -49,6 +49,7 @@ constexpr int kThreads = 192;
 constexpr int kKV = 2;  // K shared-memory stages (V has one: it is needed a whole tile later than K)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2FmaxE4M3 = 8.807354922057604f;  // log2 448
 
 template <int D>
 struct FwdCfg {
@@ -318,7 +319,8 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
       const float m_new = fmaxf(m, tmax);
       const float4 x4 = *reinterpret_cast<const float4*>(s_red[t & 1]);  // 16-byte aligned row
       const float xmax = fmaxf(max3(x4.x, x4.y, x4.z), x4.w);
-      const float amax = ex2(fminf(xmax, 0.0f));
+      const float xm = fminf(xmax, 0.0f);  // log2 of the tile amax of P~
+      const float amax = ex2(xm);
       float r;
       const float sp = tile_scale_fast<0>(amax, r);
       const float alpha = ex2(m - m_new);
@@ -365,7 +367,8 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
       // its rescale of tile t-1); the
       // unquantised row sum is sum(P~ r) * s_P.  A flushed tile (r = 0)
       // gives codes 0.
-      const float bias = (r > 0.0f ? __log2f(r) : -INFINITY) - m_new;
+      // log2 r = log2 FMAX - log2 amax, formed without a logarithm
+      const float bias = (r > 0.0f ? kLog2FmaxE4M3 - xm : -INFINITY) - m_new;
       const float2 c1_2 = make_float2(c1, c1), b2 = make_float2(bias, bias);
       float2 rs2 = make_float2(0.0f, 0.0f);
       const uint32_t sP = L::kP + (t & 1) * kTile * kTile + SwTile<128>::row_base(row);  // chunk c at sP ^ 16 c
