@@ -306,9 +306,9 @@ def run_native(args, rank, world, local_rank):
 
     # ---- end to end through the public API from pinned host buffers: every
     # step copies its inputs in, computes, and copies dQ, dK, dV out.  The
-    # copies run on streams of their own, overlapped with the neighbouring
-    # steps' compute (two device input slots); the L2 flush stays in front of
-    # every step's compute, inside the timed region.
+    # copies run on streams of their own, each beside a neighbouring step's
+    # backward (two device input slots); the L2 flush stays in front of every
+    # step's compute, inside the timed region.
     h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh, doh))
     out_shapes = {"dQ": (w.B, w.Hq, w.N, w.d), "dK": (w.B, w.Hkv, w.N, w.d), "dV": (w.B, w.Hkv, w.N, w.d_v)}
     outs = [{k2: torch.empty(sh, dtype=torch.float32).pin_memory() for k2, sh in out_shapes.items()}
@@ -323,11 +323,29 @@ def run_native(args, rank, world, local_rank):
     t_start, t_end = ev(), ev()
     done = [None] * e2e_steps
     t_start.record(s_in)
+    # the copies run beside the backward, which shares HBM and L2 with them
+    # far less than the quantiser, forward and delta pass do
+    fwd_done = [None] * e2e_steps  # per step: its quantiser, forward and delta pass have finished
+    grads = [None] * e2e_steps
+
+    def copy_out(j):
+        # step j's gradients to the host
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(done[j])
+            if j + 1 < e2e_steps:
+                s_out.wait_event(fwd_done[j + 1])
+            for name, host in outs[j % 2].items():
+                grads[j][name].record_stream(s_out)
+                host.copy_(grads[j][name], non_blocking=True)
+        grads[j] = None
+
     for i in range(e2e_steps):
         sl = i % 2
         with torch.cuda.stream(s_in):
             if i >= 2:
                 s_in.wait_event(done[i - 2])  # step i - 2 has finished reading this slot
+            if i >= 1:
+                s_in.wait_event(fwd_done[i - 1])
             for dst, src in zip(slots[sl], (qh, kh, vh, doh)):
                 dst.copy_(src, non_blocking=True)
             arrived = torch.cuda.Event()
@@ -335,14 +353,14 @@ def run_native(args, rank, world, local_rank):
         with torch.cuda.stream(st):
             st.wait_event(arrived)
             flush.zero_()
-            g = step(slots[sl], st)
+            m = []
+            grads[i] = step(slots[sl], st, m)
+            fwd_done[i] = m[0][3]  # recorded after the step's quantiser, forward and delta pass
             done[i] = torch.cuda.Event()
             done[i].record(st)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(done[i])
-            for name, host in outs[sl].items():
-                g[name].record_stream(s_out)
-                host.copy_(g[name], non_blocking=True)
+        if i >= 1:
+            copy_out(i - 1)
+    copy_out(e2e_steps - 1)
     s_out.wait_event(done[-1])
     t_end.record(s_out)
     torch.cuda.synchronize(dev)
@@ -443,7 +461,7 @@ def run_native(args, rank, world, local_rank):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                 "steps": e2e_steps,
                 "how": "pinned host buffers; eager calls of the public API; H2D, compute (with the L2 flush) and "
-                       "D2H on three streams, two input slots, copies overlapped with neighbouring steps"},
+                       "D2H on three streams, two input slots, each copy beside a neighbouring step's backward"},
         # Q and K prologue: x read + 1 B code per element, tile scales, the
         # rotary table (read once; every head shares it) and the gains
         "prologue": prologue_line,
