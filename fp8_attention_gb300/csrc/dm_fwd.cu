@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
       } else {
         // unit / c, with 1 / s_P = r (the tile's code reciprocal); up to 2^64
         // every row accumulates (its factor is at most unit / c)
-        const float ratio = (u_p * r) * (u_v / sv);
+        const float ratio = (u_p * r) * __fdividef(u_v, sv);  // s_V <= FLT_MAX / 448 < 2^126
         if (ratio <= 0x1p64f) {
           mode = 2;
           g = alpha * ratio;
