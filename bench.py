@@ -195,24 +195,26 @@ def run_native(args, rank, world, local_rank):
         vv, dd = dm.dm_quantize_batch([(vx, dm.DM_E4M3), (dox, dm.DM_E5M2)], stream=stream)
         return qq, kk, vv, dd
 
+    ws = torch.empty(max(16, dm.dm_attn_bwd_workspace_size(p)), dtype=torch.uint8, device=dev)
+
     def step(inputs, stream, times=None):
         qx, kx, vx, dox = inputs
-        marks = [ev() for _ in range(5)]
+        marks = [ev() for _ in range(4)]
         marks[0].record(stream)
         qq, kk, vv, dd = quantize(qx, kx, vx, dox, stream)
         marks[1].record(stream)
         O, lse = dm.dm_attn_fwd(p, qq, kk, vv, stream=stream)
         marks[2].record(stream)
-        delta = dm.dm_attn_delta(p, dm.DM_DELTA_MATCHED, qq, kk, vv, dd, lse, stream=stream)
+        # the backward computes the matched delta itself (into ws); that
+        # kernel also clears dQ, dK and dV, so no fill launch runs
+        g = dm.dm_attn_bwd(p, dm.DM_DELTA_MATCHED, qq, kk, vv, dd, lse, None, workspace=ws, stream=stream)
         marks[3].record(stream)
-        g = dm.dm_attn_bwd(p, dm.DM_DELTA_MATCHED, qq, kk, vv, dd, lse, delta, stream=stream)
-        marks[4].record(stream)
         if times is not None:
             times.append(marks)
         return g
 
-    # quantise (Q, K, V, dO in one launch; two when the widths differ), forward, delta, zero fill + backward
-    launches_per_step = (1 if w.d == w.d_v else 2) + 1 + 1 + 2
+    # quantise (Q, K, V, dO in one launch; two when the widths differ), forward, delta, backward
+    launches_per_step = (1 if w.d == w.d_v else 2) + 1 + 1 + 1
     inputs = (qd, kd, vd, dod)
     with torch.cuda.stream(st):
         for _ in range(args.warmup):
@@ -222,24 +224,26 @@ def run_native(args, rank, world, local_rank):
     if dm.dm_get_status(st) != 0:
         raise RuntimeError("device status error during warm-up")
 
-    # ---- the step captured once as four CUDA graphs (quantise, forward, delta,
-    # zero fill + backward), replayed back to back with events between them:
-    # the same launches, without host work between them, so that host-side
-    # launch latency cannot leave the GPU idle inside the timed region
+    # ---- the step captured once as a CUDA graph and replayed: the timed
+    # region (no host work between its launches, so that host-side launch
+    # latency cannot leave the GPU idle).  The per-kernel split times four
+    # separate calls instead, each its own graph with events between them:
+    # quantise, forward, the delta pass alone (dm_attn_delta) and the
+    # backward given that delta (with its own zero fill launch).
+    cap = {}
+    stages = [
+        lambda: cap.update(zip(("qq", "kk", "vv", "dd"), quantize(qd, kd, vd, dod, st))),
+        lambda: cap.update(zip(("O", "lse"), dm.dm_attn_fwd(p, cap["qq"], cap["kk"], cap["vv"], stream=st))),
+        lambda: cap.update(delta=dm.dm_attn_delta(p, dm.DM_DELTA_MATCHED, cap["qq"], cap["kk"], cap["vv"],
+                                                  cap["dd"], cap["lse"], stream=st)),
+        lambda: cap.update(g=dm.dm_attn_bwd(p, dm.DM_DELTA_MATCHED, cap["qq"], cap["kk"], cap["vv"],
+                                            cap["dd"], cap["lse"], cap["delta"], stream=st)),
+    ]
     graphs = None
     if not args.no_graph:
         try:
             graphs = [torch.cuda.CUDAGraph() for _ in range(4)]
             pool = None
-            cap = {}
-            stages = [
-                lambda: cap.update(zip(("qq", "kk", "vv", "dd"), quantize(qd, kd, vd, dod, st))),
-                lambda: cap.update(zip(("O", "lse"), dm.dm_attn_fwd(p, cap["qq"], cap["kk"], cap["vv"], stream=st))),
-                lambda: cap.update(delta=dm.dm_attn_delta(p, dm.DM_DELTA_MATCHED, cap["qq"], cap["kk"], cap["vv"],
-                                                          cap["dd"], cap["lse"], stream=st)),
-                lambda: cap.update(g=dm.dm_attn_bwd(p, dm.DM_DELTA_MATCHED, cap["qq"], cap["kk"], cap["vv"],
-                                                    cap["dd"], cap["lse"], cap["delta"], stream=st)),
-            ]
             for gph, fn in zip(graphs, stages):
                 with torch.cuda.graph(gph, stream=st, pool=pool):
                     fn()
@@ -288,27 +292,32 @@ def run_native(args, rank, world, local_rank):
         raise RuntimeError(f"device status {dm.dm_status_string(status)}")
     if graphs is not None:
         step_ms = [a.elapsed_time(b) for a, b in smarks]
-        # per-kernel split: the four stage graphs with events between them
-        with torch.cuda.stream(st):
-            for _ in range(max(3, min(args.steps, 100))):
-                flush.zero_()
-                m = [ev() for _ in range(5)]
-                m[0].record(st)
-                for i, gph in enumerate(graphs):
-                    gph.replay()
-                    m[i + 1].record(st)
-                marks.append(m)
-        torch.cuda.synchronize(dev)
-    per = [[m[i].elapsed_time(m[i + 1]) for i in range(4)] for m in marks]
-    if graphs is None:
-        step_ms = [sum(x) for x in per]
+    else:
+        step_ms = [m[0].elapsed_time(m[-1]) for m in marks]
+    # per-kernel split: the four stage calls (graphs when captured) with
+    # events between them
+    split = []
+    with torch.cuda.stream(st):
+        for _ in range(max(3, min(args.steps, 100))):
+            flush.zero_()
+            m = [ev() for _ in range(5)]
+            m[0].record(st)
+            for i in range(4):
+                if graphs is not None:
+                    graphs[i].replay()
+                else:
+                    stages[i]()
+                m[i + 1].record(st)
+            split.append(m)
+    torch.cuda.synchronize(dev)
+    per = [[m[i].elapsed_time(m[i + 1]) for i in range(4)] for m in split]
     total_ms = max_over_ranks(sum(step_ms), dist, dev)
 
     # ---- end to end through the public API from pinned host buffers: every
     # step copies its inputs in, computes, and copies dQ, dK, dV out.  The
     # copies run on streams of their own, each beside a neighbouring step's
-    # backward (two device input slots); the L2 flush stays in front of every
-    # step's compute, inside the timed region.
+    # delta pass and backward (two device input slots); the L2 flush stays in
+    # front of every step's compute, inside the timed region.
     h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh, doh))
     out_shapes = {"dQ": (w.B, w.Hq, w.N, w.d), "dK": (w.B, w.Hkv, w.N, w.d), "dV": (w.B, w.Hkv, w.N, w.d_v)}
     outs = [{k2: torch.empty(sh, dtype=torch.float32).pin_memory() for k2, sh in out_shapes.items()}
@@ -323,9 +332,9 @@ def run_native(args, rank, world, local_rank):
     t_start, t_end = ev(), ev()
     done = [None] * e2e_steps
     t_start.record(s_in)
-    # the copies run beside the backward, which shares HBM and L2 with them
-    # far less than the quantiser, forward and delta pass do
-    fwd_done = [None] * e2e_steps  # per step: its quantiser, forward and delta pass have finished
+    # the copies run beside the delta pass and backward, which share HBM and
+    # L2 with them far less than the quantiser and forward do
+    fwd_done = [None] * e2e_steps  # per step: its quantiser and forward have finished
     grads = [None] * e2e_steps
 
     def copy_out(j):
@@ -355,7 +364,7 @@ def run_native(args, rank, world, local_rank):
             flush.zero_()
             m = []
             grads[i] = step(slots[sl], st, m)
-            fwd_done[i] = m[0][3]  # recorded after the step's quantiser, forward and delta pass
+            fwd_done[i] = m[0][2]  # recorded after the step's quantiser and forward
             done[i] = torch.cuda.Event()
             done[i].record(st)
         if i >= 1:
@@ -421,7 +430,9 @@ def run_native(args, rank, world, local_rank):
                    "flop_accounting": "issued, causal-halved: fwd S+O, delta S+dP, bwd S+dP+dV+dQ+dK "
                                       "(9U per step when d_v = d)",
                    "l2": "flushed between timed steps (256 MiB write)", "parallelism": f"independent x{world}",
-                   "launch": "CUDA graph of the step, replayed (per-kernel split: one graph per stage)"
+                   "launch": "CUDA graph of the step, replayed; the backward computes the delta itself, whose "
+                             "kernel clears dQ, dK, dV (per-kernel split: the four stages as separate calls, one "
+                             "graph each, the backward's with its own zero fill)"
                    if graphs is not None else "eager launches"},
         "pct_of_fp8_peak": round(100.0 * value / (world * fp8_peak), 2),
         "fp8_peak": {"used_tflops": round(fp8_peak, 1), "used": peak_name, "stand_in_tflops": round(stand_in, 1),
@@ -461,7 +472,7 @@ def run_native(args, rank, world, local_rank):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                 "steps": e2e_steps,
                 "how": "pinned host buffers; eager calls of the public API; H2D, compute (with the L2 flush) and "
-                       "D2H on three streams, two input slots, each copy beside a neighbouring step's backward"},
+                       "D2H on three streams, two input slots, each copy beside a neighbouring step's delta pass and backward"},
         # Q and K prologue: x read + 1 B code per element, tile scales, the
         # rotary table (read once; every head shares it) and the gains
         "prologue": prologue_line,

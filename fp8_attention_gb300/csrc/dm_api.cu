@@ -217,7 +217,7 @@ dm_status check_delta_inputs(dm_delta_mode mode, dm_fp8_tensor q, dm_fp8_tensor 
 dm_status delta_impl(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor q, dm_fp8_tensor k,
                      dm_fp8_tensor v, dm_fp8_tensor do_hat, const float* lse, const void* dO, dm_dtype do_dtype,
                      const void* O, dm_dtype o_dtype, float* delta, unsigned int* status, cudaStream_t st,
-                     float* den = nullptr) {
+                     float* den = nullptr, const dm::DeltaClear* clear = nullptr) {
   dm::AttnArgs a = make_args(p, status);
   if (mode == DM_DELTA_MATCHED) {
     dm::DeltaLaunch f{};
@@ -231,6 +231,7 @@ dm_status delta_impl(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor 
     f.lse = lse;
     f.delta = delta;
     f.den = den;
+    if (clear) f.clear = *clear;
     return cuda_status(dm::launch_delta_matched(f, kw, kernel_value_dim(p), st));
   }
   a.do_scales = do_hat.scales;
@@ -496,21 +497,29 @@ dm_status dm_attn_bwd(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor
   unsigned int* status = nullptr;
   DM_TRY(device_state(&status));
   cudaStream_t st = as_stream(stream);
+  // dQ, dK and dV are sums of bulk reduce-adds, the diagnostics sums of
+  // atomics: all start at zero.  When the matched delta is computed here, its
+  // kernel clears them on the way (no key block here: dK and dV have N rows);
+  // otherwise one fill launch does.
+  const bool clear_in_delta = !delta && mode == DM_DELTA_MATCHED;
   if (!delta) {
     float* ws = static_cast<float*>(workspace);
-    DM_TRY(delta_impl(p, mode, q, k, v, do_hat, lse, dO, do_dtype, O, o_dtype, ws, status, st));
+    const dm::DeltaClear clr{dQ, dK, dV, {dg.rowsum_pre, dg.abssum_pre, dg.rowsum_post, dg.abssum_post}};
+    DM_TRY(delta_impl(p, mode, q, k, v, do_hat, lse, dO, do_dtype, O, o_dtype, ws, status, st, nullptr,
+                      clear_in_delta ? &clr : nullptr));
     dl = ws;
   }
-  // dQ, dK and dV are sums of bulk reduce-adds; the diagnostics sums of atomics
-  dm::ZeroList z{};
   const int kw = kernel_dim(p), dv = value_dim(p);
-  z.add(dQ, (size_t)p->B * p->Hq * p->N * p->d);
   const int nk = key_rows(p);
-  z.add(dK, (size_t)p->B * p->Hkv * nk * p->d);
-  z.add(dV, (size_t)p->B * p->Hkv * nk * dv);
-  const size_t nrow = (size_t)p->B * p->Hq * p->N;
-  for (float* ptr : {dg.rowsum_pre, dg.abssum_pre, dg.rowsum_post, dg.abssum_post}) z.add(ptr, nrow);
-  DM_TRY(cuda_status(dm::launch_zero(z, st)));
+  if (!clear_in_delta) {
+    dm::ZeroList z{};
+    z.add(dQ, (size_t)p->B * p->Hq * p->N * p->d);
+    z.add(dK, (size_t)p->B * p->Hkv * nk * p->d);
+    z.add(dV, (size_t)p->B * p->Hkv * nk * dv);
+    const size_t nrow = (size_t)p->B * p->Hq * p->N;
+    for (float* ptr : {dg.rowsum_pre, dg.abssum_pre, dg.rowsum_post, dg.abssum_post}) z.add(ptr, nrow);
+    DM_TRY(cuda_status(dm::launch_zero(z, st)));
+  }
   dm::BwdLaunch f{};
   DM_TRY(encode_codes_map(&f.tmQ, q.codes, p->B * p->Hq, p->N, p->d, kw));
   DM_TRY(encode_codes_map(&f.tmK, k.codes, p->B * p->Hkv, nk, p->d, kw));

@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(kThreads, DeltaCfg<D>::kCTAsPerSM)
     attn_delta_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                       const AttnArgs a, const float* __restrict__ lse, float* __restrict__ delta,
-                      float* __restrict__ den) {
+                      float* __restrict__ den, const DeltaClear clr) {
   using L = DeltaLayout<D, DV>;
   using C = DeltaCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -152,6 +152,26 @@ __global__ void __launch_bounds__(kThreads, DeltaCfg<D>::kCTAsPerSM)
         wait_drain(&bars.kfull[t % kKV], (t / kKV) & 1, wd, 210);
         wait_drain(&bars.vfull[t % kKV], (t / kKV) & 1, wd, 211);
       }
+    }
+    __syncwarp();
+    if (clr.dQ) {
+      // the backward's outputs of this query tile (and, in a group's first
+      // query head, of the key tile with its index) start at zero: 16-byte
+      // stores of whole rows (d and d_v are multiples of 64), the
+      // diagnostics rows one float at a time
+      const int rows = min(kTile, a.N - q0);
+      auto clear = [&](float* base, size_t first, size_t n) {
+        float4* p4 = reinterpret_cast<float4*>(base + first);
+        for (size_t i = lane; i < n / 4; i += 32) p4[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      };
+      clear(clr.dQ, ((size_t)bh * a.N + q0) * a.dqk, (size_t)rows * a.dqk);
+      if (h % (a.Hq / a.Hkv) == 0) {
+        clear(clr.dK, ((size_t)bg * a.N + q0) * a.dqk, (size_t)rows * a.dqk);
+        clear(clr.dV, ((size_t)bg * a.N + q0) * a.dv, (size_t)rows * a.dv);
+      }
+      for (int j = 0; j < 4; ++j)
+        if (clr.rows[j])
+          for (int i = lane; i < rows; i += 32) clr.rows[j][(size_t)bh * a.N + q0 + i] = 0.0f;
     }
   } else if (warp == 5) {
     if (lane == 0) {
@@ -285,7 +305,7 @@ cudaError_t launch_t(const DeltaLaunch& f, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(f.args.B * f.args.Hq * f.args.T);
   return launch_overlapped(k, grid, kThreads, smem, st, f.tmQ, f.tmK, f.tmV, f.tmDO, f.args, f.lse, f.delta,
-                           f.den);
+                           f.den, f.clear);
 }
 
 }  // namespace

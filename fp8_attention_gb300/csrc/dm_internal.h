@@ -37,12 +37,25 @@ struct FwdLaunch {
   float* lse;
 };
 
+// The backward's outputs that the matched delta pass sets to zero on its way
+// (the backward adds into them), when the backward computes delta itself:
+// each CTA clears the dQ rows and diagnostics rows of its query tile, and
+// the CTAs of a GQA group's first query head the dK and dV rows of the key
+// tile with the same index.  All null: nothing is cleared.
+struct DeltaClear {
+  float* dQ;       // [B*Hq][N][d]
+  float* dK;       // [B*Hkv][N][d]
+  float* dV;       // [B*Hkv][N][d_v]
+  float* rows[4];  // nullable [B*Hq][N] each
+};
+
 struct DeltaLaunch {
   CUtensorMap tmQ, tmK, tmV, tmDO;
   AttnArgs args;
   const float* lse;
   float* delta;  // delta, or (with den) sum_j P dP^ over the key block
   float* den;    // nullable: sum_j P over the key block
+  DeltaClear clear;
 };
 
 struct BwdLaunch {

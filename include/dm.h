@@ -244,7 +244,9 @@ dm_status dm_attn_delta(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tens
  * [B][Hq][N][d] (overwritten, not accumulated), dK float [B][Hkv][N][d] and
  * dV float [B][Hkv][N][d_v] (summed over each kv head's query heads).  diag: optional
  * row-sum diagnostics (NULL = off).  dO/O are needed only when delta is NULL
- * and the mode is stale.  Over a key block: lse and delta must be the whole
+ * and the mode is stale.  The outputs start at zero inside the call (with
+ * delta NULL and the matched mode, the delta kernel clears them on its way;
+ * otherwise one fill launch does).  Over a key block: lse and delta must be the whole
  * sequence's (merged; delta NULL gives DM_ERR_INVALID_ARG), dK and dV are the
  * block's rows ([B][Hkv][kv_len][.]) and dQ and diag hold the block's partial
  * sums (the blocks' dQ add up to the sequence's). */
