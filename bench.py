@@ -49,6 +49,8 @@ BWD_TRAFFIC = {
 }
 # head dimensions the Q/K prologue is built for
 PROLOGUE_DIMS = (64, 128, 256)
+# steps of the end-to-end loop (whatever --steps is)
+E2E_STEPS = 50
 
 
 def bwd_source_hash():
@@ -325,7 +327,7 @@ def run_native(args, rank, world, local_rank):
     d2h = sum(t.numel() * t.element_size() for t in outs[0].values())
     slots = [tuple(torch.empty(t.shape, dtype=t.dtype, device=dev) for t in (qh, kh, vh, doh)) for _ in range(2)]
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    e2e_steps = max(4, min(args.steps, 50))
+    e2e_steps = E2E_STEPS  # fixed, so that the first copy in and the last copy out weigh the same at any --steps
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -813,9 +815,12 @@ def oracle_sample(w, rounds=1):
     return sample_flops / secs / 1e12, secs, desc
 
 
-def cpu_baseline(w):
+def cpu_baseline(w, min_seconds=10.0, max_rounds=30):
+    """The oracle on the bounded sample, repeated until about min_seconds of CPU work."""
     import oracle
-    val, secs, desc = oracle_sample(w)
+    val, secs, _ = oracle_sample(w)
+    rounds = max(1, min(max_rounds, int(min_seconds / max(secs, 1e-3)) + 1))
+    val, secs, desc = oracle_sample(w, rounds=rounds)
     return {"value": round(val, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": desc, "seconds": round(secs, 2)}
 
