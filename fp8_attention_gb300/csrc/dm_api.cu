@@ -91,6 +91,18 @@ dm_status encode_f32_rows_map(CUtensorMap* m, const float* x, int BH, int N, int
   return r == CUDA_SUCCESS ? DM_OK : DM_ERR_CUDA;
 }
 
+// bf16 [BH][N][d] (O), box = 128 rows x 64 columns with the 128-byte swizzle.
+dm_status encode_bf16_rows_map(CUtensorMap* m, void* x, int BH, int N, int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * (cuuint64_t)N};
+  cuuint32_t box[3] = {64, (cuuint32_t)kTileRows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, x, dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DM_OK : DM_ERR_CUDA;
+}
+
 // Head dimension of V, dO, O and dV (0 selects d).
 inline int value_dim(const dm_attn_params* p) { return p->d_v ? p->d_v : p->d; }
 
@@ -439,7 +451,10 @@ dm_status dm_attn_fwd(const dm_attn_params* p, dm_fp8_tensor q, dm_fp8_tensor k,
     f.args.stall_test = g_stall_test;
     g_stall_test = 0;
   }
-  f.O = O;
+  if (o_dtype == DM_BF16)
+    DM_TRY(encode_bf16_rows_map(&f.tmO, O, p->B * p->Hq, p->N, value_dim(p)));
+  else
+    DM_TRY(encode_f32_rows_map(&f.tmO, static_cast<float*>(O), p->B * p->Hq, p->N, value_dim(p)));
   f.lse = lse;
   return cuda_status(dm::launch_attn_fwd(f, kw, kernel_value_dim(p), o_dtype == DM_BF16, as_stream(stream)));
 }

@@ -78,6 +78,9 @@ struct FwdLayout {
   static constexpr int kBars = kMode + 16;
   static constexpr int kMisc = kBars + ((int)(sizeof(FwdBars) + 15) / 16) * 16;  // tmem address, abort flag
   static constexpr int kBytes = kMisc + 16;
+  // the epilogue stages O (up to 4 bytes x DV columns a row) over K, V and P
+  static_assert(kRed - kK >= kTile * DV * 4, "K, V and P buffers hold an fp32 O tile");
+  static_assert(kK % 1024 == 0, "staging boxes need 1024-byte alignment");
 };
 
 // O (this warp's lanes, D columns at taddr) *= f, 64 columns per TMEM round trip.
@@ -103,8 +106,8 @@ __device__ __forceinline__ void rescale_o(uint32_t taddr, float f) {
 template <int D, int DV, bool OUT_BF16>
 __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const AttnArgs a, void* __restrict__ O,
-                    float* __restrict__ lse) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const AttnArgs a, float* __restrict__ lse) {
   using L = FwdLayout<D, DV>;
   using C = FwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -170,6 +173,7 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmO);
       mbar_arrive_expect_tx(&bars.q, L::kTileBytes);
       tma_load_tile<D>(sm + L::kQ, &tmQ, &bars.q, q0, bh);
       // K runs one tile ahead of V: K(t) needs only S(t-2) to have finished
@@ -437,39 +441,57 @@ __global__ void __launch_bounds__(kThreads, FwdCfg<D>::kCTAsPerSM)
       tc_fence_after();
     }
     const float linv = nkv > 0 ? u_p / l : 0.0f;  // O = O_tmem * (u_p / l) * u_v, two products so that no factor underflows
+    // O / l staged over the K, V and P buffers (every product has completed)
+    // in boxes of 128 rows x 128 bytes with the 128-byte swizzle, then
+    // written by TMA tile stores (rows past N are not written); O rows are
+    // a.dv wide (the kernel's columns past the value head dimension are
+    // not stored)
+    constexpr int kBoxCols = OUT_BF16 ? 64 : 32;  // O columns per 128-byte box row
+    const uint32_t rsw = SwTile<128>::row_base(row);
     const int dv = a.dv;
 #pragma unroll
     for (int c0 = 0; c0 < DV; c0 += 64) {
       if (c0 >= dv) break;  // uniform over the CTA
       float o[64];
-      if (nkv > 0) {  // uniform: TMEM loads are warp-collective, before the row guard
+      if (nkv > 0) {  // uniform: TMEM loads are warp-collective
         tmem_load64(tl + C::kColO + c0, tl + C::kColO + c0 + 32, o);
       } else {
 #pragma unroll
         for (int k = 0; k < 64; ++k) o[k] = 0.0f;
       }
-      if (row_valid) {
-        if (OUT_BF16) {
-          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(O) + ((size_t)bh * a.N + qi) * dv + c0;
+      if (OUT_BF16) {
+        const uint32_t box = L::kK + (uint32_t)(c0 / kBoxCols) * (kTile * 128) + rsw;
 #pragma unroll
-          for (int k = 0; k < 64; k += 8) {
-            uint4 w;
-            uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+        for (int e = 0; e < 8; ++e) {
+          uint32_t w[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              __nv_bfloat162 h2 = __floats2bfloat162_rn((o[k + 2 * e] * linv) * u_v, (o[k + 2 * e + 1] * linv) * u_v);
-              wp[e] = *reinterpret_cast<uint32_t*>(&h2);
-            }
-            *reinterpret_cast<uint4*>(dst + k) = w;
+          for (int j = 0; j < 4; ++j) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn((o[8 * e + 2 * j] * linv) * u_v,
+                                                      (o[8 * e + 2 * j + 1] * linv) * u_v);
+            w[j] = *reinterpret_cast<uint32_t*>(&h2);
           }
-        } else {
-          float* dst = reinterpret_cast<float*>(O) + ((size_t)bh * a.N + qi) * dv + c0;
+          *reinterpret_cast<uint4*>(sm + (box ^ (16u * e))) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      } else {
 #pragma unroll
-          for (int k = 0; k < 64; k += 4)
-            *reinterpret_cast<float4*>(dst + k) = make_float4((o[k] * linv) * u_v, (o[k + 1] * linv) * u_v,
-                                                              (o[k + 2] * linv) * u_v, (o[k + 3] * linv) * u_v);
+        for (int b = 0; b < 2; ++b) {
+          const uint32_t box = L::kK + (uint32_t)((c0 + 32 * b) / kBoxCols) * (kTile * 128) + rsw;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float* x = &o[32 * b + 4 * e];
+            *reinterpret_cast<float4*>(sm + (box ^ (16u * e))) =
+                make_float4((x[0] * linv) * u_v, (x[1] * linv) * u_v, (x[2] * linv) * u_v, (x[3] * linv) * u_v);
+          }
         }
       }
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1, 128);
+    if (tid == 0) {
+      for (int bx = 0; bx * kBoxCols < dv && bx * kBoxCols < DV; ++bx)
+        tma_store_3d(&tmO, sm + L::kK + bx * (kTile * 128), bx * kBoxCols, q0, bh);
+      bulk_commit();
+      bulk_wait_all();  // the staging tile is read and O written before the CTA ends
     }
   }
 
@@ -489,7 +511,7 @@ cudaError_t launch_fwd_t(const FwdLaunch& f, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)(f.args.B * f.args.Hq * f.args.T);
-  return launch_overlapped(k, grid, kThreads, smem, st, f.tmQ, f.tmK, f.tmV, f.args, f.O, f.lse);
+  return launch_overlapped(k, grid, kThreads, smem, st, f.tmQ, f.tmK, f.tmV, f.tmO, f.args, f.lse);
 }
 
 }  // namespace

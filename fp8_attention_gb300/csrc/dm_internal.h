@@ -32,8 +32,8 @@ inline cudaError_t launch_overlapped(void (*k)(P...), unsigned grid, unsigned th
 
 struct FwdLaunch {
   CUtensorMap tmQ, tmK, tmV;  // [B*H][N][d] FP8 codes, box 128 x d, hardware swizzle of width d
+  CUtensorMap tmO;            // O [B*Hq][N][d_v] fp32 or bf16, box 128 rows x 128 bytes, 128-byte swizzle
   AttnArgs args;
-  void* O;
   float* lse;
 };
 
