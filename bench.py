@@ -43,9 +43,9 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # summarised in profiles/ (valid only for the kernel source it was taken on;
 # reported as null once dm_bwd.cu or dm_device.cuh changes).
 BWD_TRAFFIC = {
-    "gqa_b1_n8192_d128": {"sha1": "bc47305d5d20107e027d3de4cf8aedf51b170cce", "bytes": 262611200},
-    "gqa_b1_n8192_d256": {"sha1": "bc47305d5d20107e027d3de4cf8aedf51b170cce", "bytes": 262288128},
-    "mla_b1_n8192_d192_dv128": {"sha1": "bc47305d5d20107e027d3de4cf8aedf51b170cce", "bytes": 1961824768},
+    "gqa_b1_n8192_d128": {"sha1": "17c7fa1674cecbb88539b225c0dbaec0d7c491c9", "bytes": 267005696},
+    "gqa_b1_n8192_d256": {"sha1": "17c7fa1674cecbb88539b225c0dbaec0d7c491c9", "bytes": 263831296},
+    "mla_b1_n8192_d192_dv128": {"sha1": "17c7fa1674cecbb88539b225c0dbaec0d7c491c9", "bytes": 1857419776},
 }
 # head dimensions the Q/K prologue is built for
 PROLOGUE_DIMS = (64, 128, 256)
