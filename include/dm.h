@@ -240,7 +240,8 @@ dm_status dm_attn_delta(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tens
 /* dm_attn_bwd -- dQ, dK, dV (section 01) with the five backward matmuls in
  * FP8.  delta: float [B][Hq][N] from dm_attn_delta, or NULL, in which case it
  * is computed first for `mode` into `workspace` (which then needs
- * dm_attn_bwd_workspace_size(p) bytes, 16-byte aligned).  dQ float
+ * dm_attn_bwd_workspace_size(p) bytes, 16-byte aligned, and must not overlap
+ * the outputs or the diagnostics buffers).  dQ float
  * [B][Hq][N][d] (overwritten, not accumulated), dK float [B][Hkv][N][d] and
  * dV float [B][Hkv][N][d_v] (summed over each kv head's query heads).  diag: optional
  * row-sum diagnostics (NULL = off).  dO/O are needed only when delta is NULL
