@@ -21,7 +21,9 @@
 //   warps 0-3   one warpgroup, thread = query row (TMEM lane), all key
 //               columns in 32-column chunks: P = exp2(S*c1 - LSE*log2e),
 //               sums of P*dP (scaled by s_dO * s_V,t per key tile) and of P
-//   warp 4      TMA: Q and dO tiles once, K/V tiles double-buffered
+//   warp 4      TMA: Q and dO tiles once, K/V tiles double-buffered; when
+//               the backward computes delta itself, the clearing of its
+//               outputs (dQ, dK, dV, diagnostics) after the last loads
 //   warp 5      MMA issuer (+ TMEM owner): S(t) and dP(t)
 // TMEM columns: S 0-127, dP 128-255 (d = 256: a second pair at 256-511 for
 // odd key tiles).

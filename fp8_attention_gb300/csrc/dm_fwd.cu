@@ -14,7 +14,8 @@
 //               exchange through shared memory), P~ in FP32 straight into
 //               E4M3 codes in shared memory, the row sum from the unquantised
 //               P~, and the rescale of the O accumulator in TMEM to the units
-//               of tile t's scale product before P^_t V_t is added
+//               of tile t's scale product before P^_t V_t is added; at the
+//               end O / l, staged in shared memory for TMA tile stores
 //   warp 4      TMA producer: Q tile once, K and V tiles in two stages each
 //               (K one tile ahead of V)
 //   warp 5      MMA issuer (+ TMEM owner): S(t) = Q K_t^T, O += P^_t V_t
