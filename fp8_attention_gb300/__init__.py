@@ -378,6 +378,7 @@ def dm_attn_bwd(p: AttnParams, mode: int, q: Fp8, k: Fp8, v: Fp8, do_hat: Fp8, l
     out = {"dQ": dQ, "dK": dK, "dV": dV}
     cdiag = _diag(p, diag, dev, out)
     ws_bytes = 0
+    own_ws = delta is None and workspace is None
     if delta is None:
         ws_bytes = dm_attn_bwd_workspace_size(p)
         if workspace is None:
@@ -390,6 +391,12 @@ def dm_attn_bwd(p: AttnParams, mode: int, q: Fp8, k: Fp8, v: Fp8, do_hat: Fp8, l
                                _ptr(dV), ctypes.byref(cdiag) if cdiag is not None else None, _ptr(workspace),
                                ws_bytes, _stream(stream))
     _check(rc, "dm_attn_bwd")
+    if own_ws and stream is not None:
+        # the workspace was allocated on the current stream but is used on
+        # `stream`: keep the allocator from handing it out again before the
+        # work queued there has finished
+        s = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.ExternalStream(int(stream), device=dev)
+        workspace.record_stream(s)
     return out
 
 

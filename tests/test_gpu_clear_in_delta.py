@@ -59,3 +59,29 @@ def test_outputs_cleared_by_the_delta_pass(shape, causal):
     for key in ("dQ", "dK", "dV"):
         err = rel_err(np32(one[key]), r[key])
         assert err <= TOL, (key, err)
+
+
+def test_one_call_backward_on_a_side_stream():
+    """The one-call backward on a stream other than the current one, with the
+    workspace allocated by the binding: the same gradients as on the current
+    stream, also when the current stream allocates and writes right after."""
+    B, Hq, Hkv, N, d = 1, 4, 2, 384, 128
+    w = custom(B, Hq, Hkv, N, d, causal=True, seed=71)
+    q, k, v, do = make_inputs(w)
+    p = dm.AttnParams(B, Hq, Hkv, N, d, causal=True)
+    qh = dm.dm_quantize(q.to(DEV), dm.DM_E4M3)
+    kh = dm.dm_quantize(k.to(DEV), dm.DM_E4M3)
+    vh = dm.dm_quantize(v.to(DEV), dm.DM_E4M3)
+    doh = dm.dm_quantize(do.to(DEV), dm.DM_E5M2)
+    _, lse = dm.dm_attn_fwd(p, qh, kh, vh)
+    ref = dm.dm_attn_bwd(p, dm.DM_DELTA_MATCHED, qh, kh, vh, doh, lse, None)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream(DEV)
+    side.wait_stream(torch.cuda.current_stream())
+    got = dm.dm_attn_bwd(p, dm.DM_DELTA_MATCHED, qh, kh, vh, doh, lse, None, stream=side)
+    junk = torch.full((dm.dm_attn_bwd_workspace_size(p) // 4,), float("nan"), device=DEV)  # may not take its place
+    torch.cuda.synchronize()
+    assert dm.dm_get_status() == dm.DM_OK
+    for key in ("dQ", "dK", "dV"):
+        assert rel_err(np32(got[key]), np32(ref[key])) <= 1e-5, key
+    del junk
