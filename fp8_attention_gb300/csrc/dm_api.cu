@@ -512,6 +512,18 @@ dm_status dm_attn_bwd(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor
   unsigned int* status = nullptr;
   DM_TRY(device_state(&status));
   cudaStream_t st = as_stream(stream);
+  // the backward's tensor maps first: nothing is launched before every
+  // argument has passed, these encodings included
+  const int kw = kernel_dim(p), dv = value_dim(p);
+  const int nk = key_rows(p);
+  dm::BwdLaunch f{};
+  DM_TRY(encode_codes_map(&f.tmQ, q.codes, p->B * p->Hq, p->N, p->d, kw));
+  DM_TRY(encode_codes_map(&f.tmK, k.codes, p->B * p->Hkv, nk, p->d, kw));
+  DM_TRY(encode_codes_map(&f.tmV, v.codes, p->B * p->Hkv, nk, dv, kw));
+  DM_TRY(encode_codes_map(&f.tmDO, do_hat.codes, p->B * p->Hq, p->N, dv, kw));
+  DM_TRY(encode_f32_rows_map(&f.tmDQ, dQ, p->B * p->Hq, p->N, p->d));
+  DM_TRY(encode_f32_rows_map(&f.tmDK, dK, p->B * p->Hkv, nk, p->d));
+  DM_TRY(encode_f32_rows_map(&f.tmDV, dV, p->B * p->Hkv, nk, dv));
   // dQ, dK and dV are sums of bulk reduce-adds, the diagnostics sums of
   // atomics: all start at zero.  When the matched delta is computed here, its
   // kernel clears them on the way (no key block here: dK and dV have N rows);
@@ -524,8 +536,6 @@ dm_status dm_attn_bwd(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor
                       clear_in_delta ? &clr : nullptr));
     dl = ws;
   }
-  const int kw = kernel_dim(p), dv = value_dim(p);
-  const int nk = key_rows(p);
   if (!clear_in_delta) {
     dm::ZeroList z{};
     z.add(dQ, (size_t)p->B * p->Hq * p->N * p->d);
@@ -535,14 +545,6 @@ dm_status dm_attn_bwd(const dm_attn_params* p, dm_delta_mode mode, dm_fp8_tensor
     for (float* ptr : {dg.rowsum_pre, dg.abssum_pre, dg.rowsum_post, dg.abssum_post}) z.add(ptr, nrow);
     DM_TRY(cuda_status(dm::launch_zero(z, st)));
   }
-  dm::BwdLaunch f{};
-  DM_TRY(encode_codes_map(&f.tmQ, q.codes, p->B * p->Hq, p->N, p->d, kw));
-  DM_TRY(encode_codes_map(&f.tmK, k.codes, p->B * p->Hkv, nk, p->d, kw));
-  DM_TRY(encode_codes_map(&f.tmV, v.codes, p->B * p->Hkv, nk, dv, kw));
-  DM_TRY(encode_codes_map(&f.tmDO, do_hat.codes, p->B * p->Hq, p->N, dv, kw));
-  DM_TRY(encode_f32_rows_map(&f.tmDQ, dQ, p->B * p->Hq, p->N, p->d));
-  DM_TRY(encode_f32_rows_map(&f.tmDK, dK, p->B * p->Hkv, nk, p->d));
-  DM_TRY(encode_f32_rows_map(&f.tmDV, dV, p->B * p->Hkv, nk, dv));
   f.args = make_args(p, status);
   f.args.q_scales = q.scales, f.args.k_scales = k.scales, f.args.v_scales = v.scales;
   f.args.do_scales = do_hat.scales;
